@@ -1,0 +1,438 @@
+"""Benchmark: C = alpha*A*B + beta*C (FP16 inputs, FP32 accumulation) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 3] [--impl ours|reference]
+
+One step is one call of the library's GEMM (mpgemm_run) on the named
+workload, default the 8192^3 square GEMM (inputs larger than L2, so no flush
+is needed between steps). Prints one JSON line (rank 0).
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and torch.cuda.synchronize() on both sides, timed with CUDA events on the
+launching stream; the maximum over ranks is taken. Several GPUs run
+independent replicas (a GEMM of this size needs no collective), so
+`value` = all ranks' FLOPs / the slowest rank's time ("weak" scaling).
+
+Extra keys:
+  roofline      the tensor-core kernel's achieved TFLOP/s (2MNK per launch over
+                its average event-timed duration) against the measured bf16
+                dense peak (the fp16 kind::f16 rate is the same);
+  e2e           the same metric through mpgemm_run_host with pinned HOST
+                buffers: every step copies A and B in and C out;
+  cpu_baseline  the CPU oracle timed on a bounded sample of the same workload;
+  clocks        nvidia-smi samples taken during the timed region.
+
+--impl reference times the CPU oracle (the project's correctness reference)
+on the same workload, metric and unit, one bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "TFLOP/s (2MNK/device time) fp16->fp32 GEMM; % of GB300 dense FP16 tensor peak"
+
+
+# ----------------------------------------------------------------------------- counters
+
+def gemm_flops(M: int, N: int, K: int) -> int:
+    """2*M*N*K: one multiply and one add per (i, j, k)."""
+    return 2 * M * N * K
+
+
+def gemm_bytes(M: int, N: int, K: int, beta: float, a_bytes=2, b_bytes=2, c_bytes=4) -> int:
+    """Algorithmic HBM bytes: A and B read once, C written once (and read once if beta != 0)."""
+    c_traffic = M * N * c_bytes * (2 if beta != 0 else 1)
+    return M * K * a_bytes + K * N * b_bytes + c_traffic
+
+
+def source_hash() -> str:
+    """Hash of the kernel sources; a stored ncu traffic figure is only valid for this hash."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mixed_precision_dense_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"tflops": d["bf16_tflops"], "tflops_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"tflops": 1900.0, "tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def stored_traffic(workload_index: int):
+    """Per-launch DRAM bytes of the tensor-core kernel from a committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"gemm_tc_kernel_traffic_w{workload_index}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("source_hash") != source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_seconds: float, local_flops: float, group=None, device=None):
+    """(max seconds over ranks, total flops over ranks)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return local_seconds, local_flops
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=device)
+    f = torch.tensor([local_flops], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(f, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(f.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples every 200 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1])); smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def time_oracle_sample(w, ops, target_seconds: float, max_elements: int, seed: int):
+    """Time the oracle on seeded sampled elements of the workload; returns
+    (TFLOP/s-equivalent, seconds, elements, threads)."""
+    import oracle
+    threads = os.cpu_count() or 1
+    A, B, C = ops.bits("A"), ops.bits("B"), ops.bits("C")
+    n = 256
+    while True:
+        I, J = workloads.sample_indices(w.M, w.N, n, seed=seed, edges=False)
+        t0 = time.perf_counter()
+        oracle.elements(w.M, w.N, w.K, w.alpha, A, w.lda, B, w.ldb, w.beta, C, w.ldc, I, J,
+                        threads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= target_seconds or n >= max_elements:
+            break
+        n = min(max_elements, max(n * 2, int(n * target_seconds / max(dt, 1e-3))))
+    return gemm_flops(1, n, w.K) / dt / 1e12, dt, n, threads
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import mixed_precision_dense_gb300 as mp
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    mp.build()
+    w = workloads.WORKLOADS[args.workload]
+    ops = workloads.workload_operands(args.workload)
+    stream = torch.cuda.current_stream(device)
+    A = ops.A.to(device)
+    B = ops.B.to(device)
+    C0 = ops.C.to(device)
+    C = C0.clone()
+    handle = mp.Handle()
+
+    def step():
+        handle.run(w.M, w.N, w.K, w.alpha, A.data_ptr(), w.lda, B.data_ptr(), w.ldb, w.beta,
+                   C.data_ptr(), w.ldc, stream.cuda_stream)
+
+    plan = mp.plan(w.M, w.N, w.K, w.alpha, A.data_ptr(), w.lda, B.data_ptr(), w.ldb, w.beta,
+                   C.data_ptr(), w.ldc, num_sms=torch.cuda.get_device_properties(device).multi_processor_count)
+    launches_per_step = 1 + plan["stage_a"] + plan["stage_b"]
+
+    # correctness first, on a NaN-poisoned (beta == 0) or restored (beta != 0) C
+    if w.beta == 0:
+        C.fill_(float("nan"))
+    step()
+    st, info = handle.sync_status(stream.cuda_stream)
+    if st != mp.Status.OK:
+        raise RuntimeError(f"device reported {st.name} {info}")
+    check = None
+    if rank == 0 and not args.no_check:
+        import oracle
+        I, J = workloads.sample_indices(w.M, w.N, 2048, seed=w.seed_base + 3)
+        ref, S = oracle.elements(w.M, w.N, w.K, w.alpha, ops.bits("A"), w.lda, ops.bits("B"), w.ldb,
+                                 w.beta, ops.bits("C"), w.ldc, I, J)
+        got = C.cpu().numpy()[I, J].astype(np.float64)
+        ratio = np.abs(got - ref) / oracle.tolerance(S)
+        if not np.all(ratio <= 1.0):
+            raise AssertionError(f"bench correctness check failed: max err/tol {np.nanmax(ratio)}")
+        check = float(np.max(ratio))
+    C.copy_(C0)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(device)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    clocks = sampler.stop()
+    st, info = handle.sync_status(stream.cuda_stream)
+    if st != mp.Status.OK:
+        raise RuntimeError(f"device reported {st.name} {info}")
+    local_s = ev0.elapsed_time(ev1) / 1e3
+    flops_local = gemm_flops(w.M, w.N, w.K) * args.steps
+    max_s, flops_all = aggregate(local_s, flops_local, device=device)
+    value = flops_all / max_s / 1e12
+    ms_per_step = max_s * 1e3 / args.steps
+
+    # the dominant kernel alone: event-timed tensor-core launches (one per step
+    # when no operand needs staging; otherwise the staging launches are
+    # timed separately and subtracted)
+    kernel_ms = ms_per_step
+    if launches_per_step > 1:
+        kernel_ms = time_tc_kernel_only(handle, w, A, B, C, stream, args.steps)
+    peaks = measured_peaks()
+    achieved = gemm_flops(w.M, w.N, w.K) / (kernel_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["tflops"], 4),
+                "traffic": stored_traffic(args.workload),
+                "peak_kind": f"bf16 dense burst, {peaks['source']}",
+                "frac_of_sustained": (round(achieved / peaks["tflops_sustained"], 4)
+                                      if peaks["tflops_sustained"] else None),
+                "kernel": "gemm_tc_kernel", "algorithmic_bytes": gemm_bytes(w.M, w.N, w.K, w.beta)}
+
+    # end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(handle, w, ops, stream, device, args)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, dt, n, threads = time_oracle_sample(w, ops, args.cpu_seconds, 1 << 20, w.seed_base + 5)
+        cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} seeded elements of C (K = {w.K} MACs each) in {dt:.2f} s"}
+
+    handle.close()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16 inputs, f32 accumulate", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "lda": w.lda,
+                       "ldb": w.ldb, "ldc": w.ldc, "alpha": w.alpha, "beta": w.beta,
+                       "inputs": w.dist, "tile": f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}",
+                       "grid": plan["grid"], "parallelism": f"replicas x{world}",
+                       "l2": f"inputs larger than L2 ({gemm_bytes(w.M, w.N, w.K, w.beta) / 2**20:.0f} MiB "
+                             f"> {L2_BYTES // 2**20} MiB): no flush"
+                             if gemm_bytes(w.M, w.N, w.K, w.beta) > L2_BYTES else "L2 flushed between steps"},
+            "pct_of_peak": round(100 * value / world / peaks["tflops"], 2),
+            "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
+            "gpu_launches": launches_per_step * args.steps, "check_max_err_over_tol": check,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def time_tc_kernel_only(handle, w, A, B, C, stream, steps):
+    """Event-time the tensor-core launch on pre-staged aligned operands."""
+    import torch
+    M, N, K = w.M, w.N, w.K
+    lda, ldb = (K + 7) // 8 * 8, (N + 7) // 8 * 8
+    A2 = torch.zeros((M, lda), dtype=torch.float16, device=A.device)
+    B2 = torch.zeros((K, ldb), dtype=torch.float16, device=A.device)
+    A2[:, :K] = A[:, :K]
+    B2[:, :N] = B[:, :N]
+    for _ in range(3):
+        handle.run(M, N, K, w.alpha, A2.data_ptr(), lda, B2.data_ptr(), ldb, w.beta, C.data_ptr(),
+                   w.ldc, stream.cuda_stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        handle.run(M, N, K, w.alpha, A2.data_ptr(), lda, B2.data_ptr(), ldb, w.beta, C.data_ptr(),
+                   w.ldc, stream.cuda_stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_e2e(handle, w, ops, stream, device, args):
+    import torch
+    A_h = ops.A.pin_memory()
+    B_h = ops.B.pin_memory()
+    C_h = ops.C.clone().pin_memory()
+    steps = max(1, min(args.steps, args.e2e_steps))
+
+    def step():
+        handle.run_host(w.M, w.N, w.K, w.alpha, A_h.data_ptr(), w.lda, B_h.data_ptr(), w.ldb,
+                        w.beta, C_h.data_ptr(), w.ldc, stream.cuda_stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(device)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+        stream.synchronize()   # the step's result is on the host
+    dt = time.perf_counter() - t0
+    max_s, flops_all = aggregate(dt, gemm_flops(w.M, w.N, w.K) * steps, device=device)
+    h2d = (w.M * w.K * 2 + w.K * w.N * 2) + (w.M * w.N * 4 if w.beta != 0 else 0)
+    return {"value": round(flops_all / max_s / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": w.M * w.N * 4, "steps": steps,
+            "api": "mpgemm_run_host (pinned host buffers, host-timed, stream synchronised per step)"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = workloads.WORKLOADS[args.workload]
+    ops = workloads.workload_operands(args.workload)
+    import oracle
+    threads = os.cpu_count() or 1
+    # one bounded sample per step, sized so warm-up + steps stay within a few minutes
+    budget_s = 120.0
+    per_step = max(1, min(512, int(budget_s / max(1, args.steps + args.warmup) * 2e9 / (2 * w.K))))
+    A, B, C = ops.bits("A"), ops.bits("B"), ops.bits("C")
+
+    def step(i):
+        I, J = workloads.sample_indices(w.M, w.N, per_step, seed=w.seed_base + 100 + i, edges=False)
+        oracle.elements(w.M, w.N, w.K, w.alpha, A, w.lda, B, w.ldb, w.beta, C, w.ldc, I, J,
+                        threads=threads)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = gemm_flops(1, per_step, w.K) * args.steps / dt / 1e12
+    sample = f"{per_step} seeded elements of C per step (K = {w.K} MACs each)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle: FP16 decoded, double sums)",
+        "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", type=int, default=3, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-check", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)   # at least three warm-up steps, whatever was asked
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

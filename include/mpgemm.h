@@ -1,0 +1,150 @@
+/*
+ * mpgemm: mixed-precision GEMM for one NVIDIA GB300 (sm_103a).
+ *
+ *     C = alpha * A * B + beta * C
+ *
+ * A is M x K and B is K x N, both row-major IEEE binary16 (FP16). C is M x N,
+ * row-major IEEE binary32 (FP32). Products are accumulated in FP32 on the
+ * fifth-generation tensor cores (tcgen05, accumulators in tensor memory).
+ *
+ * The operation is the one defined on "Day 80, Capstone 4: a tensor-core
+ * GEMM" (sections "Capability" and "Minimal model": FP16 inputs, FP32
+ * accumulation and FP32 C, correct when no tile divides the matrix), with
+ * the alpha/beta scaling of the matched cublasGemmEx baseline that page and
+ * "Day 72: Tensor cores with WMMA" ("Why this program calls cuBLAS twice")
+ * compare against. The pages' own gate entry point ("Independent gate":
+ * solve(a, b, c, m, n, k, stream)) takes no alpha, beta or leading
+ * dimensions; this interface adds them in the BLAS way.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Element (i, k) of A is A[i*lda + k]; (k, j) of B is B[k*ldb + j];
+ *    (i, j) of C is C[i*ldc + j]. lda >= max(1, K), ldb >= max(1, N),
+ *    ldc >= max(1, N). Any leading dimension is accepted: operands whose
+ *    base address or row pitch is not a multiple of 16 bytes are staged
+ *    through an aligned copy on the device before the tensor-core pass.
+ *  - A and B must be aligned to 2 bytes and C to 4 bytes (their element
+ *    sizes); otherwise MPGEMM_ERR_INVALID_VALUE.
+ *  - beta == 0: C is only written, never read, so it may hold NaN on entry.
+ *    alpha == 0 or K == 0: A and B are not read and C = beta * C.
+ *    M == 0 or N == 0: nothing happens.
+ *  - Every dimension must be below 2^31, and M*N*K below 2^62.
+ *  - `stream` is a cudaStream_t (or CUstream) passed as void*; NULL is the
+ *    legacy default stream. Device entry points are asynchronous: they
+ *    enqueue work on `stream` and return without synchronising.
+ *  - The caller owns A, B, C and the stream. The handle owns its workspace
+ *    (aligned staging copies, grown on demand with stream-ordered
+ *    allocation), the tensor-core launch configuration and a status word
+ *    that the device writes if one of its bounded waits gives up.
+ *  - A handle is bound to the device that was current at mpgemm_create and
+ *    may be used from one stream at a time (its workspace is reused in
+ *    stream order). Use one handle per concurrently used stream.
+ */
+#ifndef MPGEMM_H
+#define MPGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mpgemm_handle_st* mpgemm_handle_t;
+
+typedef enum {
+    MPGEMM_OK = 0,
+    MPGEMM_ERR_INVALID_VALUE = 1,      /* bad argument; nothing was enqueued */
+    MPGEMM_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not compute capability 10.3 */
+    MPGEMM_ERR_ALLOC = 3,              /* device or pinned host allocation failed */
+    MPGEMM_ERR_LAUNCH = 4,             /* a kernel launch or copy could not be enqueued */
+    MPGEMM_ERR_DEVICE_TIMEOUT = 5,     /* a device wait gave up (reported by a later call) */
+    MPGEMM_ERR_CUDA = 6                /* another CUDA runtime or driver error */
+} mpgemm_status_t;
+
+/* Create a handle bound to the current CUDA device. Fails with
+ * MPGEMM_ERR_UNSUPPORTED_DEVICE unless that device is compute capability
+ * 10.3 (GB300). *out is set to NULL on failure. */
+mpgemm_status_t mpgemm_create(mpgemm_handle_t* out);
+
+/* Release the handle and its workspace. NULL is accepted. Work enqueued
+ * with the handle must have completed (synchronise its stream first). */
+mpgemm_status_t mpgemm_destroy(mpgemm_handle_t h);
+
+/* C = alpha*A*B + beta*C on device memory (see the conventions above).
+ * A, B and C are device pointers. Invalid arguments return
+ * MPGEMM_ERR_INVALID_VALUE before anything is enqueued. If an earlier call
+ * on this handle reported a device timeout that was not yet collected,
+ * this call returns MPGEMM_ERR_DEVICE_TIMEOUT without enqueuing work and
+ * clears the report. */
+mpgemm_status_t mpgemm_run(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                           float alpha, const void* A, int64_t lda,
+                           const void* B, int64_t ldb,
+                           float beta, float* C, int64_t ldc, void* stream);
+
+/* The same operation on HOST buffers: A, B (and C when beta != 0) are
+ * copied to device workspace owned by the handle, the GEMM runs there and
+ * C is copied back, all in order on `stream`. Host buffers may be pageable
+ * or pinned (pinned buffers make the copies asynchronous). The caller must
+ * synchronise `stream` before reading C or releasing the host buffers. */
+mpgemm_status_t mpgemm_run_host(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                float alpha, const void* A, int64_t lda,
+                                const void* B, int64_t ldb,
+                                float beta, float* C, int64_t ldc, void* stream);
+
+/* Synchronise `stream`, then report the state of the handle's device status
+ * word: MPGEMM_OK, or MPGEMM_ERR_DEVICE_TIMEOUT if a bounded device wait gave
+ * up since the last report (the report is cleared), or MPGEMM_ERR_CUDA if
+ * the synchronisation itself failed. If info is not NULL it receives four
+ * integers describing the last timeout: {code, role, block, detail}
+ * (all zero when there was none). */
+mpgemm_status_t mpgemm_sync_status(mpgemm_handle_t h, void* stream, int32_t info[4]);
+
+/* Tunables and test switches, set per handle. */
+typedef enum {
+    MPGEMM_OPT_TILE_N = 1,        /* 0 = automatic (default), or 128 or 256 columns per tile */
+    MPGEMM_OPT_MAX_CTAS = 2,      /* 0 = one persistent CTA per SM (default), else an upper bound */
+    MPGEMM_OPT_FORCE_STAGING = 3, /* 1 = stage A and B through aligned copies even when aligned */
+    MPGEMM_OPT_WAIT_LIMIT_US = 4, /* limit of every bounded device wait, microseconds (default 4e6) */
+    MPGEMM_OPT_RASTER_GROUP = 5,  /* M-tiles per rasterisation group, 0 = automatic (default) */
+    MPGEMM_OPT_TEST_STALL = 6     /* test only: 1 = the load warp issues no loads, so the
+                                     kernel's bounded waits expire and a timeout is reported */
+} mpgemm_option_t;
+
+/* Set an option. Unknown options or out-of-range values return
+ * MPGEMM_ERR_INVALID_VALUE and leave the handle unchanged. */
+mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_t value);
+
+/* What mpgemm_run would do for these arguments, computed on the host only
+ * (no device work; usable without a GPU). `num_sms` stands in for the
+ * device's SM count; tile_n and max_ctas mirror the options above. */
+typedef struct {
+    int32_t quick;          /* 0 = tensor-core path, 1 = nothing to do, 2 = C = beta*C only */
+    int32_t stage_a;        /* 1 if A is copied to an aligned buffer first */
+    int32_t stage_b;        /* 1 if B is copied to an aligned buffer first */
+    int32_t tile_m;         /* rows per output tile (128) */
+    int32_t tile_n;         /* columns per output tile (128 or 256) */
+    int32_t tile_k;         /* K per pipeline stage (64) */
+    int32_t stages;         /* shared-memory pipeline depth */
+    int32_t m_tiles, n_tiles, k_blocks;
+    int64_t tiles;          /* m_tiles * n_tiles */
+    int32_t grid;           /* persistent CTAs launched */
+    int32_t raster_group;   /* M-tiles walked per column band */
+    int32_t smem_bytes;     /* dynamic shared memory per CTA */
+    int32_t last_k_valid;   /* valid K columns in the last pipeline stage */
+    int64_t workspace_bytes;/* device staging bytes the call needs */
+} mpgemm_plan_t;
+
+mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha,
+                            const void* A, int64_t lda, const void* B, int64_t ldb,
+                            float beta, const float* C, int64_t ldc,
+                            int32_t num_sms, int32_t tile_n, int32_t max_ctas, int32_t force_staging,
+                            mpgemm_plan_t* out);
+
+/* A static description of a status code. Never NULL. */
+const char* mpgemm_status_string(mpgemm_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MPGEMM_H */

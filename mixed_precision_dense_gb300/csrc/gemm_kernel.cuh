@@ -1,0 +1,358 @@
+// The tensor-core pass of C = alpha*A*B + beta*C for sm_103a.
+//
+// One persistent CTA per SM walks output tiles of 128 x BN. Its six warps
+// have fixed roles:
+//   warp 0      load warp: one lane issues TMA loads of A (128 x 64, K-major)
+//               and B (64 x BN, N-major) into a ring of shared-memory stages;
+//               rows, columns and K past the matrix edge arrive as zeros
+//               (TMA out-of-bounds fill), which replaces the padding and
+//               guarded tail loads of "Day 80, Capstone 4: a tensor-core
+//               GEMM" ("Faded practice", practice 3; "Common failures").
+//   warp 1      MMA warp: allocates tensor memory; one lane issues
+//               tcgen05.mma (M = 128, N <= BN, K = 16; FP16 x FP16 -> FP32)
+//               into one of two accumulator buffers and frees each stage
+//               with tcgen05.commit.
+//   warps 2-5   epilogue: each warp reads its 32 accumulator rows with
+//               tcgen05.ld, applies alpha (and beta * C when beta != 0) in
+//               FP32, and writes C with row and column masks, so any M, N
+//               and any ldc are handled. While it works on tile i, the MMA
+//               warp already accumulates tile i+1 into the other buffer.
+//
+// The staged-tile reuse, asynchronous copies and block rasterisation that
+// the pages build up with WMMA ("Day 80", "Worked path"; "02_mixed_precision
+// _gemm" README, "Summary": cp.async double buffering and cross-block L2
+// reuse) map onto this design as: the 128 x BN tile held in shared memory
+// and consumed by one MMA thread, the multistage TMA + mbarrier ring, and
+// grouped rasterisation of the persistent tile walk.
+//
+// Every wait is bounded: if a barrier does not complete within the limit,
+// the thread records the fact in the handle's status word, raises a CTA-wide
+// abort flag, lets its own in-flight copies and MMAs drain (again bounded),
+// and the CTA releases its tensor memory and exits.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "ptx.cuh"
+
+namespace mpgemm {
+
+struct GemmParams {
+    int32_t M, N, K;
+    int32_t m_tiles, n_tiles, k_blocks;
+    int32_t tiles;
+    int32_t raster_group;
+    float alpha, beta;
+    float* C;
+    int64_t ldc;
+    int32_t* status;        // {code, role, block, detail}, mapped host memory
+    uint64_t wait_limit_ns;
+    int32_t test_stall;     // 1: the load warp issues nothing (timeout test)
+};
+
+enum : int32_t { kRoleLoad = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4 };
+enum : int32_t { kStatusTimeout = 1 };
+
+template <int BN_, int STAGES_>
+struct TileConfig {
+    static constexpr int BM = 128;
+    static constexpr int BN = BN_;
+    static constexpr int BK = 64;                     // 64 halves = one 128-byte swizzle row
+    static constexpr int STAGES = STAGES_;
+    static constexpr int A_BYTES = BM * BK * 2;       // 16 KB
+    static constexpr int B_ATOM_BYTES = BK * 64 * 2;  // one 64-column box of B: 8 KB
+    static constexpr int B_BYTES = BK * BN * 2;
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int EPI_PITCH = 33;              // floats per row of a transpose buffer
+    static constexpr int EPI_BYTES = EPI_WARPS * 32 * EPI_PITCH * 4;
+    static constexpr int TMEM_COLS = 2 * BN;          // two accumulator buffers
+    static constexpr int NUM_BARRIERS = 2 * STAGES + 4;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = STAGES * A_BYTES;
+    static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARRIERS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+    static constexpr int THREADS = 192;
+    static_assert(BN == 128 || BN == 256, "tile width");
+    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "tensor memory allocation");
+};
+
+// Tile t of the persistent walk -> (m block, n block). Tiles are visited in
+// bands of `raster_group` M-blocks: down the band for one N-block, then the
+// next N-block, so CTAs running at the same time share A and B panels in L2.
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int32_t t, int32_t& mb,
+                                            int32_t& nb) {
+    const int32_t per_band = p.raster_group * p.n_tiles;
+    const int32_t band = t / per_band;
+    const int32_t first_m = band * p.raster_group;
+    const int32_t rows = min(p.m_tiles - first_m, p.raster_group);
+    const int32_t r = t - band * per_band;
+    mb = first_m + r % rows;
+    nb = r / rows;
+}
+
+struct Waiter {
+    const GemmParams* p;
+    volatile int32_t* abort_flag;
+
+    // Spin until the phase of `bar` with parity `parity` completes. Returns
+    // false if the limit passes or another thread of the CTA aborted.
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (true) {
+            if (ptx::mbar_try_wait(bar, parity)) return true;
+            if (*abort_flag) return false;
+            if (ptx::globaltimer_ns() - t0 > p->wait_limit_ns) return false;
+        }
+    }
+
+    __device__ __forceinline__ void fail(int32_t role, int32_t detail) const {
+        *abort_flag = 1;
+        volatile int32_t* s = p->status;
+        if (s[0] == 0) {
+            s[1] = role;
+            s[2] = static_cast<int32_t>(blockIdx.x);
+            s[3] = detail;
+            __threadfence_system();
+            s[0] = kStatusTimeout;
+        }
+        __threadfence_system();
+    }
+};
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw_addr);
+
+    const uint32_t sA = base + Cfg::OFF_A;
+    const uint32_t sB = base + Cfg::OFF_B;
+    float* epi_buf = reinterpret_cast<float*>(gbase + Cfg::OFF_EPI);
+    const uint32_t bar0 = base + Cfg::OFF_BAR;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto acc_full_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto acc_empty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Cfg::OFF_MISC);
+    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + Cfg::OFF_MISC + 4);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const Waiter waiter{&p, abort_flag};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(acc_full_bar(b), 1);
+            ptx::mbar_init(acc_empty_bar(b), Cfg::EPI_WARPS);
+        }
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmap_a);
+        ptx::prefetch_tensormap(&tmap_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), Cfg::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ loads
+        if (lane == 0) {
+            const uint64_t pol_a = ptx::policy_evict_first();
+            const uint64_t pol_b = ptx::policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0;               // stages that received loads
+            uint32_t armed_parity = 0;        // parity of the last load per stage
+            bool ok = true;
+            if (!p.test_stall) {
+                for (int32_t t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+                    int32_t mb, nb;
+                    tile_coords(p, t, mb, nb);
+                    const int32_t n0 = nb * BN;
+                    const int32_t n_atoms = min(BN / 64, (p.N - n0 + 63) / 64);
+                    const uint32_t bytes = Cfg::A_BYTES + n_atoms * Cfg::B_ATOM_BYTES;
+                    for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+                        if (!waiter.wait(empty_bar(stage), phase ^ 1u)) {
+                            waiter.fail(kRoleLoad, kb);
+                            ok = false;
+                            break;
+                        }
+                        ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
+                        ptx::tma_load_2d(sA + stage * Cfg::A_BYTES, &tmap_a, full_bar(stage),
+                                         kb * BK, mb * BM, pol_a);
+                        for (int j = 0; j < n_atoms; ++j)
+                            ptx::tma_load_2d(sB + stage * Cfg::B_BYTES + j * Cfg::B_ATOM_BYTES,
+                                             &tmap_b, full_bar(stage), n0 + j * 64, kb * BK, pol_b);
+                        armed |= 1u << stage;
+                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                // Let every load this thread issued land before the CTA exits.
+                for (int s = 0; s < STAGES; ++s) {
+                    if (!(armed & (1u << s))) continue;
+                    const uint32_t par = (armed_parity >> s) & 1u;
+                    const uint64_t t0 = ptx::globaltimer_ns();
+                    while (!ptx::mbar_try_wait(full_bar(s), par) &&
+                           ptx::globaltimer_ns() - t0 < p.wait_limit_ns) {
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int32_t local = 0;
+            bool ok = true;
+            bool issued = false;
+            for (int32_t t = blockIdx.x; ok && t < p.tiles; t += gridDim.x, ++local) {
+                int32_t mb, nb;
+                tile_coords(p, t, mb, nb);
+                const int32_t n0 = nb * BN;
+                const int32_t n_atoms = min(BN / 64, (p.N - n0 + 63) / 64);
+                const uint32_t idesc = ptx::idesc_f16_f32(BM, n_atoms * 64, false, true);
+                const int buf = local & 1;
+                const uint32_t acc_phase = (local >> 1) & 1;
+                if (!waiter.wait(acc_empty_bar(buf), acc_phase ^ 1u)) {
+                    waiter.fail(kRoleMma, -1);
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!waiter.wait(full_bar(stage), phase)) {
+                        waiter.fail(kRoleMma, kb);
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                    const uint32_t a_base = sA + stage * Cfg::A_BYTES;
+                    const uint32_t b_base = sB + stage * Cfg::B_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // A: K-major, 128-byte rows, 8-row groups 1024 B apart;
+                        //    the k-th 16-wide slice starts 32 bytes further.
+                        const uint64_t a_desc = ptx::smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                        // B: N-major, 64-column boxes B_ATOM_BYTES apart (leading
+                        //    offset), 8 K-rows of 128 B per group (stride offset);
+                        //    the k-th 16-row slice starts 16 * 128 bytes further.
+                        const uint64_t b_desc =
+                            ptx::smem_desc_sw128(b_base + kk * 2048, Cfg::B_ATOM_BYTES, 1024);
+                        ptx::mma_f16(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0);
+                    }
+                    issued = true;
+                    ptx::mma_commit(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) ptx::mma_commit(acc_full_bar(buf));
+            }
+            if (!ok && issued) {
+                // Drain this thread's MMAs before tensor memory is released:
+                // the last commit arrives on the stage before `stage`.
+                const int last = (stage + STAGES - 1) % STAGES;
+                const uint32_t par = (stage == 0) ? (phase ^ 1u) : phase;
+                const uint64_t t0 = ptx::globaltimer_ns();
+                while (!ptx::mbar_try_wait(empty_bar(last), par) &&
+                       ptx::globaltimer_ns() - t0 < p.wait_limit_ns) {
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;             // tensor-memory lanes 32*quarter ..
+        float* buf = epi_buf + (warp - 2) * 32 * Cfg::EPI_PITCH;
+        const float alpha = p.alpha, beta = p.beta;
+        int32_t local = 0;
+        for (int32_t t = blockIdx.x; t < p.tiles; t += gridDim.x, ++local) {
+            int32_t mb, nb;
+            tile_coords(p, t, mb, nb);
+            const int32_t m0 = mb * BM + quarter * 32;
+            const int32_t n0 = nb * BN;
+            const int accb = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            const bool ready = waiter.wait(acc_full_bar(accb), acc_phase);
+            if (!__all_sync(0xffffffffu, ready)) {
+                if (lane == 0) waiter.fail(kRoleEpilogue, t);
+                break;
+            }
+            ptx::tc_fence_after_sync();
+            const uint32_t t_row =
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(accb * BN);
+            const int32_t ncols = min(BN, p.N - n0);
+            const int32_t chunks = (ncols + 31) / 32;
+            for (int32_t c = 0; c < chunks; ++c) {
+                uint32_t r[32];
+                ptx::tmem_load_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
+                ptx::tmem_load_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) buf[lane * Cfg::EPI_PITCH + j] = alpha * __uint_as_float(r[j]);
+                __syncwarp();
+                const int32_t col = n0 + c * 32 + lane;
+                if (col < p.N) {
+                    float* cp = p.C + static_cast<int64_t>(m0) * p.ldc + col;
+                    const int32_t rows = min(32, p.M - m0);
+                    if (beta != 0.0f) {
+#pragma unroll 8
+                        for (int32_t rr = 0; rr < rows; ++rr) {
+                            float* q = cp + static_cast<int64_t>(rr) * p.ldc;
+                            *q = fmaf(beta, *q, buf[rr * Cfg::EPI_PITCH + lane]);
+                        }
+                    } else {
+#pragma unroll 8
+                        for (int32_t rr = 0; rr < rows; ++rr)
+                            cp[static_cast<int64_t>(rr) * p.ldc] = buf[rr * Cfg::EPI_PITCH + lane];
+                    }
+                }
+                __syncwarp();
+            }
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(acc_empty_bar(accb));
+        }
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+}  // namespace mpgemm

@@ -1,0 +1,509 @@
+// mpgemm: host side of the C ABI declared in include/mpgemm.h.
+//
+// mpgemm_run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream):
+//   1. validate and classify (host): quick returns for M*N == 0 (nothing)
+//      and K == 0 or alpha == 0 (C = beta*C); for A and B, whether base
+//      address and row pitch are both multiples of 16 bytes, which the
+//      tensor memory accelerator (TMA) requires;
+//   2. stage an operand that fails that test into an aligned copy in the
+//      handle's workspace (stage_rows_u16);
+//   3. encode 2-D tensor maps with 128-byte swizzle and zero fill past the
+//      matrix edge;
+//   4. launch the persistent tensor-core kernel (gemm_kernel.cuh) with one
+//      CTA per SM on `stream`.
+// Everything is stream-ordered; nothing here synchronises the device.
+//
+// The operation: "Day 80, Capstone 4: a tensor-core GEMM" ("Capability",
+// "Minimal model"); the alpha/beta scaling of its matched cublasGemmEx
+// baseline ("Compare like with like"); ragged edges by zero fill ("Faded
+// practice", practice 3: zero is safe for a matrix product); unaligned
+// leading dimensions ("Common failures": a misaligned address is a broken
+// load promise) by an aligned staging copy, the GB300 counterpart of the
+// padded operand of "GEMM kernels 1-7 + Tensor Cores" (TC-02, K padded to
+// 1008).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mpgemm.h"
+#include "gemm_kernel.cuh"
+
+namespace mpgemm {
+namespace {
+
+constexpr int64_t kDimLimit = (int64_t{1} << 31) - 1;
+constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;
+
+using Cfg256 = TileConfig<256, 4>;
+using Cfg128 = TileConfig<128, 6>;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+struct Options {
+    int32_t tile_n = 0;
+    int32_t max_ctas = 0;
+    int32_t force_staging = 0;
+    int32_t raster_group = 0;
+    int32_t test_stall = 0;
+    uint64_t wait_limit_ns = kDefaultWaitLimitNs;
+};
+
+bool aligned16(const void* p, int64_t ld_elems, int64_t elem_bytes) {
+    return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld_elems * elem_bytes) % 16 == 0);
+}
+
+mpgemm_status_t validate(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+                         const void* B, int64_t ldb, float beta, const void* C, int64_t ldc) {
+    if (M < 0 || N < 0 || K < 0) return MPGEMM_ERR_INVALID_VALUE;
+    if (M > kDimLimit || N > kDimLimit || K > kDimLimit) return MPGEMM_ERR_INVALID_VALUE;
+    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+        return MPGEMM_ERR_INVALID_VALUE;
+    if (lda > kDimLimit || ldb > kDimLimit || ldc > kDimLimit) return MPGEMM_ERR_INVALID_VALUE;
+    if (M > 0 && N > 0 && K > 0 && M * N > (int64_t{1} << 62) / K) return MPGEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return MPGEMM_OK;
+    if (!C || reinterpret_cast<uintptr_t>(C) % 4 != 0) return MPGEMM_ERR_INVALID_VALUE;
+    if (K > 0 && alpha != 0.0f) {
+        if (!A || !B) return MPGEMM_ERR_INVALID_VALUE;
+        if (reinterpret_cast<uintptr_t>(A) % 2 != 0 || reinterpret_cast<uintptr_t>(B) % 2 != 0)
+            return MPGEMM_ERR_INVALID_VALUE;
+    }
+    (void)beta;
+    return MPGEMM_OK;
+}
+
+int32_t auto_tile_n(int64_t M, int64_t N, int32_t num_sms) {
+    if (N <= 128) return 128;
+    const int64_t tiles256 = ceil_div(M, 128) * ceil_div(N, 256);
+    return tiles256 >= num_sms ? 256 : 128;
+}
+
+mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+                          const void* B, int64_t ldb, float beta, const void* C, int64_t ldc,
+                          int32_t num_sms, const Options& opt, mpgemm_plan_t* out) {
+    mpgemm_status_t st = validate(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
+    if (st != MPGEMM_OK) return st;
+    if (num_sms <= 0) return MPGEMM_ERR_INVALID_VALUE;
+    mpgemm_plan_t p;
+    std::memset(&p, 0, sizeof(p));
+    p.tile_m = 128;
+    p.tile_k = 64;
+    if (M == 0 || N == 0) {
+        p.quick = 1;
+    } else if (K == 0 || alpha == 0.0f) {
+        p.quick = 2;
+    }
+    if (p.quick) {
+        *out = p;
+        return MPGEMM_OK;
+    }
+    p.stage_a = (opt.force_staging || !aligned16(A, lda, 2)) ? 1 : 0;
+    p.stage_b = (opt.force_staging || !aligned16(B, ldb, 2)) ? 1 : 0;
+    p.tile_n = opt.tile_n ? opt.tile_n : auto_tile_n(M, N, num_sms);
+    p.stages = (p.tile_n == 256) ? Cfg256::STAGES : Cfg128::STAGES;
+    p.smem_bytes = (p.tile_n == 256) ? Cfg256::SMEM_BYTES : Cfg128::SMEM_BYTES;
+    const int64_t m_tiles = ceil_div(M, 128), n_tiles = ceil_div(N, p.tile_n);
+    const int64_t k_blocks = ceil_div(K, 64);
+    if (m_tiles * n_tiles > kDimLimit) return MPGEMM_ERR_INVALID_VALUE;
+    p.m_tiles = static_cast<int32_t>(m_tiles);
+    p.n_tiles = static_cast<int32_t>(n_tiles);
+    p.k_blocks = static_cast<int32_t>(k_blocks);
+    p.tiles = m_tiles * n_tiles;
+    p.last_k_valid = static_cast<int32_t>(K - (k_blocks - 1) * 64);
+    int64_t grid = p.tiles < num_sms ? p.tiles : num_sms;
+    if (opt.max_ctas > 0 && grid > opt.max_ctas) grid = opt.max_ctas;
+    p.grid = static_cast<int32_t>(grid);
+    int32_t group = opt.raster_group ? opt.raster_group : 16;
+    if (group > p.m_tiles) group = p.m_tiles;
+    p.raster_group = group;
+    int64_t ws = 0;
+    if (p.stage_a) ws += round_up(M * round_up(K, 8) * 2, 256);
+    if (p.stage_b) ws += round_up(K * round_up(N, 8) * 2, 256);
+    p.workspace_bytes = ws;
+    *out = p;
+    return MPGEMM_OK;
+}
+
+// ------------------------------------------------------------------ kernels
+
+// dst[r][c] = src[r][c] for c < cols, zero for cols <= c < round_up(cols, 8);
+// 16-bit elements, dst rows 16-byte aligned. One thread per 16-byte chunk.
+__global__ void stage_rows_u16(const uint16_t* __restrict__ src, int64_t lds,
+                               uint16_t* __restrict__ dst, int64_t ldd, int64_t rows,
+                               int64_t cols) {
+    const int64_t chunks = (cols + 7) / 8;
+    const int64_t total = rows * chunks;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = idx / chunks;
+        const int64_t c = (idx - r * chunks) * 8;
+        const uint16_t* s = src + r * lds + c;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t lo = (c + 2 * e < cols) ? s[2 * e] : 0u;
+            const uint32_t hi = (c + 2 * e + 1 < cols) ? s[2 * e + 1] : 0u;
+            w[e] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4*>(dst + r * ldd + c) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// C = beta * C over M x N (beta == 0 writes zeros without reading C).
+__global__ void scale_c(float* __restrict__ C, int64_t ldc, int64_t M, int64_t N, float beta) {
+    const int64_t total = M * N;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t i = idx / N, j = idx - (idx / N) * N;
+        float* p = C + i * ldc + j;
+        *p = (beta == 0.0f) ? 0.0f : beta * *p;
+    }
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Row-major FP16 matrix rows x cols with pitch ld (elements), boxes of
+// box_cols x box_rows, 128-byte swizzle, zeros outside the matrix.
+bool encode_f16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
+                uint32_t box_cols, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int grid_for(int64_t work, int num_sms) {
+    const int64_t blocks = ceil_div(work, 256);
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+template <class Cfg>
+cudaError_t set_smem_attr() {
+    return cudaFuncSetAttribute(gemm_tc_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg::SMEM_BYTES);
+}
+
+template <class Cfg>
+void launch_tc(const mpgemm_plan_t& plan, const CUtensorMap& ta, const CUtensorMap& tb,
+               const GemmParams& gp, cudaStream_t stream) {
+    gemm_tc_kernel<Cfg><<<plan.grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, gp);
+}
+
+}  // namespace
+}  // namespace mpgemm
+
+using namespace mpgemm;
+
+struct mpgemm_handle_st {
+    int device = 0;
+    int num_sms = 0;
+    Options opt;
+    int32_t* status_host = nullptr;  // mapped pinned memory: {code, role, block, detail}
+    int32_t* status_dev = nullptr;
+    void* ws = nullptr;              // staging copies of unaligned operands
+    size_t ws_bytes = 0;
+    void* host_ws = nullptr;         // device copies for mpgemm_run_host
+    size_t host_ws_bytes = 0;
+};
+
+namespace {
+
+mpgemm_status_t ensure_buffer(void** ptr, size_t* cap, size_t need, cudaStream_t s) {
+    if (need <= *cap) return MPGEMM_OK;
+    if (*ptr) cudaFreeAsync(*ptr, s);
+    *ptr = nullptr;
+    *cap = 0;
+    if (cudaMallocAsync(ptr, need, s) != cudaSuccess) {
+        cudaGetLastError();
+        *ptr = nullptr;
+        return MPGEMM_ERR_ALLOC;
+    }
+    *cap = need;
+    return MPGEMM_OK;
+}
+
+mpgemm_status_t take_device_report(mpgemm_handle_t h, int32_t info[4]) {
+    volatile int32_t* s = h->status_host;
+    const int32_t code = s[0];
+    if (info) {
+        info[0] = code;
+        info[1] = code ? s[1] : 0;
+        info[2] = code ? s[2] : 0;
+        info[3] = code ? s[3] : 0;
+    }
+    if (code == 0) return MPGEMM_OK;
+    s[1] = s[2] = s[3] = 0;
+    s[0] = 0;
+    return MPGEMM_ERR_DEVICE_TIMEOUT;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mpgemm_status_string(mpgemm_status_t s) {
+    switch (s) {
+        case MPGEMM_OK: return "success";
+        case MPGEMM_ERR_INVALID_VALUE: return "invalid argument";
+        case MPGEMM_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+        case MPGEMM_ERR_ALLOC: return "allocation failed";
+        case MPGEMM_ERR_LAUNCH: return "kernel launch or copy failed";
+        case MPGEMM_ERR_DEVICE_TIMEOUT: return "a bounded device wait gave up";
+        case MPGEMM_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                            int64_t lda, const void* B, int64_t ldb, float beta, const float* C,
+                            int64_t ldc, int32_t num_sms, int32_t tile_n, int32_t max_ctas,
+                            int32_t force_staging, mpgemm_plan_t* out) {
+    if (!out) return MPGEMM_ERR_INVALID_VALUE;
+    if (tile_n != 0 && tile_n != 128 && tile_n != 256) return MPGEMM_ERR_INVALID_VALUE;
+    if (max_ctas < 0) return MPGEMM_ERR_INVALID_VALUE;
+    Options opt;
+    opt.tile_n = tile_n;
+    opt.max_ctas = max_ctas;
+    opt.force_staging = force_staging ? 1 : 0;
+    return make_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, num_sms, opt, out);
+}
+
+mpgemm_status_t mpgemm_create(mpgemm_handle_t* out) {
+    if (!out) return MPGEMM_ERR_INVALID_VALUE;
+    *out = nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MPGEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MPGEMM_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return MPGEMM_ERR_UNSUPPORTED_DEVICE;
+    if (!encode_fn()) return MPGEMM_ERR_CUDA;
+    if (set_smem_attr<Cfg256>() != cudaSuccess || set_smem_attr<Cfg128>() != cudaSuccess) {
+        cudaGetLastError();
+        return MPGEMM_ERR_CUDA;
+    }
+    mpgemm_handle_st* h = new (std::nothrow) mpgemm_handle_st();
+    if (!h) return MPGEMM_ERR_ALLOC;
+    h->device = dev;
+    h->num_sms = sms;
+    void* st = nullptr;
+    if (cudaHostAlloc(&st, 4 * sizeof(int32_t), cudaHostAllocMapped) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return MPGEMM_ERR_ALLOC;
+    }
+    h->status_host = static_cast<int32_t*>(st);
+    std::memset(h->status_host, 0, 4 * sizeof(int32_t));
+    void* dptr = nullptr;
+    if (cudaHostGetDevicePointer(&dptr, st, 0) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFreeHost(st);
+        delete h;
+        return MPGEMM_ERR_CUDA;
+    }
+    h->status_dev = static_cast<int32_t*>(dptr);
+    *out = h;
+    return MPGEMM_OK;
+}
+
+mpgemm_status_t mpgemm_destroy(mpgemm_handle_t h) {
+    if (!h) return MPGEMM_OK;
+    if (h->ws) cudaFree(h->ws);
+    if (h->host_ws) cudaFree(h->host_ws);
+    if (h->status_host) cudaFreeHost(h->status_host);
+    cudaGetLastError();
+    delete h;
+    return MPGEMM_OK;
+}
+
+mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_t value) {
+    if (!h) return MPGEMM_ERR_INVALID_VALUE;
+    switch (opt) {
+        case MPGEMM_OPT_TILE_N:
+            if (value != 0 && value != 128 && value != 256) return MPGEMM_ERR_INVALID_VALUE;
+            h->opt.tile_n = static_cast<int32_t>(value);
+            return MPGEMM_OK;
+        case MPGEMM_OPT_MAX_CTAS:
+            if (value < 0 || value > kDimLimit) return MPGEMM_ERR_INVALID_VALUE;
+            h->opt.max_ctas = static_cast<int32_t>(value);
+            return MPGEMM_OK;
+        case MPGEMM_OPT_FORCE_STAGING:
+            if (value != 0 && value != 1) return MPGEMM_ERR_INVALID_VALUE;
+            h->opt.force_staging = static_cast<int32_t>(value);
+            return MPGEMM_OK;
+        case MPGEMM_OPT_WAIT_LIMIT_US:
+            if (value < 1000 || value > 60000000) return MPGEMM_ERR_INVALID_VALUE;
+            h->opt.wait_limit_ns = static_cast<uint64_t>(value) * 1000ull;
+            return MPGEMM_OK;
+        case MPGEMM_OPT_RASTER_GROUP:
+            if (value < 0 || value > 65536) return MPGEMM_ERR_INVALID_VALUE;
+            h->opt.raster_group = static_cast<int32_t>(value);
+            return MPGEMM_OK;
+        case MPGEMM_OPT_TEST_STALL:
+            if (value != 0 && value != 1) return MPGEMM_ERR_INVALID_VALUE;
+            h->opt.test_stall = static_cast<int32_t>(value);
+            return MPGEMM_OK;
+    }
+    return MPGEMM_ERR_INVALID_VALUE;
+}
+
+mpgemm_status_t mpgemm_run(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha,
+                           const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
+                           float* C, int64_t ldc, void* stream_ptr) {
+    if (!h) return MPGEMM_ERR_INVALID_VALUE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    mpgemm_plan_t plan;
+    mpgemm_status_t st =
+        make_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, h->num_sms, h->opt, &plan);
+    if (st != MPGEMM_OK) return st;
+    if (take_device_report(h, nullptr) != MPGEMM_OK) return MPGEMM_ERR_DEVICE_TIMEOUT;
+    if (plan.quick == 1) return MPGEMM_OK;
+    if (plan.quick == 2) {
+        scale_c<<<grid_for(M * N, h->num_sms), 256, 0, stream>>>(C, ldc, M, N, beta);
+        return cudaGetLastError() == cudaSuccess ? MPGEMM_OK : MPGEMM_ERR_LAUNCH;
+    }
+
+    const void* a_use = A;
+    const void* b_use = B;
+    int64_t lda_use = lda, ldb_use = ldb;
+    if (plan.workspace_bytes > 0) {
+        st = ensure_buffer(&h->ws, &h->ws_bytes, static_cast<size_t>(plan.workspace_bytes), stream);
+        if (st != MPGEMM_OK) return st;
+        uint8_t* ws = static_cast<uint8_t*>(h->ws);
+        if (plan.stage_a) {
+            lda_use = round_up(K, 8);
+            stage_rows_u16<<<grid_for(M * ceil_div(K, 8), h->num_sms), 256, 0, stream>>>(
+                static_cast<const uint16_t*>(A), lda, reinterpret_cast<uint16_t*>(ws), lda_use, M, K);
+            a_use = ws;
+            ws += round_up(M * lda_use * 2, 256);
+        }
+        if (plan.stage_b) {
+            ldb_use = round_up(N, 8);
+            stage_rows_u16<<<grid_for(K * ceil_div(N, 8), h->num_sms), 256, 0, stream>>>(
+                static_cast<const uint16_t*>(B), ldb, reinterpret_cast<uint16_t*>(ws), ldb_use, K, N);
+            b_use = ws;
+        }
+        if (cudaGetLastError() != cudaSuccess) return MPGEMM_ERR_LAUNCH;
+    }
+
+    CUtensorMap ta, tb;
+    if (!encode_f16(&ta, a_use, M, K, lda_use, 64, 128) ||
+        !encode_f16(&tb, b_use, K, N, ldb_use, 64, 64))
+        return MPGEMM_ERR_CUDA;
+
+    GemmParams gp;
+    gp.M = static_cast<int32_t>(M);
+    gp.N = static_cast<int32_t>(N);
+    gp.K = static_cast<int32_t>(K);
+    gp.m_tiles = plan.m_tiles;
+    gp.n_tiles = plan.n_tiles;
+    gp.k_blocks = plan.k_blocks;
+    gp.tiles = static_cast<int32_t>(plan.tiles);
+    gp.raster_group = plan.raster_group;
+    gp.alpha = alpha;
+    gp.beta = beta;
+    gp.C = C;
+    gp.ldc = ldc;
+    gp.status = h->status_dev;
+    gp.wait_limit_ns = h->opt.wait_limit_ns;
+    gp.test_stall = h->opt.test_stall;
+    if (plan.tile_n == 256)
+        launch_tc<Cfg256>(plan, ta, tb, gp, stream);
+    else
+        launch_tc<Cfg128>(plan, ta, tb, gp, stream);
+    return cudaGetLastError() == cudaSuccess ? MPGEMM_OK : MPGEMM_ERR_LAUNCH;
+}
+
+mpgemm_status_t mpgemm_run_host(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha,
+                                const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
+                                float* C, int64_t ldc, void* stream_ptr) {
+    if (!h) return MPGEMM_ERR_INVALID_VALUE;
+    mpgemm_status_t st = validate(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
+    if (st != MPGEMM_OK) return st;
+    if (M == 0 || N == 0) return MPGEMM_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    const bool need_ab = (K > 0 && alpha != 0.0f);
+    const int64_t lda_d = round_up(K > 0 ? K : 1, 8), ldb_d = round_up(N, 8), ldc_d = round_up(N, 4);
+    const int64_t a_bytes = need_ab ? round_up(M * lda_d * 2, 256) : 0;
+    const int64_t b_bytes = need_ab ? round_up(K * ldb_d * 2, 256) : 0;
+    const int64_t c_bytes = round_up(M * ldc_d * 4, 256);
+    st = ensure_buffer(&h->host_ws, &h->host_ws_bytes, static_cast<size_t>(a_bytes + b_bytes + c_bytes),
+                       stream);
+    if (st != MPGEMM_OK) return st;
+    uint8_t* base = static_cast<uint8_t*>(h->host_ws);
+    void* dA = base;
+    void* dB = base + a_bytes;
+    float* dC = reinterpret_cast<float*>(base + a_bytes + b_bytes);
+    if (need_ab) {
+        if (cudaMemcpy2DAsync(dA, lda_d * 2, A, lda * 2, K * 2, M, cudaMemcpyHostToDevice, stream) !=
+                cudaSuccess ||
+            cudaMemcpy2DAsync(dB, ldb_d * 2, B, ldb * 2, N * 2, K, cudaMemcpyHostToDevice, stream) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            return MPGEMM_ERR_LAUNCH;
+        }
+    }
+    if (beta != 0.0f &&
+        cudaMemcpy2DAsync(dC, ldc_d * 4, C, ldc * 4, N * 4, M, cudaMemcpyHostToDevice, stream) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return MPGEMM_ERR_LAUNCH;
+    }
+    st = mpgemm_run(h, M, N, K, alpha, need_ab ? dA : nullptr, need_ab ? lda_d : (K > 1 ? K : 1),
+                    need_ab ? dB : nullptr, ldb_d, beta, dC, ldc_d, stream_ptr);
+    if (st != MPGEMM_OK) return st;
+    if (cudaMemcpy2DAsync(C, ldc * 4, dC, ldc_d * 4, N * 4, M, cudaMemcpyDeviceToHost, stream) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return MPGEMM_ERR_LAUNCH;
+    }
+    return MPGEMM_OK;
+}
+
+mpgemm_status_t mpgemm_sync_status(mpgemm_handle_t h, void* stream, int32_t info[4]) {
+    if (!h) return MPGEMM_ERR_INVALID_VALUE;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return MPGEMM_ERR_CUDA;
+    }
+    return take_device_report(h, info);
+}
+
+}  // extern "C"

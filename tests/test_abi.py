@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for
+sm_103a, loads, exports every function include/mpgemm.h declares, and its
+host planning (validation, quick returns, alignment classification, tiling)
+behaves as documented."""
+import ctypes
+import subprocess
+
+import pytest
+
+import mixed_precision_dense_gb300 as mp
+from mixed_precision_dense_gb300 import Status
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mp.build()
+    return mp.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = mp.header_functions()
+    assert {"mpgemm_create", "mpgemm_run", "mpgemm_destroy", "mpgemm_status_string",
+            "mpgemm_plan", "mpgemm_run_host", "mpgemm_sync_status", "mpgemm_set_option"} <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", mp.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in names:
+        assert n in exported, f"{n} declared but not exported"
+        assert hasattr(lib, n)
+
+
+def test_built_for_sm103a_only():
+    text = open(mp.LIB_PATH.replace("libmpgemm.so", "ptxas.txt")).read()
+    assert "arch=compute_103a,code=sm_103a" in text
+    assert "spill stores" in text and " 0 bytes spill stores" in text
+
+
+def test_status_strings(lib):
+    for s in Status:
+        assert mp.status_string(s)
+    assert mp.status_string(99) == "unknown status"
+
+
+def test_null_handle_is_rejected(lib):
+    assert lib.mpgemm_run(None, 1, 1, 1, 1.0, 16, 1, 16, 1, 0.0, 16, 1, None) == Status.ERR_INVALID_VALUE
+    assert lib.mpgemm_destroy(None) == Status.OK
+    assert lib.mpgemm_set_option(None, 1, 0) == Status.ERR_INVALID_VALUE
+    assert lib.mpgemm_create(None) == Status.ERR_INVALID_VALUE
+
+
+def test_create_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p(1)
+    st = lib.mpgemm_create(ctypes.byref(h))
+    assert st in (Status.ERR_UNSUPPORTED_DEVICE, Status.ERR_CUDA)
+    assert not h.value
+
+
+def _plan(**kw):
+    base = dict(M=200, N=136, K=617, alpha=1.0, A=256, lda=617, B=256, ldb=136, beta=0.0,
+                C=256, ldc=136)
+    base.update(kw)
+    return mp.plan(**base)
+
+
+@pytest.mark.parametrize("kw", [dict(M=-1), dict(N=-1), dict(K=-1), dict(lda=616), dict(ldb=135),
+                                dict(ldc=135), dict(A=0), dict(B=0), dict(C=0), dict(C=258),
+                                dict(A=257), dict(B=255), dict(M=2 ** 31), dict(lda=2 ** 31)])
+def test_invalid_arguments(kw):
+    with pytest.raises(mp.MpgemmError) as e:
+        _plan(**kw)
+    assert e.value.status == Status.ERR_INVALID_VALUE
+
+
+def test_quick_returns():
+    assert _plan(M=0, A=0, B=0, C=0)["quick"] == 1
+    assert _plan(N=0, ldb=1, ldc=1, A=0, B=0, C=0)["quick"] == 1
+    assert _plan(K=0, lda=1, A=0, B=0)["quick"] == 2     # C = beta*C, A and B never read
+    assert _plan(alpha=0.0, A=0, B=0)["quick"] == 2
+    assert _plan()["quick"] == 0
+
+
+def test_alignment_classification():
+    # lda = 617 halves = 1234 bytes: not a multiple of 16 -> A is staged
+    p = _plan()
+    assert (p["stage_a"], p["stage_b"]) == (1, 0)
+    assert p["workspace_bytes"] == 200 * 624 * 2
+    p = _plan(M=2048, N=2048, K=2048, lda=2048, ldb=2048, ldc=2048)
+    assert (p["stage_a"], p["stage_b"]) == (0, 0) and p["workspace_bytes"] == 0
+    p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257, beta=0.5)
+    assert (p["stage_a"], p["stage_b"]) == (1, 1)
+    # a base address 2 bytes past a 16-byte boundary is staged even with an aligned pitch
+    p = _plan(M=128, N=128, K=128, lda=128, ldb=128, ldc=128, A=256 + 2)
+    assert (p["stage_a"], p["stage_b"]) == (1, 0)
+    p = _plan(M=128, N=128, K=128, lda=128, ldb=128, ldc=128, force_staging=True)
+    assert (p["stage_a"], p["stage_b"]) == (1, 1)
+
+
+def test_tiling_of_the_ragged_k_tail(golden_facts):
+    # The page's K loop steps by 16 and its last step starts at 608 with 9 valid
+    # values; this library steps by 64, and the same K = 617 ends with 41 valid.
+    g = golden_facts
+    K, step = int(g["tail_k"]), int(g["tail_step"])
+    assert (K // step) * step == int(g["tail_last_start"])
+    assert K - int(g["tail_last_start"]) == int(g["tail_valid"])
+    assert step - int(g["tail_valid"]) == int(g["tail_invalid"])
+    p = _plan()
+    assert p["tile_k"] == 64 and p["k_blocks"] == 10 and p["last_k_valid"] == 41
+    assert (p["k_blocks"] - 1) * p["tile_k"] + p["last_k_valid"] == K
+
+
+def test_tile_selection_and_grid():
+    p = _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192)
+    assert p["tile_n"] == 256 and p["tiles"] == 64 * 32 and p["grid"] == 152
+    assert p["smem_bytes"] <= 232448
+    p = _plan(M=2048, N=2048, K=2048, lda=2048, ldb=2048, ldc=2048)
+    assert p["tile_n"] == 128 and p["tiles"] == 16 * 16 and p["grid"] == 152
+    p = _plan()
+    assert p["tiles"] == 2 * 2 and p["grid"] == 4
+    p = _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192, tile_n=128, max_ctas=10)
+    assert p["tile_n"] == 128 and p["grid"] == 10
+    with pytest.raises(mp.MpgemmError):
+        _plan(tile_n=192)

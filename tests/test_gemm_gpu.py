@@ -1,0 +1,233 @@
+"""Parity of the CUDA library (called through its C ABI) with the CPU oracle.
+
+Every case draws seeded operands (workloads.py), runs mpgemm_run on the GPU
+with a NaN-poisoned C when beta == 0 (the poison-before-launch convention of
+the "02_mixed_precision_gemm" README, "Verification"), and compares with the
+oracle element by element within |err| <= 1e-3 * sum_k|A_ik B_kj| + 1e-5.
+Exact small-integer inputs ("Day 72: Tensor cores with WMMA", "Why this
+program calls cuBLAS twice") must match bit for bit.
+"""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from parity import check_full, check_sampled, run_gpu, c_result
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mp():
+    import mixed_precision_dense_gb300 as m
+    m.build()
+    m.load()
+    return m
+
+
+@pytest.fixture()
+def handle(mp):
+    h = mp.Handle()
+    yield h
+    h.close()
+
+
+# --------------------------------------------------------------------------- configs
+
+@pytest.mark.parametrize("index", [0, 1, 2])
+def test_workload_every_element(handle, index):
+    check_full(handle, workloads.workload_operands(index))
+
+
+@pytest.mark.parametrize("index", [3, 4])
+def test_workload_sampled_and_edges(handle, index):
+    ops = workloads.workload_operands(index)
+    I, J = workloads.workload_sample(index)
+    check_sampled(handle, ops, I, J)
+
+
+# --------------------------------------------------------------------------- the capstone gate shapes
+
+GATE = [  # "Day 80, Capstone 4: a tensor-core GEMM", "Independent gate" (B row-major here)
+    ("unit", 16, 16, 16, "int"), ("onefrag", 16, 8, 16, "int"),
+    ("small", 128, 128, 128, "uniform"), ("odd", 611, 613, 617, "uniform"),
+    ("skinny", 4096, 16, 4096, "uniform"), ("square", 1024, 1024, 1024, "normal"),
+    ("adversarial", 256, 256, 256, "edge"),
+]
+
+
+@pytest.mark.parametrize("name,M,N,K,dist", GATE, ids=[g[0] for g in GATE])
+def test_gate_cases(handle, name, M, N, K, dist):
+    if dist == "int":
+        ops = workloads.make_operands(M, N, K, dist="int3", dist_b="int2", seed=31)
+        check_full(handle, ops, exact=True)
+    else:
+        ops = workloads.make_operands(M, N, K, dist=dist, seed=32)
+        check_full(handle, ops)
+
+
+def test_gate_perf_shape_sampled(handle):
+    ops = workloads.make_operands(4096, 4096, 4096, dist="uniform", seed=33)
+    I, J = workloads.sample_indices(4096, 4096, 20000, seed=34)
+    check_sampled(handle, ops, I, J)
+
+
+# --------------------------------------------------------------------------- ragged sizes
+
+EDGE_SIZES = [1, 15, 16, 17, 63, 64, 65, 127, 128, 129, 255, 256, 257, 617]
+
+
+@pytest.mark.parametrize("size", EDGE_SIZES)
+def test_ragged_M(handle, size):
+    check_full(handle, workloads.make_operands(size, 129, 65, seed=40 + size))
+
+
+@pytest.mark.parametrize("size", EDGE_SIZES)
+def test_ragged_N(handle, size):
+    check_full(handle, workloads.make_operands(131, size, 65, seed=41 + size))
+
+
+@pytest.mark.parametrize("size", EDGE_SIZES)
+def test_ragged_K(handle, size):
+    check_full(handle, workloads.make_operands(131, 129, size, seed=42 + size))
+
+
+def test_random_ragged_triples(handle):
+    rng = random.Random(2024)
+    for _ in range(40):
+        M, N, K = (rng.choice(EDGE_SIZES) for _ in range(3))
+        check_full(handle, workloads.make_operands(M, N, K, seed=rng.randint(0, 10 ** 6)))
+
+
+def test_integer_inputs_bitwise_large_k(handle):
+    # partial sums are integers of magnitude <= 6 * 2048 = 12,288: exact in FP32
+    ops = workloads.make_operands(300, 520, 2048, dist="int3", dist_b="int2", seed=7)
+    check_full(handle, ops, exact=True)
+
+
+# --------------------------------------------------------------------------- strides and alignment
+
+@pytest.mark.parametrize("delta", range(0, 9))
+def test_leading_dimension_sweep(handle, delta):
+    M, N, K = 150, 200, 300
+    ops = workloads.make_operands(M, N, K, lda=K + delta, ldb=N + delta, ldc=N + delta,
+                                  beta=0.5, c_dist="normal", seed=50 + delta)
+    check_full(handle, ops)
+
+
+@pytest.mark.parametrize("which", ["a", "b", "c", "abc"])
+def test_misaligned_base_pointers(handle, which):
+    ops = workloads.make_operands(200, 136, 256, beta=1.0, c_dist="normal", seed=60)
+    kw = {}
+    if "a" in which:
+        kw["a_offset"] = 1   # 2 bytes past a 16-byte boundary
+    if "b" in which:
+        kw["b_offset"] = 3
+    if "c" in which:
+        kw["c_offset"] = 1   # 4 bytes
+    check_full(handle, ops, **kw)
+
+
+# --------------------------------------------------------------------------- alpha, beta and quick returns
+
+def test_beta_zero_never_reads_nan_c(handle):
+    ops = workloads.make_operands(333, 444, 555, alpha=2.0, beta=0.0, seed=70)
+    check_full(handle, ops)  # C is NaN-poisoned before the launch
+
+
+@pytest.mark.parametrize("alpha,beta", [(1.0, 1.0), (1.5, -0.5), (-2.0, 0.25), (0.0, 0.5),
+                                        (0.0, 0.0), (3.0, 1.0)])
+def test_alpha_beta(handle, alpha, beta):
+    ops = workloads.make_operands(257, 129, 200, alpha=alpha, beta=beta, c_dist="normal", seed=71)
+    check_full(handle, ops)
+
+
+def test_k_zero_scales_c(handle):
+    ops = workloads.make_operands(100, 60, 0, alpha=1.0, beta=0.5, c_dist="normal", seed=72)
+    check_full(handle, ops)
+
+
+def test_empty_m_and_n(handle):
+    for (M, N) in [(0, 10), (10, 0)]:
+        ops = workloads.make_operands(M, N, 32, beta=0.0, seed=73)
+        d = run_gpu(handle, ops)
+        got, buf, full = c_result(d, ops)
+        assert got.size == 0
+
+
+# --------------------------------------------------------------------------- kernel configurations
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("max_ctas", [0, 1, 3])
+def test_tile_width_and_persistence(mp, tile_n, max_ctas):
+    # few CTAs walk many tiles: both accumulator buffers and every ring phase wrap
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_N, tile_n)
+        h.set_option(mp.Option.MAX_CTAS, max_ctas)
+        check_full(h, workloads.make_operands(700, 600, 450, beta=1.0, c_dist="normal", seed=80))
+
+
+def test_forced_staging_matches(mp):
+    with mp.Handle() as h:
+        h.set_option(mp.Option.FORCE_STAGING, 1)
+        check_full(h, workloads.make_operands(300, 300, 300, seed=81))
+
+
+@pytest.mark.parametrize("group", [1, 2, 5, 64])
+def test_raster_groups(mp, group):
+    with mp.Handle() as h:
+        h.set_option(mp.Option.RASTER_GROUP, group)
+        h.set_option(mp.Option.MAX_CTAS, 7)
+        check_full(h, workloads.make_operands(1100, 900, 130, seed=82))
+
+
+def test_side_stream_and_back_to_back_shapes(handle):
+    s = torch.cuda.Stream()
+    for (M, N, K, seed) in [(64, 64, 64, 1), (900, 1000, 700, 2), (65, 17, 3000, 3), (64, 64, 64, 4)]:
+        ops = workloads.make_operands(M, N, K, seed=90 + seed)
+        d = run_gpu(handle, ops, stream=s)
+        got, _, _ = c_result(d, ops)
+        from parity import reference, assert_close
+        ref, S = reference(ops)
+        assert_close(got, ref, S)
+
+
+# --------------------------------------------------------------------------- host-buffer entry point
+
+def test_run_host_matches_oracle(handle):
+    ops = workloads.make_operands(321, 257, 617, lda=620, ldb=259, ldc=260, alpha=1.5, beta=0.5,
+                                  c_dist="normal", seed=95)
+    C = ops.C.clone()
+    s = torch.cuda.current_stream()
+    handle.run_host(ops.M, ops.N, ops.K, ops.alpha, ops.A.data_ptr(), ops.lda, ops.B.data_ptr(),
+                    ops.ldb, ops.beta, C.data_ptr(), ops.ldc, s.cuda_stream)
+    s.synchronize()
+    from parity import reference, assert_close
+    ref, S = reference(ops)
+    assert_close(C[:, :ops.N].double().numpy(), ref, S)
+    assert torch.isnan(C[:, ops.N:]).all()  # padding untouched
+
+
+# --------------------------------------------------------------------------- bounded waits
+
+def test_stalled_pipeline_reports_timeout_and_context_survives(mp):
+    # The load warp issues nothing, so the MMA warp's bounded wait expires; the
+    # kernel records the timeout and exits, and the next call works normally.
+    ops = workloads.make_operands(256, 256, 128, seed=99)
+    with mp.Handle() as h:
+        h.set_option(mp.Option.WAIT_LIMIT_US, 20000)
+        h.set_option(mp.Option.TEST_STALL, 1)
+        from parity import device_operands
+        d = device_operands(ops)
+        s = torch.cuda.current_stream()
+        h.run(ops.M, ops.N, ops.K, 1.0, d["a_ptr"], ops.lda, d["b_ptr"], ops.ldb, 0.0, d["c_ptr"],
+              ops.ldc, s.cuda_stream)
+        st, info = h.sync_status(s.cuda_stream)
+        assert st == mp.Status.ERR_DEVICE_TIMEOUT
+        assert info[0] == 1 and info[1] in (2, 3)
+        st, info = h.sync_status(s.cuda_stream)   # the report is collected once
+        assert st == mp.Status.OK
+        h.set_option(mp.Option.TEST_STALL, 0)
+        check_full(h, ops)
