@@ -190,6 +190,22 @@ def time_oracle_sample(w, ops, target_seconds: float, max_elements: int, seed: i
     return gemm_flops(1, n, w.K) / dt / 1e12, dt, n, threads
 
 
+# ----------------------------------------------------------------------------- workloads
+
+def select_workload(args):
+    """The named workload, or (--shape MxNxK) the same recipe at another size."""
+    import dataclasses
+    w = workloads.WORKLOADS[args.workload]
+    if not args.shape:
+        return w, workloads.workload_operands(args.workload)
+    M, N, K = (int(x) for x in args.shape.lower().split("x"))
+    w = dataclasses.replace(w, name=f"{w.name}_recipe_at_{M}x{N}x{K}", M=M, N=N, K=K,
+                            lda=K, ldb=N, ldc=N, full_check=False)
+    ops = workloads.make_operands(M, N, K, lda=K, ldb=N, ldc=N, alpha=w.alpha, beta=w.beta,
+                                  dist=w.dist, c_dist=w.c_dist, seed=w.seed_base)
+    return w, ops
+
+
 # ----------------------------------------------------------------------------- our arm
 
 def run_ours(args):
@@ -205,8 +221,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
     mp.build()
-    w = workloads.WORKLOADS[args.workload]
-    ops = workloads.workload_operands(args.workload)
+    w, ops = select_workload(args)
     stream = torch.cuda.current_stream(device)
     A = ops.A.to(device)
     B = ops.B.to(device)
@@ -279,7 +294,7 @@ def run_ours(args):
     achieved = gemm_flops(w.M, w.N, w.K) / (kernel_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["tflops"], 4),
-                "traffic": stored_traffic(args.workload),
+                "traffic": None if args.shape else stored_traffic(args.workload),
                 "peak_kind": f"bf16 dense burst, {peaks['source']}",
                 "frac_of_sustained": (round(achieved / peaks["tflops_sustained"], 4)
                                       if peaks["tflops_sustained"] else None),
@@ -376,8 +391,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    w = workloads.WORKLOADS[args.workload]
-    ops = workloads.workload_operands(args.workload)
+    w, ops = select_workload(args)
     import oracle
     threads = os.cpu_count() or 1
     # one bounded sample per step, sized so warm-up + steps stay within a few minutes
@@ -420,6 +434,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", type=int, default=3, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--shape", default="", help="MxNxK: the workload's recipe at another size")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
