@@ -58,7 +58,9 @@ typedef enum {
     MPGEMM_ERR_ALLOC = 3,              /* device or pinned host allocation failed */
     MPGEMM_ERR_LAUNCH = 4,             /* a kernel launch or copy could not be enqueued */
     MPGEMM_ERR_DEVICE_TIMEOUT = 5,     /* a device wait gave up (reported by a later call) */
-    MPGEMM_ERR_CUDA = 6                /* another CUDA runtime or driver error */
+    MPGEMM_ERR_CUDA = 6,               /* another CUDA runtime or driver error */
+    MPGEMM_ERR_SCRATCH_LIMIT = 7       /* mpgemm_run_noalloc: the operands need more staging
+                                          scratch than its fixed area holds; nothing enqueued */
 } mpgemm_status_t;
 
 /* Create a handle bound to the current CUDA device. Fails with
@@ -139,6 +141,38 @@ mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha,
                             float beta, const float* C, int64_t ldc,
                             int32_t num_sms, int32_t tile_n, int32_t max_ctas, int32_t force_staging,
                             mpgemm_plan_t* out);
+
+/* C = alpha*A*B + beta*C on device memory, like mpgemm_run, for callers that
+ * cannot allocate: no handle, and no device or host allocation of any kind
+ * (no cudaMalloc, cudaMallocAsync, cudaHostAlloc or allocating library call)
+ * at any call. Such callers include code that runs where the allocator must
+ * not be touched (inside another library's memory-pool budget, or while a
+ * stream is being captured into a graph by someone else), and code that
+ * cannot own a handle's lifetime. The pages have no counterpart of this
+ * entry point: it exists for those callers only.
+ *
+ * Operands that need an aligned staging copy (a base address or row pitch
+ * that is not a multiple of 16 bytes) are staged into one fixed, file-scope
+ * device array of MPGEMM_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU which
+ * loads this library holds until the process exits. If the staged copies of
+ * A and B together need more than that, the call returns
+ * MPGEMM_ERR_SCRATCH_LIMIT and enqueues nothing; aligned operands need no
+ * scratch and have no size limit beyond mpgemm_run's.
+ *
+ * The first call on each device (with that device current) looks up the
+ * array's device address and sets the kernels' shared-memory limits; make
+ * that first call before any stream capture. All calls share the one array
+ * and the work is stream-ordered only: calls whose work overlaps on the GPU
+ * (different streams, or several host threads) race on the scratch and must
+ * be serialised by the caller. A bounded device wait that gives up is
+ * recorded only in the array's status words, not returned (use mpgemm_run
+ * and mpgemm_sync_status where such reports are needed). Other arguments,
+ * return codes and asynchrony are those of mpgemm_run. */
+#define MPGEMM_NOALLOC_SCRATCH_BYTES (16ll * 1024 * 1024)
+mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K,
+                                   float alpha, const void* A, int64_t lda,
+                                   const void* B, int64_t ldb,
+                                   float beta, float* C, int64_t ldc, void* stream);
 
 /* A static description of a status code. Never NULL. */
 const char* mpgemm_status_string(mpgemm_status_t s);

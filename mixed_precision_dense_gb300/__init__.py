@@ -6,8 +6,10 @@ The computation lives in the CUDA library ``libmpgemm.so`` (C ABI in
 ctypes (``binding``). PyTorch is only used for device memory and streams.
 """
 from .binding import (Handle, MpgemmError, Option, Plan, Status, default_handle, gemm,
-                      header_functions, load, plan, status_string)
+                      header_functions, load, plan, run_noalloc, status_string,
+                      NOALLOC_SCRATCH_BYTES)
 from .build import LIB_PATH, build
 
 __all__ = ["Handle", "MpgemmError", "Option", "Plan", "Status", "default_handle", "gemm",
-           "header_functions", "load", "plan", "status_string", "LIB_PATH", "build"]
+           "header_functions", "load", "plan", "run_noalloc", "status_string",
+           "NOALLOC_SCRATCH_BYTES", "LIB_PATH", "build"]

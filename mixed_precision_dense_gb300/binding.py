@@ -23,6 +23,7 @@ class Status(enum.IntEnum):
     ERR_LAUNCH = 4
     ERR_DEVICE_TIMEOUT = 5
     ERR_CUDA = 6
+    ERR_SCRATCH_LIMIT = 7
 
 
 class Option(enum.IntEnum):
@@ -78,13 +79,14 @@ def load(path: str = LIB_PATH):
         gemm_args = [p, i64, i64, i64, f32, p, i64, p, i64, f32, p, i64, p]
         lib.mpgemm_run.argtypes = gemm_args
         lib.mpgemm_run_host.argtypes = gemm_args
+        lib.mpgemm_run_noalloc.argtypes = gemm_args[1:]
         lib.mpgemm_sync_status.argtypes = [p, p, ctypes.POINTER(i32)]
         lib.mpgemm_set_option.argtypes = [p, ctypes.c_int, i64]
         lib.mpgemm_plan.argtypes = [i64, i64, i64, f32, p, i64, p, i64, f32, p, i64,
                                     i32, i32, i32, i32, ctypes.POINTER(Plan)]
         lib.mpgemm_status_string.restype = ctypes.c_char_p
         lib.mpgemm_status_string.argtypes = [ctypes.c_int]
-        for name in ("mpgemm_create", "mpgemm_destroy", "mpgemm_run", "mpgemm_run_host",
+        for name in ("mpgemm_create", "mpgemm_destroy", "mpgemm_run", "mpgemm_run_host", "mpgemm_run_noalloc",
                      "mpgemm_sync_status", "mpgemm_set_option", "mpgemm_plan"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -111,6 +113,18 @@ def plan(M, N, K, alpha=1.0, A=0, lda=None, B=0, ldb=None, beta=0.0, C=0, ldc=No
                             num_sms, tile_n, max_ctas, int(bool(force_staging)), ctypes.byref(out))
     _check(st, "mpgemm_plan")
     return out.as_dict()
+
+
+def run_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> Status:
+    """mpgemm_run_noalloc on device addresses (ints): the GEMM without a handle
+    and without any allocation, for callers that cannot allocate; staging
+    copies go to the library's fixed 16 MiB device scratch area. Returns the
+    status instead of raising (ERR_SCRATCH_LIMIT when that area is too small)."""
+    return Status(load().mpgemm_run_noalloc(M, N, K, alpha, A or None, lda, B or None, ldb, beta,
+                                            C or None, ldc, stream or None))
+
+
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class Handle:

@@ -26,6 +26,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <mutex>
 
 #include "../../include/mpgemm.h"
@@ -280,6 +281,8 @@ const char* mpgemm_status_string(mpgemm_status_t s) {
         case MPGEMM_ERR_LAUNCH: return "kernel launch or copy failed";
         case MPGEMM_ERR_DEVICE_TIMEOUT: return "a bounded device wait gave up";
         case MPGEMM_ERR_CUDA: return "CUDA error";
+        case MPGEMM_ERR_SCRATCH_LIMIT:
+            return "operands need more staging scratch than mpgemm_run_noalloc's fixed area holds";
     }
     return "unknown status";
 }
@@ -507,3 +510,138 @@ mpgemm_status_t mpgemm_sync_status(mpgemm_handle_t h, void* stream, int32_t info
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ no-allocation entry point
+//
+// mpgemm_run_noalloc serves callers that cannot allocate (see the header):
+// the staging copies that mpgemm_run puts in a handle's workspace go into a
+// fixed file-scope device array instead, and the bounded-wait status words
+// live at its start. In host code `g_noalloc_scratch` is only a host-side
+// stand-in for the symbol: the kernels get the device address that
+// cudaGetSymbolAddress returns for the current device, looked up once per
+// device on that device's first call.
+
+namespace {
+
+constexpr int64_t kNoAllocScratchBytes = MPGEMM_NOALLOC_SCRATCH_BYTES;
+constexpr int64_t kNoAllocStatusBytes = 256;  // 4 status words, padded to keep staging aligned
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocStatusBytes + kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+    std::once_flag once;
+    mpgemm_status_t status = MPGEMM_ERR_CUDA;
+    unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+    int num_sms = 0;
+};
+
+NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];
+
+// Runs once per device, with that device current.
+void noalloc_setup(NoAllocDevice& d, int dev) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        d.status = MPGEMM_ERR_CUDA;
+        return;
+    }
+    if (major != 10 || minor != 3) {
+        d.status = MPGEMM_ERR_UNSUPPORTED_DEVICE;
+        return;
+    }
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr ||
+        !encode_fn() || set_smem_attr<Cfg256>() != cudaSuccess ||
+        set_smem_attr<Cfg128>() != cudaSuccess) {
+        cudaGetLastError();
+        d.status = MPGEMM_ERR_CUDA;
+        return;
+    }
+    d.scratch = static_cast<unsigned char*>(ptr);
+    d.num_sms = sms;
+    d.status = MPGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                                              const void* A, int64_t lda, const void* B,
+                                              int64_t ldb, float beta, float* C, int64_t ldc,
+                                              void* stream_ptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MPGEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return MPGEMM_ERR_CUDA;
+    NoAllocDevice& d = g_noalloc_devices[dev];
+    std::call_once(d.once, noalloc_setup, std::ref(d), dev);
+    if (d.status != MPGEMM_OK) return d.status;
+
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    const Options opt;  // defaults: automatic tile width, one CTA per SM, 4 s wait limit
+    mpgemm_plan_t plan;
+    mpgemm_status_t st =
+        make_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d.num_sms, opt, &plan);
+    if (st != MPGEMM_OK) return st;
+    if (plan.quick == 1) return MPGEMM_OK;
+    if (plan.quick == 2) {
+        scale_c<<<grid_for(M * N, d.num_sms), 256, 0, stream>>>(C, ldc, M, N, beta);
+        return cudaGetLastError() == cudaSuccess ? MPGEMM_OK : MPGEMM_ERR_LAUNCH;
+    }
+    if (plan.workspace_bytes > kNoAllocScratchBytes) return MPGEMM_ERR_SCRATCH_LIMIT;
+
+    // The status words must start at zero; the array keeps the last call's contents.
+    int32_t* status = reinterpret_cast<int32_t*>(d.scratch);
+    if (cudaMemsetAsync(status, 0, 4 * sizeof(int32_t), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MPGEMM_ERR_LAUNCH;
+    }
+    const void* a_use = A;
+    const void* b_use = B;
+    int64_t lda_use = lda, ldb_use = ldb;
+    unsigned char* ws = d.scratch + kNoAllocStatusBytes;
+    if (plan.stage_a) {
+        lda_use = round_up(K, 8);
+        stage_rows_u16<<<grid_for(M * ceil_div(K, 8), d.num_sms), 256, 0, stream>>>(
+            static_cast<const uint16_t*>(A), lda, reinterpret_cast<uint16_t*>(ws), lda_use, M, K);
+        a_use = ws;
+        ws += round_up(M * lda_use * 2, 256);
+    }
+    if (plan.stage_b) {
+        ldb_use = round_up(N, 8);
+        stage_rows_u16<<<grid_for(K * ceil_div(N, 8), d.num_sms), 256, 0, stream>>>(
+            static_cast<const uint16_t*>(B), ldb, reinterpret_cast<uint16_t*>(ws), ldb_use, K, N);
+        b_use = ws;
+    }
+    if (cudaGetLastError() != cudaSuccess) return MPGEMM_ERR_LAUNCH;
+
+    CUtensorMap ta, tb;
+    if (!encode_f16(&ta, a_use, M, K, lda_use, 64, 128) ||
+        !encode_f16(&tb, b_use, K, N, ldb_use, 64, 64))
+        return MPGEMM_ERR_CUDA;
+    GemmParams gp;
+    gp.M = static_cast<int32_t>(M);
+    gp.N = static_cast<int32_t>(N);
+    gp.K = static_cast<int32_t>(K);
+    gp.m_tiles = plan.m_tiles;
+    gp.n_tiles = plan.n_tiles;
+    gp.k_blocks = plan.k_blocks;
+    gp.tiles = static_cast<int32_t>(plan.tiles);
+    gp.raster_group = plan.raster_group;
+    gp.alpha = alpha;
+    gp.beta = beta;
+    gp.C = C;
+    gp.ldc = ldc;
+    gp.status = status;
+    gp.wait_limit_ns = opt.wait_limit_ns;
+    gp.test_stall = 0;
+    if (plan.tile_n == 256)
+        launch_tc<Cfg256>(plan, ta, tb, gp, stream);
+    else
+        launch_tc<Cfg128>(plan, ta, tb, gp, stream);
+    return cudaGetLastError() == cudaSuccess ? MPGEMM_OK : MPGEMM_ERR_LAUNCH;
+}
