@@ -206,6 +206,91 @@ def select_workload(args):
     return w, ops
 
 
+# ----------------------------------------------------------------------------- cuBLAS context
+
+def _cublas_lib():
+    import ctypes
+    import glob
+    cands = []
+    try:
+        import nvidia.cublas  # noqa: F401  (wheel-installed cuBLAS next to torch)
+        import nvidia.cublas as nc
+        cands += glob.glob(os.path.join(os.path.dirname(nc.__file__), "lib", "libcublas.so*"))
+    except Exception:
+        pass
+    cands += sorted(glob.glob("/usr/local/cuda/lib64/libcublas.so*"), reverse=True)
+    for c in cands:
+        try:
+            return ctypes.CDLL(c)
+        except OSError:
+            continue
+    return None
+
+
+def time_cublas_context(w, A, B, C, stream, steps, flush=None):
+    """cublasGemmEx(FP16 A and B, FP32 C, CUBLAS_COMPUTE_32F, default algorithm)
+    on the same buffers, timed like our step. Row-major C = A*B is issued as
+    the column-major product C^T = B^T * A^T, so no copies are needed. This is
+    context measured by the harness only; the library does not use cuBLAS."""
+    import ctypes
+    import torch
+    lib = _cublas_lib()
+    if lib is None:
+        return None
+    h = ctypes.c_void_p()
+    if lib.cublasCreate_v2(ctypes.byref(h)) != 0:
+        return None
+    try:
+        lib.cublasSetStream_v2(h, ctypes.c_void_p(stream.cuda_stream))
+        alpha = ctypes.c_float(w.alpha)
+        beta = ctypes.c_float(w.beta)
+        CUDA_R_16F, CUDA_R_32F, COMPUTE_32F, GEMM_DEFAULT = 2, 0, 68, -1
+
+        def call():
+            return lib.cublasGemmEx(h, 0, 0, w.N, w.M, w.K, ctypes.byref(alpha),
+                                    ctypes.c_void_p(B.data_ptr()), CUDA_R_16F, w.ldb,
+                                    ctypes.c_void_p(A.data_ptr()), CUDA_R_16F, w.lda,
+                                    ctypes.byref(beta), ctypes.c_void_p(C.data_ptr()), CUDA_R_32F,
+                                    w.ldc, COMPUTE_32F, GEMM_DEFAULT)
+
+        for _ in range(3):
+            if call() != 0:
+                return None
+        ms = timed_loop(call, stream, steps, flush)
+        return {"value": round(gemm_flops(w.M, w.N, w.K) / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(ms, 5),
+                "call": "cublasGemmEx(CUDA_R_16F, CUDA_R_16F, CUDA_R_32F, CUBLAS_COMPUTE_32F, "
+                        "CUBLAS_GEMM_DEFAULT), harness only"}
+    finally:
+        lib.cublasDestroy_v2(h)
+
+
+def timed_loop(fn, stream, steps, flush=None):
+    """Mean milliseconds per call of fn() over `steps` calls, CUDA events on
+    `stream`. With `flush` (a tensor larger than L2), L2 is overwritten before
+    every call and only the calls are timed."""
+    import torch
+    if flush is None:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            fn()
+            ends[i].record(stream)
+    ends[-1].synchronize()
+    return sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
+
+
 # ----------------------------------------------------------------------------- our arm
 
 def run_ours(args):
@@ -261,24 +346,21 @@ def run_ours(args):
         step()
     torch.cuda.synchronize(device)
 
+    small = gemm_bytes(w.M, w.N, w.K, w.beta) < L2_BYTES
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=device) if small else None
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
     barrier()
     torch.cuda.synchronize(device)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
+    local_ms = timed_loop(step, stream, args.steps, flush)
     torch.cuda.synchronize(device)
     barrier()
     clocks = sampler.stop()
     st, info = handle.sync_status(stream.cuda_stream)
     if st != mp.Status.OK:
         raise RuntimeError(f"device reported {st.name} {info}")
-    local_s = ev0.elapsed_time(ev1) / 1e3
+    local_s = local_ms * args.steps / 1e3
     flops_local = gemm_flops(w.M, w.N, w.K) * args.steps
     max_s, flops_all = aggregate(local_s, flops_local, device=device)
     value = flops_all / max_s / 1e12
@@ -289,7 +371,7 @@ def run_ours(args):
     # timed separately and subtracted)
     kernel_ms = ms_per_step
     if launches_per_step > 1:
-        kernel_ms = time_tc_kernel_only(handle, w, A, B, C, stream, args.steps)
+        kernel_ms = time_tc_kernel_only(handle, w, A, B, C, stream, args.steps, flush)
     peaks = measured_peaks()
     achieved = gemm_flops(w.M, w.N, w.K) / (kernel_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["tflops"],
@@ -299,6 +381,12 @@ def run_ours(args):
                 "frac_of_sustained": (round(achieved / peaks["tflops_sustained"], 4)
                                       if peaks["tflops_sustained"] else None),
                 "kernel": "gemm_tc_kernel", "algorithmic_bytes": gemm_bytes(w.M, w.N, w.K, w.beta)}
+
+    cublas = None
+    if not args.no_cublas:
+        cublas = time_cublas_context(w, A, B, C, stream, min(args.steps, 200), flush)
+        if cublas:
+            cublas["ours_over_cublas"] = round(value / world / cublas["value"], 4)
 
     # end to end through the host-buffer entry point
     e2e = None
@@ -322,11 +410,13 @@ def run_ours(args):
                        "ldb": w.ldb, "ldc": w.ldc, "alpha": w.alpha, "beta": w.beta,
                        "inputs": w.dist, "tile": f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}",
                        "grid": plan["grid"], "parallelism": f"replicas x{world}",
-                       "l2": f"inputs larger than L2 ({gemm_bytes(w.M, w.N, w.K, w.beta) / 2**20:.0f} MiB "
-                             f"> {L2_BYTES // 2**20} MiB): no flush"
-                             if gemm_bytes(w.M, w.N, w.K, w.beta) > L2_BYTES else "L2 flushed between steps"},
+                       "l2": (f"L2 flushed between steps (a {2 * L2_BYTES // 2**20} MiB write before each "
+                              "step, outside the timed calls)" if small else
+                              f"inputs larger than L2 ({gemm_bytes(w.M, w.N, w.K, w.beta) / 2**20:.0f} MiB "
+                              f"> {L2_BYTES // 2**20} MiB): no flush")},
             "pct_of_peak": round(100 * value / world / peaks["tflops"], 2),
             "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
+            "context_cublas": cublas,
             "gpu_launches": launches_per_step * args.steps, "check_max_err_over_tol": check,
         }
         print(json.dumps(line), flush=True)
@@ -335,7 +425,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def time_tc_kernel_only(handle, w, A, B, C, stream, steps):
+def time_tc_kernel_only(handle, w, A, B, C, stream, steps, flush=None):
     """Event-time the tensor-core launch on pre-staged aligned operands."""
     import torch
     M, N, K = w.M, w.N, w.K
@@ -347,15 +437,9 @@ def time_tc_kernel_only(handle, w, A, B, C, stream, steps):
     for _ in range(3):
         handle.run(M, N, K, w.alpha, A2.data_ptr(), lda, B2.data_ptr(), ldb, w.beta, C.data_ptr(),
                    w.ldc, stream.cuda_stream)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        handle.run(M, N, K, w.alpha, A2.data_ptr(), lda, B2.data_ptr(), ldb, w.beta, C.data_ptr(),
-                   w.ldc, stream.cuda_stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / steps
+    return timed_loop(lambda: handle.run(M, N, K, w.alpha, A2.data_ptr(), lda, B2.data_ptr(), ldb,
+                                         w.beta, C.data_ptr(), w.ldc, stream.cuda_stream),
+                      stream, steps, flush)
 
 
 def run_e2e(handle, w, ops, stream, device, args):
@@ -431,8 +515,8 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", type=int, default=3, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--shape", default="", help="MxNxK: the workload's recipe at another size")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -441,6 +525,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-check", action="store_true")
+    ap.add_argument("--no-cublas", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least three warm-up steps, whatever was asked
     if args.impl == "reference":

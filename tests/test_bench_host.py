@@ -1,0 +1,117 @@
+"""Host logic of bench.py (no GPU): the FLOP and byte counters against the
+numbers the pages print, the reference arm's JSON line, and the multi-rank
+aggregation (max time, summed FLOPs) on two gloo ranks."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as tmp
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_worked_tile_counts(golden_facts):
+    # "Day 80", Worked path: a 128x16 A tile plus a 16x128 B tile, FP16
+    g = golden_facts
+    m, n, k = int(g["worked_tile_m"]), int(g["worked_tile_n"]), int(g["worked_tile_k"])
+    values = m * k + k * n
+    assert values == int(g["worked_tile_values"])
+    assert 2 * values == int(g["worked_tile_bytes"])
+    assert bench.gemm_flops(m, n, k) == int(g["worked_tile_flops"])
+    assert bench.gemm_flops(m, n, k) / (2 * values) == int(g["worked_flop_per_byte"])
+
+
+def test_arithmetic_intensity_at_2048(golden_facts):
+    # "02_mixed_precision_gemm" README, Experimental Setup: A+B = 16.8 MB,
+    # C = 16 MB (MiB), intensity ~682 flop/byte. The 682 counts C at FP16
+    # size (2*2048^3 / (3 * 2048^2 * 2 bytes)); this bench counts C at its
+    # FP32 size, which gives 512.
+    g = golden_facts
+    n = 2048
+    ab = bench.gemm_bytes(n, n, n, 0.0) - 4 * n * n
+    assert round(ab / 1e6, 1) == float(g["ai_2048_ab_megabytes"])
+    assert 4 * n * n / 2 ** 20 == float(g["ai_2048_c_megabytes"])
+    pages_ai = bench.gemm_flops(n, n, n) / bench.gemm_bytes(n, n, n, 0.0, c_bytes=2)
+    assert int(pages_ai) == int(g["ai_2048_flop_per_byte"])
+    assert bench.gemm_flops(n, n, n) / bench.gemm_bytes(n, n, n, 0.0) == 512
+
+
+def test_tflops_formula_reproduces_the_pages_rows(golden_facts):
+    g = golden_facts
+    n = 2048
+    for ms_key, gf_key in [("t4_cublas_2048_ms", "t4_cublas_2048_gflops"),
+                           ("t4_staged_2048_ms", "t4_staged_2048_gflops"),
+                           ("rtx3050_cp_async_2048_ms", "rtx3050_cp_async_2048_gflops")]:
+        gflops = bench.gemm_flops(n, n, n) / (float(g[ms_key]) / 1e3) / 1e9
+        # the printed times are rounded to 3-4 significant digits
+        assert gflops == pytest.approx(float(g[gf_key]), rel=4e-3)
+
+
+def test_smem_and_peak_arithmetic(golden_facts):
+    g = golden_facts
+    assert 2 * (128 * 40 + 32 * 72) * 2 == int(g["cp_async_smem_bytes"])
+    assert round(512 * 16 * 2 * 1.5e9 / 1e12, 1) == float(g["rtx3050_hmma_peak_tflops"])
+
+
+def test_beta_doubles_c_traffic():
+    assert bench.gemm_bytes(10, 20, 30, 0.0) == 10 * 30 * 2 + 30 * 20 * 2 + 10 * 20 * 4
+    assert bench.gemm_bytes(10, 20, 30, 0.5) == 10 * 30 * 2 + 30 * 20 * 2 + 2 * 10 * 20 * 4
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        seconds = [0.5, 0.8][rank]
+        flops = [1e12, 2e12][rank]
+        t, f = bench.aggregate(seconds, flops)
+        out[rank] = (t, f)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_aggregate_over_two_gloo_ranks():
+    port = _free_port()
+    mgr = tmp.Manager()
+    out = mgr.dict()
+    tmp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
+    for r in range(2):
+        assert out[r] == (0.8, 3e12)   # slowest rank's time, all ranks' work
+
+
+def test_aggregate_single_process_is_identity():
+    assert bench.aggregate(1.5, 7.0) == (1.5, 7.0)
+
+
+def test_reference_arm_prints_one_json_line():
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "0", "--steps", "3", "--warmup", "3"],
+                         capture_output=True, text=True, env=env, timeout=300, check=True).stdout
+    lines = [l for l in out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "ragged_tiny_200x136x617"
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, WORLD_SIZE="2", RANK="1")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "0", "--steps", "3", "--warmup", "3"],
+                         capture_output=True, text=True, env=env, timeout=300, check=True).stdout
+    assert out.strip() == ""
