@@ -108,8 +108,10 @@ typedef enum {
     MPGEMM_OPT_FORCE_STAGING = 3, /* 1 = stage A and B through aligned copies even when aligned */
     MPGEMM_OPT_WAIT_LIMIT_US = 4, /* limit of every bounded device wait, microseconds (default 4e6) */
     MPGEMM_OPT_RASTER_GROUP = 5,  /* M-tiles per rasterisation group, 0 = automatic (default) */
-    MPGEMM_OPT_TEST_STALL = 6     /* test only: 1 = the load warp issues no loads, so the
+    MPGEMM_OPT_TEST_STALL = 6,    /* test only: 1 = the load warp issues no loads, so the
                                      kernel's bounded waits expire and a timeout is reported */
+    MPGEMM_OPT_TILE_M = 7         /* 0 = automatic (default); 128 = one CTA per tile;
+                                     256 = a cluster of two CTAs per 256 x 256 tile */
 } mpgemm_option_t;
 
 /* Set an option. Unknown options or out-of-range values return
@@ -118,12 +120,14 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
 
 /* What mpgemm_run would do for these arguments, computed on the host only
  * (no device work; usable without a GPU). `num_sms` stands in for the
- * device's SM count; tile_n and max_ctas mirror the options above. */
+ * device's SM count; tile_m, tile_n, max_ctas and force_staging mirror the
+ * options above. The grid of the CTA-pair kernel is further capped at run
+ * time by the number of two-CTA clusters the device can hold at once. */
 typedef struct {
     int32_t quick;          /* 0 = tensor-core path, 1 = nothing to do, 2 = C = beta*C only */
     int32_t stage_a;        /* 1 if A is copied to an aligned buffer first */
     int32_t stage_b;        /* 1 if B is copied to an aligned buffer first */
-    int32_t tile_m;         /* rows per output tile (128) */
+    int32_t tile_m;         /* rows per output tile: 128 (one CTA) or 256 (a CTA pair) */
     int32_t tile_n;         /* columns per output tile (128 or 256) */
     int32_t tile_k;         /* K per pipeline stage (64) */
     int32_t stages;         /* shared-memory pipeline depth */
@@ -139,8 +143,8 @@ typedef struct {
 mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha,
                             const void* A, int64_t lda, const void* B, int64_t ldb,
                             float beta, const float* C, int64_t ldc,
-                            int32_t num_sms, int32_t tile_n, int32_t max_ctas, int32_t force_staging,
-                            mpgemm_plan_t* out);
+                            int32_t num_sms, int32_t tile_m, int32_t tile_n, int32_t max_ctas,
+                            int32_t force_staging, mpgemm_plan_t* out);
 
 /* C = alpha*A*B + beta*C on device memory, like mpgemm_run, for callers that
  * cannot allocate: no handle, and no device or host allocation of any kind

@@ -33,6 +33,7 @@ class Option(enum.IntEnum):
     WAIT_LIMIT_US = 4
     RASTER_GROUP = 5
     TEST_STALL = 6
+    TILE_M = 7
 
 
 class MpgemmError(RuntimeError):
@@ -83,7 +84,7 @@ def load(path: str = LIB_PATH):
         lib.mpgemm_sync_status.argtypes = [p, p, ctypes.POINTER(i32)]
         lib.mpgemm_set_option.argtypes = [p, ctypes.c_int, i64]
         lib.mpgemm_plan.argtypes = [i64, i64, i64, f32, p, i64, p, i64, f32, p, i64,
-                                    i32, i32, i32, i32, ctypes.POINTER(Plan)]
+                                    i32, i32, i32, i32, i32, ctypes.POINTER(Plan)]
         lib.mpgemm_status_string.restype = ctypes.c_char_p
         lib.mpgemm_status_string.argtypes = [ctypes.c_int]
         for name in ("mpgemm_create", "mpgemm_destroy", "mpgemm_run", "mpgemm_run_host", "mpgemm_run_noalloc",
@@ -103,14 +104,15 @@ def _check(status, where):
 
 
 def plan(M, N, K, alpha=1.0, A=0, lda=None, B=0, ldb=None, beta=0.0, C=0, ldc=None, *,
-         num_sms=152, tile_n=0, max_ctas=0, force_staging=False) -> dict:
+         num_sms=152, tile_m=0, tile_n=0, max_ctas=0, force_staging=False) -> dict:
     """Host-only description of what mpgemm_run would do (addresses as ints)."""
     lda = max(K, 1) if lda is None else lda
     ldb = max(N, 1) if ldb is None else ldb
     ldc = max(N, 1) if ldc is None else ldc
     out = Plan()
     st = load().mpgemm_plan(M, N, K, alpha, A or None, lda, B or None, ldb, beta, C or None, ldc,
-                            num_sms, tile_n, max_ctas, int(bool(force_staging)), ctypes.byref(out))
+                            num_sms, tile_m, tile_n, max_ctas, int(bool(force_staging)),
+                            ctypes.byref(out))
     _check(st, "mpgemm_plan")
     return out.as_dict()
 

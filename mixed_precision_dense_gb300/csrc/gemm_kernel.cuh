@@ -1,34 +1,45 @@
 // The tensor-core pass of C = alpha*A*B + beta*C for sm_103a.
 //
-// One persistent CTA per SM walks output tiles of 128 x BN. Its six warps
-// have fixed roles:
+// Persistent CTAs walk the output in tiles. Each CTA has six warps with fixed
+// roles:
 //   warp 0      load warp: one lane issues TMA loads of A (128 x 64, K-major)
-//               and B (64 x BN, N-major) into a ring of shared-memory stages;
-//               rows, columns and K past the matrix edge arrive as zeros
-//               (TMA out-of-bounds fill), which replaces the padding and
-//               guarded tail loads of "Day 80, Capstone 4: a tensor-core
-//               GEMM" ("Faded practice", practice 3; "Common failures").
+//               and B (64 x width, N-major) into a ring of shared-memory
+//               stages; rows, columns and K past the matrix edge arrive as
+//               zeros (TMA out-of-bounds fill), which replaces the padding and
+//               guarded tail loads of "Day 80, Capstone 4: a tensor-core GEMM"
+//               ("Faded practice", practice 3; "Common failures").
 //   warp 1      MMA warp: allocates tensor memory; one lane issues
-//               tcgen05.mma (M = 128, N <= BN, K = 16; FP16 x FP16 -> FP32)
-//               into one of two accumulator buffers and frees each stage
-//               with tcgen05.commit.
+//               tcgen05.mma (K = 16 per instruction, FP16 x FP16 -> FP32) into
+//               one of two accumulator buffers and frees each stage with
+//               tcgen05.commit.
 //   warps 2-5   epilogue: each warp reads its 32 accumulator rows with
 //               tcgen05.ld, applies alpha (and beta * C when beta != 0) in
-//               FP32, and writes C with row and column masks, so any M, N
-//               and any ldc are handled. While it works on tile i, the MMA
-//               warp already accumulates tile i+1 into the other buffer.
+//               FP32, and writes C with row and column masks, so any M, N and
+//               any ldc are handled. While it works on tile i, the MMA warp
+//               already accumulates tile i+1 into the other buffer.
 //
-// The staged-tile reuse, asynchronous copies and block rasterisation that
-// the pages build up with WMMA ("Day 80", "Worked path"; "02_mixed_precision
-// _gemm" README, "Summary": cp.async double buffering and cross-block L2
-// reuse) map onto this design as: the 128 x BN tile held in shared memory
-// and consumed by one MMA thread, the multistage TMA + mbarrier ring, and
-// grouped rasterisation of the persistent tile walk.
+// Two shapes of the same pipeline:
+//   single  one CTA per tile of 128 x BN (BN = 128 or 256), tcgen05.mma with
+//           cta_group::1, M = 128, N = 64 * ceil(valid columns / 64);
+//   pair    a cluster of two CTAs per tile of 256 x 256: each CTA loads its
+//           own 128 rows of A and its own 128 columns of B, the even CTA
+//           issues tcgen05.mma with cta_group::2 (M = 256, N = 256) over both
+//           CTAs' shared memory, and each CTA's tensor memory receives its
+//           own 128 rows of the accumulator. Per SM this moves a third less
+//           operand data per FLOP than the single shape, which leaves room
+//           for a deeper ring.
 //
-// Every wait is bounded: if a barrier does not complete within the limit,
-// the thread records the fact in the handle's status word, raises a CTA-wide
-// abort flag, lets its own in-flight copies and MMAs drain (again bounded),
-// and the CTA releases its tensor memory and exits.
+// The staged-tile reuse, asynchronous copies and block rasterisation that the
+// pages build up with WMMA ("Day 80", "Worked path"; "02_mixed_precision_gemm"
+// README, "Summary": cp.async double buffering and cross-block L2 reuse) map
+// onto this design as: the tile held in shared memory and consumed by one
+// MMA thread, the multistage TMA + mbarrier ring, and grouped rasterisation of
+// the persistent tile walk.
+//
+// Every wait is bounded: if a barrier does not complete within the limit, the
+// thread records the fact in the status words, raises a CTA-wide abort flag,
+// lets its own in-flight copies and MMAs drain (again bounded), and the CTA
+// releases its tensor memory and exits.
 #pragma once
 
 #include <cstdint>
@@ -40,33 +51,37 @@ namespace mpgemm {
 
 struct GemmParams {
     int32_t M, N, K;
-    int32_t m_tiles, n_tiles, k_blocks;
+    int32_t m_tiles, n_tiles, k_blocks;   // tiles counted in units of the kernel's tile
     int32_t tiles;
     int32_t raster_group;
     float alpha, beta;
     float* C;
     int64_t ldc;
-    int32_t* status;        // {code, role, block, detail}, mapped host memory
+    int32_t* status;        // {code, role, block, detail}
     uint64_t wait_limit_ns;
     int32_t test_stall;     // 1: the load warp issues nothing (timeout test)
 };
 
-enum : int32_t { kRoleLoad = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4 };
+enum : int32_t { kRoleLoad = 1, kRoleMma = 2, kRoleEpilogue = 3 };
 enum : int32_t { kStatusTimeout = 1 };
 
-template <int BN_, int STAGES_>
+template <int BN_, int STAGES_, bool PAIR_>
 struct TileConfig {
-    static constexpr int BM = 128;
-    static constexpr int BN = BN_;
-    static constexpr int BK = 64;                     // 64 halves = one 128-byte swizzle row
+    static constexpr bool PAIR = PAIR_;
+    static constexpr int CTAS = PAIR ? 2 : 1;
+    static constexpr int BM = 128;                     // accumulator rows per CTA
+    static constexpr int TILE_M = BM * CTAS;           // rows per output tile
+    static constexpr int BN = BN_;                     // columns per output tile
+    static constexpr int B_COLS = BN / CTAS;           // columns of B each CTA loads
+    static constexpr int BK = 64;                      // 64 halves = one 128-byte swizzle row
     static constexpr int STAGES = STAGES_;
-    static constexpr int A_BYTES = BM * BK * 2;       // 16 KB
-    static constexpr int B_ATOM_BYTES = BK * 64 * 2;  // one 64-column box of B: 8 KB
-    static constexpr int B_BYTES = BK * BN * 2;
+    static constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+    static constexpr int B_ATOM_BYTES = BK * 64 * 2;   // one 64-column box of B: 8 KB
+    static constexpr int B_BYTES = BK * B_COLS * 2;
     static constexpr int EPI_WARPS = 4;
-    static constexpr int EPI_PITCH = 33;              // floats per row of a transpose buffer
+    static constexpr int EPI_PITCH = 33;               // floats per row of a transpose buffer
     static constexpr int EPI_BYTES = EPI_WARPS * 32 * EPI_PITCH * 4;
-    static constexpr int TMEM_COLS = 2 * BN;          // two accumulator buffers
+    static constexpr int TMEM_COLS = 2 * BN;           // two accumulator buffers
     static constexpr int NUM_BARRIERS = 2 * STAGES + 4;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = STAGES * A_BYTES;
@@ -76,6 +91,7 @@ struct TileConfig {
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
     static constexpr int THREADS = 192;
     static_assert(BN == 128 || BN == 256, "tile width");
+    static_assert(!PAIR || BN == 256, "pair tiles are 256 x 256");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "tensor memory allocation");
@@ -111,6 +127,13 @@ struct Waiter {
         }
     }
 
+    // Bounded wait used while draining after an abort (ignores the flag).
+    __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) const {
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(bar, parity) && ptx::globaltimer_ns() - t0 < p->wait_limit_ns) {
+        }
+    }
+
     __device__ __forceinline__ void fail(int32_t role, int32_t detail) const {
         *abort_flag = 1;
         volatile int32_t* s = p->status;
@@ -125,11 +148,66 @@ struct Waiter {
     }
 };
 
+// One lane's column `col` of 32 consecutive rows of C (rows at or past `rows`
+// and columns at or past N read as 0). The 32 loads are independent, so they
+// are in flight together.
+__device__ __forceinline__ void load_c_chunk(const float* c_rows, int64_t ldc, int32_t col, int32_t N,
+                                             int32_t rows, float (&v)[32]) {
+    const bool col_ok = col < N;
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr)
+        v[rr] = (col_ok && rr < rows) ? __ldg(c_rows + static_cast<int64_t>(rr) * ldc + col) : 0.0f;
+}
+
+// The epilogue of one tile for one warp: rows m0 .. m0+31 (TMEM lanes of this
+// warp's quarter, starting at t_row) and columns n0 .. n0+BN-1. c_cur holds the
+// first chunk of C when beta != 0 (loaded before the accumulator was ready).
+template <int BN, int PITCH>
+__device__ __forceinline__ void store_tile(const GemmParams& p, uint32_t t_row, int32_t m0,
+                                          int32_t n0, float* buf, int lane, float (&c_cur)[32]) {
+    const float alpha = p.alpha, beta = p.beta;
+    const bool read_c = (beta != 0.0f);
+    const int32_t rows = min(32, p.M - m0);
+    const int32_t chunks = (min(BN, p.N - n0) + 31) / 32;
+    const float* c_rows = p.C + static_cast<int64_t>(m0) * p.ldc;
+    float c_next[32];
+    for (int32_t c = 0; c < chunks; ++c) {
+        uint32_t r[32];
+        ptx::tmem_load_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
+        if (read_c && c + 1 < chunks)
+            load_c_chunk(c_rows, p.ldc, n0 + (c + 1) * 32 + lane, p.N, rows, c_next);
+        ptx::tmem_load_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) buf[lane * PITCH + j] = alpha * __uint_as_float(r[j]);
+        __syncwarp();
+        const int32_t col = n0 + c * 32 + lane;
+        if (col < p.N) {
+            float* cp = p.C + static_cast<int64_t>(m0) * p.ldc + col;
+            if (read_c) {
+#pragma unroll
+                for (int rr = 0; rr < 32; ++rr)
+                    if (rr < rows)
+                        cp[static_cast<int64_t>(rr) * p.ldc] = fmaf(beta, c_cur[rr], buf[rr * PITCH + lane]);
+            } else {
+#pragma unroll
+                for (int rr = 0; rr < 32; ++rr)
+                    if (rr < rows) cp[static_cast<int64_t>(rr) * p.ldc] = buf[rr * PITCH + lane];
+            }
+        }
+        if (read_c) {
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) c_cur[rr] = c_next[rr];
+        }
+        __syncwarp();
+    }
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+    constexpr bool PAIR = Cfg::PAIR;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
@@ -150,6 +228,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const Waiter waiter{&p, abort_flag};
+    // Pair: the even CTA of the cluster issues the MMAs and owns the barriers
+    // both CTAs' loads and epilogues report to.
+    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+    const int32_t first_tile = PAIR ? static_cast<int32_t>(blockIdx.x / 2) : static_cast<int32_t>(blockIdx.x);
+    const int32_t tile_step = PAIR ? static_cast<int32_t>(gridDim.x / 2) : static_cast<int32_t>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -158,7 +241,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(acc_full_bar(b), 1);
-            ptx::mbar_init(acc_empty_bar(b), Cfg::EPI_WARPS);
+            ptx::mbar_init(acc_empty_bar(b), Cfg::EPI_WARPS * Cfg::CTAS);
         }
         *abort_flag = 0;
         ptx::fence_barrier_init();
@@ -168,11 +251,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         ptx::prefetch_tensormap(&tmap_b);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), Cfg::TMEM_COLS);
-        ptx::tmem_relinquish();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), Cfg::TMEM_COLS);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_addr(tmem_slot), Cfg::TMEM_COLS);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR) ptx::cluster_sync();   // peer barriers initialised before any remote use
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -183,30 +272,45 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint64_t pol_b = ptx::policy_evict_last();
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t armed = 0;               // stages that received loads
-            uint32_t armed_parity = 0;        // parity of the last load per stage
+            uint32_t armed = 0;               // stages this CTA armed with expect_tx
+            uint32_t armed_parity = 0;        // parity of the last armed phase per stage
             bool ok = true;
             if (!p.test_stall) {
-                for (int32_t t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+                for (int32_t t = first_tile; ok && t < p.tiles; t += tile_step) {
                     int32_t mb, nb;
                     tile_coords(p, t, mb, nb);
-                    const int32_t n0 = nb * BN;
-                    const int32_t n_atoms = min(BN / 64, (p.N - n0 + 63) / 64);
-                    const uint32_t bytes = Cfg::A_BYTES + n_atoms * Cfg::B_ATOM_BYTES;
+                    const int32_t n0 = nb * BN + static_cast<int32_t>(rank) * Cfg::B_COLS;
+                    const int32_t m0 = mb * Cfg::TILE_M + static_cast<int32_t>(rank) * BM;
+                    // single: only the boxes that hold valid columns; pair: all boxes
+                    const int32_t n_atoms =
+                        PAIR ? Cfg::B_COLS / 64 : min(BN / 64, (p.N - nb * BN + 63) / 64);
+                    const uint32_t bytes = (Cfg::A_BYTES + n_atoms * Cfg::B_ATOM_BYTES) * Cfg::CTAS;
                     for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
                         if (!waiter.wait(empty_bar(stage), phase ^ 1u)) {
                             waiter.fail(kRoleLoad, kb);
                             ok = false;
                             break;
                         }
-                        ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
-                        ptx::tma_load_2d(sA + stage * Cfg::A_BYTES, &tmap_a, full_bar(stage),
-                                         kb * BK, mb * BM, pol_a);
-                        for (int j = 0; j < n_atoms; ++j)
-                            ptx::tma_load_2d(sB + stage * Cfg::B_BYTES + j * Cfg::B_ATOM_BYTES,
-                                             &tmap_b, full_bar(stage), n0 + j * 64, kb * BK, pol_b);
-                        armed |= 1u << stage;
-                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                        if constexpr (PAIR) {
+                            const uint32_t lead_full = ptx::mapa_shared(full_bar(stage), 0);
+                            if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
+                            ptx::tma_load_2d_pair(sA + stage * Cfg::A_BYTES, &tmap_a, lead_full, kb * BK,
+                                                  m0, pol_a);
+                            for (int j = 0; j < n_atoms; ++j)
+                                ptx::tma_load_2d_pair(sB + stage * Cfg::B_BYTES + j * Cfg::B_ATOM_BYTES,
+                                                      &tmap_b, lead_full, n0 + j * 64, kb * BK, pol_b);
+                        } else {
+                            ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
+                            ptx::tma_load_2d(sA + stage * Cfg::A_BYTES, &tmap_a, full_bar(stage), kb * BK,
+                                             m0, pol_a);
+                            for (int j = 0; j < n_atoms; ++j)
+                                ptx::tma_load_2d(sB + stage * Cfg::B_BYTES + j * Cfg::B_ATOM_BYTES,
+                                                 &tmap_b, full_bar(stage), n0 + j * 64, kb * BK, pol_b);
+                        }
+                        if (rank == 0) {
+                            armed |= 1u << stage;
+                            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                        }
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -215,32 +319,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
             }
             if (!ok) {
-                // Let every load this thread issued land before the CTA exits.
-                for (int s = 0; s < STAGES; ++s) {
-                    if (!(armed & (1u << s))) continue;
-                    const uint32_t par = (armed_parity >> s) & 1u;
-                    const uint64_t t0 = ptx::globaltimer_ns();
-                    while (!ptx::mbar_try_wait(full_bar(s), par) &&
-                           ptx::globaltimer_ns() - t0 < p.wait_limit_ns) {
-                    }
-                }
+                // Let the loads of every armed stage land before the CTA exits.
+                for (int s = 0; s < STAGES; ++s)
+                    if (armed & (1u << s)) waiter.drain(full_bar(s), (armed_parity >> s) & 1u);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             int stage = 0;
             uint32_t phase = 0;
             int32_t local = 0;
             bool ok = true;
             bool issued = false;
-            for (int32_t t = blockIdx.x; ok && t < p.tiles; t += gridDim.x, ++local) {
+            for (int32_t t = first_tile; ok && t < p.tiles; t += tile_step, ++local) {
                 int32_t mb, nb;
                 tile_coords(p, t, mb, nb);
-                const int32_t n0 = nb * BN;
-                const int32_t n_atoms = min(BN / 64, (p.N - n0 + 63) / 64);
-                const uint32_t idesc = ptx::idesc_f16_f32(BM, n_atoms * 64, false, true);
+                const int32_t n_mma = PAIR ? BN : 64 * min(BN / 64, (p.N - nb * BN + 63) / 64);
+                const uint32_t idesc = ptx::idesc_f16_f32(Cfg::TILE_M, n_mma, false, true);
                 const int buf = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
                 if (!waiter.wait(acc_empty_bar(buf), acc_phase ^ 1u)) {
@@ -269,26 +366,33 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         //    the k-th 16-row slice starts 16 * 128 bytes further.
                         const uint64_t b_desc =
                             ptx::smem_desc_sw128(b_base + kk * 2048, Cfg::B_ATOM_BYTES, 1024);
-                        ptx::mma_f16(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0);
+                        if constexpr (PAIR)
+                            ptx::mma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0);
+                        else
+                            ptx::mma_f16(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0);
                     }
                     issued = true;
-                    ptx::mma_commit(empty_bar(stage));
+                    if constexpr (PAIR)
+                        ptx::mma_commit_pair_multicast(empty_bar(stage), 0x3);
+                    else
+                        ptx::mma_commit(empty_bar(stage));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                if (ok) ptx::mma_commit(acc_full_bar(buf));
+                if (ok) {
+                    if constexpr (PAIR)
+                        ptx::mma_commit_pair_multicast(acc_full_bar(buf), 0x3);
+                    else
+                        ptx::mma_commit(acc_full_bar(buf));
+                }
             }
             if (!ok && issued) {
                 // Drain this thread's MMAs before tensor memory is released:
                 // the last commit arrives on the stage before `stage`.
                 const int last = (stage + STAGES - 1) % STAGES;
-                const uint32_t par = (stage == 0) ? (phase ^ 1u) : phase;
-                const uint64_t t0 = ptx::globaltimer_ns();
-                while (!ptx::mbar_try_wait(empty_bar(last), par) &&
-                       ptx::globaltimer_ns() - t0 < p.wait_limit_ns) {
-                }
+                waiter.drain(empty_bar(last), (stage == 0) ? (phase ^ 1u) : phase);
             }
         }
         __syncwarp();
@@ -296,13 +400,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;             // tensor-memory lanes 32*quarter ..
         float* buf = epi_buf + (warp - 2) * 32 * Cfg::EPI_PITCH;
-        const float alpha = p.alpha, beta = p.beta;
+        const bool read_c = (p.beta != 0.0f);
         int32_t local = 0;
-        for (int32_t t = blockIdx.x; t < p.tiles; t += gridDim.x, ++local) {
+        for (int32_t t = first_tile; t < p.tiles; t += tile_step, ++local) {
             int32_t mb, nb;
             tile_coords(p, t, mb, nb);
-            const int32_t m0 = mb * BM + quarter * 32;
+            const int32_t m0 = mb * Cfg::TILE_M + static_cast<int32_t>(rank) * BM + quarter * 32;
             const int32_t n0 = nb * BN;
+            // beta * C needs C's old values: the first chunk's loads go out now,
+            // while the MMAs of this tile are still running.
+            float c_cur[32];
+            if (read_c)
+                load_c_chunk(p.C + static_cast<int64_t>(m0) * p.ldc, p.ldc, n0 + lane, p.N,
+                             min(32, p.M - m0), c_cur);
             const int accb = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             const bool ready = waiter.wait(acc_full_bar(accb), acc_phase);
@@ -313,45 +423,37 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             ptx::tc_fence_after_sync();
             const uint32_t t_row =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(accb * BN);
-            const int32_t ncols = min(BN, p.N - n0);
-            const int32_t chunks = (ncols + 31) / 32;
-            for (int32_t c = 0; c < chunks; ++c) {
-                uint32_t r[32];
-                ptx::tmem_load_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
-                ptx::tmem_load_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) buf[lane * Cfg::EPI_PITCH + j] = alpha * __uint_as_float(r[j]);
-                __syncwarp();
-                const int32_t col = n0 + c * 32 + lane;
-                if (col < p.N) {
-                    float* cp = p.C + static_cast<int64_t>(m0) * p.ldc + col;
-                    const int32_t rows = min(32, p.M - m0);
-                    if (beta != 0.0f) {
-#pragma unroll 8
-                        for (int32_t rr = 0; rr < rows; ++rr) {
-                            float* q = cp + static_cast<int64_t>(rr) * p.ldc;
-                            *q = fmaf(beta, *q, buf[rr * Cfg::EPI_PITCH + lane]);
-                        }
-                    } else {
-#pragma unroll 8
-                        for (int32_t rr = 0; rr < rows; ++rr)
-                            cp[static_cast<int64_t>(rr) * p.ldc] = buf[rr * Cfg::EPI_PITCH + lane];
-                    }
-                }
-                __syncwarp();
-            }
+            store_tile<BN, Cfg::EPI_PITCH>(p, t_row, m0, n0, buf, lane, c_cur);
             ptx::tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(acc_empty_bar(accb));
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    ptx::mbar_arrive_cluster(ptx::mapa_shared(acc_empty_bar(accb), 0));
+                else
+                    ptx::mbar_arrive(acc_empty_bar(accb));
+            }
         }
         __syncwarp();
     }
 
     ptx::tc_fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR) {
+        // After an abort the peer's loads into this pair may still be landing:
+        // give them a moment before the cluster (and its shared memory) goes away.
+        if (*abort_flag) {
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (ptx::globaltimer_ns() - t0 < 200000ull) {
+            }
+        }
+        ptx::cluster_sync();
+    }
     if (warp == 1) {
         ptx::tc_fence_after_sync();
-        ptx::tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        if constexpr (PAIR)
+            ptx::tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+        else
+            ptx::tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
 }
 

@@ -26,6 +26,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <functional>
 #include <mutex>
 
@@ -38,13 +39,15 @@ namespace {
 constexpr int64_t kDimLimit = (int64_t{1} << 31) - 1;
 constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;
 
-using Cfg256 = TileConfig<256, 4>;
-using Cfg128 = TileConfig<128, 6>;
+using Cfg256 = TileConfig<256, 4, false>;   // one CTA per 128 x 256 tile
+using Cfg128 = TileConfig<128, 6, false>;   // one CTA per 128 x 128 tile
+using CfgPair = TileConfig<256, 6, true>;   // a CTA pair per 256 x 256 tile
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 struct Options {
+    int32_t tile_m = 0;
     int32_t tile_n = 0;
     int32_t max_ctas = 0;
     int32_t force_staging = 0;
@@ -82,6 +85,14 @@ int32_t auto_tile_n(int64_t M, int64_t N, int32_t num_sms) {
     return tiles256 >= num_sms ? 256 : 128;
 }
 
+// CTA pairs (256 x 256 tiles) pay off once there is at least a full wave of
+// pair tiles and the last column band wastes at most a fifth of its width.
+bool auto_pair(int64_t M, int64_t N, int32_t num_sms) {
+    if (M < 512 || N < 512) return false;
+    if (ceil_div(N, 256) * 256 * 4 > 5 * N) return false;
+    return ceil_div(M, 256) * ceil_div(N, 256) >= num_sms / 2;
+}
+
 mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                           const void* B, int64_t ldb, float beta, const void* C, int64_t ldc,
                           int32_t num_sms, const Options& opt, mpgemm_plan_t* out) {
@@ -103,10 +114,18 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     }
     p.stage_a = (opt.force_staging || !aligned16(A, lda, 2)) ? 1 : 0;
     p.stage_b = (opt.force_staging || !aligned16(B, ldb, 2)) ? 1 : 0;
-    p.tile_n = opt.tile_n ? opt.tile_n : auto_tile_n(M, N, num_sms);
-    p.stages = (p.tile_n == 256) ? Cfg256::STAGES : Cfg128::STAGES;
-    p.smem_bytes = (p.tile_n == 256) ? Cfg256::SMEM_BYTES : Cfg128::SMEM_BYTES;
-    const int64_t m_tiles = ceil_div(M, 128), n_tiles = ceil_div(N, p.tile_n);
+    const bool pair = opt.tile_m ? (opt.tile_m == 256) : (!opt.tile_n && auto_pair(M, N, num_sms));
+    if (pair) {
+        p.tile_m = 256;
+        p.tile_n = 256;
+        p.stages = CfgPair::STAGES;
+        p.smem_bytes = CfgPair::SMEM_BYTES;
+    } else {
+        p.tile_n = opt.tile_n ? opt.tile_n : auto_tile_n(M, N, num_sms);
+        p.stages = (p.tile_n == 256) ? Cfg256::STAGES : Cfg128::STAGES;
+        p.smem_bytes = (p.tile_n == 256) ? Cfg256::SMEM_BYTES : Cfg128::SMEM_BYTES;
+    }
+    const int64_t m_tiles = ceil_div(M, p.tile_m), n_tiles = ceil_div(N, p.tile_n);
     const int64_t k_blocks = ceil_div(K, 64);
     if (m_tiles * n_tiles > kDimLimit) return MPGEMM_ERR_INVALID_VALUE;
     p.m_tiles = static_cast<int32_t>(m_tiles);
@@ -114,9 +133,12 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     p.k_blocks = static_cast<int32_t>(k_blocks);
     p.tiles = m_tiles * n_tiles;
     p.last_k_valid = static_cast<int32_t>(K - (k_blocks - 1) * 64);
-    int64_t grid = p.tiles < num_sms ? p.tiles : num_sms;
-    if (opt.max_ctas > 0 && grid > opt.max_ctas) grid = opt.max_ctas;
-    p.grid = static_cast<int32_t>(grid);
+    // persistent grid: one CTA (single) or one CTA pair (pair) per SM or SM pair
+    const int64_t per_unit = pair ? 2 : 1;
+    int64_t units = num_sms / per_unit;
+    if (opt.max_ctas > 0) units = std::min<int64_t>(units, std::max<int64_t>(1, opt.max_ctas / per_unit));
+    units = std::max<int64_t>(1, std::min<int64_t>(units, p.tiles));
+    p.grid = static_cast<int32_t>(units * per_unit);
     int32_t group = opt.raster_group ? opt.raster_group : 16;
     if (group > p.m_tiles) group = p.m_tiles;
     p.raster_group = group;
@@ -215,9 +237,63 @@ cudaError_t set_smem_attr() {
 }
 
 template <class Cfg>
-void launch_tc(const mpgemm_plan_t& plan, const CUtensorMap& ta, const CUtensorMap& tb,
-               const GemmParams& gp, cudaStream_t stream) {
-    gemm_tc_kernel<Cfg><<<plan.grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, gp);
+cudaError_t launch_tc(int grid, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& gp,
+                      cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    if (Cfg::PAIR) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<Cfg>, ta, tb, gp);
+}
+
+// Clusters of two CTAs of the pair kernel that fit on the device at once.
+int max_pair_clusters() {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(CfgPair::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = CfgPair::SMEM_BYTES;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<CfgPair>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+// All kernel attributes the launches need, for the current device.
+cudaError_t prepare_kernels() {
+    cudaError_t e = set_smem_attr<Cfg256>();
+    if (e == cudaSuccess) e = set_smem_attr<Cfg128>();
+    if (e == cudaSuccess) e = set_smem_attr<CfgPair>();
+    return e;
+}
+
+cudaError_t launch_plan(const mpgemm_plan_t& plan, int max_clusters, const CUtensorMap& ta,
+                        const CUtensorMap& tb, const GemmParams& gp, cudaStream_t stream) {
+    if (plan.tile_m == 256) {
+        int grid = plan.grid;
+        if (max_clusters > 0 && grid > 2 * max_clusters) grid = 2 * max_clusters;
+        return launch_tc<CfgPair>(grid, ta, tb, gp, stream);
+    }
+    if (plan.tile_n == 256) return launch_tc<Cfg256>(plan.grid, ta, tb, gp, stream);
+    return launch_tc<Cfg128>(plan.grid, ta, tb, gp, stream);
 }
 
 }  // namespace
@@ -228,6 +304,7 @@ using namespace mpgemm;
 struct mpgemm_handle_st {
     int device = 0;
     int num_sms = 0;
+    int max_clusters = 0;            // CTA pairs of the pair kernel resident at once
     Options opt;
     int32_t* status_host = nullptr;  // mapped pinned memory: {code, role, block, detail}
     int32_t* status_dev = nullptr;
@@ -289,12 +366,14 @@ const char* mpgemm_status_string(mpgemm_status_t s) {
 
 mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
                             int64_t lda, const void* B, int64_t ldb, float beta, const float* C,
-                            int64_t ldc, int32_t num_sms, int32_t tile_n, int32_t max_ctas,
-                            int32_t force_staging, mpgemm_plan_t* out) {
+                            int64_t ldc, int32_t num_sms, int32_t tile_m, int32_t tile_n,
+                            int32_t max_ctas, int32_t force_staging, mpgemm_plan_t* out) {
     if (!out) return MPGEMM_ERR_INVALID_VALUE;
+    if (tile_m != 0 && tile_m != 128 && tile_m != 256) return MPGEMM_ERR_INVALID_VALUE;
     if (tile_n != 0 && tile_n != 128 && tile_n != 256) return MPGEMM_ERR_INVALID_VALUE;
     if (max_ctas < 0) return MPGEMM_ERR_INVALID_VALUE;
     Options opt;
+    opt.tile_m = tile_m;
     opt.tile_n = tile_n;
     opt.max_ctas = max_ctas;
     opt.force_staging = force_staging ? 1 : 0;
@@ -318,7 +397,7 @@ mpgemm_status_t mpgemm_create(mpgemm_handle_t* out) {
     }
     if (major != 10 || minor != 3) return MPGEMM_ERR_UNSUPPORTED_DEVICE;
     if (!encode_fn()) return MPGEMM_ERR_CUDA;
-    if (set_smem_attr<Cfg256>() != cudaSuccess || set_smem_attr<Cfg128>() != cudaSuccess) {
+    if (prepare_kernels() != cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_CUDA;
     }
@@ -326,6 +405,7 @@ mpgemm_status_t mpgemm_create(mpgemm_handle_t* out) {
     if (!h) return MPGEMM_ERR_ALLOC;
     h->device = dev;
     h->num_sms = sms;
+    h->max_clusters = max_pair_clusters();
     void* st = nullptr;
     if (cudaHostAlloc(&st, 4 * sizeof(int32_t), cudaHostAllocMapped) != cudaSuccess) {
         cudaGetLastError();
@@ -378,6 +458,10 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
         case MPGEMM_OPT_RASTER_GROUP:
             if (value < 0 || value > 65536) return MPGEMM_ERR_INVALID_VALUE;
             h->opt.raster_group = static_cast<int32_t>(value);
+            return MPGEMM_OK;
+        case MPGEMM_OPT_TILE_M:
+            if (value != 0 && value != 128 && value != 256) return MPGEMM_ERR_INVALID_VALUE;
+            h->opt.tile_m = static_cast<int32_t>(value);
             return MPGEMM_OK;
         case MPGEMM_OPT_TEST_STALL:
             if (value != 0 && value != 1) return MPGEMM_ERR_INVALID_VALUE;
@@ -447,11 +531,11 @@ mpgemm_status_t mpgemm_run(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K, f
     gp.status = h->status_dev;
     gp.wait_limit_ns = h->opt.wait_limit_ns;
     gp.test_stall = h->opt.test_stall;
-    if (plan.tile_n == 256)
-        launch_tc<Cfg256>(plan, ta, tb, gp, stream);
-    else
-        launch_tc<Cfg128>(plan, ta, tb, gp, stream);
-    return cudaGetLastError() == cudaSuccess ? MPGEMM_OK : MPGEMM_ERR_LAUNCH;
+    if (launch_plan(plan, h->max_clusters, ta, tb, gp, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MPGEMM_ERR_LAUNCH;
+    }
+    return MPGEMM_OK;
 }
 
 mpgemm_status_t mpgemm_run_host(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha,
@@ -534,6 +618,7 @@ struct NoAllocDevice {
     mpgemm_status_t status = MPGEMM_ERR_CUDA;
     unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
     int num_sms = 0;
+    int max_clusters = 0;
 };
 
 NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];
@@ -554,14 +639,14 @@ void noalloc_setup(NoAllocDevice& d, int dev) {
     }
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr ||
-        !encode_fn() || set_smem_attr<Cfg256>() != cudaSuccess ||
-        set_smem_attr<Cfg128>() != cudaSuccess) {
+        !encode_fn() || prepare_kernels() != cudaSuccess) {
         cudaGetLastError();
         d.status = MPGEMM_ERR_CUDA;
         return;
     }
     d.scratch = static_cast<unsigned char*>(ptr);
     d.num_sms = sms;
+    d.max_clusters = max_pair_clusters();
     d.status = MPGEMM_OK;
 }
 
@@ -639,9 +724,9 @@ extern "C" mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K, f
     gp.status = status;
     gp.wait_limit_ns = opt.wait_limit_ns;
     gp.test_stall = 0;
-    if (plan.tile_n == 256)
-        launch_tc<Cfg256>(plan, ta, tb, gp, stream);
-    else
-        launch_tc<Cfg128>(plan, ta, tb, gp, stream);
-    return cudaGetLastError() == cudaSuccess ? MPGEMM_OK : MPGEMM_ERR_LAUNCH;
+    if (launch_plan(plan, d.max_clusters, ta, tb, gp, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MPGEMM_ERR_LAUNCH;
+    }
+    return MPGEMM_OK;
 }

@@ -112,9 +112,20 @@ def test_tiling_of_the_ragged_k_tail(golden_facts):
 
 
 def test_tile_selection_and_grid():
+    # large square: CTA pairs on 256 x 256 tiles, one pair per two SMs
     p = _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192)
-    assert p["tile_n"] == 256 and p["tiles"] == 64 * 32 and p["grid"] == 152
-    assert p["smem_bytes"] <= 232448
+    assert (p["tile_m"], p["tile_n"]) == (256, 256) and p["tiles"] == 32 * 32 and p["grid"] == 152
+    assert p["smem_bytes"] <= 232448 and p["stages"] == 6
+    # N = 257 would waste half of the last column band: single CTAs
+    p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257, beta=0.5)
+    assert (p["tile_m"], p["tile_n"]) == (128, 256)
+    # forced pairs with a CTA cap: the grid stays even
+    p = _plan(M=1000, N=800, K=64, lda=64, ldb=800, ldc=800, tile_m=256, max_ctas=5)
+    assert p["tile_m"] == 256 and p["grid"] == 4 and p["tiles"] == 4 * 4
+    p = _plan(M=300, N=300, K=64, lda=64, ldb=300, ldc=300, tile_m=256, max_ctas=1)
+    assert p["grid"] == 2
+    p = _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192, tile_m=128)
+    assert (p["tile_m"], p["tile_n"]) == (128, 256) and p["tiles"] == 64 * 32
     p = _plan(M=2048, N=2048, K=2048, lda=2048, ldb=2048, ldc=2048)
     assert p["tile_n"] == 128 and p["tiles"] == 16 * 16 and p["grid"] == 152
     p = _plan()
@@ -123,3 +134,5 @@ def test_tile_selection_and_grid():
     assert p["tile_n"] == 128 and p["grid"] == 10
     with pytest.raises(mp.MpgemmError):
         _plan(tile_n=192)
+    with pytest.raises(mp.MpgemmError):
+        _plan(tile_m=64)

@@ -169,6 +169,54 @@ def test_tile_width_and_persistence(mp, tile_n, max_ctas):
         check_full(h, workloads.make_operands(700, 600, 450, beta=1.0, c_dist="normal", seed=80))
 
 
+PAIR_SHAPES = [  # (M, N, K): one pair tile, ragged in every dimension, many tiles
+    (256, 256, 64), (256, 256, 192), (200, 136, 617), (300, 500, 700), (511, 257, 129),
+    (1024, 768, 1000), (257, 1025, 65), (1000, 800, 1200),
+]
+
+
+@pytest.mark.parametrize("M,N,K", PAIR_SHAPES)
+def test_cta_pair_tiles(mp, M, N, K):
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_M, 256)
+        check_full(h, workloads.make_operands(M, N, K, beta=0.75, c_dist="normal", seed=M + N + K))
+
+
+def test_cta_pair_integer_bitwise(mp):
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_M, 256)
+        ops = workloads.make_operands(512, 512, 1024, dist="int3", dist_b="int2", seed=83)
+        check_full(h, ops, exact=True)
+
+
+@pytest.mark.parametrize("max_ctas", [2, 6])
+def test_cta_pair_persistence_and_staging(mp, max_ctas):
+    # few pairs walk many tiles; unaligned lda, ldb and ldc go through staging
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_M, 256)
+        h.set_option(mp.Option.MAX_CTAS, max_ctas)
+        ops = workloads.make_operands(1300, 1100, 333, lda=335, ldb=1103, ldc=1101, alpha=-1.5,
+                                      beta=0.5, c_dist="normal", seed=84)
+        check_full(h, ops)
+
+
+def test_cta_pair_stall_reports_timeout(mp):
+    ops = workloads.make_operands(512, 512, 128, seed=85)
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_M, 256)
+        h.set_option(mp.Option.WAIT_LIMIT_US, 20000)
+        h.set_option(mp.Option.TEST_STALL, 1)
+        from parity import device_operands
+        d = device_operands(ops)
+        s = torch.cuda.current_stream()
+        h.run(ops.M, ops.N, ops.K, 1.0, d["a_ptr"], ops.lda, d["b_ptr"], ops.ldb, 0.0, d["c_ptr"],
+              ops.ldc, s.cuda_stream)
+        st, info = h.sync_status(s.cuda_stream)
+        assert st == mp.Status.ERR_DEVICE_TIMEOUT
+        h.set_option(mp.Option.TEST_STALL, 0)
+        check_full(h, ops)
+
+
 def test_forced_staging_matches(mp):
     with mp.Handle() as h:
         h.set_option(mp.Option.FORCE_STAGING, 1)
