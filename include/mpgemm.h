@@ -110,8 +110,11 @@ typedef enum {
     MPGEMM_OPT_RASTER_GROUP = 5,  /* M-tiles per rasterisation group, 0 = automatic (default) */
     MPGEMM_OPT_TEST_STALL = 6,    /* test only: 1 = the load warp issues no loads, so the
                                      kernel's bounded waits expire and a timeout is reported */
-    MPGEMM_OPT_TILE_M = 7         /* 0 = automatic (default); 128 = one CTA per tile;
+    MPGEMM_OPT_TILE_M = 7,        /* 0 = automatic (default); 128 = one CTA per tile;
                                      256 = a cluster of two CTAs per 256 x 256 tile */
+    MPGEMM_OPT_L2_KEEP = 8        /* L2 hints for the operand loads: 0 = automatic (default,
+                                     keep the operand more tiles re-read), 1 = keep A,
+                                     2 = keep B */
 } mpgemm_option_t;
 
 /* Set an option. Unknown options or out-of-range values return
@@ -138,6 +141,8 @@ typedef struct {
     int32_t smem_bytes;     /* dynamic shared memory per CTA */
     int32_t last_k_valid;   /* valid K columns in the last pipeline stage */
     int64_t workspace_bytes;/* device staging bytes the call needs */
+    int32_t split_tiles;    /* tiles of the last partial wave done as two half-width items */
+    int64_t items;          /* work items the persistent CTAs walk: tiles + split_tiles */
 } mpgemm_plan_t;
 
 mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha,

@@ -34,6 +34,7 @@ class Option(enum.IntEnum):
     RASTER_GROUP = 5
     TEST_STALL = 6
     TILE_M = 7
+    L2_KEEP = 8
 
 
 class MpgemmError(RuntimeError):
@@ -48,7 +49,8 @@ class Plan(ctypes.Structure):
                 ("stages", ctypes.c_int32), ("m_tiles", ctypes.c_int32), ("n_tiles", ctypes.c_int32),
                 ("k_blocks", ctypes.c_int32), ("tiles", ctypes.c_int64), ("grid", ctypes.c_int32),
                 ("raster_group", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
-                ("last_k_valid", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64)]
+                ("last_k_valid", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+                ("split_tiles", ctypes.c_int32), ("items", ctypes.c_int64)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -13,10 +13,13 @@
 //               one of two accumulator buffers and frees each stage with
 //               tcgen05.commit.
 //   warps 2-5   epilogue: each warp reads its 32 accumulator rows with
-//               tcgen05.ld, applies alpha (and beta * C when beta != 0) in
-//               FP32, and writes C with row and column masks, so any M, N and
-//               any ldc are handled. While it works on tile i, the MMA warp
-//               already accumulates tile i+1 into the other buffer.
+//               tcgen05.ld (32x32b: TMEM lane = row), applies alpha in FP32,
+//               turns each 32 x 32 chunk around through shared memory so that
+//               every store instruction writes 128 contiguous bytes of one
+//               row of C, adds beta * C when beta != 0, and masks rows and
+//               columns, so any M, N and any ldc are handled. While it works
+//               on tile i, the MMA warp already accumulates tile i+1 into the
+//               other buffer.
 //
 // Two shapes of the same pipeline:
 //   single  one CTA per tile of 128 x BN (BN = 128 or 256), tcgen05.mma with
@@ -53,6 +56,8 @@ struct GemmParams {
     int32_t M, N, K;
     int32_t m_tiles, n_tiles, k_blocks;   // tiles counted in units of the kernel's tile
     int32_t tiles;
+    int32_t tail_start;     // tiles from here on (raster order) are done as two half-width items
+    int32_t items;          // work items: tail_start + 2 * (tiles - tail_start)
     int32_t raster_group;
     float alpha, beta;
     float* C;
@@ -60,6 +65,7 @@ struct GemmParams {
     int32_t* status;        // {code, role, block, detail}
     uint64_t wait_limit_ns;
     int32_t test_stall;     // 1: the load warp issues nothing (timeout test)
+    int32_t keep_a;         // L2 hints: 1 = keep A (evict B first), 0 = keep B (evict A first)
 };
 
 enum : int32_t { kRoleLoad = 1, kRoleMma = 2, kRoleEpilogue = 3 };
@@ -111,6 +117,32 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int32_t t, int3
     nb = r / rows;
 }
 
+// Work item i of the persistent walk: a whole tile of width BN, or, past
+// tail_start, one half (BN / 2 columns) of a tile. Splitting the last partial
+// wave of tiles in halves lets it finish in half the time.
+struct WorkItem {
+    int32_t mb;      // tile row block
+    int32_t n0;      // first column
+    int32_t width;   // columns: BN or BN / 2
+};
+
+template <int BN>
+__device__ __forceinline__ WorkItem work_item(const GemmParams& p, int32_t i) {
+    int32_t t = i, half = -1;
+    if (i >= p.tail_start) {
+        const int32_t h = i - p.tail_start;
+        t = p.tail_start + h / 2;
+        half = h % 2;
+    }
+    int32_t mb, nb;
+    tile_coords(p, t, mb, nb);
+    WorkItem w;
+    w.mb = mb;
+    w.n0 = nb * BN + (half > 0 ? BN / 2 : 0);
+    w.width = half < 0 ? BN : BN / 2;
+    return w;
+}
+
 struct Waiter {
     const GemmParams* p;
     volatile int32_t* abort_flag;
@@ -159,16 +191,19 @@ __device__ __forceinline__ void load_c_chunk(const float* c_rows, int64_t ldc, i
         v[rr] = (col_ok && rr < rows) ? __ldg(c_rows + static_cast<int64_t>(rr) * ldc + col) : 0.0f;
 }
 
-// The epilogue of one tile for one warp: rows m0 .. m0+31 (TMEM lanes of this
-// warp's quarter, starting at t_row) and columns n0 .. n0+BN-1. c_cur holds the
-// first chunk of C when beta != 0 (loaded before the accumulator was ready).
-template <int BN, int PITCH>
+// The epilogue of one work item for one warp: rows m0 .. m0+31 (the TMEM
+// lanes of this warp's quarter; t_row addresses them at the accumulator's
+// first column) and columns n0 .. n0+width-1. c_cur holds the first chunk of
+// C when beta != 0 (loaded before the accumulator was ready); each later
+// chunk's loads go out before the previous chunk is stored.
+template <int PITCH>
 __device__ __forceinline__ void store_tile(const GemmParams& p, uint32_t t_row, int32_t m0,
-                                          int32_t n0, float* buf, int lane, float (&c_cur)[32]) {
+                                          int32_t n0, int32_t width, float* buf, int lane,
+                                          float (&c_cur)[32]) {
     const float alpha = p.alpha, beta = p.beta;
     const bool read_c = (beta != 0.0f);
     const int32_t rows = min(32, p.M - m0);
-    const int32_t chunks = (min(BN, p.N - n0) + 31) / 32;
+    const int32_t chunks = (min(width, p.N - n0) + 31) / 32;
     const float* c_rows = p.C + static_cast<int64_t>(m0) * p.ldc;
     float c_next[32];
     for (int32_t c = 0; c < chunks; ++c) {
@@ -231,8 +266,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // Pair: the even CTA of the cluster issues the MMAs and owns the barriers
     // both CTAs' loads and epilogues report to.
     const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
-    const int32_t first_tile = PAIR ? static_cast<int32_t>(blockIdx.x / 2) : static_cast<int32_t>(blockIdx.x);
-    const int32_t tile_step = PAIR ? static_cast<int32_t>(gridDim.x / 2) : static_cast<int32_t>(gridDim.x);
+    const int32_t first_item = PAIR ? static_cast<int32_t>(blockIdx.x / 2) : static_cast<int32_t>(blockIdx.x);
+    const int32_t item_step = PAIR ? static_cast<int32_t>(gridDim.x / 2) : static_cast<int32_t>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -268,22 +303,24 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ loads
         if (lane == 0) {
-            const uint64_t pol_a = ptx::policy_evict_first();
-            const uint64_t pol_b = ptx::policy_evict_last();
+            // The operand that more tiles re-read while it is still useful is
+            // loaded with evict_last, the other with evict_first.
+            const uint64_t pol_a = p.keep_a ? ptx::policy_evict_last() : ptx::policy_evict_first();
+            const uint64_t pol_b = p.keep_a ? ptx::policy_evict_first() : ptx::policy_evict_last();
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0;               // stages this CTA armed with expect_tx
             uint32_t armed_parity = 0;        // parity of the last armed phase per stage
             bool ok = true;
             if (!p.test_stall) {
-                for (int32_t t = first_tile; ok && t < p.tiles; t += tile_step) {
-                    int32_t mb, nb;
-                    tile_coords(p, t, mb, nb);
-                    const int32_t n0 = nb * BN + static_cast<int32_t>(rank) * Cfg::B_COLS;
-                    const int32_t m0 = mb * Cfg::TILE_M + static_cast<int32_t>(rank) * BM;
+                for (int32_t i = first_item; ok && i < p.items; i += item_step) {
+                    const WorkItem w = work_item<BN>(p, i);
+                    if (w.n0 >= p.N) continue;   // a half tile wholly past the last column
+                    const int32_t b_cols = w.width / Cfg::CTAS;   // columns of B this CTA loads
+                    const int32_t n0 = w.n0 + static_cast<int32_t>(rank) * b_cols;
+                    const int32_t m0 = w.mb * Cfg::TILE_M + static_cast<int32_t>(rank) * BM;
                     // single: only the boxes that hold valid columns; pair: all boxes
-                    const int32_t n_atoms =
-                        PAIR ? Cfg::B_COLS / 64 : min(BN / 64, (p.N - nb * BN + 63) / 64);
+                    const int32_t n_atoms = PAIR ? b_cols / 64 : min(w.width / 64, (p.N - w.n0 + 63) / 64);
                     const uint32_t bytes = (Cfg::A_BYTES + n_atoms * Cfg::B_ATOM_BYTES) * Cfg::CTAS;
                     for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
                         if (!waiter.wait(empty_bar(stage), phase ^ 1u)) {
@@ -333,10 +370,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int32_t local = 0;
             bool ok = true;
             bool issued = false;
-            for (int32_t t = first_tile; ok && t < p.tiles; t += tile_step, ++local) {
-                int32_t mb, nb;
-                tile_coords(p, t, mb, nb);
-                const int32_t n_mma = PAIR ? BN : 64 * min(BN / 64, (p.N - nb * BN + 63) / 64);
+            for (int32_t i = first_item; ok && i < p.items; i += item_step) {
+                const WorkItem w = work_item<BN>(p, i);
+                if (w.n0 >= p.N) continue;
+                const int32_t n_mma = PAIR ? w.width : 64 * min(w.width / 64, (p.N - w.n0 + 63) / 64);
                 const uint32_t idesc = ptx::idesc_f16_f32(Cfg::TILE_M, n_mma, false, true);
                 const int buf = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
@@ -387,6 +424,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     else
                         ptx::mma_commit(acc_full_bar(buf));
                 }
+                ++local;
             }
             if (!ok && issued) {
                 // Drain this thread's MMAs before tensor memory is released:
@@ -402,11 +440,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         float* buf = epi_buf + (warp - 2) * 32 * Cfg::EPI_PITCH;
         const bool read_c = (p.beta != 0.0f);
         int32_t local = 0;
-        for (int32_t t = first_tile; t < p.tiles; t += tile_step, ++local) {
-            int32_t mb, nb;
-            tile_coords(p, t, mb, nb);
-            const int32_t m0 = mb * Cfg::TILE_M + static_cast<int32_t>(rank) * BM + quarter * 32;
-            const int32_t n0 = nb * BN;
+        for (int32_t i = first_item; i < p.items; i += item_step) {
+            const WorkItem w = work_item<BN>(p, i);
+            if (w.n0 >= p.N) continue;
+            const int32_t m0 = w.mb * Cfg::TILE_M + static_cast<int32_t>(rank) * BM + quarter * 32;
+            const int32_t n0 = w.n0;
             // beta * C needs C's old values: the first chunk's loads go out now,
             // while the MMAs of this tile are still running.
             float c_cur[32];
@@ -417,13 +455,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint32_t acc_phase = (local >> 1) & 1;
             const bool ready = waiter.wait(acc_full_bar(accb), acc_phase);
             if (!__all_sync(0xffffffffu, ready)) {
-                if (lane == 0) waiter.fail(kRoleEpilogue, t);
+                if (lane == 0) waiter.fail(kRoleEpilogue, i);
                 break;
             }
             ptx::tc_fence_after_sync();
             const uint32_t t_row =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(accb * BN);
-            store_tile<BN, Cfg::EPI_PITCH>(p, t_row, m0, n0, buf, lane, c_cur);
+            store_tile<Cfg::EPI_PITCH>(p, t_row, m0, n0, w.width, buf, lane, c_cur);
             ptx::tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
@@ -432,6 +470,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 else
                     ptx::mbar_arrive(acc_empty_bar(accb));
             }
+            ++local;
         }
         __syncwarp();
     }

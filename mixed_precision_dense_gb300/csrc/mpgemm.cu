@@ -52,6 +52,8 @@ struct Options {
     int32_t max_ctas = 0;
     int32_t force_staging = 0;
     int32_t raster_group = 0;
+    int32_t l2_keep = 0;            // 0 automatic, 1 keep A, 2 keep B
+    int32_t pair_units = 0;         // CTA pairs resident at once (0: num_sms / 2)
     int32_t test_stall = 0;
     uint64_t wait_limit_ns = kDefaultWaitLimitNs;
 };
@@ -127,7 +129,7 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     }
     const int64_t m_tiles = ceil_div(M, p.tile_m), n_tiles = ceil_div(N, p.tile_n);
     const int64_t k_blocks = ceil_div(K, 64);
-    if (m_tiles * n_tiles > kDimLimit) return MPGEMM_ERR_INVALID_VALUE;
+    if (m_tiles * n_tiles > kDimLimit / 2) return MPGEMM_ERR_INVALID_VALUE;
     p.m_tiles = static_cast<int32_t>(m_tiles);
     p.n_tiles = static_cast<int32_t>(n_tiles);
     p.k_blocks = static_cast<int32_t>(k_blocks);
@@ -136,9 +138,16 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     // persistent grid: one CTA (single) or one CTA pair (pair) per SM or SM pair
     const int64_t per_unit = pair ? 2 : 1;
     int64_t units = num_sms / per_unit;
+    if (pair && opt.pair_units > 0) units = std::min<int64_t>(units, opt.pair_units);
     if (opt.max_ctas > 0) units = std::min<int64_t>(units, std::max<int64_t>(1, opt.max_ctas / per_unit));
     units = std::max<int64_t>(1, std::min<int64_t>(units, p.tiles));
     p.grid = static_cast<int32_t>(units * per_unit);
+    // If the last wave of tiles would keep at most half of the CTAs (pairs)
+    // busy, do those tiles as two half-width items each: the wave then
+    // finishes in half the time.
+    const int64_t rem = p.tiles % units;
+    p.split_tiles = (p.tiles > units && rem > 0 && 2 * rem <= units) ? static_cast<int32_t>(rem) : 0;
+    p.items = p.tiles + p.split_tiles;
     int32_t group = opt.raster_group ? opt.raster_group : 16;
     if (group > p.m_tiles) group = p.m_tiles;
     p.raster_group = group;
@@ -275,6 +284,16 @@ int max_pair_clusters() {
         return 0;
     }
     return n;
+}
+
+// Which operand to keep in L2. Within a band of raster_group M-tiles an A
+// panel is re-read by each of the n_tiles column tiles, while a B panel is
+// re-read once per band; keep the one with more re-reads.
+int32_t keep_a_operand(const mpgemm_plan_t& plan, int32_t l2_keep) {
+    if (l2_keep == 1) return 1;
+    if (l2_keep == 2) return 0;
+    const int64_t bands = ceil_div(plan.m_tiles, plan.raster_group);
+    return plan.n_tiles >= bands ? 1 : 0;
 }
 
 // All kernel attributes the launches need, for the current device.
@@ -459,6 +478,10 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
             if (value < 0 || value > 65536) return MPGEMM_ERR_INVALID_VALUE;
             h->opt.raster_group = static_cast<int32_t>(value);
             return MPGEMM_OK;
+        case MPGEMM_OPT_L2_KEEP:
+            if (value < 0 || value > 2) return MPGEMM_ERR_INVALID_VALUE;
+            h->opt.l2_keep = static_cast<int32_t>(value);
+            return MPGEMM_OK;
         case MPGEMM_OPT_TILE_M:
             if (value != 0 && value != 128 && value != 256) return MPGEMM_ERR_INVALID_VALUE;
             h->opt.tile_m = static_cast<int32_t>(value);
@@ -477,8 +500,9 @@ mpgemm_status_t mpgemm_run(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K, f
     if (!h) return MPGEMM_ERR_INVALID_VALUE;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     mpgemm_plan_t plan;
-    mpgemm_status_t st =
-        make_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, h->num_sms, h->opt, &plan);
+    Options opt = h->opt;
+    opt.pair_units = h->max_clusters;
+    mpgemm_status_t st = make_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, h->num_sms, opt, &plan);
     if (st != MPGEMM_OK) return st;
     if (take_device_report(h, nullptr) != MPGEMM_OK) return MPGEMM_ERR_DEVICE_TIMEOUT;
     if (plan.quick == 1) return MPGEMM_OK;
@@ -523,6 +547,8 @@ mpgemm_status_t mpgemm_run(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K, f
     gp.n_tiles = plan.n_tiles;
     gp.k_blocks = plan.k_blocks;
     gp.tiles = static_cast<int32_t>(plan.tiles);
+    gp.tail_start = static_cast<int32_t>(plan.tiles - plan.split_tiles);
+    gp.items = static_cast<int32_t>(plan.items);
     gp.raster_group = plan.raster_group;
     gp.alpha = alpha;
     gp.beta = beta;
@@ -531,6 +557,7 @@ mpgemm_status_t mpgemm_run(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K, f
     gp.status = h->status_dev;
     gp.wait_limit_ns = h->opt.wait_limit_ns;
     gp.test_stall = h->opt.test_stall;
+    gp.keep_a = keep_a_operand(plan, h->opt.l2_keep);
     if (launch_plan(plan, h->max_clusters, ta, tb, gp, stream) != cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;
@@ -667,7 +694,8 @@ extern "C" mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K, f
     if (d.status != MPGEMM_OK) return d.status;
 
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-    const Options opt;  // defaults: automatic tile width, one CTA per SM, 4 s wait limit
+    Options opt;  // defaults: automatic tile width, one CTA per SM, 4 s wait limit
+    opt.pair_units = d.max_clusters;
     mpgemm_plan_t plan;
     mpgemm_status_t st =
         make_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d.num_sms, opt, &plan);
@@ -716,6 +744,8 @@ extern "C" mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K, f
     gp.n_tiles = plan.n_tiles;
     gp.k_blocks = plan.k_blocks;
     gp.tiles = static_cast<int32_t>(plan.tiles);
+    gp.tail_start = static_cast<int32_t>(plan.tiles - plan.split_tiles);
+    gp.items = static_cast<int32_t>(plan.items);
     gp.raster_group = plan.raster_group;
     gp.alpha = alpha;
     gp.beta = beta;
@@ -724,6 +754,7 @@ extern "C" mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K, f
     gp.status = status;
     gp.wait_limit_ns = opt.wait_limit_ns;
     gp.test_stall = 0;
+    gp.keep_a = keep_a_operand(plan, 0);
     if (launch_plan(plan, d.max_clusters, ta, tb, gp, stream) != cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;

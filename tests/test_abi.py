@@ -128,6 +128,12 @@ def test_tile_selection_and_grid():
     assert (p["tile_m"], p["tile_n"]) == (128, 256) and p["tiles"] == 64 * 32
     p = _plan(M=2048, N=2048, K=2048, lda=2048, ldb=2048, ldc=2048)
     assert p["tile_n"] == 128 and p["tiles"] == 16 * 16 and p["grid"] == 152
+    # 8192^3: 1024 pair tiles on 76 pairs leave a last wave of 36 tiles, split in halves
+    p = _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192)
+    assert p["split_tiles"] == 1024 % 76 and p["items"] == 1024 + 36
+    # a last wave more than half full is not split
+    p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257)
+    assert p["split_tiles"] == 0 and p["items"] == p["tiles"]
     p = _plan()
     assert p["tiles"] == 2 * 2 and p["grid"] == 4
     p = _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192, tile_n=128, max_ctas=10)

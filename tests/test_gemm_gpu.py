@@ -217,6 +217,27 @@ def test_cta_pair_stall_reports_timeout(mp):
         check_full(h, ops)
 
 
+SPLIT_CASES = [  # (tile_m, tile_n, max_ctas, M, N, K): the last partial wave is split in halves
+    (128, 256, 5, 1000, 800, 200),     # half tiles wholly past column 800 are skipped
+    (128, 128, 7, 700, 600, 333),
+    (256, 256, 8, 1300, 1100, 150),
+    (256, 256, 10, 768, 1024, 320),
+]
+
+
+@pytest.mark.parametrize("tile_m,tile_n,max_ctas,M,N,K", SPLIT_CASES)
+def test_split_tail_tiles(mp, tile_m, tile_n, max_ctas, M, N, K):
+    plan = mp.plan(M, N, K, 1.0, 256, K, 256, N, 0.5, 256, N, tile_m=tile_m,
+                   tile_n=0 if tile_m == 256 else tile_n, max_ctas=max_ctas)
+    assert plan["split_tiles"] > 0 and plan["items"] == plan["tiles"] + plan["split_tiles"]
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_M, tile_m)
+        if tile_m == 128:
+            h.set_option(mp.Option.TILE_N, tile_n)
+        h.set_option(mp.Option.MAX_CTAS, max_ctas)
+        check_full(h, workloads.make_operands(M, N, K, beta=0.5, c_dist="normal", seed=M + K))
+
+
 def test_forced_staging_matches(mp):
     with mp.Handle() as h:
         h.set_option(mp.Option.FORCE_STAGING, 1)
