@@ -162,7 +162,12 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
 // ------------------------------------------------------------------ kernels
 
 // dst[r][c] = src[r][c] for c < cols, zero for cols <= c < round_up(cols, 8);
-// 16-bit elements, dst rows 16-byte aligned. One thread per 16-byte chunk.
+// 16-bit elements; dst rows are 16-byte aligned, src rows only 2-byte aligned.
+// One thread per 16-byte output chunk: it reads the (one or two) aligned
+// 16-byte source chunks that hold the chunk's eight elements and shifts them
+// into place in registers. A source chunk is read only if it holds at least
+// one element of the row, so no read leaves the 16-byte blocks the operand
+// occupies.
 __global__ void stage_rows_u16(const uint16_t* __restrict__ src, int64_t lds,
                                uint16_t* __restrict__ dst, int64_t ldd, int64_t rows,
                                int64_t cols) {
@@ -172,15 +177,38 @@ __global__ void stage_rows_u16(const uint16_t* __restrict__ src, int64_t lds,
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t r = idx / chunks;
         const int64_t c = (idx - r * chunks) * 8;
-        const uint16_t* s = src + r * lds + c;
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const uint32_t lo = (c + 2 * e < cols) ? s[2 * e] : 0u;
-            const uint32_t hi = (c + 2 * e + 1 < cols) ? s[2 * e + 1] : 0u;
-            w[e] = lo | (hi << 16);
+        const uintptr_t row_begin = reinterpret_cast<uintptr_t>(src + r * lds);
+        const uintptr_t row_end = row_begin + 2 * static_cast<uintptr_t>(cols);
+        const uintptr_t a = row_begin + 2 * static_cast<uintptr_t>(c);
+        const uintptr_t a0 = a & ~static_cast<uintptr_t>(15);
+        const uint32_t sh = static_cast<uint32_t>(a - a0);       // 0, 2, ..., 14
+        uint32_t w[8];
+        const uint4 lo = __ldg(reinterpret_cast<const uint4*>(a0));
+        w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
+        if (sh != 0 && a0 + 16 < row_end) {
+            const uint4 hi = __ldg(reinterpret_cast<const uint4*>(a0 + 16));
+            w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
+        } else {
+            w[4] = w[5] = w[6] = w[7] = 0u;
         }
-        *reinterpret_cast<uint4*>(dst + r * ldd + c) = make_uint4(w[0], w[1], w[2], w[3]);
+        // words q .. q+4 of the 32 loaded bytes, q = sh / 4, without dynamic indexing
+        const uint32_t q = sh >> 2;
+        uint32_t v[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i)
+            v[i] = q == 0 ? w[i] : (q == 1 ? w[i + 1] : (q == 2 ? w[i + 2] : w[i + 3]));
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = (sh & 2) ? __funnelshift_r(v[j], v[j + 1], 16) : v[j];
+        const int64_t valid = cols - c;                           // >= 1
+        if (valid < 8) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (2 * j >= valid) o[j] = 0u;
+                else if (2 * j + 1 >= valid) o[j] &= 0xFFFFu;
+            }
+        }
+        *reinterpret_cast<uint4*>(dst + r * ldd + c) = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
