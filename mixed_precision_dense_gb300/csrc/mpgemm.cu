@@ -81,10 +81,12 @@ mpgemm_status_t validate(int64_t M, int64_t N, int64_t K, float alpha, const voi
     return MPGEMM_OK;
 }
 
+// 256-wide tiles move less operand data per FLOP; they are worth it as soon
+// as they keep at least four fifths of the SMs busy.
 int32_t auto_tile_n(int64_t M, int64_t N, int32_t num_sms) {
     if (N <= 128) return 128;
     const int64_t tiles256 = ceil_div(M, 128) * ceil_div(N, 256);
-    return tiles256 >= num_sms ? 256 : 128;
+    return tiles256 * 5 >= static_cast<int64_t>(num_sms) * 4 ? 256 : 128;
 }
 
 // CTA pairs (256 x 256 tiles) pay off once there is at least a full wave of
@@ -602,10 +604,19 @@ mpgemm_status_t mpgemm_run_host(mpgemm_handle_t h, int64_t M, int64_t N, int64_t
     if (M == 0 || N == 0) return MPGEMM_OK;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     const bool need_ab = (K > 0 && alpha != 0.0f);
-    const int64_t lda_d = round_up(K > 0 ? K : 1, 8), ldb_d = round_up(N, 8), ldc_d = round_up(N, 4);
-    const int64_t a_bytes = need_ab ? round_up(M * lda_d * 2, 256) : 0;
-    const int64_t b_bytes = need_ab ? round_up(K * ldb_d * 2, 256) : 0;
-    const int64_t c_bytes = round_up(M * ldc_d * 4, 256);
+    // Every operand travels verbatim with its own pitch, as one contiguous
+    // copy (one large DMA instead of one per row); mpgemm_run then stages A
+    // or B on the device if that pitch breaks the 16-byte rule, and the
+    // epilogue writes C at any pitch. Only when beta == 0 and C has padding
+    // columns is C copied back row by row, so the host's padding columns
+    // (never sent to the device) are not overwritten.
+    const int64_t a_elems = need_ab ? (M - 1) * lda + K : 0;
+    const int64_t b_elems = need_ab ? (K - 1) * ldb + N : 0;
+    const int64_t c_elems = (M - 1) * ldc + N;
+    const int64_t ldc_d = ldc;
+    const int64_t a_bytes = round_up(a_elems * 2, 256);
+    const int64_t b_bytes = round_up(b_elems * 2, 256);
+    const int64_t c_bytes = round_up(c_elems * 4, 256);
     st = ensure_buffer(&h->host_ws, &h->host_ws_bytes, static_cast<size_t>(a_bytes + b_bytes + c_bytes),
                        stream);
     if (st != MPGEMM_OK) return st;
@@ -614,25 +625,28 @@ mpgemm_status_t mpgemm_run_host(mpgemm_handle_t h, int64_t M, int64_t N, int64_t
     void* dB = base + a_bytes;
     float* dC = reinterpret_cast<float*>(base + a_bytes + b_bytes);
     if (need_ab) {
-        if (cudaMemcpy2DAsync(dA, lda_d * 2, A, lda * 2, K * 2, M, cudaMemcpyHostToDevice, stream) !=
+        if (cudaMemcpyAsync(dA, A, static_cast<size_t>(a_elems) * 2, cudaMemcpyHostToDevice, stream) !=
                 cudaSuccess ||
-            cudaMemcpy2DAsync(dB, ldb_d * 2, B, ldb * 2, N * 2, K, cudaMemcpyHostToDevice, stream) !=
+            cudaMemcpyAsync(dB, B, static_cast<size_t>(b_elems) * 2, cudaMemcpyHostToDevice, stream) !=
                 cudaSuccess) {
             cudaGetLastError();
             return MPGEMM_ERR_LAUNCH;
         }
     }
     if (beta != 0.0f &&
-        cudaMemcpy2DAsync(dC, ldc_d * 4, C, ldc * 4, N * 4, M, cudaMemcpyHostToDevice, stream) !=
+        cudaMemcpyAsync(dC, C, static_cast<size_t>(c_elems) * 4, cudaMemcpyHostToDevice, stream) !=
             cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;
     }
-    st = mpgemm_run(h, M, N, K, alpha, need_ab ? dA : nullptr, need_ab ? lda_d : (K > 1 ? K : 1),
-                    need_ab ? dB : nullptr, ldb_d, beta, dC, ldc_d, stream_ptr);
+    st = mpgemm_run(h, M, N, K, alpha, need_ab ? dA : nullptr, need_ab ? lda : (K > 1 ? K : 1),
+                    need_ab ? dB : nullptr, need_ab ? ldb : (N > 1 ? N : 1), beta, dC, ldc_d, stream_ptr);
     if (st != MPGEMM_OK) return st;
-    if (cudaMemcpy2DAsync(C, ldc * 4, dC, ldc_d * 4, N * 4, M, cudaMemcpyDeviceToHost, stream) !=
-        cudaSuccess) {
+    const cudaError_t back =
+        (beta != 0.0f || ldc == N)
+            ? cudaMemcpyAsync(C, dC, static_cast<size_t>(c_elems) * 4, cudaMemcpyDeviceToHost, stream)
+            : cudaMemcpy2DAsync(C, ldc * 4, dC, ldc_d * 4, N * 4, M, cudaMemcpyDeviceToHost, stream);
+    if (back != cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;
     }

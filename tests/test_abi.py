@@ -126,8 +126,12 @@ def test_tile_selection_and_grid():
     assert p["grid"] == 2
     p = _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192, tile_m=128)
     assert (p["tile_m"], p["tile_n"]) == (128, 256) and p["tiles"] == 64 * 32
+    # 2048^3: 128 tiles of 128 x 256 keep 84 % of the SMs busy: wide tiles
     p = _plan(M=2048, N=2048, K=2048, lda=2048, ldb=2048, ldc=2048)
-    assert p["tile_n"] == 128 and p["tiles"] == 16 * 16 and p["grid"] == 152
+    assert p["tile_n"] == 256 and p["tiles"] == 16 * 8 and p["grid"] == 128
+    # 1000 x 800: 32 wide tiles would leave most SMs idle: 128 x 128
+    p = _plan(M=1000, N=800, K=1200, lda=1200, ldb=800, ldc=800)
+    assert p["tile_n"] == 128 and p["tiles"] == 8 * 7
     # 8192^3: 1024 pair tiles on 76 pairs leave a last wave of 36 tiles, split in halves
     p = _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192)
     assert p["split_tiles"] == 1024 % 76 and p["items"] == 1024 + 36

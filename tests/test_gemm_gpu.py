@@ -279,6 +279,23 @@ def test_run_host_matches_oracle(handle):
     assert torch.isnan(C[:, ops.N:]).all()  # padding untouched
 
 
+@pytest.mark.parametrize("beta", [0.0, 0.5])
+def test_run_host_keeps_host_padding(handle, beta):
+    # padding columns of the host C hold a marker that must survive the call
+    ops = workloads.make_operands(97, 130, 71, lda=75, ldb=130, ldc=133, beta=beta,
+                                  c_dist="normal", seed=96)
+    C = ops.C.clone()
+    C[:, ops.N:] = 7.25
+    s = torch.cuda.current_stream()
+    handle.run_host(ops.M, ops.N, ops.K, ops.alpha, ops.A.data_ptr(), ops.lda, ops.B.data_ptr(),
+                    ops.ldb, ops.beta, C.data_ptr(), ops.ldc, s.cuda_stream)
+    s.synchronize()
+    from parity import reference, assert_close
+    ref, S = reference(ops)
+    assert_close(C[:, :ops.N].double().numpy(), ref, S)
+    assert bool((C[:, ops.N:] == 7.25).all())
+
+
 # --------------------------------------------------------------------------- bounded waits
 
 def test_stalled_pipeline_reports_timeout_and_context_survives(mp):
