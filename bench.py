@@ -59,12 +59,18 @@ def gemm_bytes(M: int, N: int, K: int, beta: float, a_bytes=2, b_bytes=2, c_byte
 
 
 def source_hash() -> str:
-    """Hash of the kernel sources; a stored ncu traffic figure is only valid for this hash."""
+    """Hash of what fixes the tensor-core kernel's memory traffic: its device
+    sources and the tile configurations it is instantiated with. A stored ncu
+    traffic figure is only reported while this hash matches."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mixed_precision_dense_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in ("gemm_kernel.cuh", "ptx.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
+    with open(os.path.join(csrc, "mpgemm.cu")) as f:
+        for line in f:
+            if line.startswith("using Cfg"):
+                h.update(line.encode())
     return h.hexdigest()[:16]
 
 
