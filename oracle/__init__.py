@@ -17,7 +17,9 @@ Definitions and sources are in the header of ``oracle.c``:
 Operands are passed as flat arrays with a leading dimension, exactly as a
 BLAS caller would: ``A`` holds binary16 bit patterns (``numpy.uint16``) with
 element (i, k) at ``A[i*lda + k]``; ``B`` likewise with (k, j) at
-``B[k*ldb + j]``; ``C`` is ``numpy.float32`` with (i, j) at ``C[i*ldc + j]``.
+``B[k*ldb + j]`` (row-major, the default) or ``B[j*ldb + k]`` with
+``b_col_major=True`` (the gate's layout on "Day 80", "Independent gate");
+``C`` is ``numpy.float32`` with (i, j) at ``C[i*ldc + j]``.
 """
 from __future__ import annotations
 
@@ -69,6 +71,10 @@ def bind(path: str):
     lib.oracle_elements.restype = ctypes.c_int
     lib.oracle_elements.argtypes = [i64, i64, i64, f64, p, i64, p, i64, f64, p, i64,
                                     i64, p, p, p, p, ctypes.c_int, ctypes.c_int]
+    lib.oracle_gemm_ex.restype = ctypes.c_int
+    lib.oracle_gemm_ex.argtypes = lib.oracle_gemm.argtypes + [ctypes.c_int]
+    lib.oracle_elements_ex.restype = ctypes.c_int
+    lib.oracle_elements_ex.argtypes = lib.oracle_elements.argtypes + [ctypes.c_int]
     return lib
 
 
@@ -118,7 +124,7 @@ def half_to_double(bits: int, lib=None) -> float:
 
 
 def gemm(M, N, K, alpha, A, lda, B, ldb, beta, C=None, ldc=None, *, kahan=False, threads=0,
-         lib=None):
+         lib=None, b_col_major=False):
     """Every element of alpha*A*B + beta*C.
 
     Returns ``(out, S)``, both float64 arrays of shape (M, N), where
@@ -129,20 +135,21 @@ def gemm(M, N, K, alpha, A, lda, B, ldb, beta, C=None, ldc=None, *, kahan=False,
     need_ab = alpha != 0 and K > 0
     if need_ab:
         _check_extent(A, M, lda, K, "A")
-        _check_extent(B, K, ldb, N, "B")
+        _check_extent(B, N, ldb, K, "B") if b_col_major else _check_extent(B, K, ldb, N, "B")
     if beta != 0:
         _check_extent(C, M, ldc, N, "C")
     out = np.empty((M, N), dtype=np.float64)
     S = np.empty((M, N), dtype=np.float64)
-    rc = (lib or _load()).oracle_gemm(M, N, K, float(alpha), _ptr(A), lda, _ptr(B), ldb, float(beta),
-                             _ptr(C), ldc, _ptr(out), _ptr(S), int(bool(kahan)), int(threads))
+    rc = (lib or _load()).oracle_gemm_ex(M, N, K, float(alpha), _ptr(A), lda, _ptr(B), ldb,
+                                         float(beta), _ptr(C), ldc, _ptr(out), _ptr(S),
+                                         int(bool(kahan)), int(threads), int(bool(b_col_major)))
     if rc != 0:
         raise ValueError(f"oracle_gemm rejected the arguments (status {rc})")
     return out, S
 
 
 def elements(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, I, J, *, kahan=False, threads=0,
-             lib=None):
+             lib=None, b_col_major=False):
     """The listed elements (I[e], J[e]) of alpha*A*B + beta*C; returns ``(out, S)``."""
     A, B, C = _as_bits(A, "A"), _as_bits(B, "B"), _as_f32(C)
     I = np.ascontiguousarray(I, dtype=np.int64).reshape(-1)
@@ -151,14 +158,15 @@ def elements(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, I, J, *, kahan=False,
         raise ValueError("I and J differ in length")
     if alpha != 0 and K > 0:
         _check_extent(A, M, lda, K, "A")
-        _check_extent(B, K, ldb, N, "B")
+        _check_extent(B, N, ldb, K, "B") if b_col_major else _check_extent(B, K, ldb, N, "B")
     if beta != 0:
         _check_extent(C, M, ldc, N, "C")
     out = np.empty(I.shape, dtype=np.float64)
     S = np.empty(I.shape, dtype=np.float64)
-    rc = (lib or _load()).oracle_elements(M, N, K, float(alpha), _ptr(A), lda, _ptr(B), ldb, float(beta),
-                                 _ptr(C), ldc, I.size, _ptr(I), _ptr(J), _ptr(out), _ptr(S),
-                                 int(bool(kahan)), int(threads))
+    rc = (lib or _load()).oracle_elements_ex(M, N, K, float(alpha), _ptr(A), lda, _ptr(B), ldb,
+                                             float(beta), _ptr(C), ldc, I.size, _ptr(I), _ptr(J),
+                                             _ptr(out), _ptr(S), int(bool(kahan)), int(threads),
+                                             int(bool(b_col_major)))
     if rc != 0:
         raise ValueError(f"oracle_elements rejected the arguments (status {rc})")
     return out, S

@@ -8,10 +8,14 @@
  *
  * What it computes (the plain definition, element by element, in double):
  *
- *   out[i][j] = alpha * sum_{k=0}^{K-1} dec(A[i*lda + k]) * dec(B[k*ldb + j])
+ *   out[i][j] = alpha * sum_{k=0}^{K-1} dec(A[i*lda + k]) * dec(B(k, j))
  *             + beta  * C[i*ldc + j]                      (term dropped if beta == 0)
  *
- *   S[i][j]   = sum_{k=0}^{K-1} |dec(A[i*lda + k]) * dec(B[k*ldb + j])|
+ *   S[i][j]   = sum_{k=0}^{K-1} |dec(A[i*lda + k]) * dec(B(k, j))|
+ *
+ * with B(k, j) = B[k*ldb + j] for row-major B (K x N, the default) or
+ * B[j*ldb + k] for column-major B ("Day 80, Capstone 4", "Independent gate":
+ * the gate's solve() takes B column-major).
  *
  * Sources:
  *  - "Day 80, Capstone 4: a tensor-core GEMM", sections "Capability" and
@@ -90,6 +94,7 @@ typedef struct {
     const uint16_t* B; int64_t ldb;
     const float* C;    int64_t ldc;
     int kahan;
+    int64_t b_sk, b_sj;   /* B(k, j) = B[k*b_sk + j*b_sj] */
 } problem_t;
 
 /* sum_k dec(A[i,k]) * dec(B[k,j]) with B's column j given as a strided
@@ -148,7 +153,7 @@ static void* run_columns(void* arg) {
     double* bdec = (double*)malloc((size_t)(p->K > 0 ? p->K : 1) * sizeof(double));
     if (!bdec) { job->status = -1; return NULL; }
     for (int64_t j = job->begin; j < job->end; ++j) {
-        for (int64_t k = 0; k < p->K; ++k) bdec[k] = dec[p->B[k * p->ldb + j]];
+        for (int64_t k = 0; k < p->K; ++k) bdec[k] = dec[p->B[k * p->b_sk + j * p->b_sj]];
         for (int64_t i = 0; i < p->M; ++i) {
             double sum = 0.0, sabs = 0.0;
             if (p->alpha != 0.0) dot_row(p, dec, i, NULL, 0, bdec, &sum, &sabs);
@@ -168,7 +173,7 @@ static void* run_elements(void* arg) {
     for (int64_t e = job->begin; e < job->end; ++e) {
         const int64_t i = job->I[e], j = job->J[e];
         double sum = 0.0, sabs = 0.0;
-        if (p->alpha != 0.0) dot_row(p, dec, i, p->B + j, p->ldb, NULL, &sum, &sabs);
+        if (p->alpha != 0.0) dot_row(p, dec, i, p->B + j * p->b_sj, p->b_sk, NULL, &sum, &sabs);
         job->out[e] = finish(p, i, j, sum);
         if (job->S) job->S[e] = sabs;
     }
@@ -204,9 +209,11 @@ static int run_parallel(void* (*fn)(void*), const problem_t* p, int64_t count,
 }
 
 static int check(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                 const void* A, const void* B, const void* C, double alpha, double beta) {
+                 const void* A, const void* B, const void* C, double alpha, double beta,
+                 int b_col_major) {
+    const int64_t b_min = b_col_major ? K : N;
     if (M < 0 || N < 0 || K < 0) return -2;
-    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1)) return -2;
+    if (lda < (K > 1 ? K : 1) || ldb < (b_min > 1 ? b_min : 1) || ldc < (N > 1 ? N : 1)) return -2;
     if (M > 0 && N > 0) {
         if (alpha != 0.0 && K > 0 && (!A || !B)) return -2;
         if (beta != 0.0 && !C) return -2;
@@ -214,30 +221,57 @@ static int check(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int6
     return 0;
 }
 
+static problem_t make_problem(int64_t M, int64_t N, int64_t K, double alpha, const uint16_t* A,
+                              int64_t lda, const uint16_t* B, int64_t ldb, double beta,
+                              const float* C, int64_t ldc, int kahan, int b_col_major) {
+    problem_t p = {M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, kahan,
+                   b_col_major ? 1 : ldb, b_col_major ? ldb : 1};
+    return p;
+}
+
 /* Every element: out and S are M x N, row-major with leading dimension N.
- * Returns 0 on success, -2 on invalid arguments, -1 on allocation failure. */
-int oracle_gemm(int64_t M, int64_t N, int64_t K, double alpha,
-                const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
-                double beta, const float* C, int64_t ldc,
-                double* out, double* S, int kahan, int nthreads) {
-    int rc = check(M, N, K, lda, ldb, ldc, A, B, C, alpha, beta);
+ * b_col_major selects B(k, j) = B[j*ldb + k] (ldb >= K) instead of
+ * B[k*ldb + j] (ldb >= N). Returns 0 on success, -2 on invalid arguments,
+ * -1 on allocation failure. */
+int oracle_gemm_ex(int64_t M, int64_t N, int64_t K, double alpha,
+                   const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                   double beta, const float* C, int64_t ldc,
+                   double* out, double* S, int kahan, int nthreads, int b_col_major) {
+    int rc = check(M, N, K, lda, ldb, ldc, A, B, C, alpha, beta, b_col_major);
     if (rc) return rc;
     if (M == 0 || N == 0) return 0;
-    problem_t p = {M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, kahan};
+    problem_t p = make_problem(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, kahan, b_col_major);
     return run_parallel(run_columns, &p, N, NULL, NULL, out, S, nthreads);
 }
 
 /* The listed elements (I[e], J[e]) only: out[e] and S[e]. */
+int oracle_elements_ex(int64_t M, int64_t N, int64_t K, double alpha,
+                       const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                       double beta, const float* C, int64_t ldc,
+                       int64_t count, const int64_t* I, const int64_t* J,
+                       double* out, double* S, int kahan, int nthreads, int b_col_major) {
+    int rc = check(M, N, K, lda, ldb, ldc, A, B, C, alpha, beta, b_col_major);
+    if (rc) return rc;
+    for (int64_t e = 0; e < count; ++e)
+        if (I[e] < 0 || I[e] >= M || J[e] < 0 || J[e] >= N) return -2;
+    if (count == 0) return 0;
+    problem_t p = make_problem(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, kahan, b_col_major);
+    return run_parallel(run_elements, &p, count, I, J, out, S, nthreads);
+}
+
+/* Row-major B. */
+int oracle_gemm(int64_t M, int64_t N, int64_t K, double alpha,
+                const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                double beta, const float* C, int64_t ldc,
+                double* out, double* S, int kahan, int nthreads) {
+    return oracle_gemm_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, out, S, kahan, nthreads, 0);
+}
+
 int oracle_elements(int64_t M, int64_t N, int64_t K, double alpha,
                     const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
                     double beta, const float* C, int64_t ldc,
                     int64_t count, const int64_t* I, const int64_t* J,
                     double* out, double* S, int kahan, int nthreads) {
-    int rc = check(M, N, K, lda, ldb, ldc, A, B, C, alpha, beta);
-    if (rc) return rc;
-    for (int64_t e = 0; e < count; ++e)
-        if (I[e] < 0 || I[e] >= M || J[e] < 0 || J[e] >= N) return -2;
-    if (count == 0) return 0;
-    problem_t p = {M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, kahan};
-    return run_parallel(run_elements, &p, count, I, J, out, S, nthreads);
+    return oracle_elements_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, count, I, J, out, S,
+                              kahan, nthreads, 0);
 }

@@ -291,13 +291,58 @@ def test_edge_values_need_fp32_range(golden_facts):
 
 
 # ---------------------------------------------------------------------------
+# column-major B (the gate's layout)
+# ---------------------------------------------------------------------------
+
+def test_column_major_b_equals_row_major_of_the_transpose():
+    # B stored column-major with ldb >= K; numpy builds the row-major copy
+    M, N, K = 37, 29, 53
+    ldb_c = K + 3
+    rng = np.random.default_rng(17)
+    bt = rng.uniform(-1, 1, size=(N, ldb_c)).astype(np.float16)   # row j holds column j of B
+    b_rm = np.ascontiguousarray(bt[:, :K].T)                        # K x N row-major
+    ops = workloads.make_operands(M, N, K, beta=0.5, c_dist="normal", seed=18)
+    A, C = ops.bits("A"), ops.bits("C")
+    col, Sc = oracle.gemm(M, N, K, 1.5, A, K, bt.view(np.uint16), ldb_c, 0.5, C, N, b_col_major=True)
+    row, Sr = oracle.gemm(M, N, K, 1.5, A, K, b_rm.view(np.uint16), N, 0.5, C, N)
+    assert np.array_equal(col, row) and np.array_equal(Sc, Sr)
+    I, J = workloads.sample_indices(M, N, 200, seed=19)
+    got, gS = oracle.elements(M, N, K, 1.5, A, K, bt.view(np.uint16), ldb_c, 0.5, C, N, I, J,
+                              b_col_major=True)
+    assert np.array_equal(got, row[I, J]) and np.array_equal(gS, Sr[I, J])
+
+
+def test_column_major_b_brute_force_exact():
+    rng = random.Random(99)
+    for _ in range(40):
+        M, N, K = rng.randint(1, 6), rng.randint(1, 6), rng.randint(1, 8)
+        lda, ldb, ldc = K + rng.randint(0, 2), K + rng.randint(0, 2), N + rng.randint(0, 2)
+        A = _f16([rng.randint(-3, 3) for _ in range(M * lda)])
+        B = _f16([rng.randint(-2, 2) for _ in range(N * ldb)])
+        out, _ = oracle.gemm(M, N, K, 1.0, A, lda, B, ldb, 0.0, b_col_major=True)
+        for i in range(M):
+            for j in range(N):
+                want = sum(Fraction(float(np.uint16(A[i * lda + k]).view(np.float16))) *
+                           Fraction(float(np.uint16(B[j * ldb + k]).view(np.float16))) for k in range(K))
+                assert out[i, j] == float(want)
+
+
+def test_column_major_b_checks_ldb_against_k():
+    A = np.zeros(64, dtype=np.uint16)
+    with pytest.raises(ValueError):
+        oracle.gemm(2, 8, 4, 1.0, A, 4, A, 3, 0.0, b_col_major=True)   # ldb < K
+    oracle.gemm(2, 8, 4, 1.0, A, 4, A, 4, 0.0, b_col_major=True)       # ldb = K < N is fine
+
+
+# ---------------------------------------------------------------------------
 # mutation check: plausible mistakes planted in a copy of the oracle (CPU only)
 # ---------------------------------------------------------------------------
 
 MUTANTS = {
     "sign": ("sum += prod;", "sum -= prod;"),
     "dropped_beta": ("if (p->beta != 0.0) v += p->beta", "if (0) v += p->beta"),
-    "transposed_b": ("dec[p->B[k * p->ldb + j]]", "dec[p->B[j * p->ldb + k]]"),
+    "transposed_b": ("b_col_major ? 1 : ldb, b_col_major ? ldb : 1",
+                     "b_col_major ? ldb : 1, b_col_major ? 1 : ldb"),
     "lda_ignored": ("p->A + i * p->lda", "p->A + i * p->K"),
     "k_off_by_one": ("for (int64_t k = 0; k < p->K; ++k) {\n        const double a",
                      "for (int64_t k = 1; k < p->K; ++k) {\n        const double a"),
