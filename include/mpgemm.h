@@ -43,6 +43,7 @@
 #ifndef MPGEMM_H
 #define MPGEMM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -82,6 +83,31 @@ mpgemm_status_t mpgemm_run(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K,
                            float alpha, const void* A, int64_t lda,
                            const void* B, int64_t ldb,
                            float beta, float* C, int64_t ldc, void* stream);
+
+/* Layout of B for mpgemm_run_ex. */
+typedef enum {
+    MPGEMM_B_ROW_MAJOR = 0,   /* (k, j) at B[k*ldb + j], ldb >= max(1, N) (as mpgemm_run) */
+    MPGEMM_B_COL_MAJOR = 1    /* (k, j) at B[j*ldb + k], ldb >= max(1, K): B stored as N rows
+                                 of K, the layout of the capstone gate's solve() */
+} mpgemm_b_layout_t;
+
+/* mpgemm_run with a choice of B layout; everything else as mpgemm_run. */
+mpgemm_status_t mpgemm_run_ex(mpgemm_handle_t h, mpgemm_b_layout_t b_layout,
+                              int64_t M, int64_t N, int64_t K,
+                              float alpha, const void* A, int64_t lda,
+                              const void* B, int64_t ldb,
+                              float beta, float* C, int64_t ldc, void* stream);
+
+/* The interface of "Day 80, Capstone 4: a tensor-core GEMM", section
+ * "Independent gate": C = A * B with A (m x k) row-major, B (k x n)
+ * column-major and C (m x n) row-major, all densely packed (lda = k,
+ * ldb = k, ldc = n), asynchronous on `stream`. The first call on a device
+ * creates a handle for that device that lives until the process exits; all
+ * calls on a device share its workspace, so calls on different streams of
+ * one device must not overlap (use mpgemm_run_ex with a handle per stream
+ * for that). */
+mpgemm_status_t mpgemm_solve(const void* a, const void* b, float* c,
+                             size_t m, size_t n, size_t k, void* stream);
 
 /* The same operation on HOST buffers: A, B (and C when beta != 0) are
  * copied to device workspace owned by the handle, the GEMM runs there and
@@ -124,7 +150,7 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
 /* What mpgemm_run would do for these arguments, computed on the host only
  * (no device work; usable without a GPU). `num_sms` stands in for the
  * device's SM count; tile_m, tile_n, max_ctas and force_staging mirror the
- * options above. The grid of the CTA-pair kernel is further capped at run
+ * options above; b_col_major selects the layout of B (ldb >= K when set). The grid of the CTA-pair kernel is further capped at run
  * time by the number of two-CTA clusters the device can hold at once. */
 typedef struct {
     int32_t quick;          /* 0 = tensor-core path, 1 = nothing to do, 2 = C = beta*C only */
@@ -149,7 +175,7 @@ mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha,
                             const void* A, int64_t lda, const void* B, int64_t ldb,
                             float beta, const float* C, int64_t ldc,
                             int32_t num_sms, int32_t tile_m, int32_t tile_n, int32_t max_ctas,
-                            int32_t force_staging, mpgemm_plan_t* out);
+                            int32_t force_staging, int32_t b_col_major, mpgemm_plan_t* out);
 
 /* C = alpha*A*B + beta*C on device memory, like mpgemm_run, for callers that
  * cannot allocate: no handle, and no device or host allocation of any kind

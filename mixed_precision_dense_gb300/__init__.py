@@ -5,11 +5,11 @@ The computation lives in the CUDA library ``libmpgemm.so`` (C ABI in
 ``include/mpgemm.h``); this package builds it (``build``) and binds it with
 ctypes (``binding``). PyTorch is only used for device memory and streams.
 """
-from .binding import (Handle, MpgemmError, Option, Plan, Status, default_handle, gemm,
-                      header_functions, load, plan, run_noalloc, status_string,
+from .binding import (BLayout, Handle, MpgemmError, Option, Plan, Status, default_handle, gemm,
+                      header_functions, load, plan, run_noalloc, solve, status_string,
                       NOALLOC_SCRATCH_BYTES)
 from .build import LIB_PATH, build
 
-__all__ = ["Handle", "MpgemmError", "Option", "Plan", "Status", "default_handle", "gemm",
-           "header_functions", "load", "plan", "run_noalloc", "status_string",
+__all__ = ["BLayout", "Handle", "MpgemmError", "Option", "Plan", "Status", "default_handle", "gemm",
+           "header_functions", "load", "plan", "run_noalloc", "solve", "status_string",
            "NOALLOC_SCRATCH_BYTES", "LIB_PATH", "build"]

@@ -37,6 +37,11 @@ class Option(enum.IntEnum):
     L2_KEEP = 8
 
 
+class BLayout(enum.IntEnum):
+    ROW_MAJOR = 0   # (k, j) at B[k*ldb + j]
+    COL_MAJOR = 1   # (k, j) at B[j*ldb + k]
+
+
 class MpgemmError(RuntimeError):
     def __init__(self, status, where):
         self.status = Status(status)
@@ -81,15 +86,18 @@ def load(path: str = LIB_PATH):
         lib.mpgemm_destroy.argtypes = [p]
         gemm_args = [p, i64, i64, i64, f32, p, i64, p, i64, f32, p, i64, p]
         lib.mpgemm_run.argtypes = gemm_args
+        lib.mpgemm_run_ex.argtypes = [p, ctypes.c_int] + gemm_args[1:]
+        lib.mpgemm_solve.argtypes = [p, p, p, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_size_t, p]
         lib.mpgemm_run_host.argtypes = gemm_args
         lib.mpgemm_run_noalloc.argtypes = gemm_args[1:]
         lib.mpgemm_sync_status.argtypes = [p, p, ctypes.POINTER(i32)]
         lib.mpgemm_set_option.argtypes = [p, ctypes.c_int, i64]
         lib.mpgemm_plan.argtypes = [i64, i64, i64, f32, p, i64, p, i64, f32, p, i64,
-                                    i32, i32, i32, i32, i32, ctypes.POINTER(Plan)]
+                                    i32, i32, i32, i32, i32, i32, ctypes.POINTER(Plan)]
         lib.mpgemm_status_string.restype = ctypes.c_char_p
         lib.mpgemm_status_string.argtypes = [ctypes.c_int]
-        for name in ("mpgemm_create", "mpgemm_destroy", "mpgemm_run", "mpgemm_run_host", "mpgemm_run_noalloc",
+        for name in ("mpgemm_create", "mpgemm_destroy", "mpgemm_run", "mpgemm_run_ex", "mpgemm_solve",
+                     "mpgemm_run_host", "mpgemm_run_noalloc",
                      "mpgemm_sync_status", "mpgemm_set_option", "mpgemm_plan"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -106,15 +114,16 @@ def _check(status, where):
 
 
 def plan(M, N, K, alpha=1.0, A=0, lda=None, B=0, ldb=None, beta=0.0, C=0, ldc=None, *,
-         num_sms=152, tile_m=0, tile_n=0, max_ctas=0, force_staging=False) -> dict:
-    """Host-only description of what mpgemm_run would do (addresses as ints)."""
+         num_sms=152, tile_m=0, tile_n=0, max_ctas=0, force_staging=False,
+         b_col_major=False) -> dict:
+    """Host-only description of what mpgemm_run(_ex) would do (addresses as ints)."""
     lda = max(K, 1) if lda is None else lda
-    ldb = max(N, 1) if ldb is None else ldb
+    ldb = max(K if b_col_major else N, 1) if ldb is None else ldb
     ldc = max(N, 1) if ldc is None else ldc
     out = Plan()
     st = load().mpgemm_plan(M, N, K, alpha, A or None, lda, B or None, ldb, beta, C or None, ldc,
                             num_sms, tile_m, tile_n, max_ctas, int(bool(force_staging)),
-                            ctypes.byref(out))
+                            int(bool(b_col_major)), ctypes.byref(out))
     _check(st, "mpgemm_plan")
     return out.as_dict()
 
@@ -129,6 +138,13 @@ def run_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> Statu
 
 
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+
+
+def solve(a, b, c, m, n, k, stream=0):
+    """mpgemm_solve: the capstone gate's interface, C = A * B with A row-major,
+    B column-major, C row-major, densely packed (device addresses as ints)."""
+    _check(load().mpgemm_solve(a or None, b or None, c or None, m, n, k, stream or None),
+           "mpgemm_solve")
 
 
 class Handle:
@@ -164,6 +180,12 @@ class Handle:
         st = self._lib.mpgemm_run(self._h, M, N, K, alpha, A or None, lda, B or None, ldb, beta,
                                   C or None, ldc, stream or None)
         _check(st, "mpgemm_run")
+
+    def run_ex(self, b_layout, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0):
+        """mpgemm_run_ex: b_layout is BLayout.ROW_MAJOR or BLayout.COL_MAJOR."""
+        st = self._lib.mpgemm_run_ex(self._h, int(b_layout), M, N, K, alpha, A or None, lda,
+                                     B or None, ldb, beta, C or None, ldc, stream or None)
+        _check(st, "mpgemm_run_ex")
 
     def run_status(self, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> Status:
         """mpgemm_run returning the status instead of raising."""

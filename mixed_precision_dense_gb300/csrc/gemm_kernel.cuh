@@ -3,8 +3,8 @@
 // Persistent CTAs walk the output in tiles. Each CTA has six warps with fixed
 // roles:
 //   warp 0      load warp: one lane issues TMA loads of A (128 x 64, K-major)
-//               and B (64 x width, N-major) into a ring of shared-memory
-//               stages; rows, columns and K past the matrix edge arrive as
+//               and B (64 x width: N-major when B is row-major, K-major when B
+//               is column-major) into a ring of shared-memory stages; rows, columns and K past the matrix edge arrive as
 //               zeros (TMA out-of-bounds fill), which replaces the padding and
 //               guarded tail loads of "Day 80, Capstone 4: a tensor-core GEMM"
 //               ("Faded practice", practice 3; "Common failures").
@@ -71,9 +71,14 @@ struct GemmParams {
 enum : int32_t { kRoleLoad = 1, kRoleMma = 2, kRoleEpilogue = 3 };
 enum : int32_t { kStatusTimeout = 1 };
 
-template <int BN_, int STAGES_, bool PAIR_>
+template <int BN_, int STAGES_, bool PAIR_, bool B_KMAJOR_ = false>
 struct TileConfig {
     static constexpr bool PAIR = PAIR_;
+    // B column-major ([N, K] rows of K): a K-major operand like A. Its 64-row
+    // boxes stack in shared memory exactly like the 64-column boxes of a
+    // row-major B, so the ring layout is the same; only the box coordinates,
+    // the shared-memory descriptor and the instruction's B-major bit differ.
+    static constexpr bool B_KMAJOR = B_KMAJOR_;
     static constexpr int CTAS = PAIR ? 2 : 1;
     static constexpr int BM = 128;                     // accumulator rows per CTA
     static constexpr int TILE_M = BM * CTAS;           // rows per output tile
@@ -335,14 +340,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                                   m0, pol_a);
                             for (int j = 0; j < n_atoms; ++j)
                                 ptx::tma_load_2d_pair(sB + stage * Cfg::B_BYTES + j * Cfg::B_ATOM_BYTES,
-                                                      &tmap_b, lead_full, n0 + j * 64, kb * BK, pol_b);
+                                                      &tmap_b, lead_full, Cfg::B_KMAJOR ? kb * BK : n0 + j * 64,
+                                                      Cfg::B_KMAJOR ? n0 + j * 64 : kb * BK, pol_b);
                         } else {
                             ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
                             ptx::tma_load_2d(sA + stage * Cfg::A_BYTES, &tmap_a, full_bar(stage), kb * BK,
                                              m0, pol_a);
                             for (int j = 0; j < n_atoms; ++j)
                                 ptx::tma_load_2d(sB + stage * Cfg::B_BYTES + j * Cfg::B_ATOM_BYTES,
-                                                 &tmap_b, full_bar(stage), n0 + j * 64, kb * BK, pol_b);
+                                                 &tmap_b, full_bar(stage), Cfg::B_KMAJOR ? kb * BK : n0 + j * 64,
+                                                 Cfg::B_KMAJOR ? n0 + j * 64 : kb * BK, pol_b);
                         }
                         if (rank == 0) {
                             armed |= 1u << stage;
@@ -374,7 +381,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const WorkItem w = work_item<BN>(p, i);
                 if (w.n0 >= p.N) continue;
                 const int32_t n_mma = PAIR ? w.width : 64 * min(w.width / 64, (p.N - w.n0 + 63) / 64);
-                const uint32_t idesc = ptx::idesc_f16_f32(Cfg::TILE_M, n_mma, false, true);
+                const uint32_t idesc = ptx::idesc_f16_f32(Cfg::TILE_M, n_mma, false, !Cfg::B_KMAJOR);
                 const int buf = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
                 if (!waiter.wait(acc_empty_bar(buf), acc_phase ^ 1u)) {
@@ -398,11 +405,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         // A: K-major, 128-byte rows, 8-row groups 1024 B apart;
                         //    the k-th 16-wide slice starts 32 bytes further.
                         const uint64_t a_desc = ptx::smem_desc_sw128(a_base + kk * 32, 16, 1024);
-                        // B: N-major, 64-column boxes B_ATOM_BYTES apart (leading
-                        //    offset), 8 K-rows of 128 B per group (stride offset);
-                        //    the k-th 16-row slice starts 16 * 128 bytes further.
+                        // B row-major: N-major, 64-column boxes B_ATOM_BYTES apart
+                        //    (leading offset), 8 K-rows of 128 B per group (stride
+                        //    offset); the k-th 16-row slice starts 16 * 128 bytes
+                        //    further. B column-major: K-major like A.
                         const uint64_t b_desc =
-                            ptx::smem_desc_sw128(b_base + kk * 2048, Cfg::B_ATOM_BYTES, 1024);
+                            Cfg::B_KMAJOR ? ptx::smem_desc_sw128(b_base + kk * 32, 16, 1024)
+                                          : ptx::smem_desc_sw128(b_base + kk * 2048, Cfg::B_ATOM_BYTES, 1024);
                         if constexpr (PAIR)
                             ptx::mma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0);
                         else

@@ -42,11 +42,16 @@ constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;
 using Cfg256 = TileConfig<256, 4, false>;   // one CTA per 128 x 256 tile
 using Cfg128 = TileConfig<128, 6, false>;   // one CTA per 128 x 128 tile
 using CfgPair = TileConfig<256, 6, true>;   // a CTA pair per 256 x 256 tile
+// the same three shapes for a column-major B (a K-major B operand)
+using Cfg256K = TileConfig<256, 4, false, true>;
+using Cfg128K = TileConfig<128, 6, false, true>;
+using CfgPairK = TileConfig<256, 6, true, true>;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 struct Options {
+    int32_t b_col_major = 0;        // per call: B(k, j) = B[j*ldb + k]
     int32_t tile_m = 0;
     int32_t tile_n = 0;
     int32_t max_ctas = 0;
@@ -63,10 +68,12 @@ bool aligned16(const void* p, int64_t ld_elems, int64_t elem_bytes) {
 }
 
 mpgemm_status_t validate(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
-                         const void* B, int64_t ldb, float beta, const void* C, int64_t ldc) {
+                         const void* B, int64_t ldb, float beta, const void* C, int64_t ldc,
+                         int32_t b_col_major = 0) {
+    const int64_t b_min = b_col_major ? K : N;   // row length of B as stored
     if (M < 0 || N < 0 || K < 0) return MPGEMM_ERR_INVALID_VALUE;
     if (M > kDimLimit || N > kDimLimit || K > kDimLimit) return MPGEMM_ERR_INVALID_VALUE;
-    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+    if (lda < (K > 1 ? K : 1) || ldb < (b_min > 1 ? b_min : 1) || ldc < (N > 1 ? N : 1))
         return MPGEMM_ERR_INVALID_VALUE;
     if (lda > kDimLimit || ldb > kDimLimit || ldc > kDimLimit) return MPGEMM_ERR_INVALID_VALUE;
     if (M > 0 && N > 0 && K > 0 && M * N > (int64_t{1} << 62) / K) return MPGEMM_ERR_INVALID_VALUE;
@@ -100,7 +107,7 @@ bool auto_pair(int64_t M, int64_t N, int32_t num_sms) {
 mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                           const void* B, int64_t ldb, float beta, const void* C, int64_t ldc,
                           int32_t num_sms, const Options& opt, mpgemm_plan_t* out) {
-    mpgemm_status_t st = validate(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
+    mpgemm_status_t st = validate(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, opt.b_col_major);
     if (st != MPGEMM_OK) return st;
     if (num_sms <= 0) return MPGEMM_ERR_INVALID_VALUE;
     mpgemm_plan_t p;
@@ -155,7 +162,8 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     p.raster_group = group;
     int64_t ws = 0;
     if (p.stage_a) ws += round_up(M * round_up(K, 8) * 2, 256);
-    if (p.stage_b) ws += round_up(K * round_up(N, 8) * 2, 256);
+    if (p.stage_b)
+        ws += opt.b_col_major ? round_up(N * round_up(K, 8) * 2, 256) : round_up(K * round_up(N, 8) * 2, 256);
     p.workspace_bytes = ws;
     *out = p;
     return MPGEMM_OK;
@@ -331,24 +339,46 @@ cudaError_t prepare_kernels() {
     cudaError_t e = set_smem_attr<Cfg256>();
     if (e == cudaSuccess) e = set_smem_attr<Cfg128>();
     if (e == cudaSuccess) e = set_smem_attr<CfgPair>();
+    if (e == cudaSuccess) e = set_smem_attr<Cfg256K>();
+    if (e == cudaSuccess) e = set_smem_attr<Cfg128K>();
+    if (e == cudaSuccess) e = set_smem_attr<CfgPairK>();
     return e;
 }
 
-cudaError_t launch_plan(const mpgemm_plan_t& plan, int max_clusters, const CUtensorMap& ta,
-                        const CUtensorMap& tb, const GemmParams& gp, cudaStream_t stream) {
+cudaError_t launch_plan(const mpgemm_plan_t& plan, bool b_col_major, int max_clusters,
+                        const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& gp,
+                        cudaStream_t stream) {
     if (plan.tile_m == 256) {
         int grid = plan.grid;
         if (max_clusters > 0 && grid > 2 * max_clusters) grid = 2 * max_clusters;
-        return launch_tc<CfgPair>(grid, ta, tb, gp, stream);
+        return b_col_major ? launch_tc<CfgPairK>(grid, ta, tb, gp, stream)
+                           : launch_tc<CfgPair>(grid, ta, tb, gp, stream);
     }
-    if (plan.tile_n == 256) return launch_tc<Cfg256>(plan.grid, ta, tb, gp, stream);
-    return launch_tc<Cfg128>(plan.grid, ta, tb, gp, stream);
+    if (plan.tile_n == 256)
+        return b_col_major ? launch_tc<Cfg256K>(plan.grid, ta, tb, gp, stream)
+                           : launch_tc<Cfg256>(plan.grid, ta, tb, gp, stream);
+    return b_col_major ? launch_tc<Cfg128K>(plan.grid, ta, tb, gp, stream)
+                       : launch_tc<Cfg128>(plan.grid, ta, tb, gp, stream);
 }
 
 }  // namespace
 }  // namespace mpgemm
 
 using namespace mpgemm;
+
+struct mpgemm_handle_st;
+
+namespace {
+// mpgemm_solve's handle per device, created on the first call on that device
+// and kept until the process exits.
+constexpr int kSolveMaxDevices = 64;
+struct SolveDevice {
+    std::once_flag once;
+    mpgemm_status_t status = MPGEMM_ERR_CUDA;
+    mpgemm_handle_st* handle = nullptr;
+};
+SolveDevice g_solve_devices[kSolveMaxDevices];
+}  // namespace
 
 struct mpgemm_handle_st {
     int device = 0;
@@ -416,7 +446,8 @@ const char* mpgemm_status_string(mpgemm_status_t s) {
 mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
                             int64_t lda, const void* B, int64_t ldb, float beta, const float* C,
                             int64_t ldc, int32_t num_sms, int32_t tile_m, int32_t tile_n,
-                            int32_t max_ctas, int32_t force_staging, mpgemm_plan_t* out) {
+                            int32_t max_ctas, int32_t force_staging, int32_t b_col_major,
+                            mpgemm_plan_t* out) {
     if (!out) return MPGEMM_ERR_INVALID_VALUE;
     if (tile_m != 0 && tile_m != 128 && tile_m != 256) return MPGEMM_ERR_INVALID_VALUE;
     if (tile_n != 0 && tile_n != 128 && tile_n != 256) return MPGEMM_ERR_INVALID_VALUE;
@@ -425,6 +456,7 @@ mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const 
     opt.tile_m = tile_m;
     opt.tile_n = tile_n;
     opt.max_ctas = max_ctas;
+    opt.b_col_major = b_col_major ? 1 : 0;
     opt.force_staging = force_staging ? 1 : 0;
     return make_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, num_sms, opt, out);
 }
@@ -524,14 +556,17 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
     return MPGEMM_ERR_INVALID_VALUE;
 }
 
-mpgemm_status_t mpgemm_run(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha,
-                           const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
-                           float* C, int64_t ldc, void* stream_ptr) {
+mpgemm_status_t mpgemm_run_ex(mpgemm_handle_t h, mpgemm_b_layout_t b_layout, int64_t M, int64_t N,
+                              int64_t K, float alpha, const void* A, int64_t lda, const void* B,
+                              int64_t ldb, float beta, float* C, int64_t ldc, void* stream_ptr) {
     if (!h) return MPGEMM_ERR_INVALID_VALUE;
+    if (b_layout != MPGEMM_B_ROW_MAJOR && b_layout != MPGEMM_B_COL_MAJOR) return MPGEMM_ERR_INVALID_VALUE;
+    const bool b_col = (b_layout == MPGEMM_B_COL_MAJOR);
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     mpgemm_plan_t plan;
     Options opt = h->opt;
     opt.pair_units = h->max_clusters;
+    opt.b_col_major = b_col ? 1 : 0;
     mpgemm_status_t st = make_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, h->num_sms, opt, &plan);
     if (st != MPGEMM_OK) return st;
     if (take_device_report(h, nullptr) != MPGEMM_OK) return MPGEMM_ERR_DEVICE_TIMEOUT;
@@ -556,9 +591,12 @@ mpgemm_status_t mpgemm_run(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K, f
             ws += round_up(M * lda_use * 2, 256);
         }
         if (plan.stage_b) {
-            ldb_use = round_up(N, 8);
-            stage_rows_u16<<<grid_for(K * ceil_div(N, 8), h->num_sms), 256, 0, stream>>>(
-                static_cast<const uint16_t*>(B), ldb, reinterpret_cast<uint16_t*>(ws), ldb_use, K, N);
+            // B as stored: K rows of N (row-major) or N rows of K (column-major)
+            const int64_t b_rows = b_col ? N : K, b_cols = b_col ? K : N;
+            ldb_use = round_up(b_cols, 8);
+            stage_rows_u16<<<grid_for(b_rows * ceil_div(b_cols, 8), h->num_sms), 256, 0, stream>>>(
+                static_cast<const uint16_t*>(B), ldb, reinterpret_cast<uint16_t*>(ws), ldb_use, b_rows,
+                b_cols);
             b_use = ws;
         }
         if (cudaGetLastError() != cudaSuccess) return MPGEMM_ERR_LAUNCH;
@@ -566,7 +604,8 @@ mpgemm_status_t mpgemm_run(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K, f
 
     CUtensorMap ta, tb;
     if (!encode_f16(&ta, a_use, M, K, lda_use, 64, 128) ||
-        !encode_f16(&tb, b_use, K, N, ldb_use, 64, 64))
+        !(b_col ? encode_f16(&tb, b_use, N, K, ldb_use, 64, 64)
+                : encode_f16(&tb, b_use, K, N, ldb_use, 64, 64)))
         return MPGEMM_ERR_CUDA;
 
     GemmParams gp;
@@ -588,11 +627,18 @@ mpgemm_status_t mpgemm_run(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K, f
     gp.wait_limit_ns = h->opt.wait_limit_ns;
     gp.test_stall = h->opt.test_stall;
     gp.keep_a = keep_a_operand(plan, h->opt.l2_keep);
-    if (launch_plan(plan, h->max_clusters, ta, tb, gp, stream) != cudaSuccess) {
+    if (launch_plan(plan, b_col, h->max_clusters, ta, tb, gp, stream) != cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;
     }
     return MPGEMM_OK;
+}
+
+mpgemm_status_t mpgemm_run(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha,
+                           const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
+                           float* C, int64_t ldc, void* stream_ptr) {
+    return mpgemm_run_ex(h, MPGEMM_B_ROW_MAJOR, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                         stream_ptr);
 }
 
 mpgemm_status_t mpgemm_run_host(mpgemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha,
@@ -651,6 +697,25 @@ mpgemm_status_t mpgemm_run_host(mpgemm_handle_t h, int64_t M, int64_t N, int64_t
         return MPGEMM_ERR_LAUNCH;
     }
     return MPGEMM_OK;
+}
+
+mpgemm_status_t mpgemm_solve(const void* a, const void* b, float* c, size_t m, size_t n, size_t k,
+                             void* stream) {
+    if (m > static_cast<size_t>(kDimLimit) || n > static_cast<size_t>(kDimLimit) ||
+        k > static_cast<size_t>(kDimLimit))
+        return MPGEMM_ERR_INVALID_VALUE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MPGEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (dev < 0 || dev >= kSolveMaxDevices) return MPGEMM_ERR_CUDA;
+    SolveDevice& d = g_solve_devices[dev];
+    std::call_once(d.once, [&d] { d.status = mpgemm_create(&d.handle); });
+    if (d.status != MPGEMM_OK) return d.status;
+    const int64_t M = static_cast<int64_t>(m), N = static_cast<int64_t>(n), K = static_cast<int64_t>(k);
+    return mpgemm_run_ex(d.handle, MPGEMM_B_COL_MAJOR, M, N, K, 1.0f, a, K > 1 ? K : 1, b,
+                         K > 1 ? K : 1, 0.0f, c, N > 1 ? N : 1, stream);
 }
 
 mpgemm_status_t mpgemm_sync_status(mpgemm_handle_t h, void* stream, int32_t info[4]) {
@@ -797,7 +862,7 @@ extern "C" mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K, f
     gp.wait_limit_ns = opt.wait_limit_ns;
     gp.test_stall = 0;
     gp.keep_a = keep_a_operand(plan, 0);
-    if (launch_plan(plan, d.max_clusters, ta, tb, gp, stream) != cudaSuccess) {
+    if (launch_plan(plan, false, d.max_clusters, ta, tb, gp, stream) != cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;
     }

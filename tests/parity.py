@@ -38,7 +38,7 @@ def device_operands(ops: workloads.Operands, *, a_offset=0, b_offset=0, c_offset
         return buf, start
 
     a_buf, a_start = place(ops.A, M, ops.lda, a_offset, 0.0)
-    b_buf, b_start = place(ops.B, K, ops.ldb, b_offset, 0.0)
+    b_buf, b_start = place(ops.B, N if ops.b_col_major else K, ops.ldb, b_offset, 0.0)
     c_src = ops.C
     if ops.beta == 0 and poison:
         c_src = torch.full_like(ops.C, float("nan"))
@@ -53,8 +53,13 @@ def run_gpu(handle, ops, *, a_offset=0, b_offset=0, c_offset=0, stream=None):
     d = device_operands(ops, a_offset=a_offset, b_offset=b_offset, c_offset=c_offset)
     s = torch.cuda.current_stream() if stream is None else stream
     with torch.cuda.stream(s):
-        handle.run(ops.M, ops.N, ops.K, ops.alpha, d["a_ptr"], ops.lda, d["b_ptr"], ops.ldb,
-                   ops.beta, d["c_ptr"], ops.ldc, s.cuda_stream)
+        if ops.b_col_major:
+            from mixed_precision_dense_gb300 import BLayout
+            handle.run_ex(BLayout.COL_MAJOR, ops.M, ops.N, ops.K, ops.alpha, d["a_ptr"], ops.lda,
+                          d["b_ptr"], ops.ldb, ops.beta, d["c_ptr"], ops.ldc, s.cuda_stream)
+        else:
+            handle.run(ops.M, ops.N, ops.K, ops.alpha, d["a_ptr"], ops.lda, d["b_ptr"], ops.ldb,
+                       ops.beta, d["c_ptr"], ops.ldc, s.cuda_stream)
     s.synchronize()
     st, info = handle.sync_status(s.cuda_stream)
     assert st == 0, f"device reported {st} {info}"
@@ -85,9 +90,10 @@ def check_guards(d, ops, buf, full):
 def reference(ops, I=None, J=None):
     A, B, C = ops.bits("A"), ops.bits("B"), ops.bits("C")
     if I is None:
-        return oracle.gemm(ops.M, ops.N, ops.K, ops.alpha, A, ops.lda, B, ops.ldb, ops.beta, C, ops.ldc)
+        return oracle.gemm(ops.M, ops.N, ops.K, ops.alpha, A, ops.lda, B, ops.ldb, ops.beta, C, ops.ldc,
+                           b_col_major=ops.b_col_major)
     return oracle.elements(ops.M, ops.N, ops.K, ops.alpha, A, ops.lda, B, ops.ldb, ops.beta, C,
-                           ops.ldc, I, J)
+                           ops.ldc, I, J, b_col_major=ops.b_col_major)
 
 
 def assert_close(got, ref, S, what=""):

@@ -74,6 +74,19 @@ def test_invalid_arguments(kw):
     assert e.value.status == Status.ERR_INVALID_VALUE
 
 
+def test_column_major_b_validation():
+    # column-major B: ldb counts K (rows of B are columns of the product)
+    p = _plan(M=64, N=300, K=40, lda=40, ldb=40, ldc=300, b_col_major=True)
+    assert p["quick"] == 0 and p["stage_b"] == 0
+    with pytest.raises(mp.MpgemmError):
+        _plan(M=64, N=300, K=40, lda=40, ldb=39, ldc=300, b_col_major=True)
+    with pytest.raises(mp.MpgemmError):          # the same ldb is too small for row-major B
+        _plan(M=64, N=300, K=40, lda=40, ldb=40, ldc=300)
+    p = _plan(M=64, N=300, K=617, lda=617, ldb=617, ldc=300, b_col_major=True)
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert p["stage_b"] == 1 and p["workspace_bytes"] == r256(64 * 624 * 2) + r256(300 * 624 * 2)
+
+
 def test_quick_returns():
     assert _plan(M=0, A=0, B=0, C=0)["quick"] == 1
     assert _plan(N=0, ldb=1, ldc=1, A=0, B=0, C=0)["quick"] == 1

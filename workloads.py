@@ -101,7 +101,8 @@ def _padded(values: torch.Tensor, rows: int, cols: int, ld: int, fill) -> torch.
 
 @dataclasses.dataclass
 class Operands:
-    """Host operands: A [M, lda] fp16, B [K, ldb] fp16, C [M, ldc] fp32 (row-major)."""
+    """Host operands: A [M, lda] fp16, B [K, ldb] fp16 (or [N, ldb] when
+    b_col_major: row j holds column j of B), C [M, ldc] fp32."""
     M: int
     N: int
     K: int
@@ -113,6 +114,7 @@ class Operands:
     A: torch.Tensor
     B: torch.Tensor
     C: torch.Tensor
+    b_col_major: bool = False
 
     def bits(self, name: str) -> np.ndarray:
         """Flat numpy view of an operand (uint16 bit patterns for A and B)."""
@@ -125,10 +127,11 @@ class Operands:
 def make_operands(M: int, N: int, K: int, *, lda: Optional[int] = None, ldb: Optional[int] = None,
                   ldc: Optional[int] = None, alpha: float = 1.0, beta: float = 0.0,
                   dist: str = "uniform", dist_b: Optional[str] = None, c_dist: str = "zeros",
-                  seed: int = 0) -> Operands:
-    """Seeded operands; A uses ``seed``, B ``seed + 1``, C ``seed + 2``."""
+                  seed: int = 0, b_col_major: bool = False) -> Operands:
+    """Seeded operands; A uses ``seed``, B ``seed + 1``, C ``seed + 2``. With
+    ``b_col_major`` the same values of B are stored column by column."""
     lda = max(K, 1) if lda is None else lda
-    ldb = max(N, 1) if ldb is None else ldb
+    ldb = max(K if b_col_major else N, 1) if ldb is None else ldb
     ldc = max(N, 1) if ldc is None else ldc
     ga = torch.Generator().manual_seed(seed)
     gb = torch.Generator().manual_seed(seed + 1)
@@ -138,9 +141,9 @@ def make_operands(M: int, N: int, K: int, *, lda: Optional[int] = None, ldb: Opt
     c = _draw(gc, (M, N), c_dist)
     nan16 = torch.tensor([FP16_NAN_BITS], dtype=torch.int16).view(torch.float16).item()
     A = _padded(a, M, K, lda, nan16)
-    B = _padded(b, K, N, ldb, nan16)
+    B = _padded(b.t().contiguous(), N, K, ldb, nan16) if b_col_major else _padded(b, K, N, ldb, nan16)
     C = _padded(c, M, N, ldc, float("nan"))
-    return Operands(M, N, K, lda, ldb, ldc, alpha, beta, A, B, C)
+    return Operands(M, N, K, lda, ldb, ldc, alpha, beta, A, B, C, b_col_major)
 
 
 def workload_operands(index: int) -> Operands:
