@@ -495,6 +495,108 @@ def run_e2e(handle, w, ops, stream, device, args):
                    "alternating, host wall clock"}
 
 
+# ----------------------------------------------------------------------------- the capstone gate
+
+GATE_CASES = [  # "Day 80, Capstone 4: a tensor-core GEMM", "Independent gate"
+    ("unit", 16, 16, 16, "int", "bitwise"),
+    ("onefrag", 16, 8, 16, "int", "bitwise"),
+    ("small", 128, 128, 128, "uniform", "tolerance"),
+    ("odd", 611, 613, 617, "uniform", "tolerance"),
+    ("skinny", 4096, 16, 4096, "uniform", "tolerance"),
+    ("square", 1024, 1024, 1024, "normal", "tolerance"),
+    ("adversarial", 256, 256, 256, "edge", "tolerance"),
+    ("perf", 4096, 4096, 4096, "uniform", "sampled"),
+]
+
+
+def run_gate(args):
+    """The gate's eight cases through mpgemm_solve (A row-major, B column-major,
+    C row-major): every case checked against the CPU oracle (bit for bit for
+    the exact small integers), then timed as the median of 5 runs x 20 calls
+    (the protocol of the "02_mixed_precision_gemm" README), with cuBLAS GemmEx
+    (FP16 in, FP32 out, COMPUTE_32F) on the same buffers and the coefficient of
+    variation of the perf case's runs. Prints a markdown report."""
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    import mixed_precision_dense_gb300 as mp
+    import oracle
+    mp.build()
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream(dev)
+    lib = _cublas_lib()
+    cub = ctypes.c_void_p()
+    if lib is not None and lib.cublasCreate_v2(ctypes.byref(cub)) == 0:
+        lib.cublasSetStream_v2(cub, ctypes.c_void_p(stream.cuda_stream))
+    else:
+        lib = None
+    rows = []
+    for name, m, n, k, inputs, check in GATE_CASES:
+        if inputs == "int":
+            ops = workloads.make_operands(m, n, k, dist="int3", dist_b="int2", seed=500 + m + n + k,
+                                          b_col_major=True)
+        else:
+            ops = workloads.make_operands(m, n, k, dist=inputs, seed=500 + m + n + k, b_col_major=True)
+        A = ops.A.to(dev)
+        B = ops.B.to(dev)
+        C = torch.full((m, n), float("nan"), dtype=torch.float32, device=dev)
+
+        def ours():
+            mp.solve(A.data_ptr(), B.data_ptr(), C.data_ptr(), m, n, k, stream.cuda_stream)
+
+        ours()
+        stream.synchronize()
+        got = C.cpu().double().numpy()
+        A_bits, B_bits = ops.bits("A"), ops.bits("B")
+        if check == "sampled":
+            I, J = workloads.sample_indices(m, n, 20000, seed=501)
+            ref, S = oracle.elements(m, n, k, 1.0, A_bits, k, B_bits, k, 0.0, None, n, I, J,
+                                     b_col_major=True)
+            err = float(np.max(np.abs(got[I, J] - ref) / oracle.tolerance(S)))
+            verdict = f"max err/tol {err:.2e} on {I.size} elements" + (" PASS" if err <= 1 else " FAIL")
+        else:
+            ref, S = oracle.gemm(m, n, k, 1.0, A_bits, k, B_bits, k, 0.0, b_col_major=True)
+            if check == "bitwise":
+                ok = bool(np.array_equal(got, ref))
+                verdict = "bit for bit " + ("PASS" if ok else "FAIL")
+            else:
+                err = float(np.max(np.abs(got - ref) / oracle.tolerance(S)))
+                verdict = f"max err/tol {err:.2e}" + (" PASS" if err <= 1 else " FAIL")
+        runs = []
+        for _ in range(3):
+            ours()
+        for _ in range(5):
+            runs.append(timed_loop(ours, stream, 20))
+        ours_ms = statistics.median(runs)
+        cv = statistics.pstdev(runs) / statistics.mean(runs)
+        cub_ms = None
+        if lib is not None:
+            alpha, beta = ctypes.c_float(1.0), ctypes.c_float(0.0)
+
+            def theirs():
+                lib.cublasGemmEx(cub, 1, 0, n, m, k, ctypes.byref(alpha), ctypes.c_void_p(B.data_ptr()), 2, k,
+                                 ctypes.c_void_p(A.data_ptr()), 2, k, ctypes.byref(beta),
+                                 ctypes.c_void_p(C.data_ptr()), 0, n, 68, -1)
+
+            for _ in range(3):
+                theirs()
+            cub_ms = statistics.median(timed_loop(theirs, stream, 20) for _ in range(5))
+        rows.append((name, m, n, k, check, verdict, ours_ms, cub_ms, cv))
+    if lib is not None:
+        lib.cublasDestroy_v2(cub)
+    print("| case | m, n, k | check | result | mpgemm_solve (us) | TFLOP/s | cuBLAS GemmEx (us) | % of cuBLAS | CV of 5 runs |")
+    print("|---|---|---|---|---|---|---|---|---|")
+    for name, m, n, k, check, verdict, ours_ms, cub_ms, cv in rows:
+        tf = gemm_flops(m, n, k) / (ours_ms / 1e3) / 1e12
+        pct = f"{100 * cub_ms / ours_ms:.1f} %" if cub_ms else "n/a"
+        cubs = f"{cub_ms * 1e3:.2f}" if cub_ms else "n/a"
+        print(f"| {name} | {m}, {n}, {k} | {check} | {verdict} | {ours_ms * 1e3:.2f} | {tf:.1f} | {cubs} | {pct} | {100 * cv:.2f} % |")
+    print(f"\nGPU: {torch.cuda.get_device_name(dev)}; times are medians of 5 runs x 20 back-to-back calls; "
+          "tolerance |err| <= 1e-3 * sum_k|A_ik B_kj| + 1e-5.")
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -552,9 +654,13 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-check", action="store_true")
     ap.add_argument("--no-cublas", action="store_true")
+    ap.add_argument("--gate", action="store_true",
+                    help="run the capstone gate's eight cases and print a report instead")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least three warm-up steps, whatever was asked
-    if args.impl == "reference":
+    if args.gate:
+        run_gate(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
