@@ -138,9 +138,14 @@ typedef enum {
                                      kernel's bounded waits expire and a timeout is reported */
     MPGEMM_OPT_TILE_M = 7,        /* 0 = automatic (default); 128 = one CTA per tile;
                                      256 = a cluster of two CTAs per 256 x 256 tile */
-    MPGEMM_OPT_L2_KEEP = 8        /* L2 hints for the operand loads: 0 = automatic (default,
+    MPGEMM_OPT_L2_KEEP = 8,       /* L2 hints for the operand loads: 0 = automatic (default,
                                      keep the operand more tiles re-read), 1 = keep A,
                                      2 = keep B */
+    MPGEMM_OPT_SPLIT_K = 9        /* 0 = automatic (default): when the output tiles cannot occupy
+                                     half of the SMs, each tile's K range is cut into slices
+                                     whose partial products are added into C (after C = beta*C),
+                                     so results may differ in the last bits from run to run;
+                                     1 = never; n in 2..64 = n slices (one-CTA tiles only) */
 } mpgemm_option_t;
 
 /* Set an option. Unknown options or out-of-range values return
@@ -168,7 +173,9 @@ typedef struct {
     int32_t last_k_valid;   /* valid K columns in the last pipeline stage */
     int64_t workspace_bytes;/* device staging bytes the call needs */
     int32_t split_tiles;    /* tiles of the last partial wave done as two half-width items */
-    int64_t items;          /* work items the persistent CTAs walk: tiles + split_tiles */
+    int64_t items;          /* work items the persistent CTAs walk: tiles + split_tiles, or
+                               tiles * k_splits */
+    int32_t k_splits;       /* slices of K per tile (1 = no split-K) */
 } mpgemm_plan_t;
 
 mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha,

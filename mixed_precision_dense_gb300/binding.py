@@ -35,6 +35,7 @@ class Option(enum.IntEnum):
     TEST_STALL = 6
     TILE_M = 7
     L2_KEEP = 8
+    SPLIT_K = 9
 
 
 class BLayout(enum.IntEnum):
@@ -55,7 +56,8 @@ class Plan(ctypes.Structure):
                 ("k_blocks", ctypes.c_int32), ("tiles", ctypes.c_int64), ("grid", ctypes.c_int32),
                 ("raster_group", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("last_k_valid", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
-                ("split_tiles", ctypes.c_int32), ("items", ctypes.c_int64)]
+                ("split_tiles", ctypes.c_int32), ("items", ctypes.c_int64),
+                ("k_splits", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -57,7 +57,9 @@ struct GemmParams {
     int32_t m_tiles, n_tiles, k_blocks;   // tiles counted in units of the kernel's tile
     int32_t tiles;
     int32_t tail_start;     // tiles from here on (raster order) are done as two half-width items
-    int32_t items;          // work items: tail_start + 2 * (tiles - tail_start)
+    int32_t items;          // work items: tail_start + 2 * (tiles - tail_start), or tiles * k_splits
+    int32_t k_splits;       // > 1: each tile's K range is cut into k_splits slices whose partial
+    int32_t kb_per_split;   //      products are added into C (which already holds beta * C)
     int32_t raster_group;
     float alpha, beta;
     float* C;
@@ -123,16 +125,32 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int32_t t, int3
 }
 
 // Work item i of the persistent walk: a whole tile of width BN, or, past
-// tail_start, one half (BN / 2 columns) of a tile. Splitting the last partial
-// wave of tiles in halves lets it finish in half the time.
+// tail_start, one half (BN / 2 columns) of a tile (splitting the last partial
+// wave of tiles in halves lets it finish in half the time), or, with
+// k_splits > 1, one slice of a tile's K range (when there are too few tiles
+// to occupy the GPU).
 struct WorkItem {
     int32_t mb;      // tile row block
     int32_t n0;      // first column
     int32_t width;   // columns: BN or BN / 2
+    int32_t kb0, kb1;  // k-blocks [kb0, kb1)
 };
 
 template <int BN>
 __device__ __forceinline__ WorkItem work_item(const GemmParams& p, int32_t i) {
+    if (p.k_splits > 1) {
+        const int32_t t = i / p.k_splits;
+        const int32_t slice = i - t * p.k_splits;
+        int32_t mb, nb;
+        tile_coords(p, t, mb, nb);
+        WorkItem w;
+        w.mb = mb;
+        w.n0 = nb * BN;
+        w.width = BN;
+        w.kb0 = slice * p.kb_per_split;
+        w.kb1 = min(w.kb0 + p.kb_per_split, p.k_blocks);
+        return w;
+    }
     int32_t t = i, half = -1;
     if (i >= p.tail_start) {
         const int32_t h = i - p.tail_start;
@@ -145,6 +163,8 @@ __device__ __forceinline__ WorkItem work_item(const GemmParams& p, int32_t i) {
     w.mb = mb;
     w.n0 = nb * BN + (half > 0 ? BN / 2 : 0);
     w.width = half < 0 ? BN : BN / 2;
+    w.kb0 = 0;
+    w.kb1 = p.k_blocks;
     return w;
 }
 
@@ -206,7 +226,8 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, uint32_t t_row, 
                                           int32_t n0, int32_t width, float* buf, int lane,
                                           float (&c_cur)[32]) {
     const float alpha = p.alpha, beta = p.beta;
-    const bool read_c = (beta != 0.0f);
+    const bool split = p.k_splits > 1;        // add the partial product into C
+    const bool read_c = (beta != 0.0f) && !split;
     const int32_t rows = min(32, p.M - m0);
     const int32_t chunks = (min(width, p.N - n0) + 31) / 32;
     const float* c_rows = p.C + static_cast<int64_t>(m0) * p.ldc;
@@ -228,6 +249,10 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, uint32_t t_row, 
                 for (int rr = 0; rr < 32; ++rr)
                     if (rr < rows)
                         cp[static_cast<int64_t>(rr) * p.ldc] = fmaf(beta, c_cur[rr], buf[rr * PITCH + lane]);
+            } else if (split) {
+#pragma unroll
+                for (int rr = 0; rr < 32; ++rr)
+                    if (rr < rows) atomicAdd(cp + static_cast<int64_t>(rr) * p.ldc, buf[rr * PITCH + lane]);
             } else {
 #pragma unroll
                 for (int rr = 0; rr < 32; ++rr)
@@ -327,7 +352,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     // single: only the boxes that hold valid columns; pair: all boxes
                     const int32_t n_atoms = PAIR ? b_cols / 64 : min(w.width / 64, (p.N - w.n0 + 63) / 64);
                     const uint32_t bytes = (Cfg::A_BYTES + n_atoms * Cfg::B_ATOM_BYTES) * Cfg::CTAS;
-                    for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+                    for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                         if (!waiter.wait(empty_bar(stage), phase ^ 1u)) {
                             waiter.fail(kRoleLoad, kb);
                             ok = false;
@@ -391,7 +416,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+                for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!waiter.wait(full_bar(stage), phase)) {
                         waiter.fail(kRoleMma, kb);
                         ok = false;
@@ -413,9 +438,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             Cfg::B_KMAJOR ? ptx::smem_desc_sw128(b_base + kk * 32, 16, 1024)
                                           : ptx::smem_desc_sw128(b_base + kk * 2048, Cfg::B_ATOM_BYTES, 1024);
                         if constexpr (PAIR)
-                            ptx::mma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0);
+                            ptx::mma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb != w.kb0) || kk != 0);
                         else
-                            ptx::mma_f16(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0);
+                            ptx::mma_f16(d_tmem, a_desc, b_desc, idesc, (kb != w.kb0) || kk != 0);
                     }
                     issued = true;
                     if constexpr (PAIR)
@@ -447,7 +472,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;             // tensor-memory lanes 32*quarter ..
         float* buf = epi_buf + (warp - 2) * 32 * Cfg::EPI_PITCH;
-        const bool read_c = (p.beta != 0.0f);
+        const bool read_c = (p.beta != 0.0f) && p.k_splits <= 1;
         int32_t local = 0;
         for (int32_t i = first_item; i < p.items; i += item_step) {
             const WorkItem w = work_item<BN>(p, i);

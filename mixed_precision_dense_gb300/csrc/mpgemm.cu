@@ -58,6 +58,7 @@ struct Options {
     int32_t force_staging = 0;
     int32_t raster_group = 0;
     int32_t l2_keep = 0;            // 0 automatic, 1 keep A, 2 keep B
+    int32_t split_k = 0;            // 0 automatic, 1 never, n >= 2: n slices of K per tile
     int32_t pair_units = 0;         // CTA pairs resident at once (0: num_sms / 2)
     int32_t test_stall = 0;
     uint64_t wait_limit_ns = kDefaultWaitLimitNs;
@@ -149,14 +150,38 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     int64_t units = num_sms / per_unit;
     if (pair && opt.pair_units > 0) units = std::min<int64_t>(units, opt.pair_units);
     if (opt.max_ctas > 0) units = std::min<int64_t>(units, std::max<int64_t>(1, opt.max_ctas / per_unit));
-    units = std::max<int64_t>(1, std::min<int64_t>(units, p.tiles));
+    units = std::max<int64_t>(1, units);
+    // Split-K (single-CTA tiles): when the tiles occupy at most a quarter of
+    // the CTAs and K is long (32 k-blocks or more), cut each tile's K range
+    // into slices of at least eight k-blocks; the slices' partial products are
+    // added into C. Shorter problems lose more to the extra pass over C and
+    // the atomic adds than they gain from the extra SMs.
+    int64_t splits = 1;
+    if (!pair && opt.split_k != 1) {
+        if (opt.split_k >= 2)
+            splits = opt.split_k;
+        else if (p.tiles * 4 <= units && k_blocks >= 32)
+            splits = std::min<int64_t>(k_blocks / 8, units / p.tiles);
+        splits = std::max<int64_t>(1, std::min<int64_t>(splits, k_blocks));
+        if (splits > 1) splits = ceil_div(k_blocks, ceil_div(k_blocks, splits));  // no empty slice
+    }
+    p.k_splits = static_cast<int32_t>(splits);
+    if (splits > 1) {
+        p.split_tiles = 0;
+        p.items = p.tiles * splits;
+    } else {
+        // If the last wave of tiles would keep at most half of the CTAs (pairs)
+        // busy, do those tiles as two half-width items each: the wave then
+        // finishes in half the time.
+        const int64_t tile_units = std::min<int64_t>(units, p.tiles);
+        const int64_t rem = p.tiles % tile_units;
+        p.split_tiles =
+            (p.tiles > tile_units && rem > 0 && 2 * rem <= tile_units) ? static_cast<int32_t>(rem) : 0;
+        p.items = p.tiles + p.split_tiles;
+    }
+    if (p.items > kDimLimit) return MPGEMM_ERR_INVALID_VALUE;
+    units = std::min<int64_t>(units, p.items);
     p.grid = static_cast<int32_t>(units * per_unit);
-    // If the last wave of tiles would keep at most half of the CTAs (pairs)
-    // busy, do those tiles as two half-width items each: the wave then
-    // finishes in half the time.
-    const int64_t rem = p.tiles % units;
-    p.split_tiles = (p.tiles > units && rem > 0 && 2 * rem <= units) ? static_cast<int32_t>(rem) : 0;
-    p.items = p.tiles + p.split_tiles;
     int32_t group = opt.raster_group ? opt.raster_group : 16;
     if (group > p.m_tiles) group = p.m_tiles;
     p.raster_group = group;
@@ -345,9 +370,43 @@ cudaError_t prepare_kernels() {
     return e;
 }
 
+GemmParams make_params(const mpgemm_plan_t& plan, int64_t M, int64_t N, int64_t K, float alpha,
+                       float beta, float* C, int64_t ldc, int32_t* status, uint64_t wait_limit_ns,
+                       int32_t test_stall, int32_t keep_a) {
+    GemmParams gp;
+    gp.M = static_cast<int32_t>(M);
+    gp.N = static_cast<int32_t>(N);
+    gp.K = static_cast<int32_t>(K);
+    gp.m_tiles = plan.m_tiles;
+    gp.n_tiles = plan.n_tiles;
+    gp.k_blocks = plan.k_blocks;
+    gp.tiles = static_cast<int32_t>(plan.tiles);
+    gp.tail_start = static_cast<int32_t>(plan.tiles - plan.split_tiles);
+    gp.items = static_cast<int32_t>(plan.items);
+    gp.k_splits = plan.k_splits;
+    gp.kb_per_split = static_cast<int32_t>(ceil_div(plan.k_blocks, plan.k_splits));
+    gp.raster_group = plan.raster_group;
+    gp.alpha = alpha;
+    gp.beta = beta;
+    gp.C = C;
+    gp.ldc = ldc;
+    gp.status = status;
+    gp.wait_limit_ns = wait_limit_ns;
+    gp.test_stall = test_stall;
+    gp.keep_a = keep_a;
+    return gp;
+}
+
 cudaError_t launch_plan(const mpgemm_plan_t& plan, bool b_col_major, int max_clusters,
                         const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& gp,
                         cudaStream_t stream) {
+    if (plan.k_splits > 1 && gp.beta != 1.0f) {
+        // the slices add into C: apply beta (or clear C) once, first
+        scale_c<<<grid_for(static_cast<int64_t>(gp.M) * gp.N, plan.grid), 256, 0, stream>>>(
+            gp.C, gp.ldc, gp.M, gp.N, gp.beta);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     if (plan.tile_m == 256) {
         int grid = plan.grid;
         if (max_clusters > 0 && grid > 2 * max_clusters) grid = 2 * max_clusters;
@@ -544,6 +603,10 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
             if (value < 0 || value > 2) return MPGEMM_ERR_INVALID_VALUE;
             h->opt.l2_keep = static_cast<int32_t>(value);
             return MPGEMM_OK;
+        case MPGEMM_OPT_SPLIT_K:
+            if (value < 0 || value > 64) return MPGEMM_ERR_INVALID_VALUE;
+            h->opt.split_k = static_cast<int32_t>(value);
+            return MPGEMM_OK;
         case MPGEMM_OPT_TILE_M:
             if (value != 0 && value != 128 && value != 256) return MPGEMM_ERR_INVALID_VALUE;
             h->opt.tile_m = static_cast<int32_t>(value);
@@ -608,25 +671,9 @@ mpgemm_status_t mpgemm_run_ex(mpgemm_handle_t h, mpgemm_b_layout_t b_layout, int
                 : encode_f16(&tb, b_use, K, N, ldb_use, 64, 64)))
         return MPGEMM_ERR_CUDA;
 
-    GemmParams gp;
-    gp.M = static_cast<int32_t>(M);
-    gp.N = static_cast<int32_t>(N);
-    gp.K = static_cast<int32_t>(K);
-    gp.m_tiles = plan.m_tiles;
-    gp.n_tiles = plan.n_tiles;
-    gp.k_blocks = plan.k_blocks;
-    gp.tiles = static_cast<int32_t>(plan.tiles);
-    gp.tail_start = static_cast<int32_t>(plan.tiles - plan.split_tiles);
-    gp.items = static_cast<int32_t>(plan.items);
-    gp.raster_group = plan.raster_group;
-    gp.alpha = alpha;
-    gp.beta = beta;
-    gp.C = C;
-    gp.ldc = ldc;
-    gp.status = h->status_dev;
-    gp.wait_limit_ns = h->opt.wait_limit_ns;
-    gp.test_stall = h->opt.test_stall;
-    gp.keep_a = keep_a_operand(plan, h->opt.l2_keep);
+    const GemmParams gp = make_params(plan, M, N, K, alpha, beta, C, ldc, h->status_dev,
+                                      h->opt.wait_limit_ns, h->opt.test_stall,
+                                      keep_a_operand(plan, h->opt.l2_keep));
     if (launch_plan(plan, b_col, h->max_clusters, ta, tb, gp, stream) != cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;
@@ -843,25 +890,8 @@ extern "C" mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K, f
     if (!encode_f16(&ta, a_use, M, K, lda_use, 64, 128) ||
         !encode_f16(&tb, b_use, K, N, ldb_use, 64, 64))
         return MPGEMM_ERR_CUDA;
-    GemmParams gp;
-    gp.M = static_cast<int32_t>(M);
-    gp.N = static_cast<int32_t>(N);
-    gp.K = static_cast<int32_t>(K);
-    gp.m_tiles = plan.m_tiles;
-    gp.n_tiles = plan.n_tiles;
-    gp.k_blocks = plan.k_blocks;
-    gp.tiles = static_cast<int32_t>(plan.tiles);
-    gp.tail_start = static_cast<int32_t>(plan.tiles - plan.split_tiles);
-    gp.items = static_cast<int32_t>(plan.items);
-    gp.raster_group = plan.raster_group;
-    gp.alpha = alpha;
-    gp.beta = beta;
-    gp.C = C;
-    gp.ldc = ldc;
-    gp.status = status;
-    gp.wait_limit_ns = opt.wait_limit_ns;
-    gp.test_stall = 0;
-    gp.keep_a = keep_a_operand(plan, 0);
+    const GemmParams gp = make_params(plan, M, N, K, alpha, beta, C, ldc, status, opt.wait_limit_ns, 0,
+                                      keep_a_operand(plan, 0));
     if (launch_plan(plan, false, d.max_clusters, ta, tb, gp, stream) != cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;

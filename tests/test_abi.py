@@ -148,6 +148,15 @@ def test_tile_selection_and_grid():
     # 8192^3: 1024 pair tiles on 76 pairs leave a last wave of 36 tiles, split in halves
     p = _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192)
     assert p["split_tiles"] == 1024 % 76 and p["items"] == 1024 + 36
+    # too few tiles to occupy the GPU: K is cut into slices (no empty slice)
+    p = _plan(M=4096, N=16, K=4096, lda=4096, ldb=16, ldc=16)
+    assert p["k_splits"] == 4 and p["items"] == 32 * 4 and p["split_tiles"] == 0
+    p = _plan(M=4096, N=16, K=4096, lda=4096, ldb=16, ldc=16, tile_m=256)
+    assert p["k_splits"] == 1                       # pairs never split K
+    for K in (520, 576, 9 * 64):
+        p = _plan(M=256, N=128, K=K, lda=K, ldb=128, ldc=128)
+        per = -(-p["k_blocks"] // p["k_splits"])
+        assert (p["k_splits"] - 1) * per < p["k_blocks"]
     # a last wave more than half full is not split
     p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257)
     assert p["split_tiles"] == 0 and p["items"] == p["tiles"]

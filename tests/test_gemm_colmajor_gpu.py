@@ -112,6 +112,7 @@ def test_column_major_matches_row_major_bitwise(mp):
     from parity import run_gpu, c_result
     with mp.Handle() as h:
         h.set_option(mp.Option.TILE_N, 128)
+        h.set_option(mp.Option.SPLIT_K, 1)      # no atomics: a fixed summation order
         g1, _, _ = c_result(run_gpu(h, rm), rm)
         g2, _, _ = c_result(run_gpu(h, cm), cm)
     assert np.array_equal(g1, g2)

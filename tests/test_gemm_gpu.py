@@ -238,6 +238,35 @@ def test_split_tail_tiles(mp, tile_m, tile_n, max_ctas, M, N, K):
         check_full(h, workloads.make_operands(M, N, K, beta=0.5, c_dist="normal", seed=M + K))
 
 
+SPLITK_CASES = [  # (M, N, K, alpha, beta, splits)
+    (4096, 16, 4096, 1.0, 0.0, 0),      # the gate's skinny case: automatic split
+    (1000, 800, 1200, 1.5, 1.0, 2),     # beta = 1: no pre-pass, slices add onto C
+    (300, 200, 1000, -0.5, 0.25, 3),
+    (129, 65, 617, 2.0, 0.0, 7),        # ragged K tail in the last slice
+    (256, 300, 513, 1.0, -1.0, 5),
+]
+
+
+@pytest.mark.parametrize("M,N,K,alpha,beta,splits", SPLITK_CASES)
+def test_split_k(mp, M, N, K, alpha, beta, splits):
+    plan = mp.plan(M, N, K, alpha, 256, K, 256, N, beta, 256, N)
+    if splits == 0:
+        assert plan["k_splits"] > 1
+    with mp.Handle() as h:
+        h.set_option(mp.Option.SPLIT_K, splits)
+        check_full(h, workloads.make_operands(M, N, K, alpha=alpha, beta=beta, c_dist="normal",
+                                              seed=M + N + K))
+
+
+def test_split_k_integer_bitwise_and_column_major(mp):
+    with mp.Handle() as h:
+        h.set_option(mp.Option.SPLIT_K, 4)
+        check_full(h, workloads.make_operands(200, 300, 2048, dist="int3", dist_b="int2", seed=86),
+                   exact=True)
+        check_full(h, workloads.make_operands(200, 300, 2048, dist="int3", dist_b="int2", seed=87,
+                                              b_col_major=True), exact=True)
+
+
 def test_forced_staging_matches(mp):
     with mp.Handle() as h:
         h.set_option(mp.Option.FORCE_STAGING, 1)
