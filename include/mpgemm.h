@@ -20,9 +20,12 @@
  * ---------------------------------------
  *  - Element (i, k) of A is A[i*lda + k]; (k, j) of B is B[k*ldb + j];
  *    (i, j) of C is C[i*ldc + j]. lda >= max(1, K), ldb >= max(1, N),
- *    ldc >= max(1, N). Any leading dimension is accepted: operands whose
- *    base address or row pitch is not a multiple of 16 bytes are staged
- *    through an aligned copy on the device before the tensor-core pass.
+ *    ldc >= max(1, N). Any leading dimension is accepted. When A's rows do
+ *    not start on 16-byte boundaries (an odd lda, say) and B is row-major,
+ *    the tensor-core pass reads A directly in classes of rows that share a
+ *    misalignment; otherwise an operand whose base address or row pitch is
+ *    not a multiple of 16 bytes is staged through an aligned copy on the
+ *    device first.
  *  - A and B must be aligned to 2 bytes and C to 4 bytes (their element
  *    sizes); otherwise MPGEMM_ERR_INVALID_VALUE.
  *  - beta == 0: C is only written, never read, so it may hold NaN on entry.
@@ -176,6 +179,9 @@ typedef struct {
     int64_t items;          /* work items the persistent CTAs walk: tiles + split_tiles, or
                                tiles * k_splits */
     int32_t k_splits;       /* slices of K per tile (1 = no split-K) */
+    int32_t a_classes;      /* 0: A is read through one plain tensor map (aligned, or staged);
+                               P >= 1: A's rows are not 16-byte aligned and are read in P
+                               classes of rows i = r (mod P) instead of being copied */
 } mpgemm_plan_t;
 
 mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha,
@@ -193,10 +199,11 @@ mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha,
  * cannot own a handle's lifetime. The pages have no counterpart of this
  * entry point: it exists for those callers only.
  *
- * Operands that need an aligned staging copy (a base address or row pitch
- * that is not a multiple of 16 bytes) are staged into one fixed, file-scope
- * device array of MPGEMM_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU which
- * loads this library holds until the process exits. If the staged copies of
+ * Operands that need an aligned staging copy (see the conventions above:
+ * an unaligned B, or an unaligned A that cannot be read in row classes) are
+ * staged into one fixed, file-scope device array of
+ * MPGEMM_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU which loads this
+ * library holds until the process exits. If the staged copies of
  * A and B together need more than that, the call returns
  * MPGEMM_ERR_SCRATCH_LIMIT and enqueues nothing; aligned operands need no
  * scratch and have no size limit beyond mpgemm_run's.

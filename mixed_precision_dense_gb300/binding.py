@@ -57,7 +57,7 @@ class Plan(ctypes.Structure):
                 ("raster_group", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("last_k_valid", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
                 ("split_tiles", ctypes.c_int32), ("items", ctypes.c_int64),
-                ("k_splits", ctypes.c_int32)]
+                ("k_splits", ctypes.c_int32), ("a_classes", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -52,8 +52,26 @@
 
 namespace mpgemm {
 
+// A is read through one tensor map per "row class". Usually there is one
+// class holding every row. When A's rows do not start on 16-byte boundaries
+// (an odd lda, say), the rows whose start addresses agree modulo 16 form a
+// class: rows i = r (mod P), P <= 8, have a row stride of P * lda * 2 bytes,
+// a multiple of 16, so TMA can read them from the aligned address just below
+// row r, where they sit shifted right by a_shift[r] elements. A tile then
+// holds 128 rows of one class, and the matching B rows are fetched a_shift[r]
+// rows earlier (rows before 0 arrive as zeros).
+constexpr int kMaxAClasses = 8;
+
+struct AMaps {
+    CUtensorMap map[kMaxAClasses];
+};
+
 struct GemmParams {
     int32_t M, N, K;
+    int32_t a_classes;                               // P >= 1
+    int32_t a_shift[kMaxAClasses];                   // elements left of each class's rows
+    int32_t a_class_rows[kMaxAClasses];              // rows in class r: ceil((M - r) / P)
+    int32_t a_class_first_tile[kMaxAClasses + 1];    // first M-tile of each class
     int32_t m_tiles, n_tiles, k_blocks;   // tiles counted in units of the kernel's tile
     int32_t tiles;
     int32_t tail_start;     // tiles from here on (raster order) are done as two half-width items
@@ -109,6 +127,34 @@ struct TileConfig {
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "tensor memory allocation");
 };
+
+// M-tile mb -> (row class r, first class row j0 of the tile).
+template <int TILE_M>
+__device__ __forceinline__ void a_class_of(const GemmParams& p, int32_t mb, int32_t& r, int32_t& j0) {
+    r = 0;
+    while (r + 1 < p.a_classes && mb >= p.a_class_first_tile[r + 1]) ++r;
+    j0 = (mb - p.a_class_first_tile[r]) * TILE_M;
+}
+
+// Zero the first d (1..7) elements of every row of a 128-row A tile in the
+// 128-byte-swizzled layout (row t's first 16 bytes sit at chunk t & 7). These
+// columns lie before the rows' first element; the matching B rows are zero,
+// but the bytes there are arbitrary and could hold NaN or Inf.
+__device__ __forceinline__ void zero_leading_columns(uint8_t* tile, int32_t d) {
+#pragma unroll 4
+    for (int t = 0; t < 128; ++t) {
+        uint4* q = reinterpret_cast<uint4*>(tile + t * 128 + ((t & 7) << 4));
+        uint4 v = *q;
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (2 * i + 1 < d) w[i] = 0u;
+            else if (2 * i < d) w[i] &= 0xFFFF0000u;
+        }
+        *q = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 // Tile t of the persistent walk -> (m block, n block). Tiles are visited in
 // bands of `raster_group` M-blocks: down the band for one N-block, then the
@@ -216,47 +262,47 @@ __device__ __forceinline__ void load_c_chunk(const float* c_rows, int64_t ldc, i
         v[rr] = (col_ok && rr < rows) ? __ldg(c_rows + static_cast<int64_t>(rr) * ldc + col) : 0.0f;
 }
 
-// The epilogue of one work item for one warp: rows m0 .. m0+31 (the TMEM
+// The epilogue of one work item for one warp: 32 rows of C starting at c_tile,
+// row_stride elements apart, of which the first `rows` exist (the TMEM
 // lanes of this warp's quarter; t_row addresses them at the accumulator's
 // first column) and columns n0 .. n0+width-1. c_cur holds the first chunk of
 // C when beta != 0 (loaded before the accumulator was ready); each later
 // chunk's loads go out before the previous chunk is stored.
 template <int PITCH>
-__device__ __forceinline__ void store_tile(const GemmParams& p, uint32_t t_row, int32_t m0,
-                                          int32_t n0, int32_t width, float* buf, int lane,
-                                          float (&c_cur)[32]) {
+__device__ __forceinline__ void store_tile(const GemmParams& p, uint32_t t_row, float* c_tile,
+                                          int64_t row_stride, int32_t rows, int32_t n0, int32_t width,
+                                          float* buf, int lane, float (&c_cur)[32]) {
     const float alpha = p.alpha, beta = p.beta;
     const bool split = p.k_splits > 1;        // add the partial product into C
     const bool read_c = (beta != 0.0f) && !split;
-    const int32_t rows = min(32, p.M - m0);
     const int32_t chunks = (min(width, p.N - n0) + 31) / 32;
-    const float* c_rows = p.C + static_cast<int64_t>(m0) * p.ldc;
+    const float* c_rows = c_tile;
     float c_next[32];
     for (int32_t c = 0; c < chunks; ++c) {
         uint32_t r[32];
         ptx::tmem_load_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
         if (read_c && c + 1 < chunks)
-            load_c_chunk(c_rows, p.ldc, n0 + (c + 1) * 32 + lane, p.N, rows, c_next);
+            load_c_chunk(c_rows, row_stride, n0 + (c + 1) * 32 + lane, p.N, rows, c_next);
         ptx::tmem_load_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j) buf[lane * PITCH + j] = alpha * __uint_as_float(r[j]);
         __syncwarp();
         const int32_t col = n0 + c * 32 + lane;
         if (col < p.N) {
-            float* cp = p.C + static_cast<int64_t>(m0) * p.ldc + col;
+            float* cp = c_tile + col;
             if (read_c) {
 #pragma unroll
                 for (int rr = 0; rr < 32; ++rr)
                     if (rr < rows)
-                        cp[static_cast<int64_t>(rr) * p.ldc] = fmaf(beta, c_cur[rr], buf[rr * PITCH + lane]);
+                        cp[static_cast<int64_t>(rr) * row_stride] = fmaf(beta, c_cur[rr], buf[rr * PITCH + lane]);
             } else if (split) {
 #pragma unroll
                 for (int rr = 0; rr < 32; ++rr)
-                    if (rr < rows) atomicAdd(cp + static_cast<int64_t>(rr) * p.ldc, buf[rr * PITCH + lane]);
+                    if (rr < rows) atomicAdd(cp + static_cast<int64_t>(rr) * row_stride, buf[rr * PITCH + lane]);
             } else {
 #pragma unroll
                 for (int rr = 0; rr < 32; ++rr)
-                    if (rr < rows) cp[static_cast<int64_t>(rr) * p.ldc] = buf[rr * PITCH + lane];
+                    if (rr < rows) cp[static_cast<int64_t>(rr) * row_stride] = buf[rr * PITCH + lane];
             }
         }
         if (read_c) {
@@ -269,8 +315,8 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, uint32_t t_row, 
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                   const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+    gemm_tc_kernel(const __grid_constant__ AMaps amaps, const __grid_constant__ CUtensorMap tmap_b,
+                   const GemmParams p) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr bool PAIR = Cfg::PAIR;
 
@@ -312,7 +358,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         ptx::fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        ptx::prefetch_tensormap(&tmap_a);
+        for (int r = 0; r < p.a_classes; ++r) ptx::prefetch_tensormap(&amaps.map[r]);
         ptx::prefetch_tensormap(&tmap_b);
     }
     if (warp == 1) {
@@ -348,7 +394,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     if (w.n0 >= p.N) continue;   // a half tile wholly past the last column
                     const int32_t b_cols = w.width / Cfg::CTAS;   // columns of B this CTA loads
                     const int32_t n0 = w.n0 + static_cast<int32_t>(rank) * b_cols;
-                    const int32_t m0 = w.mb * Cfg::TILE_M + static_cast<int32_t>(rank) * BM;
+                    int32_t cls, j0;
+                    a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
+                    const CUtensorMap* map_a = &amaps.map[cls];
+                    const int32_t a_row = j0 + static_cast<int32_t>(rank) * BM;   // class row
+                    const int32_t b_shift = p.a_shift[cls];
                     // single: only the boxes that hold valid columns; pair: all boxes
                     const int32_t n_atoms = PAIR ? b_cols / 64 : min(w.width / 64, (p.N - w.n0 + 63) / 64);
                     const uint32_t bytes = (Cfg::A_BYTES + n_atoms * Cfg::B_ATOM_BYTES) * Cfg::CTAS;
@@ -361,20 +411,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         if constexpr (PAIR) {
                             const uint32_t lead_full = ptx::mapa_shared(full_bar(stage), 0);
                             if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
-                            ptx::tma_load_2d_pair(sA + stage * Cfg::A_BYTES, &tmap_a, lead_full, kb * BK,
-                                                  m0, pol_a);
+                            ptx::tma_load_2d_pair(sA + stage * Cfg::A_BYTES, map_a, lead_full, kb * BK,
+                                                  a_row, pol_a);
                             for (int j = 0; j < n_atoms; ++j)
                                 ptx::tma_load_2d_pair(sB + stage * Cfg::B_BYTES + j * Cfg::B_ATOM_BYTES,
                                                       &tmap_b, lead_full, Cfg::B_KMAJOR ? kb * BK : n0 + j * 64,
-                                                      Cfg::B_KMAJOR ? n0 + j * 64 : kb * BK, pol_b);
+                                                      Cfg::B_KMAJOR ? n0 + j * 64 : kb * BK - b_shift, pol_b);
                         } else {
                             ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
-                            ptx::tma_load_2d(sA + stage * Cfg::A_BYTES, &tmap_a, full_bar(stage), kb * BK,
-                                             m0, pol_a);
+                            ptx::tma_load_2d(sA + stage * Cfg::A_BYTES, map_a, full_bar(stage), kb * BK,
+                                             a_row, pol_a);
                             for (int j = 0; j < n_atoms; ++j)
                                 ptx::tma_load_2d(sB + stage * Cfg::B_BYTES + j * Cfg::B_ATOM_BYTES,
                                                  &tmap_b, full_bar(stage), Cfg::B_KMAJOR ? kb * BK : n0 + j * 64,
-                                                 Cfg::B_KMAJOR ? n0 + j * 64 : kb * BK, pol_b);
+                                                 Cfg::B_KMAJOR ? n0 + j * 64 : kb * BK - b_shift, pol_b);
                         }
                         if (rank == 0) {
                             armed |= 1u << stage;
@@ -406,6 +456,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const WorkItem w = work_item<BN>(p, i);
                 if (w.n0 >= p.N) continue;
                 const int32_t n_mma = PAIR ? w.width : 64 * min(w.width / 64, (p.N - w.n0 + 63) / 64);
+                int32_t cls, j0;
+                a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
+                const int32_t lead_cols = p.a_shift[cls];   // columns before the rows' start
                 const uint32_t idesc = ptx::idesc_f16_f32(Cfg::TILE_M, n_mma, false, !Cfg::B_KMAJOR);
                 const int buf = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
@@ -423,6 +476,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         break;
                     }
                     ptx::tc_fence_after_sync();
+                    if (kb == 0 && lead_cols > 0)
+                        zero_leading_columns(gbase + Cfg::OFF_A + stage * Cfg::A_BYTES, lead_cols);
                     const uint32_t a_base = sA + stage * Cfg::A_BYTES;
                     const uint32_t b_base = sB + stage * Cfg::B_BYTES;
 #pragma unroll
@@ -477,14 +532,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int32_t i = first_item; i < p.items; i += item_step) {
             const WorkItem w = work_item<BN>(p, i);
             if (w.n0 >= p.N) continue;
-            const int32_t m0 = w.mb * Cfg::TILE_M + static_cast<int32_t>(rank) * BM + quarter * 32;
+            int32_t cls, j0;
+            a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
+            const int32_t jb = j0 + static_cast<int32_t>(rank) * BM + quarter * 32;  // class row
+            const int32_t rows = min(32, p.a_class_rows[cls] - jb);
+            // C rows of class cls are cls, cls + P, cls + 2P, ...
+            const int64_t row_stride = static_cast<int64_t>(p.a_classes) * p.ldc;
+            float* c_tile = p.C + (cls + static_cast<int64_t>(p.a_classes) * jb) * p.ldc;
             const int32_t n0 = w.n0;
             // beta * C needs C's old values: the first chunk's loads go out now,
             // while the MMAs of this tile are still running.
             float c_cur[32];
-            if (read_c)
-                load_c_chunk(p.C + static_cast<int64_t>(m0) * p.ldc, p.ldc, n0 + lane, p.N,
-                             min(32, p.M - m0), c_cur);
+            if (read_c) load_c_chunk(c_tile, row_stride, n0 + lane, p.N, rows, c_cur);
             const int accb = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             const bool ready = waiter.wait(acc_full_bar(accb), acc_phase);
@@ -495,7 +554,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             ptx::tc_fence_after_sync();
             const uint32_t t_row =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(accb * BN);
-            store_tile<Cfg::EPI_PITCH>(p, t_row, m0, n0, w.width, buf, lane, c_cur);
+            store_tile<Cfg::EPI_PITCH>(p, t_row, c_tile, row_stride, rows, n0, w.width, buf, lane, c_cur);
             ptx::tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {

@@ -28,6 +28,7 @@
 #include <cstring>
 #include <algorithm>
 #include <functional>
+#include <numeric>
 #include <mutex>
 
 #include "../../include/mpgemm.h"
@@ -105,6 +106,35 @@ bool auto_pair(int64_t M, int64_t N, int32_t num_sms) {
     return ceil_div(M, 256) * ceil_div(N, 256) >= num_sms / 2;
 }
 
+// How the tensor-core pass reads A (see AMaps in gemm_kernel.cuh): one row
+// class when A's rows start on 16-byte boundaries (or A was staged), else
+// P = 16 / gcd(2 * lda, 16) classes of rows i = r (mod P), each read from the
+// aligned address at or below row r with a shift of a few elements.
+struct AClassLayout {
+    int32_t P = 1;
+    int32_t max_shift = 0;
+    int32_t shift[kMaxAClasses] = {};
+    int64_t rows[kMaxAClasses] = {};
+    int64_t first_tile[kMaxAClasses + 1] = {};
+    uintptr_t base[kMaxAClasses] = {};
+};
+
+AClassLayout a_class_layout(const void* A, int64_t lda, int64_t M, bool classes, int64_t tile_m) {
+    AClassLayout L;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(A);
+    L.P = classes ? static_cast<int32_t>(16 / std::gcd<int64_t>(2 * lda, 16)) : 1;
+    for (int32_t r = 0; r < L.P; ++r) {
+        const uintptr_t addr = a + static_cast<uintptr_t>(r) * static_cast<uintptr_t>(lda) * 2;
+        const int32_t off = classes ? static_cast<int32_t>(addr % 16) : 0;
+        L.shift[r] = off / 2;
+        L.max_shift = std::max(L.max_shift, L.shift[r]);
+        L.base[r] = addr - off;
+        L.rows[r] = r < M ? (M - r + L.P - 1) / L.P : 0;
+        L.first_tile[r + 1] = L.first_tile[r] + ceil_div(L.rows[r], tile_m);
+    }
+    return L;
+}
+
 mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                           const void* B, int64_t ldb, float beta, const void* C, int64_t ldc,
                           int32_t num_sms, const Options& opt, mpgemm_plan_t* out) {
@@ -124,7 +154,6 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
         *out = p;
         return MPGEMM_OK;
     }
-    p.stage_a = (opt.force_staging || !aligned16(A, lda, 2)) ? 1 : 0;
     p.stage_b = (opt.force_staging || !aligned16(B, ldb, 2)) ? 1 : 0;
     const bool pair = opt.tile_m ? (opt.tile_m == 256) : (!opt.tile_n && auto_pair(M, N, num_sms));
     if (pair) {
@@ -137,8 +166,15 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
         p.stages = (p.tile_n == 256) ? Cfg256::STAGES : Cfg128::STAGES;
         p.smem_bytes = (p.tile_n == 256) ? Cfg256::SMEM_BYTES : Cfg128::SMEM_BYTES;
     }
-    const int64_t m_tiles = ceil_div(M, p.tile_m), n_tiles = ceil_div(N, p.tile_n);
-    const int64_t k_blocks = ceil_div(K, 64);
+    // An A whose rows break TMA's 16-byte rule is read in row classes
+    // (one-CTA tiles with a row-major B), else copied to an aligned buffer.
+    const bool a_aligned = aligned16(A, lda, 2);
+    const bool a_classes = !a_aligned && !opt.force_staging && !pair && !opt.b_col_major;
+    p.stage_a = (opt.force_staging || (!a_aligned && !a_classes)) ? 1 : 0;
+    const AClassLayout L = a_class_layout(A, lda, M, a_classes, p.tile_m);
+    p.a_classes = a_classes ? L.P : 0;
+    const int64_t m_tiles = L.first_tile[L.P], n_tiles = ceil_div(N, p.tile_n);
+    const int64_t k_blocks = ceil_div(K + L.max_shift, 64);
     if (m_tiles * n_tiles > kDimLimit / 2) return MPGEMM_ERR_INVALID_VALUE;
     p.m_tiles = static_cast<int32_t>(m_tiles);
     p.n_tiles = static_cast<int32_t>(n_tiles);
@@ -309,7 +345,7 @@ cudaError_t set_smem_attr() {
 }
 
 template <class Cfg>
-cudaError_t launch_tc(int grid, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& gp,
+cudaError_t launch_tc(int grid, const AMaps& ta, const CUtensorMap& tb, const GemmParams& gp,
                       cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -370,10 +406,33 @@ cudaError_t prepare_kernels() {
     return e;
 }
 
+// The A tensor maps (one per row class) and the class fields of the kernel
+// parameters, for A as the kernel will read it (staged or not).
+bool encode_a(const mpgemm_plan_t& plan, const void* a_use, int64_t lda_use, int64_t M, int64_t K,
+              AMaps* maps, GemmParams* gp) {
+    std::memset(maps, 0, sizeof(*maps));
+    const AClassLayout L = a_class_layout(a_use, lda_use, M, plan.a_classes > 0, plan.tile_m);
+    gp->a_classes = L.P;
+    for (int32_t r = 0; r < kMaxAClasses; ++r) {
+        gp->a_shift[r] = L.shift[r];
+        gp->a_class_rows[r] = static_cast<int32_t>(L.rows[r]);
+        gp->a_class_first_tile[r] = static_cast<int32_t>(L.first_tile[r < L.P ? r : L.P]);
+    }
+    gp->a_class_first_tile[kMaxAClasses] = static_cast<int32_t>(L.first_tile[L.P]);
+    for (int32_t r = 0; r < L.P; ++r) {
+        if (L.rows[r] == 0) continue;
+        if (!encode_f16(&maps->map[r], reinterpret_cast<const void*>(L.base[r]), L.rows[r], K + L.shift[r],
+                        L.P * lda_use, 64, 128))
+            return false;
+    }
+    return true;
+}
+
 GemmParams make_params(const mpgemm_plan_t& plan, int64_t M, int64_t N, int64_t K, float alpha,
                        float beta, float* C, int64_t ldc, int32_t* status, uint64_t wait_limit_ns,
                        int32_t test_stall, int32_t keep_a) {
     GemmParams gp;
+    std::memset(&gp, 0, sizeof(gp));
     gp.M = static_cast<int32_t>(M);
     gp.N = static_cast<int32_t>(N);
     gp.K = static_cast<int32_t>(K);
@@ -398,7 +457,7 @@ GemmParams make_params(const mpgemm_plan_t& plan, int64_t M, int64_t N, int64_t 
 }
 
 cudaError_t launch_plan(const mpgemm_plan_t& plan, bool b_col_major, int max_clusters,
-                        const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& gp,
+                        const AMaps& ta, const CUtensorMap& tb, const GemmParams& gp,
                         cudaStream_t stream) {
     if (plan.k_splits > 1 && gp.beta != 1.0f) {
         // the slices add into C: apply beta (or clear C) once, first
@@ -665,15 +724,16 @@ mpgemm_status_t mpgemm_run_ex(mpgemm_handle_t h, mpgemm_b_layout_t b_layout, int
         if (cudaGetLastError() != cudaSuccess) return MPGEMM_ERR_LAUNCH;
     }
 
-    CUtensorMap ta, tb;
-    if (!encode_f16(&ta, a_use, M, K, lda_use, 64, 128) ||
-        !(b_col ? encode_f16(&tb, b_use, N, K, ldb_use, 64, 64)
+    CUtensorMap tb;
+    if (!(b_col ? encode_f16(&tb, b_use, N, K, ldb_use, 64, 64)
                 : encode_f16(&tb, b_use, K, N, ldb_use, 64, 64)))
         return MPGEMM_ERR_CUDA;
 
-    const GemmParams gp = make_params(plan, M, N, K, alpha, beta, C, ldc, h->status_dev,
-                                      h->opt.wait_limit_ns, h->opt.test_stall,
-                                      keep_a_operand(plan, h->opt.l2_keep));
+    GemmParams gp = make_params(plan, M, N, K, alpha, beta, C, ldc, h->status_dev,
+                                h->opt.wait_limit_ns, h->opt.test_stall,
+                                keep_a_operand(plan, h->opt.l2_keep));
+    AMaps ta;
+    if (!encode_a(plan, a_use, lda_use, M, K, &ta, &gp)) return MPGEMM_ERR_CUDA;
     if (launch_plan(plan, b_col, h->max_clusters, ta, tb, gp, stream) != cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;
@@ -886,12 +946,12 @@ extern "C" mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K, f
     }
     if (cudaGetLastError() != cudaSuccess) return MPGEMM_ERR_LAUNCH;
 
-    CUtensorMap ta, tb;
-    if (!encode_f16(&ta, a_use, M, K, lda_use, 64, 128) ||
-        !encode_f16(&tb, b_use, K, N, ldb_use, 64, 64))
-        return MPGEMM_ERR_CUDA;
-    const GemmParams gp = make_params(plan, M, N, K, alpha, beta, C, ldc, status, opt.wait_limit_ns, 0,
-                                      keep_a_operand(plan, 0));
+    CUtensorMap tb;
+    if (!encode_f16(&tb, b_use, K, N, ldb_use, 64, 64)) return MPGEMM_ERR_CUDA;
+    GemmParams gp = make_params(plan, M, N, K, alpha, beta, C, ldc, status, opt.wait_limit_ns, 0,
+                                keep_a_operand(plan, 0));
+    AMaps ta;
+    if (!encode_a(plan, a_use, lda_use, M, K, &ta, &gp)) return MPGEMM_ERR_CUDA;
     if (launch_plan(plan, false, d.max_clusters, ta, tb, gp, stream) != cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;

@@ -96,17 +96,32 @@ def test_quick_returns():
 
 
 def test_alignment_classification():
-    # lda = 617 halves = 1234 bytes: not a multiple of 16 -> A is staged
+    # lda = 617 halves = 1234 bytes: rows start at 8 different offsets modulo
+    # 16, so A is read directly in 8 row classes (one-CTA tiles, row-major B)
     p = _plan()
-    assert (p["stage_a"], p["stage_b"]) == (1, 0)
-    assert p["workspace_bytes"] == 200 * 624 * 2
+    assert (p["stage_a"], p["stage_b"], p["a_classes"]) == (0, 0, 8)
+    assert p["workspace_bytes"] == 0
+    # the same A staged when asked, or under a column-major B
+    p = _plan(force_staging=True)
+    assert p["stage_a"] == 1 and p["a_classes"] == 0
+    p = _plan(ldb=617, b_col_major=True)
+    assert p["stage_a"] == 1 and p["a_classes"] == 0
+    assert p["workspace_bytes"] == 200 * 624 * 2 + 136 * 624 * 2
     p = _plan(M=2048, N=2048, K=2048, lda=2048, ldb=2048, ldc=2048)
     assert (p["stage_a"], p["stage_b"]) == (0, 0) and p["workspace_bytes"] == 0
     p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257, beta=0.5)
-    assert (p["stage_a"], p["stage_b"]) == (1, 1)
-    # a base address 2 bytes past a 16-byte boundary is staged even with an aligned pitch
+    assert (p["stage_a"], p["stage_b"], p["a_classes"]) == (0, 1, 8)
+    # lda = 4094: rows start at four offsets; lda = 4100: two
+    assert _plan(M=4096, N=257, K=4093, lda=4094, ldb=257, ldc=257)["a_classes"] == 4
+    assert _plan(M=4096, N=257, K=4093, lda=4100, ldb=257, ldc=257)["a_classes"] == 2
+    # a base address 2 bytes past a 16-byte boundary with an aligned pitch: one
+    # class, read with a shift of one element
     p = _plan(M=128, N=128, K=128, lda=128, ldb=128, ldc=128, A=256 + 2)
-    assert (p["stage_a"], p["stage_b"]) == (1, 0)
+    assert (p["stage_a"], p["stage_b"], p["a_classes"]) == (0, 0, 1)
+    assert p["k_blocks"] == 3                      # K + 1 view columns
+    # CTA pairs read A through one plain map: an unaligned A is staged
+    p = _plan(M=8192, N=8192, K=8192, lda=8193, ldb=8192, ldc=8192)
+    assert p["tile_m"] == 256 and p["stage_a"] == 1 and p["a_classes"] == 0
     p = _plan(M=128, N=128, K=128, lda=128, ldb=128, ldc=128, force_staging=True)
     assert (p["stage_a"], p["stage_b"]) == (1, 1)
 
@@ -161,7 +176,7 @@ def test_tile_selection_and_grid():
     p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257)
     assert p["split_tiles"] == 0 and p["items"] == p["tiles"]
     p = _plan()
-    assert p["tiles"] == 2 * 2 and p["grid"] == 4
+    assert p["a_classes"] == 8 and p["tiles"] == 8 * 2 and p["grid"] == 16   # 8 classes of 25 rows
     p = _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192, tile_n=128, max_ctas=10)
     assert p["tile_n"] == 128 and p["grid"] == 10
     with pytest.raises(mp.MpgemmError):

@@ -219,7 +219,7 @@ def test_cta_pair_stall_reports_timeout(mp):
 
 SPLIT_CASES = [  # (tile_m, tile_n, max_ctas, M, N, K): the last partial wave is split in halves
     (128, 256, 5, 1000, 800, 200),     # half tiles wholly past column 800 are skipped
-    (128, 128, 7, 700, 600, 333),
+    (128, 128, 7, 700, 600, 336),
     (256, 256, 8, 1300, 1100, 150),
     (256, 256, 10, 768, 1024, 320),
 ]
@@ -265,6 +265,38 @@ def test_split_k_integer_bitwise_and_column_major(mp):
                    exact=True)
         check_full(h, workloads.make_operands(200, 300, 2048, dist="int3", dist_b="int2", seed=87,
                                               b_col_major=True), exact=True)
+
+
+CLASS_CASES = [  # (M, N, K, lda, a_offset, tile_n, split_k): A read in row classes
+    (200, 136, 617, 617, 0, 0, 0),      # 8 classes of 25 rows
+    (1000, 300, 500, 503, 0, 128, 0),   # NaN padding between rows: leading columns zeroed
+    (700, 257, 1000, 1002, 0, 256, 0),  # 4 classes
+    (513, 200, 333, 340, 0, 0, 0),      # 2 classes
+    (300, 200, 256, 256, 1, 0, 0),      # aligned pitch, base 2 bytes off: 1 class, shift 1
+    (3, 50, 70, 71, 0, 0, 0),           # fewer rows than classes
+    (640, 128, 2049, 2049, 3, 128, 4),  # classes with split-K
+]
+
+
+@pytest.mark.parametrize("M,N,K,lda,a_offset,tile_n,split_k", CLASS_CASES)
+def test_a_row_classes(mp, M, N, K, lda, a_offset, tile_n, split_k):
+    plan = mp.plan(M, N, K, 1.0, 256 + 2 * a_offset, lda, 256, N, 0.5, 256, N, tile_n=tile_n)
+    assert plan["a_classes"] >= 1 and plan["stage_a"] == 0
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_N, tile_n)
+        h.set_option(mp.Option.SPLIT_K, split_k)
+        ops = workloads.make_operands(M, N, K, lda=lda, alpha=1.25, beta=0.5, c_dist="normal",
+                                      seed=M + lda)
+        check_full(h, ops, a_offset=a_offset)
+        # the same problem through the staging copy gives the same result within tolerance
+        h.set_option(mp.Option.FORCE_STAGING, 1)
+        check_full(h, ops, a_offset=a_offset)
+
+
+def test_a_row_classes_integer_bitwise(mp):
+    ops = workloads.make_operands(777, 260, 1021, lda=1021, dist="int3", dist_b="int2", seed=88)
+    with mp.Handle() as h:
+        check_full(h, ops, exact=True)
 
 
 def test_forced_staging_matches(mp):

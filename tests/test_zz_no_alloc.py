@@ -56,9 +56,9 @@ def _both(mp, ops):
 
 def test_noalloc_matches_run_on_consecutive_calls(mp):
     cases = [
-        # lda = 617 halves: A goes through the scratch area
+        # lda = 617 halves: A is read in row classes, no scratch needed
         workloads.workload_operands(0),
-        # A and B both staged (unaligned pitches), beta != 0, different shape
+        # ldb = 259 halves: B goes through the scratch area; beta != 0, another shape
         workloads.make_operands(321, 257, 617, lda=620, ldb=259, ldc=260, alpha=1.5, beta=0.5,
                                 c_dist="normal", seed=123),
         # aligned operands: no scratch at all
@@ -73,10 +73,10 @@ def test_noalloc_matches_run_on_consecutive_calls(mp):
 
 
 def test_noalloc_rejects_staging_beyond_its_scratch(mp):
-    # A needs staging (lda = 2049 halves) and its aligned copy would take
+    # B needs staging (ldb = 2049 halves) and its aligned copy would take
     # 4200 * 2056 * 2 bytes > 16 MiB: rejected, nothing enqueued, C untouched.
-    M, N, K = 4200, 64, 2049
-    assert M * ((K + 7) // 8 * 8) * 2 > mp.NOALLOC_SCRATCH_BYTES
+    M, N, K = 64, 2049, 4200
+    assert K * ((N + 7) // 8 * 8) * 2 > mp.NOALLOC_SCRATCH_BYTES
     A = torch.zeros((M, K), dtype=torch.float16, device="cuda")
     B = torch.zeros((K, N), dtype=torch.float16, device="cuda")
     C = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
