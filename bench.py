@@ -319,13 +319,16 @@ def run_ours(args):
     C0 = ops.C.to(device)
     C = C0.clone()
     handle = mp.Handle()
+    handle.set_option(mp.Option.TILE_M, args.tile_m)
+    handle.set_option(mp.Option.TILE_N, args.tile_n)
 
     def step():
         handle.run(w.M, w.N, w.K, w.alpha, A.data_ptr(), w.lda, B.data_ptr(), w.ldb, w.beta,
                    C.data_ptr(), w.ldc, stream.cuda_stream)
 
     plan = mp.plan(w.M, w.N, w.K, w.alpha, A.data_ptr(), w.lda, B.data_ptr(), w.ldb, w.beta,
-                   C.data_ptr(), w.ldc, num_sms=torch.cuda.get_device_properties(device).multi_processor_count)
+                   C.data_ptr(), w.ldc, num_sms=torch.cuda.get_device_properties(device).multi_processor_count,
+                   tile_m=args.tile_m, tile_n=args.tile_n)
     launches_per_step = 1 + plan["stage_a"] + plan["stage_b"]
 
     # correctness first, on a NaN-poisoned (beta == 0) or restored (beta != 0) C
@@ -461,6 +464,8 @@ def run_e2e(handle, w, ops, stream, device, args):
     B_h = ops.B.pin_memory()
     C_h = [ops.C.clone().pin_memory() for _ in range(2)]
     handles = [handle, mp.Handle()]
+    handles[1].set_option(mp.Option.TILE_M, args.tile_m)
+    handles[1].set_option(mp.Option.TILE_N, args.tile_n)
     streams = [stream, torch.cuda.Stream(device)]
     steps = max(1, min(args.steps, args.e2e_steps))
 
@@ -654,6 +659,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-check", action="store_true")
     ap.add_argument("--no-cublas", action="store_true")
+    ap.add_argument("--tile-m", type=int, default=0, choices=[0, 128, 256],
+                    help="force the tile height (0 = the library's choice)")
+    ap.add_argument("--tile-n", type=int, default=0, choices=[0, 128, 256, 512],
+                    help="force the tile width (0 = the library's choice)")
     ap.add_argument("--gate", action="store_true",
                     help="run the capstone gate's eight cases and print a report instead")
     args = ap.parse_args(argv)

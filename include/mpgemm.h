@@ -132,7 +132,9 @@ mpgemm_status_t mpgemm_sync_status(mpgemm_handle_t h, void* stream, int32_t info
 
 /* Tunables and test switches, set per handle. */
 typedef enum {
-    MPGEMM_OPT_TILE_N = 1,        /* 0 = automatic (default), or 128 or 256 columns per tile */
+    MPGEMM_OPT_TILE_N = 1,        /* 0 = automatic (default), or 128 or 256 columns per tile;
+                                     512 = a cluster of two CTAs per 256 x 512 tile (with
+                                     TILE_M 0 or 256) */
     MPGEMM_OPT_MAX_CTAS = 2,      /* 0 = one persistent CTA per SM (default), else an upper bound */
     MPGEMM_OPT_FORCE_STAGING = 3, /* 1 = stage A and B through aligned copies even when aligned */
     MPGEMM_OPT_WAIT_LIMIT_US = 4, /* limit of every bounded device wait, microseconds (default 4e6) */
@@ -140,7 +142,9 @@ typedef enum {
     MPGEMM_OPT_TEST_STALL = 6,    /* test only: 1 = the load warp issues no loads, so the
                                      kernel's bounded waits expire and a timeout is reported */
     MPGEMM_OPT_TILE_M = 7,        /* 0 = automatic (default); 128 = one CTA per tile;
-                                     256 = a cluster of two CTAs per 256 x 256 tile */
+                                     256 = a cluster of two CTAs per 256 x 256 tile
+                                     (256 x 512 when TILE_N is 512). TILE_M 128 with
+                                     TILE_N 512 makes runs return INVALID_VALUE */
     MPGEMM_OPT_L2_KEEP = 8,       /* L2 hints for the operand loads: 0 = automatic (default,
                                      keep the operand more tiles re-read), 1 = keep A,
                                      2 = keep B */
@@ -165,7 +169,7 @@ typedef struct {
     int32_t stage_a;        /* 1 if A is copied to an aligned buffer first */
     int32_t stage_b;        /* 1 if B is copied to an aligned buffer first */
     int32_t tile_m;         /* rows per output tile: 128 (one CTA) or 256 (a CTA pair) */
-    int32_t tile_n;         /* columns per output tile (128 or 256) */
+    int32_t tile_n;         /* columns per output tile (128 or 256; 256 or 512 for a pair) */
     int32_t tile_k;         /* K per pipeline stage (64) */
     int32_t stages;         /* shared-memory pipeline depth */
     int32_t m_tiles, n_tiles, k_blocks;
@@ -194,9 +198,9 @@ mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha,
  * cannot allocate: no handle, and no device or host allocation of any kind
  * (no cudaMalloc, cudaMallocAsync, cudaHostAlloc or allocating library call)
  * at any call. Such callers include code that runs where the allocator must
- * not be touched (inside another library's memory-pool budget, or while a
- * stream is being captured into a graph by someone else), and code that
- * cannot own a handle's lifetime. The pages have no counterpart of this
+ * not be touched (inside another library's fixed memory-pool budget, or on
+ * a path that runs when device memory is already exhausted, where a new
+ * allocation would fail), and code that cannot own a handle's lifetime. The pages have no counterpart of this
  * entry point: it exists for those callers only.
  *
  * Operands that need an aligned staging copy (see the conventions above:

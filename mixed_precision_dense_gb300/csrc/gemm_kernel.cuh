@@ -24,13 +24,17 @@
 // Two shapes of the same pipeline:
 //   single  one CTA per tile of 128 x BN (BN = 128 or 256), tcgen05.mma with
 //           cta_group::1, M = 128, N = 64 * ceil(valid columns / 64);
-//   pair    a cluster of two CTAs per tile of 256 x 256: each CTA loads its
-//           own 128 rows of A and its own 128 columns of B, the even CTA
-//           issues tcgen05.mma with cta_group::2 (M = 256, N = 256) over both
-//           CTAs' shared memory, and each CTA's tensor memory receives its
-//           own 128 rows of the accumulator. Per SM this moves a third less
-//           operand data per FLOP than the single shape, which leaves room
-//           for a deeper ring.
+//   pair    a cluster of two CTAs per tile of 256 x BN (BN = 256 or 512):
+//           each CTA loads its own 128 rows of A and its own half of every
+//           256-column block of B, the even CTA issues tcgen05.mma with
+//           cta_group::2 (M = 256, N = 256, one instruction per 256-column
+//           block) over both CTAs' shared memory, and each CTA's tensor
+//           memory receives its own 128 rows of the accumulator. Per SM the
+//           256 x 256 tile moves a third less operand data per FLOP than the
+//           single shape, the 256 x 512 tile half as much. The 512-wide
+//           accumulator fills the whole tensor memory, so that shape has one
+//           accumulator buffer, released to the MMA warp in 256-column halves
+//           as the epilogue drains them.
 //
 // The staged-tile reuse, asynchronous copies and block rasterisation that the
 // pages build up with WMMA ("Day 80", "Worked path"; "02_mixed_precision_gemm"
@@ -106,14 +110,24 @@ struct TileConfig {
     static constexpr int B_COLS = BN / CTAS;           // columns of B each CTA loads
     static constexpr int BK = 64;                      // 64 halves = one 128-byte swizzle row
     static constexpr int STAGES = STAGES_;
+    // one MMA instruction covers SUB_N columns: BN, except that a pair tile
+    // 512 wide takes two instructions of 256 per K step
+    static constexpr int SUB_N = BN < 256 ? BN : 256;
+    static constexpr int SUBS = BN / SUB_N;
+    // two accumulator buffers (the epilogue of tile i overlaps the MMAs of
+    // tile i+1) when they fit in the 512 columns of tensor memory, else one,
+    // whose SUBS parts are handed back one by one
+    static constexpr int ACC_BUFS = 2 * BN <= 512 ? 2 : 1;
     static constexpr int A_BYTES = BM * BK * 2;        // 16 KB
     static constexpr int B_ATOM_BYTES = BK * 64 * 2;   // one 64-column box of B: 8 KB
     static constexpr int B_BYTES = BK * B_COLS * 2;
     static constexpr int EPI_WARPS = 4;
     static constexpr int EPI_PITCH = 33;               // floats per row of a transpose buffer
     static constexpr int EPI_BYTES = EPI_WARPS * 32 * EPI_PITCH * 4;
-    static constexpr int TMEM_COLS = 2 * BN;           // two accumulator buffers
-    static constexpr int NUM_BARRIERS = 2 * STAGES + 4;
+    static constexpr int TMEM_COLS = ACC_BUFS * BN;
+    // full and empty per stage; accumulator full per buffer; accumulator
+    // empty per buffer and part
+    static constexpr int NUM_BARRIERS = 2 * STAGES + ACC_BUFS + ACC_BUFS * SUBS;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = STAGES * A_BYTES;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
@@ -121,8 +135,9 @@ struct TileConfig {
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARRIERS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
     static constexpr int THREADS = 192;
-    static_assert(BN == 128 || BN == 256, "tile width");
-    static_assert(!PAIR || BN == 256, "pair tiles are 256 x 256");
+    static_assert(BN == 128 || BN == 256 || (PAIR && BN == 512), "tile width");
+    static_assert(!PAIR || BN >= 256, "pair tiles are 256 x 256 or 256 x 512");
+    static_assert(SUBS == 1 || ACC_BUFS == 1, "parts only for a single accumulator buffer");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "tensor memory allocation");
@@ -331,8 +346,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const uint32_t bar0 = base + Cfg::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    constexpr int ACC_BUFS = Cfg::ACC_BUFS, SUBS = Cfg::SUBS;
     auto acc_full_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-    auto acc_empty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    auto acc_empty_bar = [&](int b, int h) { return bar0 + 8u * (2 * STAGES + ACC_BUFS + b * SUBS + h); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Cfg::OFF_MISC);
     volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + Cfg::OFF_MISC + 4);
 
@@ -350,9 +366,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             ptx::mbar_init(full_bar(s), 1);
             ptx::mbar_init(empty_bar(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < ACC_BUFS; ++b) {
             ptx::mbar_init(acc_full_bar(b), 1);
-            ptx::mbar_init(acc_empty_bar(b), Cfg::EPI_WARPS * Cfg::CTAS);
+            for (int h = 0; h < SUBS; ++h) ptx::mbar_init(acc_empty_bar(b, h), Cfg::EPI_WARPS * Cfg::CTAS);
         }
         *abort_flag = 0;
         ptx::fence_barrier_init();
@@ -392,15 +408,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 for (int32_t i = first_item; ok && i < p.items; i += item_step) {
                     const WorkItem w = work_item<BN>(p, i);
                     if (w.n0 >= p.N) continue;   // a half tile wholly past the last column
-                    const int32_t b_cols = w.width / Cfg::CTAS;   // columns of B this CTA loads
-                    const int32_t n0 = w.n0 + static_cast<int32_t>(rank) * b_cols;
+                    // Pair: each MMA instruction covers sub_n columns of the
+                    // item, and this CTA loads sub_n / 2 of them (its half) for
+                    // each instruction, in 64-column boxes ("atoms"); atom a
+                    // belongs to instruction a / per_sub.
+                    const int32_t sub_n = PAIR ? min(w.width, Cfg::SUB_N) : w.width;
+                    const int32_t per_sub = PAIR ? sub_n / 128 : 0;
+                    const int32_t n0 = w.n0 + (PAIR ? static_cast<int32_t>(rank) * (sub_n / 2) : 0);
                     int32_t cls, j0;
                     a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
                     const CUtensorMap* map_a = &amaps.map[cls];
                     const int32_t a_row = j0 + static_cast<int32_t>(rank) * BM;   // class row
                     const int32_t b_shift = p.a_shift[cls];
                     // single: only the boxes that hold valid columns; pair: all boxes
-                    const int32_t n_atoms = PAIR ? b_cols / 64 : min(w.width / 64, (p.N - w.n0 + 63) / 64);
+                    const int32_t n_atoms = PAIR ? w.width / 128 : min(w.width / 64, (p.N - w.n0 + 63) / 64);
                     const uint32_t bytes = (Cfg::A_BYTES + n_atoms * Cfg::B_ATOM_BYTES) * Cfg::CTAS;
                     for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                         if (!waiter.wait(empty_bar(stage), phase ^ 1u)) {
@@ -413,10 +434,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
                             ptx::tma_load_2d_pair(sA + stage * Cfg::A_BYTES, map_a, lead_full, kb * BK,
                                                   a_row, pol_a);
-                            for (int j = 0; j < n_atoms; ++j)
+                            for (int j = 0; j < n_atoms; ++j) {
+                                const int32_t col = n0 + (j / per_sub) * sub_n + (j % per_sub) * 64;
                                 ptx::tma_load_2d_pair(sB + stage * Cfg::B_BYTES + j * Cfg::B_ATOM_BYTES,
-                                                      &tmap_b, lead_full, Cfg::B_KMAJOR ? kb * BK : n0 + j * 64,
-                                                      Cfg::B_KMAJOR ? n0 + j * 64 : kb * BK - b_shift, pol_b);
+                                                      &tmap_b, lead_full, Cfg::B_KMAJOR ? kb * BK : col,
+                                                      Cfg::B_KMAJOR ? col : kb * BK - b_shift, pol_b);
+                            }
                         } else {
                             ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
                             ptx::tma_load_2d(sA + stage * Cfg::A_BYTES, map_a, full_bar(stage), kb * BK,
@@ -455,19 +478,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             for (int32_t i = first_item; ok && i < p.items; i += item_step) {
                 const WorkItem w = work_item<BN>(p, i);
                 if (w.n0 >= p.N) continue;
-                const int32_t n_mma = PAIR ? w.width : 64 * min(w.width / 64, (p.N - w.n0 + 63) / 64);
+                // columns per instruction and instructions per K step
+                const int32_t n_mma = PAIR ? min(w.width, Cfg::SUB_N) : 64 * min(w.width / 64, (p.N - w.n0 + 63) / 64);
+                const int32_t n_sub = PAIR ? w.width / n_mma : 1;
                 int32_t cls, j0;
                 a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
                 const int32_t lead_cols = p.a_shift[cls];   // columns before the rows' start
                 const uint32_t idesc = ptx::idesc_f16_f32(Cfg::TILE_M, n_mma, false, !Cfg::B_KMAJOR);
-                const int buf = local & 1;
-                const uint32_t acc_phase = (local >> 1) & 1;
-                if (!waiter.wait(acc_empty_bar(buf), acc_phase ^ 1u)) {
-                    waiter.fail(kRoleMma, -1);
-                    ok = false;
-                    break;
+                const int buf = local % ACC_BUFS;
+                const uint32_t acc_phase = (local / ACC_BUFS) & 1;
+                if constexpr (SUBS == 1) {
+                    if (!waiter.wait(acc_empty_bar(buf, 0), acc_phase ^ 1u)) {
+                        waiter.fail(kRoleMma, -1);
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
                 }
-                ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!waiter.wait(full_bar(stage), phase)) {
@@ -480,23 +507,46 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         zero_leading_columns(gbase + Cfg::OFF_A + stage * Cfg::A_BYTES, lead_cols);
                     const uint32_t a_base = sA + stage * Cfg::A_BYTES;
                     const uint32_t b_base = sB + stage * Cfg::B_BYTES;
+                    bool pending = false;   // MMAs issued from this stage
+                    for (int32_t h = 0; ok && h < n_sub; ++h) {
+                        if constexpr (SUBS > 1) {
+                            // the first use of part h in this item: wait until the
+                            // epilogue has read the previous item's part h
+                            if (kb == w.kb0) {
+                                if (!waiter.wait(acc_empty_bar(0, h), acc_phase ^ 1u)) {
+                                    waiter.fail(kRoleMma, -1);
+                                    ok = false;
+                                    break;
+                                }
+                                ptx::tc_fence_after_sync();
+                            }
+                        }
+                        // part h: n_mma accumulator columns further, B atoms of
+                        // n_mma / 2 columns (this CTA's half) further
+                        const uint32_t d_part = d_tmem + static_cast<uint32_t>(h * n_mma);
+                        const uint32_t b_part = b_base + static_cast<uint32_t>(h * (n_mma / 128) * Cfg::B_ATOM_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        // A: K-major, 128-byte rows, 8-row groups 1024 B apart;
-                        //    the k-th 16-wide slice starts 32 bytes further.
-                        const uint64_t a_desc = ptx::smem_desc_sw128(a_base + kk * 32, 16, 1024);
-                        // B row-major: N-major, 64-column boxes B_ATOM_BYTES apart
-                        //    (leading offset), 8 K-rows of 128 B per group (stride
-                        //    offset); the k-th 16-row slice starts 16 * 128 bytes
-                        //    further. B column-major: K-major like A.
-                        const uint64_t b_desc =
-                            Cfg::B_KMAJOR ? ptx::smem_desc_sw128(b_base + kk * 32, 16, 1024)
-                                          : ptx::smem_desc_sw128(b_base + kk * 2048, Cfg::B_ATOM_BYTES, 1024);
-                        if constexpr (PAIR)
-                            ptx::mma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb != w.kb0) || kk != 0);
-                        else
-                            ptx::mma_f16(d_tmem, a_desc, b_desc, idesc, (kb != w.kb0) || kk != 0);
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            // A: K-major, 128-byte rows, 8-row groups 1024 B apart;
+                            //    the k-th 16-wide slice starts 32 bytes further.
+                            const uint64_t a_desc = ptx::smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                            // B row-major: N-major, 64-column boxes B_ATOM_BYTES apart
+                            //    (leading offset), 8 K-rows of 128 B per group (stride
+                            //    offset); the k-th 16-row slice starts 16 * 128 bytes
+                            //    further. B column-major: K-major like A.
+                            const uint64_t b_desc =
+                                Cfg::B_KMAJOR ? ptx::smem_desc_sw128(b_part + kk * 32, 16, 1024)
+                                              : ptx::smem_desc_sw128(b_part + kk * 2048, Cfg::B_ATOM_BYTES, 1024);
+                            if constexpr (PAIR)
+                                ptx::mma_f16_pair(d_part, a_desc, b_desc, idesc, (kb != w.kb0) || kk != 0);
+                            else
+                                ptx::mma_f16(d_part, a_desc, b_desc, idesc, (kb != w.kb0) || kk != 0);
+                        }
+                        pending = true;
                     }
+                    if (!ok && !pending) break;
+                    // (after a failed wait for part 1, part 0's MMAs still get
+                    // their commit, so the drain below covers them)
                     issued = true;
                     if constexpr (PAIR)
                         ptx::mma_commit_pair_multicast(empty_bar(stage), 0x3);
@@ -506,6 +556,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         stage = 0;
                         phase ^= 1u;
                     }
+                    if (!ok) break;
                 }
                 if (ok) {
                     if constexpr (PAIR)
@@ -544,8 +595,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // while the MMAs of this tile are still running.
             float c_cur[32];
             if (read_c) load_c_chunk(c_tile, row_stride, n0 + lane, p.N, rows, c_cur);
-            const int accb = local & 1;
-            const uint32_t acc_phase = (local >> 1) & 1;
+            const int accb = local % ACC_BUFS;
+            const uint32_t acc_phase = (local / ACC_BUFS) & 1;
             const bool ready = waiter.wait(acc_full_bar(accb), acc_phase);
             if (!__all_sync(0xffffffffu, ready)) {
                 if (lane == 0) waiter.fail(kRoleEpilogue, i);
@@ -554,14 +605,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             ptx::tc_fence_after_sync();
             const uint32_t t_row =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(accb * BN);
-            store_tile<Cfg::EPI_PITCH>(p, t_row, c_tile, row_stride, rows, n0, w.width, buf, lane, c_cur);
-            ptx::tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                if constexpr (PAIR)
-                    ptx::mbar_arrive_cluster(ptx::mapa_shared(acc_empty_bar(accb), 0));
-                else
-                    ptx::mbar_arrive(acc_empty_bar(accb));
+            // the accumulator's parts in order (SUBS == 1: the whole item);
+            // each part goes back to the MMA warp as soon as it has been read,
+            // and parts past the item's width are handed back at once
+            const int32_t part_n = SUBS > 1 ? Cfg::SUB_N : w.width;
+            for (int h = 0; h < SUBS; ++h) {
+                const int32_t pn0 = n0 + h * part_n;
+                if (h * part_n < w.width) {
+                    if (h > 0 && read_c) load_c_chunk(c_tile, row_stride, pn0 + lane, p.N, rows, c_cur);
+                    store_tile<Cfg::EPI_PITCH>(p, t_row + static_cast<uint32_t>(h * part_n), c_tile, row_stride,
+                                               rows, pn0, part_n, buf, lane, c_cur);
+                }
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (PAIR)
+                        ptx::mbar_arrive_cluster(ptx::mapa_shared(acc_empty_bar(accb, h), 0));
+                    else
+                        ptx::mbar_arrive(acc_empty_bar(accb, h));
+                }
             }
             ++local;
         }

@@ -43,10 +43,15 @@ constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;
 using Cfg256 = TileConfig<256, 4, false>;   // one CTA per 128 x 256 tile
 using Cfg128 = TileConfig<128, 6, false>;   // one CTA per 128 x 128 tile
 using CfgPair = TileConfig<256, 6, true>;   // a CTA pair per 256 x 256 tile
-// the same three shapes for a column-major B (a K-major B operand)
+using CfgWide = TileConfig<512, 4, true>;   // a CTA pair per 256 x 512 tile
+// the same four shapes for a column-major B (a K-major B operand)
 using Cfg256K = TileConfig<256, 4, false, true>;
 using Cfg128K = TileConfig<128, 6, false, true>;
 using CfgPairK = TileConfig<256, 6, true, true>;
+using CfgWideK = TileConfig<512, 4, true, true>;
+// one occupancy query (max_pair_clusters) serves both pair shapes
+static_assert(CfgWide::SMEM_BYTES <= CfgPair::SMEM_BYTES && CfgWide::THREADS == CfgPair::THREADS,
+              "the wide pair kernel fits wherever the 256 x 256 pair kernel fits");
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -106,6 +111,32 @@ bool auto_pair(int64_t M, int64_t N, int32_t num_sms) {
     return ceil_div(M, 256) * ceil_div(N, 256) >= num_sms / 2;
 }
 
+// Time of a persistent walk over `tiles` tiles on `units` CTA pairs, in
+// tile times: full waves, plus half a wave when the last wave is at most half
+// full (its tiles then run as half-width items), else a whole wave.
+double pair_waves(int64_t tiles, int64_t units) {
+    const int64_t full = tiles / units, rem = tiles % units;
+    return static_cast<double>(full) + (rem == 0 ? 0.0 : (2 * rem <= units && full > 0 ? 0.5 : 1.0));
+}
+
+// Pair tiles 512 wide instead of 256: each SM then receives 48 KB of operands
+// per 1024 MMA cycles instead of 32 KB per 512, under the rate at which TMA
+// fills one SM's shared memory (measured near 54 bytes per cycle), so the
+// tensor pipe idles less; the price is a single accumulator buffer, whose
+// epilogue overlaps the next tile only by halves, and coarser waves. The
+// relative pipe efficiencies weigh the two walks against each other (at
+// 8192^3, with waves of equal cost, 512-wide tiles ran 7.5 % faster); with
+// K below 6144 the exposed epilogue costs more than that (measured: 5 %
+// slower at 16384 x 16384 x 4096, 17 % at 8192 x 8192 x 2048).
+bool auto_wide(int64_t M, int64_t N, int64_t K, int64_t units) {
+    if (K < 6144 || N < 1024) return false;
+    constexpr double kEff256 = 0.84, kEff512 = 0.84 * 1.075;
+    const int64_t mt = ceil_div(M, 256);
+    const double t256 = pair_waves(mt * ceil_div(N, 256), units) / kEff256;
+    const double t512 = 2.0 * pair_waves(mt * ceil_div(N, 512), units) / kEff512;
+    return t512 < t256;
+}
+
 // How the tensor-core pass reads A (see AMaps in gemm_kernel.cuh): one row
 // class when A's rows start on 16-byte boundaries (or A was staged), else
 // P = 16 / gcd(2 * lda, 16) classes of rows i = r (mod P), each read from the
@@ -141,6 +172,7 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     mpgemm_status_t st = validate(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, opt.b_col_major);
     if (st != MPGEMM_OK) return st;
     if (num_sms <= 0) return MPGEMM_ERR_INVALID_VALUE;
+    if (opt.tile_n == 512 && opt.tile_m == 128) return MPGEMM_ERR_INVALID_VALUE;   // 512 wide: pairs only
     mpgemm_plan_t p;
     std::memset(&p, 0, sizeof(p));
     p.tile_m = 128;
@@ -155,12 +187,19 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
         return MPGEMM_OK;
     }
     p.stage_b = (opt.force_staging || !aligned16(B, ldb, 2)) ? 1 : 0;
-    const bool pair = opt.tile_m ? (opt.tile_m == 256) : (!opt.tile_n && auto_pair(M, N, num_sms));
+    const bool pair = opt.tile_n == 512 ||
+                      (opt.tile_m ? (opt.tile_m == 256) : (!opt.tile_n && auto_pair(M, N, num_sms)));
     if (pair) {
+        int64_t pair_units = num_sms / 2;
+        if (opt.pair_units > 0) pair_units = std::min<int64_t>(pair_units, opt.pair_units);
+        if (opt.max_ctas > 0) pair_units = std::min<int64_t>(pair_units, std::max<int64_t>(1, opt.max_ctas / 2));
+        pair_units = std::max<int64_t>(1, pair_units);
+        const bool wide = opt.tile_n == 512 ||
+                          (!opt.tile_m && !opt.tile_n && auto_wide(M, N, K, pair_units));
         p.tile_m = 256;
-        p.tile_n = 256;
-        p.stages = CfgPair::STAGES;
-        p.smem_bytes = CfgPair::SMEM_BYTES;
+        p.tile_n = wide ? 512 : 256;
+        p.stages = wide ? CfgWide::STAGES : CfgPair::STAGES;
+        p.smem_bytes = wide ? CfgWide::SMEM_BYTES : CfgPair::SMEM_BYTES;
     } else {
         p.tile_n = opt.tile_n ? opt.tile_n : auto_tile_n(M, N, num_sms);
         p.stages = (p.tile_n == 256) ? Cfg256::STAGES : Cfg128::STAGES;
@@ -400,9 +439,11 @@ cudaError_t prepare_kernels() {
     cudaError_t e = set_smem_attr<Cfg256>();
     if (e == cudaSuccess) e = set_smem_attr<Cfg128>();
     if (e == cudaSuccess) e = set_smem_attr<CfgPair>();
+    if (e == cudaSuccess) e = set_smem_attr<CfgWide>();
     if (e == cudaSuccess) e = set_smem_attr<Cfg256K>();
     if (e == cudaSuccess) e = set_smem_attr<Cfg128K>();
     if (e == cudaSuccess) e = set_smem_attr<CfgPairK>();
+    if (e == cudaSuccess) e = set_smem_attr<CfgWideK>();
     return e;
 }
 
@@ -469,6 +510,9 @@ cudaError_t launch_plan(const mpgemm_plan_t& plan, bool b_col_major, int max_clu
     if (plan.tile_m == 256) {
         int grid = plan.grid;
         if (max_clusters > 0 && grid > 2 * max_clusters) grid = 2 * max_clusters;
+        if (plan.tile_n == 512)
+            return b_col_major ? launch_tc<CfgWideK>(grid, ta, tb, gp, stream)
+                               : launch_tc<CfgWide>(grid, ta, tb, gp, stream);
         return b_col_major ? launch_tc<CfgPairK>(grid, ta, tb, gp, stream)
                            : launch_tc<CfgPair>(grid, ta, tb, gp, stream);
     }
@@ -568,7 +612,7 @@ mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const 
                             mpgemm_plan_t* out) {
     if (!out) return MPGEMM_ERR_INVALID_VALUE;
     if (tile_m != 0 && tile_m != 128 && tile_m != 256) return MPGEMM_ERR_INVALID_VALUE;
-    if (tile_n != 0 && tile_n != 128 && tile_n != 256) return MPGEMM_ERR_INVALID_VALUE;
+    if (tile_n != 0 && tile_n != 128 && tile_n != 256 && tile_n != 512) return MPGEMM_ERR_INVALID_VALUE;
     if (max_ctas < 0) return MPGEMM_ERR_INVALID_VALUE;
     Options opt;
     opt.tile_m = tile_m;
@@ -639,7 +683,7 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
     if (!h) return MPGEMM_ERR_INVALID_VALUE;
     switch (opt) {
         case MPGEMM_OPT_TILE_N:
-            if (value != 0 && value != 128 && value != 256) return MPGEMM_ERR_INVALID_VALUE;
+            if (value != 0 && value != 128 && value != 256 && value != 512) return MPGEMM_ERR_INVALID_VALUE;
             h->opt.tile_n = static_cast<int32_t>(value);
             return MPGEMM_OK;
         case MPGEMM_OPT_MAX_CTAS:

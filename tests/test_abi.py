@@ -140,10 +140,22 @@ def test_tiling_of_the_ragged_k_tail(golden_facts):
 
 
 def test_tile_selection_and_grid():
-    # large square: CTA pairs on 256 x 256 tiles, one pair per two SMs
+    # large square, long K: CTA pairs on 256 x 512 tiles, one pair per two SMs
     p = _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192)
-    assert (p["tile_m"], p["tile_n"]) == (256, 256) and p["tiles"] == 32 * 32 and p["grid"] == 152
-    assert p["smem_bytes"] <= 232448 and p["stages"] == 6
+    assert (p["tile_m"], p["tile_n"]) == (256, 512) and p["tiles"] == 32 * 16 and p["grid"] == 152
+    assert p["smem_bytes"] <= 232448 and p["stages"] == 4
+    # (512 tiles on 76 pairs: a last wave of 56 tiles, more than half full, not split)
+    assert p["split_tiles"] == 0 and p["items"] == 512
+    # the same square with a short K keeps 256 x 256 pair tiles
+    p = _plan(M=8192, N=8192, K=1024, lda=1024, ldb=8192, ldc=8192)
+    assert (p["tile_m"], p["tile_n"]) == (256, 256) and p["stages"] == 6
+    # 512-wide tiles on request, also for small or ragged shapes; never with one CTA per tile
+    p = _plan(M=300, N=700, K=200, lda=200, ldb=700, ldc=700, tile_n=512)
+    assert (p["tile_m"], p["tile_n"]) == (256, 512) and p["tiles"] == 2 * 2 and p["grid"] == 8
+    p = _plan(M=300, N=700, K=200, lda=200, ldb=700, ldc=700, tile_m=256, tile_n=512)
+    assert (p["tile_m"], p["tile_n"]) == (256, 512)
+    with pytest.raises(mp.MpgemmError):
+        _plan(tile_m=128, tile_n=512)
     # N = 257 would waste half of the last column band: single CTAs
     p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257, beta=0.5)
     assert (p["tile_m"], p["tile_n"]) == (128, 256)
@@ -160,9 +172,10 @@ def test_tile_selection_and_grid():
     # 1000 x 800: 32 wide tiles would leave most SMs idle: 128 x 128
     p = _plan(M=1000, N=800, K=1200, lda=1200, ldb=800, ldc=800)
     assert p["tile_n"] == 128 and p["tiles"] == 8 * 7
-    # 8192^3: 1024 pair tiles on 76 pairs leave a last wave of 36 tiles, split in halves
-    p = _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192)
-    assert p["split_tiles"] == 1024 % 76 and p["items"] == 1024 + 36
+    # 8192^3 in 256 x 256 pair tiles: 1024 tiles on 76 pairs leave a last wave
+    # of 36 tiles, split in halves
+    p = _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192, tile_m=256)
+    assert p["tile_n"] == 256 and p["split_tiles"] == 1024 % 76 and p["items"] == 1024 + 36
     # too few tiles to occupy the GPU: K is cut into slices (no empty slice)
     p = _plan(M=4096, N=16, K=4096, lda=4096, ldb=16, ldc=16)
     assert p["k_splits"] == 4 and p["items"] == 32 * 4 and p["split_tiles"] == 0

@@ -200,10 +200,12 @@ def test_cta_pair_persistence_and_staging(mp, max_ctas):
         check_full(h, ops)
 
 
-def test_cta_pair_stall_reports_timeout(mp):
+@pytest.mark.parametrize("tile_n", [256, 512])
+def test_cta_pair_stall_reports_timeout(mp, tile_n):
     ops = workloads.make_operands(512, 512, 128, seed=85)
     with mp.Handle() as h:
         h.set_option(mp.Option.TILE_M, 256)
+        h.set_option(mp.Option.TILE_N, tile_n)
         h.set_option(mp.Option.WAIT_LIMIT_US, 20000)
         h.set_option(mp.Option.TEST_STALL, 1)
         from parity import device_operands
@@ -217,22 +219,67 @@ def test_cta_pair_stall_reports_timeout(mp):
         check_full(h, ops)
 
 
+WIDE_SHAPES = [  # (M, N, K): 256 x 512 pair tiles; one tile, ragged edges, many tiles
+    (256, 512, 64), (256, 512, 192), (200, 136, 617), (300, 700, 700), (511, 513, 129),
+    (1024, 1536, 1000), (257, 1025, 65), (1000, 800, 1200),
+]
+
+
+@pytest.mark.parametrize("M,N,K", WIDE_SHAPES)
+def test_wide_pair_tiles(mp, M, N, K):
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_N, 512)
+        check_full(h, workloads.make_operands(M, N, K, beta=0.75, c_dist="normal", seed=M + N + K + 1))
+
+
+def test_wide_pair_integer_bitwise(mp):
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_N, 512)
+        ops = workloads.make_operands(512, 1024, 1024, dist="int3", dist_b="int2", seed=86)
+        check_full(h, ops, exact=True)
+
+
+@pytest.mark.parametrize("max_ctas", [2, 6])
+def test_wide_pair_persistence_and_staging(mp, max_ctas):
+    # few pairs walk many tiles through the single accumulator buffer (both
+    # of its halves wrap many phases); unaligned lda, ldb and ldc are staged
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_N, 512)
+        h.set_option(mp.Option.MAX_CTAS, max_ctas)
+        ops = workloads.make_operands(1300, 1100, 333, lda=335, ldb=1103, ldc=1101, alpha=-1.5,
+                                      beta=0.5, c_dist="normal", seed=87)
+        check_full(h, ops)
+
+
+def test_wide_pair_large_sampled(mp):
+    # the workload's own recipe (N(0, 0.5^2) inputs) at 4096 x 6144 x 4096 in
+    # 256 x 512 tiles, sampled
+    ops = workloads.make_operands(4096, 6144, 4096, dist="normal_0.5", seed=88)
+    I, J = workloads.sample_indices(4096, 6144, 20000, seed=89)
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_N, 512)
+        check_sampled(h, ops, I, J)
+
+
 SPLIT_CASES = [  # (tile_m, tile_n, max_ctas, M, N, K): the last partial wave is split in halves
     (128, 256, 5, 1000, 800, 200),     # half tiles wholly past column 800 are skipped
     (128, 128, 7, 700, 600, 336),
     (256, 256, 8, 1300, 1100, 150),
     (256, 256, 10, 768, 1024, 320),
+    (256, 512, 8, 1300, 1100, 150),    # 256-wide halves; the half past column 1100 is skipped
 ]
 
 
 @pytest.mark.parametrize("tile_m,tile_n,max_ctas,M,N,K", SPLIT_CASES)
 def test_split_tail_tiles(mp, tile_m, tile_n, max_ctas, M, N, K):
+    set_n = tile_m == 128 or tile_n == 512
     plan = mp.plan(M, N, K, 1.0, 256, K, 256, N, 0.5, 256, N, tile_m=tile_m,
-                   tile_n=0 if tile_m == 256 else tile_n, max_ctas=max_ctas)
+                   tile_n=tile_n if set_n else 0, max_ctas=max_ctas)
     assert plan["split_tiles"] > 0 and plan["items"] == plan["tiles"] + plan["split_tiles"]
+    assert (plan["tile_m"], plan["tile_n"]) == (tile_m, tile_n)
     with mp.Handle() as h:
         h.set_option(mp.Option.TILE_M, tile_m)
-        if tile_m == 128:
+        if set_n:
             h.set_option(mp.Option.TILE_N, tile_n)
         h.set_option(mp.Option.MAX_CTAS, max_ctas)
         check_full(h, workloads.make_operands(M, N, K, beta=0.5, c_dist="normal", seed=M + K))

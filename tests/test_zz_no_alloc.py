@@ -1,8 +1,8 @@
 """mpgemm_run_noalloc: the GEMM for callers that cannot allocate.
 
 Some callers may not allocate device memory when they call the GEMM (code
-running inside another component's memory budget, or while someone else is
-capturing the stream into a graph) and cannot own a handle. For them the
+running inside another component's fixed memory budget, or on a path that
+runs when device memory is already exhausted) and cannot own a handle. For them the
 library exports one entry point that allocates nothing: operands that need
 an aligned staging copy are staged into a fixed 16 MiB device array owned
 by the library. These tests call it through the C ABI and check its output
