@@ -84,17 +84,52 @@ def measured_peaks() -> dict:
     return {"tflops": 1900.0, "tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def stored_traffic(workload_index: int):
+def traffic_path(workload_index: int) -> str:
+    return os.path.join(ROOT, "profiles", f"gemm_tc_kernel_traffic_w{workload_index}.json")
+
+
+def stored_traffic(workload_index: int, tile: str):
     """Per-launch DRAM bytes of the tensor-core kernel from a committed ncu
-    summary, if it was taken on the current kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"gemm_tc_kernel_traffic_w{workload_index}.json")
+    summary, if it was taken on the current kernel sources and tile shape."""
+    path = traffic_path(workload_index)
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    if d.get("source_hash") != source_hash():
+    if d.get("source_hash") != source_hash() or d.get("tile") != tile:
         return None
     return d.get("dram_bytes_per_launch")
+
+
+def record_traffic(args):
+    """Write the per-launch DRAM traffic record of the tensor-core kernel
+    from an ncu CSV log holding dram__bytes_read.sum, dram__bytes_write.sum
+    and gpu__time_duration.sum of one launch (the workload's own tile shape,
+    current sources)."""
+    import csv
+
+    import mixed_precision_dense_gb300 as mp
+    w = workloads.WORKLOADS[args.workload]
+    plan = mp.plan(w.M, w.N, w.K, w.alpha, 256, w.lda, 256, w.ldb, w.beta, 256, w.ldc, num_sms=args.num_sms,
+                   tile_m=args.tile_m, tile_n=args.tile_n)
+    metrics, kernel = {}, None
+    with open(args.record_traffic) as f:
+        rows = [r for r in csv.reader(line for line in f if not line.startswith("=="))]
+    hdr = rows[0]
+    ki, mi, vi = hdr.index("Kernel Name"), hdr.index("Metric Name"), hdr.index("Metric Value")
+    for r in rows[1:]:
+        if len(r) > vi and "gemm_tc_kernel" in r[ki]:
+            kernel = r[ki]
+            metrics[r[mi]] = float(r[vi].replace(",", ""))
+    rd, wr = metrics["dram__bytes_read.sum"], metrics["dram__bytes_write.sum"]
+    rec = {"kernel": kernel, "workload": w.name, "tile": f"{plan['tile_m']}x{plan['tile_n']}",
+           "dram_bytes_read_per_launch": int(rd), "dram_bytes_write_per_launch": int(wr),
+           "dram_bytes_per_launch": int(rd + wr), "ncu_duration_ns": int(metrics["gpu__time_duration.sum"]),
+           "source_hash": source_hash(), "command": args.record_command}
+    with open(traffic_path(args.workload), "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    print(json.dumps(rec))
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -385,7 +420,7 @@ def run_ours(args):
     achieved = gemm_flops(w.M, w.N, w.K) / (kernel_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["tflops"], 4),
-                "traffic": None if args.shape else stored_traffic(args.workload),
+                "traffic": None if args.shape else stored_traffic(args.workload, f"{plan['tile_m']}x{plan['tile_n']}"),
                 "peak_kind": f"bf16 dense burst, {peaks['source']}",
                 "frac_of_sustained": (round(achieved / peaks["tflops_sustained"], 4)
                                       if peaks["tflops_sustained"] else None),
@@ -659,6 +694,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-check", action="store_true")
     ap.add_argument("--no-cublas", action="store_true")
+    ap.add_argument("--record-traffic", default="",
+                    help="write the workload's stored ncu DRAM-traffic record from this ncu CSV log and exit")
+    ap.add_argument("--record-command", default="", help="the ncu command that produced --record-traffic's log")
+    ap.add_argument("--num-sms", type=int, default=152, help="SM count assumed by --record-traffic's plan")
     ap.add_argument("--tile-m", type=int, default=0, choices=[0, 128, 256],
                     help="force the tile height (0 = the library's choice)")
     ap.add_argument("--tile-n", type=int, default=0, choices=[0, 128, 256, 512],
@@ -667,7 +706,9 @@ def main(argv=None):
                     help="run the capstone gate's eight cases and print a report instead")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least three warm-up steps, whatever was asked
-    if args.gate:
+    if args.record_traffic:
+        record_traffic(args)
+    elif args.gate:
         run_gate(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -49,8 +49,11 @@ using Cfg256K = TileConfig<256, 4, false, true>;
 using Cfg128K = TileConfig<128, 6, false, true>;
 using CfgPairK = TileConfig<256, 6, true, true>;
 using CfgWideK = TileConfig<512, 4, true, true>;
-// one occupancy query (max_pair_clusters) serves both pair shapes
-static_assert(CfgWide::SMEM_BYTES <= CfgPair::SMEM_BYTES && CfgWide::THREADS == CfgPair::THREADS,
+// one occupancy query (max_pair_clusters) serves both pair shapes: shared
+// memory limits either to one CTA per SM, and both stay far below the SM's
+// thread and register limits at that occupancy
+static_assert(CfgWide::SMEM_BYTES <= CfgPair::SMEM_BYTES && CfgPair::SMEM_BYTES > 232448 / 2 &&
+                  CfgWide::THREADS <= 256 && CfgPair::THREADS <= 256,
               "the wide pair kernel fits wherever the 256 x 256 pair kernel fits");
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -120,17 +123,16 @@ double pair_waves(int64_t tiles, int64_t units) {
 }
 
 // Pair tiles 512 wide instead of 256: each SM then receives 48 KB of operands
-// per 1024 MMA cycles instead of 32 KB per 512, under the rate at which TMA
-// fills one SM's shared memory (measured near 54 bytes per cycle), so the
-// tensor pipe idles less; the price is a single accumulator buffer, whose
-// epilogue overlaps the next tile only by halves, and coarser waves. The
-// relative pipe efficiencies weigh the two walks against each other (at
-// 8192^3, with waves of equal cost, 512-wide tiles ran 7.5 % faster); with
-// K below 6144 the exposed epilogue costs more than that (measured: 5 %
-// slower at 16384 x 16384 x 4096, 17 % at 8192 x 8192 x 2048).
+// per 1024 MMA cycles instead of 32 KB per 512, and two threads issue the
+// MMAs (one per 256-column half of the accumulator), which keeps the tensor
+// pipe fed; the price is a single accumulator buffer, whose epilogue
+// overlaps the next tile only by halves, and coarser waves. The relative pipe
+// efficiencies weigh the two walks against each other (at 8192^3, with waves
+// of nearly equal cost, 512-wide tiles ran 13 % faster); below K = 2048 the
+// exposed epilogue is no longer paid for.
 bool auto_wide(int64_t M, int64_t N, int64_t K, int64_t units) {
-    if (K < 6144 || N < 1024) return false;
-    constexpr double kEff256 = 0.84, kEff512 = 0.84 * 1.075;
+    if (K < 2048 || N < 1024) return false;
+    constexpr double kEff256 = 0.84, kEff512 = 0.84 * 1.18;
     const int64_t mt = ceil_div(M, 256);
     const double t256 = pair_waves(mt * ceil_div(N, 256), units) / kEff256;
     const double t512 = 2.0 * pair_waves(mt * ceil_div(N, 512), units) / kEff512;
