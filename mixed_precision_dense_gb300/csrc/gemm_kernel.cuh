@@ -12,14 +12,16 @@
 //               tcgen05.mma (K = 16 per instruction, FP16 x FP16 -> FP32) into
 //               one of two accumulator buffers and frees each stage with
 //               tcgen05.commit.
-//   warp 6      (256 x 512 pair tiles only) a second MMA warp: warp 1 issues
-//               the MMAs of accumulator columns 0-255, warp 6 those of
+//   warp 10     (256 x 512 pair tiles only) a second MMA warp: warp 1 issues
+//               the MMAs of accumulator columns 0-255, warp 10 those of
 //               256-511. The tensor pipe queues only about one MMA ahead of
 //               an issuing thread, and each barrier wait stalls that thread;
 //               with two issuers one keeps the pipe fed while the other
 //               waits (measured: full MMA rate with two issuers, about 60 %
 //               with one, for one barrier test per four MMAs).
-//   warps 2-5   epilogue: each warp reads its 32 accumulator rows with
+//   warps 2-5   epilogue (warps 2-9 for 256 x 512 pair tiles, two warps per
+//               32 accumulator rows, each taking half of the columns): each
+//               warp reads its 32 accumulator rows with
 //               tcgen05.ld (32x32b: TMEM lane = row), applies alpha in FP32,
 //               turns each 32 x 32 chunk around through shared memory so that
 //               every store instruction writes 128 contiguous bytes of one
@@ -131,7 +133,11 @@ struct TileConfig {
     static constexpr int A_BYTES = BM * BK * 2;        // 16 KB
     static constexpr int B_ATOM_BYTES = BK * 64 * 2;   // one 64-column box of B: 8 KB
     static constexpr int B_BYTES = BK * B_COLS * 2;
-    static constexpr int EPI_WARPS = 4;
+    // epilogue warps: 4 (one per 32 tensor-memory lanes), or 8 for the
+    // 256 x 512 tile, whose single accumulator is drained while the MMAs of
+    // the next tile wait: two warps per lane quarter, each taking half of
+    // every part's columns
+    static constexpr int EPI_WARPS = BN == 512 ? 8 : 4;
     static constexpr int EPI_PITCH = 33;               // floats per row of a transpose buffer
     static constexpr int EPI_BYTES = EPI_WARPS * 32 * EPI_PITCH * 4;
     static constexpr int TMEM_COLS = ACC_BUFS * BN;
@@ -144,7 +150,7 @@ struct TileConfig {
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARRIERS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
-    static constexpr int THREADS = 192 + 32 * (ISSUERS - 1);
+    static constexpr int THREADS = 32 * (2 + EPI_WARPS + ISSUERS - 1);
     static_assert(BN == 128 || BN == 256 || (PAIR && BN == 512), "tile width");
     static_assert(!PAIR || BN >= 256, "pair tiles are 256 x 256 or 256 x 512");
     static_assert(SUBS == 1 || ACC_BUFS == 1, "parts only for a single accumulator buffer");
@@ -594,6 +600,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     } else if (warp >= 2 && warp < 2 + Cfg::EPI_WARPS) {
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;             // tensor-memory lanes 32*quarter ..
+        const int col_half = (warp - 2) / 4;      // with 8 warps: which half of each part's columns
+        constexpr int COL_SPLIT = Cfg::EPI_WARPS / 4;
         float* buf = epi_buf + (warp - 2) * 32 * Cfg::EPI_PITCH;
         const bool read_c = (p.beta != 0.0f) && p.k_splits <= 1;
         int32_t local = 0;
@@ -608,10 +616,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const int64_t row_stride = static_cast<int64_t>(p.a_classes) * p.ldc;
             float* c_tile = p.C + (cls + static_cast<int64_t>(p.a_classes) * jb) * p.ldc;
             const int32_t n0 = w.n0;
+            const int32_t part_n = SUBS > 1 ? Cfg::SUB_N : w.width;   // columns per accumulator part
+            const int32_t my_n = part_n / COL_SPLIT;                  // of which this warp stores
+            const int32_t my_off = col_half * my_n;
             // beta * C needs C's old values: the first chunk's loads go out now,
             // while the MMAs of this tile are still running.
             float c_cur[32];
-            if (read_c) load_c_chunk(c_tile, row_stride, n0 + lane, p.N, rows, c_cur);
+            if (read_c) load_c_chunk(c_tile, row_stride, n0 + my_off + lane, p.N, rows, c_cur);
             const int accb = local % ACC_BUFS;
             const uint32_t acc_phase = (local / ACC_BUFS) & 1;
             const bool ready = waiter.wait(acc_full_bar(accb), acc_phase);
@@ -625,13 +636,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // the accumulator's parts in order (SUBS == 1: the whole item);
             // each part goes back to the MMA warp as soon as it has been read,
             // and parts past the item's width are handed back at once
-            const int32_t part_n = SUBS > 1 ? Cfg::SUB_N : w.width;
             for (int h = 0; h < SUBS; ++h) {
-                const int32_t pn0 = n0 + h * part_n;
+                const int32_t pn0 = n0 + h * part_n + my_off;
                 if (h * part_n < w.width) {
                     if (h > 0 && read_c) load_c_chunk(c_tile, row_stride, pn0 + lane, p.N, rows, c_cur);
-                    store_tile<Cfg::EPI_PITCH>(p, t_row + static_cast<uint32_t>(h * part_n), c_tile, row_stride,
-                                               rows, pn0, part_n, buf, lane, c_cur);
+                    store_tile<Cfg::EPI_PITCH>(p, t_row + static_cast<uint32_t>(h * part_n + my_off), c_tile,
+                                               row_stride, rows, pn0, my_n, buf, lane, c_cur);
                 }
                 ptx::tc_fence_before_sync();
                 __syncwarp();

@@ -52,8 +52,8 @@ using CfgWideK = TileConfig<512, 4, true, true>;
 // one occupancy query (max_pair_clusters) serves both pair shapes: shared
 // memory limits either to one CTA per SM, and both stay far below the SM's
 // thread and register limits at that occupancy
-static_assert(CfgWide::SMEM_BYTES <= CfgPair::SMEM_BYTES && CfgPair::SMEM_BYTES > 232448 / 2 &&
-                  CfgWide::THREADS <= 256 && CfgPair::THREADS <= 256,
+static_assert(CfgWide::SMEM_BYTES > 232448 / 2 && CfgPair::SMEM_BYTES > 232448 / 2 &&
+                  CfgWide::THREADS <= 384 && CfgPair::THREADS <= 384,
               "the wide pair kernel fits wherever the 256 x 256 pair kernel fits");
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
