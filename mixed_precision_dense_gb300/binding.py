@@ -36,6 +36,7 @@ class Option(enum.IntEnum):
     TILE_M = 7
     L2_KEEP = 8
     SPLIT_K = 9
+    C_STORE = 10
 
 
 class BLayout(enum.IntEnum):

@@ -75,8 +75,11 @@ namespace mpgemm {
 // rows earlier (rows before 0 arrive as zeros).
 constexpr int kMaxAClasses = 8;
 
-struct AMaps {
-    CUtensorMap map[kMaxAClasses];
+// The tensor maps of A (one per row class) and of C (FP32, 32 x 32 boxes,
+// 128-byte swizzle; used only when GemmParams::c_tma is set).
+struct TensorMaps {
+    CUtensorMap a[kMaxAClasses];
+    CUtensorMap c;
 };
 
 struct GemmParams {
@@ -99,6 +102,8 @@ struct GemmParams {
     uint64_t wait_limit_ns;
     int32_t test_stall;     // 1: the load warp issues nothing (timeout test)
     int32_t keep_a;         // L2 hints: 1 = keep A (evict B first), 0 = keep B (evict A first)
+    int32_t c_tma;          // 1: C is written by TMA stores through TensorMaps::c (beta == 0,
+                            //    no split-K, one row class, C and ldc 16-byte aligned)
 };
 
 enum : int32_t { kRoleLoad = 1, kRoleMma = 2, kRoleEpilogue = 3 };
@@ -138,8 +143,8 @@ struct TileConfig {
     // the next tile wait: two warps per lane quarter, each taking half of
     // every part's columns
     static constexpr int EPI_WARPS = BN == 512 ? 8 : 4;
-    static constexpr int EPI_PITCH = 33;               // floats per row of a transpose buffer
-    static constexpr int EPI_BYTES = EPI_WARPS * 32 * EPI_PITCH * 4;
+    static constexpr int EPI_CHUNK_BYTES = 32 * 32 * 4;  // one warp's 32 x 32 FP32 chunk buffer
+    static constexpr int EPI_BYTES = EPI_WARPS * EPI_CHUNK_BYTES;
     static constexpr int TMEM_COLS = ACC_BUFS * BN;
     // full and empty per stage; accumulator full per buffer; accumulator
     // empty per buffer and part
@@ -155,6 +160,7 @@ struct TileConfig {
     static_assert(!PAIR || BN >= 256, "pair tiles are 256 x 256 or 256 x 512");
     static_assert(SUBS == 1 || ACC_BUFS == 1, "parts only for a single accumulator buffer");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment");
+    static_assert(OFF_EPI % 1024 == 0, "chunk buffers are 1024-byte aligned (128-byte swizzle atoms)");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "tensor memory allocation");
 };
@@ -293,16 +299,31 @@ __device__ __forceinline__ void load_c_chunk(const float* c_rows, int64_t ldc, i
         v[rr] = (col_ok && rr < rows) ? __ldg(c_rows + static_cast<int64_t>(rr) * ldc + col) : 0.0f;
 }
 
-// The epilogue of one work item for one warp: 32 rows of C starting at c_tile,
-// row_stride elements apart, of which the first `rows` exist (the TMEM
-// lanes of this warp's quarter; t_row addresses them at the accumulator's
-// first column) and columns n0 .. n0+width-1. c_cur holds the first chunk of
-// C when beta != 0 (loaded before the accumulator was ready); each later
-// chunk's loads go out before the previous chunk is stored.
-template <int PITCH>
-__device__ __forceinline__ void store_tile(const GemmParams& p, uint32_t t_row, float* c_tile,
-                                          int64_t row_stride, int32_t rows, int32_t n0, int32_t width,
-                                          float* buf, int lane, float (&c_cur)[32]) {
+// Byte offset of element (row, col) in a warp's 32 x 32 FP32 chunk buffer:
+// rows of 128 bytes whose 16-byte groups sit at position group ^ (row & 7),
+// the layout of the tensor memory accelerator's 128-byte swizzle. A lane
+// writing its row as eight 16-byte stores, and 32 lanes reading one element
+// each of a row, both touch every bank once.
+__device__ __forceinline__ uint32_t chunk_off(int row, int col) {
+    return static_cast<uint32_t>(row * 128 + ((((col >> 2) ^ row) & 7) << 4) + (col & 3) * 4);
+}
+
+// The epilogue of one work item for one warp: 32 rows of C (the tensor
+// memory lanes of this warp's quarter; t_row addresses them at the
+// accumulator's first column), of which the first `rows` exist, and columns
+// n0 .. n0+width-1. Each 32 x 32 chunk goes from tensor memory through
+// registers (alpha applied) into the warp's chunk buffer (buf / buf_s, the
+// generic and shared-window addresses of the same bytes). Then either
+//  - TMA path (p.c_tma): one lane stores the chunk with a tiled TMA store at
+//    C row row0, column n0 + 32 c; the map clips rows and columns outside C;
+//  - otherwise each lane writes one column of the chunk (128 contiguous
+//    bytes per store instruction across the warp), c_tile + rr * row_stride
+//    addressing row rr, with beta * C added (c_cur: the chunk's old C values,
+//    loaded ahead of the accumulator) or, for split-K, added atomically.
+__device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMap* tmap_c, uint32_t t_row,
+                                          float* c_tile, int64_t row_stride, int32_t rows, int32_t row0,
+                                          int32_t n0, int32_t width, uint8_t* buf, uint32_t buf_s, int lane,
+                                          float (&c_cur)[32]) {
     const float alpha = p.alpha, beta = p.beta;
     const bool split = p.k_splits > 1;        // add the partial product into C
     const bool read_c = (beta != 0.0f) && !split;
@@ -315,8 +336,25 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, uint32_t t_row, 
         if (read_c && c + 1 < chunks)
             load_c_chunk(c_rows, row_stride, n0 + (c + 1) * 32 + lane, p.N, rows, c_next);
         ptx::tmem_load_wait();
+        if (p.c_tma) {
+            // the previous chunk's TMA store must have read the buffer
+            if (lane == 0) ptx::bulk_wait_read_all();
+            __syncwarp();
+        }
 #pragma unroll
-        for (int j = 0; j < 32; ++j) buf[lane * PITCH + j] = alpha * __uint_as_float(r[j]);
+        for (int q = 0; q < 8; ++q)
+            ptx::st_shared_v4(buf_s + chunk_off(lane, 4 * q), alpha * __uint_as_float(r[4 * q]),
+                              alpha * __uint_as_float(r[4 * q + 1]), alpha * __uint_as_float(r[4 * q + 2]),
+                              alpha * __uint_as_float(r[4 * q + 3]));
+        if (p.c_tma) {
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::tma_store_2d(tmap_c, buf_s, n0 + c * 32, row0);
+                ptx::bulk_commit_group();
+            }
+            continue;
+        }
         __syncwarp();
         const int32_t col = n0 + c * 32 + lane;
         if (col < p.N) {
@@ -325,15 +363,17 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, uint32_t t_row, 
 #pragma unroll
                 for (int rr = 0; rr < 32; ++rr)
                     if (rr < rows)
-                        cp[static_cast<int64_t>(rr) * row_stride] = fmaf(beta, c_cur[rr], buf[rr * PITCH + lane]);
+                        cp[static_cast<int64_t>(rr) * row_stride] =
+                            fmaf(beta, c_cur[rr], ptx::ld_shared_f32(buf_s + chunk_off(rr, lane)));
             } else if (split) {
 #pragma unroll
                 for (int rr = 0; rr < 32; ++rr)
-                    if (rr < rows) atomicAdd(cp + static_cast<int64_t>(rr) * row_stride, buf[rr * PITCH + lane]);
+                    if (rr < rows)
+                        atomicAdd(cp + static_cast<int64_t>(rr) * row_stride, ptx::ld_shared_f32(buf_s + chunk_off(rr, lane)));
             } else {
 #pragma unroll
                 for (int rr = 0; rr < 32; ++rr)
-                    if (rr < rows) cp[static_cast<int64_t>(rr) * row_stride] = buf[rr * PITCH + lane];
+                    if (rr < rows) cp[static_cast<int64_t>(rr) * row_stride] = ptx::ld_shared_f32(buf_s + chunk_off(rr, lane));
             }
         }
         if (read_c) {
@@ -342,11 +382,12 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, uint32_t t_row, 
         }
         __syncwarp();
     }
+    (void)buf;
 }
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ AMaps amaps, const __grid_constant__ CUtensorMap tmap_b,
+    gemm_tc_kernel(const __grid_constant__ TensorMaps maps, const __grid_constant__ CUtensorMap tmap_b,
                    const GemmParams p) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr bool PAIR = Cfg::PAIR;
@@ -358,7 +399,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
     const uint32_t sA = base + Cfg::OFF_A;
     const uint32_t sB = base + Cfg::OFF_B;
-    float* epi_buf = reinterpret_cast<float*>(gbase + Cfg::OFF_EPI);
+    uint8_t* epi_buf = gbase + Cfg::OFF_EPI;
     const uint32_t bar0 = base + Cfg::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -390,7 +431,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         ptx::fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        for (int r = 0; r < p.a_classes; ++r) ptx::prefetch_tensormap(&amaps.map[r]);
+        for (int r = 0; r < p.a_classes; ++r) ptx::prefetch_tensormap(&maps.a[r]);
+        if (p.c_tma) ptx::prefetch_tensormap(&maps.c);
         ptx::prefetch_tensormap(&tmap_b);
     }
     if (warp == 1) {
@@ -433,7 +475,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const int32_t n0 = w.n0 + (PAIR ? static_cast<int32_t>(rank) * (sub_n / 2) : 0);
                     int32_t cls, j0;
                     a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
-                    const CUtensorMap* map_a = &amaps.map[cls];
+                    const CUtensorMap* map_a = &maps.a[cls];
                     const int32_t a_row = j0 + static_cast<int32_t>(rank) * BM;   // class row
                     const int32_t b_shift = p.a_shift[cls];
                     // single: only the boxes that hold valid columns; pair: all boxes
@@ -602,7 +644,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const int quarter = warp & 3;             // tensor-memory lanes 32*quarter ..
         const int col_half = (warp - 2) / 4;      // with 8 warps: which half of each part's columns
         constexpr int COL_SPLIT = Cfg::EPI_WARPS / 4;
-        float* buf = epi_buf + (warp - 2) * 32 * Cfg::EPI_PITCH;
+        uint8_t* buf = epi_buf + (warp - 2) * Cfg::EPI_CHUNK_BYTES;
+        const uint32_t buf_s = base + Cfg::OFF_EPI + static_cast<uint32_t>((warp - 2) * Cfg::EPI_CHUNK_BYTES);
         const bool read_c = (p.beta != 0.0f) && p.k_splits <= 1;
         int32_t local = 0;
         for (int32_t i = first_item; i < p.items; i += item_step) {
@@ -640,8 +683,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const int32_t pn0 = n0 + h * part_n + my_off;
                 if (h * part_n < w.width) {
                     if (h > 0 && read_c) load_c_chunk(c_tile, row_stride, pn0 + lane, p.N, rows, c_cur);
-                    store_tile<Cfg::EPI_PITCH>(p, t_row + static_cast<uint32_t>(h * part_n + my_off), c_tile,
-                                               row_stride, rows, pn0, my_n, buf, lane, c_cur);
+                    store_tile(p, &maps.c, t_row + static_cast<uint32_t>(h * part_n + my_off), c_tile, row_stride,
+                               rows, jb, pn0, my_n, buf, buf_s, lane, c_cur);
                 }
                 ptx::tc_fence_before_sync();
                 __syncwarp();
@@ -654,6 +697,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
             ++local;
         }
+        // the TMA stores must complete (and stop reading this CTA's shared
+        // memory) before the CTA exits
+        if (p.c_tma && lane == 0) ptx::bulk_wait_all();
         __syncwarp();
     }
 

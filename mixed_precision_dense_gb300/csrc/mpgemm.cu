@@ -70,6 +70,7 @@ struct Options {
     int32_t split_k = 0;            // 0 automatic, 1 never, n >= 2: n slices of K per tile
     int32_t pair_units = 0;         // CTA pairs resident at once (0: num_sms / 2)
     int32_t test_stall = 0;
+    int32_t c_store = 0;            // 0 automatic (TMA stores when possible), 1 per-lane stores
     uint64_t wait_limit_ns = kDefaultWaitLimitNs;
 };
 
@@ -139,7 +140,7 @@ bool auto_wide(int64_t M, int64_t N, int64_t K, int64_t units) {
     return t512 < t256;
 }
 
-// How the tensor-core pass reads A (see AMaps in gemm_kernel.cuh): one row
+// How the tensor-core pass reads A (see TensorMaps in gemm_kernel.cuh): one row
 // class when A's rows start on 16-byte boundaries (or A was staged), else
 // P = 16 / gcd(2 * lda, 16) classes of rows i = r (mod P), each read from the
 // aligned address at or below row r with a shift of a few elements.
@@ -386,7 +387,7 @@ cudaError_t set_smem_attr() {
 }
 
 template <class Cfg>
-cudaError_t launch_tc(int grid, const AMaps& ta, const CUtensorMap& tb, const GemmParams& gp,
+cudaError_t launch_tc(int grid, const TensorMaps& ta, const CUtensorMap& tb, const GemmParams& gp,
                       cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -452,7 +453,7 @@ cudaError_t prepare_kernels() {
 // The A tensor maps (one per row class) and the class fields of the kernel
 // parameters, for A as the kernel will read it (staged or not).
 bool encode_a(const mpgemm_plan_t& plan, const void* a_use, int64_t lda_use, int64_t M, int64_t K,
-              AMaps* maps, GemmParams* gp) {
+              TensorMaps* maps, GemmParams* gp) {
     std::memset(maps, 0, sizeof(*maps));
     const AClassLayout L = a_class_layout(a_use, lda_use, M, plan.a_classes > 0, plan.tile_m);
     gp->a_classes = L.P;
@@ -464,11 +465,40 @@ bool encode_a(const mpgemm_plan_t& plan, const void* a_use, int64_t lda_use, int
     gp->a_class_first_tile[kMaxAClasses] = static_cast<int32_t>(L.first_tile[L.P]);
     for (int32_t r = 0; r < L.P; ++r) {
         if (L.rows[r] == 0) continue;
-        if (!encode_f16(&maps->map[r], reinterpret_cast<const void*>(L.base[r]), L.rows[r], K + L.shift[r],
+        if (!encode_f16(&maps->a[r], reinterpret_cast<const void*>(L.base[r]), L.rows[r], K + L.shift[r],
                         L.P * lda_use, 64, 128))
             return false;
     }
     return true;
+}
+
+// Row-major FP32 matrix rows x cols with pitch ld (elements), 32 x 32 boxes,
+// 128-byte swizzle: the tiled TMA store of the epilogue's chunks.
+bool encode_f32_store(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Let the epilogue store C with TMA when it can: C is only written
+// (beta == 0), no split-K slices add into it, its rows are contiguous (one
+// row class), its base and pitch are 16-byte aligned, and N is a multiple of
+// 4. A TMA store clips a row only at 16-byte granularity: measured on GB300,
+// with N = 1025 the store of the chunk at column 1024 also wrote columns
+// 1025-1027 of every row (the padding of C). Otherwise, or when c_store
+// forbids it, every lane stores its own column.
+void encode_c(const mpgemm_plan_t& plan, float* C, int64_t M, int64_t N, int64_t ldc, float beta,
+              int32_t c_store, TensorMaps* maps, GemmParams* gp) {
+    gp->c_tma = 0;
+    if (c_store == 1 || beta != 0.0f || plan.k_splits > 1 || gp->a_classes != 1 || N % 4 != 0) return;
+    if (!aligned16(C, ldc, 4)) return;
+    if (encode_f32_store(&maps->c, C, M, N, ldc)) gp->c_tma = 1;
 }
 
 GemmParams make_params(const mpgemm_plan_t& plan, int64_t M, int64_t N, int64_t K, float alpha,
@@ -500,7 +530,7 @@ GemmParams make_params(const mpgemm_plan_t& plan, int64_t M, int64_t N, int64_t 
 }
 
 cudaError_t launch_plan(const mpgemm_plan_t& plan, bool b_col_major, int max_clusters,
-                        const AMaps& ta, const CUtensorMap& tb, const GemmParams& gp,
+                        const TensorMaps& ta, const CUtensorMap& tb, const GemmParams& gp,
                         cudaStream_t stream) {
     if (plan.k_splits > 1 && gp.beta != 1.0f) {
         // the slices add into C: apply beta (or clear C) once, first
@@ -720,6 +750,10 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
             if (value != 0 && value != 1) return MPGEMM_ERR_INVALID_VALUE;
             h->opt.test_stall = static_cast<int32_t>(value);
             return MPGEMM_OK;
+        case MPGEMM_OPT_C_STORE:
+            if (value != 0 && value != 1) return MPGEMM_ERR_INVALID_VALUE;
+            h->opt.c_store = static_cast<int32_t>(value);
+            return MPGEMM_OK;
     }
     return MPGEMM_ERR_INVALID_VALUE;
 }
@@ -778,8 +812,9 @@ mpgemm_status_t mpgemm_run_ex(mpgemm_handle_t h, mpgemm_b_layout_t b_layout, int
     GemmParams gp = make_params(plan, M, N, K, alpha, beta, C, ldc, h->status_dev,
                                 h->opt.wait_limit_ns, h->opt.test_stall,
                                 keep_a_operand(plan, h->opt.l2_keep));
-    AMaps ta;
+    TensorMaps ta;
     if (!encode_a(plan, a_use, lda_use, M, K, &ta, &gp)) return MPGEMM_ERR_CUDA;
+    encode_c(plan, C, M, N, ldc, beta, h->opt.c_store, &ta, &gp);
     if (launch_plan(plan, b_col, h->max_clusters, ta, tb, gp, stream) != cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;
@@ -996,8 +1031,9 @@ extern "C" mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K, f
     if (!encode_f16(&tb, b_use, K, N, ldb_use, 64, 64)) return MPGEMM_ERR_CUDA;
     GemmParams gp = make_params(plan, M, N, K, alpha, beta, C, ldc, status, opt.wait_limit_ns, 0,
                                 keep_a_operand(plan, 0));
-    AMaps ta;
+    TensorMaps ta;
     if (!encode_a(plan, a_use, lda_use, M, K, &ta, &gp)) return MPGEMM_ERR_CUDA;
+    encode_c(plan, C, M, N, ldc, beta, 0, &ta, &gp);
     if (launch_plan(plan, false, d.max_clusters, ta, tb, gp, stream) != cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;

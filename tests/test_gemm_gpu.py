@@ -425,3 +425,42 @@ def test_stalled_pipeline_reports_timeout_and_context_survives(mp):
         assert st == mp.Status.OK
         h.set_option(mp.Option.TEST_STALL, 0)
         check_full(h, ops)
+
+
+C_STORE_CASES = [  # (M, N, K, ldc, tile_m, tile_n): beta == 0, C rows 16-byte aligned
+    (300, 260, 200, 260, 0, 0),          # ragged rows: the TMA store clips past row 300
+    (257, 129, 65, 132, 128, 256),       # ragged columns: clipped past column 129, padding untouched
+    (1000, 800, 1200, 804, 128, 128),
+    (511, 700, 300, 704, 256, 0),        # CTA pairs, 256 x 256
+    (513, 1025, 129, 1028, 256, 512),    # N % 4 != 0: per-lane stores (a TMA store would write
+                                         # the rest of the last 16-byte group, into the padding)
+    (513, 1028, 128, 1032, 256, 512),    # CTA pairs, 256 x 512, eight epilogue warps, partial last chunk
+    (513, 1028, 128, 1032, 256, 0),
+    (64, 4096, 700, 4096, 128, 256),
+]
+
+
+@pytest.mark.parametrize("M,N,K,ldc,tile_m,tile_n", C_STORE_CASES)
+def test_tma_store_of_c_matches_per_lane_stores(mp, M, N, K, ldc, tile_m, tile_n):
+    # C written by tiled TMA stores (the automatic choice here) against the
+    # oracle, and bit for bit against the per-lane stores of the same sums
+    ops = workloads.make_operands(M, N, K, ldc=ldc, alpha=1.25, seed=M + N + K + 5)
+    outs = []
+    for c_store in (0, 1):
+        with mp.Handle() as h:
+            h.set_option(mp.Option.TILE_M, tile_m)
+            h.set_option(mp.Option.TILE_N, tile_n)
+            h.set_option(mp.Option.C_STORE, c_store)
+            check_full(h, ops)
+            got, _, _ = c_result(run_gpu(h, ops), ops)
+            outs.append(got)
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_tma_store_falls_back_for_unaligned_c(mp):
+    # a C base 4 bytes past a 16-byte boundary cannot be a TMA target: the
+    # per-lane path writes it, guard rows and padding stay untouched
+    ops = workloads.make_operands(300, 260, 200, ldc=264, seed=91)
+    with mp.Handle() as h:
+        check_full(h, ops, c_offset=1)
+        check_full(h, ops, c_offset=2)
