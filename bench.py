@@ -549,6 +549,81 @@ GATE_CASES = [  # "Day 80, Capstone 4: a tensor-core GEMM", "Independent gate"
 ]
 
 
+def run_acc16_study(args):
+    """FP16 accumulators against FP32 ("Day 72: Tensor cores with WMMA",
+    Exercise: AccT = __half; "Day 80, Capstone 4", "Common failures"). For
+    uniform[-1, 1) inputs at growing K, the FP16-accumulated C is compared
+    with the FP32-accumulated C of the same library (parity-tested; its own
+    error is at most about K * 2^-24 * S, negligible here) in units of
+    S = sum_k |A_ik B_kj|, and against the parity tolerance 1e-3 * S + 1e-5.
+    Then the pages' integer sizes, the 4096-term overflow and a sum growing
+    by 15 per K = 16 step past 2048. Prints a markdown report."""
+    import numpy as np
+    import torch
+
+    import mixed_precision_dense_gb300 as mp
+    mp.build()
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream(dev)
+
+    def gemm(A, B, acc):
+        M, K = A.shape
+        N = B.shape[1]
+        C = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
+        with mp.Handle() as h:
+            h.set_option(mp.Option.ACCUMULATOR, acc)
+            h.run(M, N, K, 1.0, A.data_ptr(), K, B.data_ptr(), N, 0.0, C.data_ptr(), N, stream.cuda_stream)
+            stream.synchronize()
+            st, info = h.sync_status(stream.cuda_stream)
+            if st != mp.Status.OK:
+                raise RuntimeError(f"device reported {st.name} {info}")
+        return C
+
+    print("| inputs | K | max err / S (FP16 acc) | median err / S | elements over 1e-3 S + 1e-5 | max err / S (FP32 acc, vs FP64 of 2048 samples) |")
+    print("|---|---|---|---|---|---|")
+    M = N = 1024
+    for lo, K in [(lo, K) for lo in (-1.0, 0.0) for K in (256, 1024, 2048, 4096, 8192, 16384)]:
+        g = torch.Generator().manual_seed(900 + K + int(lo))
+        A = (lo + torch.rand(M, K, generator=g) * (1 - lo)).half().to(dev)
+        B = (lo + torch.rand(K, N, generator=g) * (1 - lo)).half().to(dev)
+        c32, c16 = gemm(A, B, 32), gemm(A, B, 16)
+        S = torch.matmul(A.float().abs(), B.float().abs())
+        r = ((c16 - c32).abs() / S).flatten()
+        over = int(((c16 - c32).abs() > 1e-3 * S + 1e-5).sum())
+        # FP32 path against an FP64 product on a sample (host float64 arithmetic)
+        idx = torch.randint(0, M * N, (2048,), generator=g)
+        i, j = (idx // N).tolist(), (idx % N).tolist()
+        a64, b64 = A.double().cpu(), B.double().cpu()
+        exact = (a64[i] * b64[:, j].t()).sum(1)
+        e32 = float(((c32.cpu().double().flatten()[idx] - exact).abs() / S.cpu().double().flatten()[idx]).max())
+        print(f"| uniform[{lo:g}, 1) | {K} | {float(r.max()):.2e} | {float(r.median()):.2e} | {over} of {M * N} | {e32:.1e} |")
+
+    print()
+    for size in (256, 1024, 2048):
+        g = torch.Generator().manual_seed(700 + size)
+        A = torch.randint(-3, 4, (size, size), generator=g).half().to(dev)
+        B = torch.randint(-2, 3, (size, size), generator=g).half().to(dev)
+        same = bool(torch.equal(gemm(A, B, 16), gemm(A, B, 32)))
+        print(f"- integer inputs in [-3, 3] x [-2, 2] at {size}^3: FP16-accumulated C "
+              f"{'equals' if same else 'differs from'} the exact (FP32-accumulated) C")
+    A = torch.full((256, 4096), 4.0, device=dev).half()
+    B = torch.full((4096, 256), 4.0, device=dev).half()
+    c16, c32 = gemm(A, B, 16), gemm(A, B, 32)
+    print(f"- 4096 products of 4 x 4: FP32 gives {float(c32[0, 0]):.0f} everywhere: "
+          f"{bool(torch.all(c32 == 65536.0))}; FP16 gives +inf everywhere: {bool(torch.all(torch.isinf(c16)))}")
+    steps = 512
+    A = torch.ones(128, 16 * steps, device=dev).half()
+    B = torch.ones(16 * steps, 128, device=dev)
+    B[15::16, :] = 0.0
+    c16 = gemm(A, B.half(), 16)
+    d = np.float16(0)
+    for _ in range(steps):
+        d = np.float16(d + np.float16(15))
+    print(f"- a sum growing by 15 per K = 16 step, {steps} steps (exact {15 * steps}): FP16 accumulators give "
+          f"{float(c16[0, 0]):.0f} (all elements equal: {bool(torch.all(c16 == c16[0, 0]))}); adding 15 and "
+          f"rounding to FP16 once per step gives {float(d):.0f}")
+
+
 def run_gate(args):
     """The gate's eight cases through mpgemm_solve (A row-major, B column-major,
     C row-major): every case checked against the CPU oracle (bit for bit for
@@ -702,12 +777,16 @@ def main(argv=None):
                     help="force the tile height (0 = the library's choice)")
     ap.add_argument("--tile-n", type=int, default=0, choices=[0, 128, 256, 512],
                     help="force the tile width (0 = the library's choice)")
+    ap.add_argument("--acc16-study", action="store_true",
+                    help="compare FP16 with FP32 accumulation and print a report instead")
     ap.add_argument("--gate", action="store_true",
                     help="run the capstone gate's eight cases and print a report instead")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least three warm-up steps, whatever was asked
     if args.record_traffic:
         record_traffic(args)
+    elif args.acc16_study:
+        run_acc16_study(args)
     elif args.gate:
         run_gate(args)
     elif args.impl == "reference":

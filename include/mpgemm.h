@@ -153,11 +153,19 @@ typedef enum {
                                      whose partial products are added into C (after C = beta*C),
                                      so results may differ in the last bits from run to run;
                                      1 = never; n in 2..64 = n slices (one-CTA tiles only) */
-    MPGEMM_OPT_C_STORE = 10       /* 0 = automatic (default): C is written with tiled TMA stores
+    MPGEMM_OPT_C_STORE = 10,      /* 0 = automatic (default): C is written with tiled TMA stores
                                      when beta == 0, K is not split, A is read as one row class,
                                      C's base and ldc are 16-byte aligned and N is a multiple of
                                      4; 1 = always one store per lane (the path used in every
                                      other case) */
+    MPGEMM_OPT_ACCUMULATOR = 11   /* 0 or 32 = FP32 accumulators (default, the operation defined
+                                     above); 16 = FP16 accumulators, a study variant of "Day 72:
+                                     Tensor cores with WMMA" (Exercise: AccT = __half): every
+                                     K = 16 step is rounded to FP16, so sums lose low bits once
+                                     they pass 2048 and overflow to infinity past 65504 ("Day 80,
+                                     Capstone 4", "Common failures"). K is never split then: the
+                                     whole K range accumulates in one FP16 accumulator. Not for
+                                     production use. */
 } mpgemm_option_t;
 
 /* Set an option. Unknown options or out-of-range values return

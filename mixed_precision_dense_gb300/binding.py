@@ -37,6 +37,7 @@ class Option(enum.IntEnum):
     L2_KEEP = 8
     SPLIT_K = 9
     C_STORE = 10
+    ACCUMULATOR = 11
 
 
 class BLayout(enum.IntEnum):

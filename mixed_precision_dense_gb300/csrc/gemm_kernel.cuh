@@ -60,6 +60,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "ptx.cuh"
 
@@ -104,6 +105,7 @@ struct GemmParams {
     int32_t keep_a;         // L2 hints: 1 = keep A (evict B first), 0 = keep B (evict A first)
     int32_t c_tma;          // 1: C is written by TMA stores through TensorMaps::c (beta == 0,
                             //    no split-K, one row class, C and ldc 16-byte aligned)
+    int32_t acc16;          // 1: FP16 accumulators (the study variant; the product path is FP32)
 };
 
 enum : int32_t { kRoleLoad = 1, kRoleMma = 2, kRoleEpilogue = 3 };
@@ -299,6 +301,13 @@ __device__ __forceinline__ void load_c_chunk(const float* c_rows, int64_t ldc, i
         v[rr] = (col_ok && rr < rows) ? __ldg(c_rows + static_cast<int64_t>(rr) * ldc + col) : 0.0f;
 }
 
+// An accumulator element as read from tensor memory: FP32, or (FP16
+// accumulators) an FP16 value in the low 16 bits of the 32-bit column
+// (measured layout for kind::f16 with an F16 D: one element per column).
+__device__ __forceinline__ float acc_value(uint32_t word, int32_t acc16) {
+    return acc16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(word & 0xFFFFu))) : __uint_as_float(word);
+}
+
 // Byte offset of element (row, col) in a warp's 32 x 32 FP32 chunk buffer:
 // rows of 128 bytes whose 16-byte groups sit at position group ^ (row & 7),
 // the layout of the tensor memory accelerator's 128-byte swizzle. A lane
@@ -343,9 +352,9 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMa
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-            ptx::st_shared_v4(buf_s + chunk_off(lane, 4 * q), alpha * __uint_as_float(r[4 * q]),
-                              alpha * __uint_as_float(r[4 * q + 1]), alpha * __uint_as_float(r[4 * q + 2]),
-                              alpha * __uint_as_float(r[4 * q + 3]));
+            ptx::st_shared_v4(buf_s + chunk_off(lane, 4 * q), alpha * acc_value(r[4 * q], p.acc16),
+                              alpha * acc_value(r[4 * q + 1], p.acc16), alpha * acc_value(r[4 * q + 2], p.acc16),
+                              alpha * acc_value(r[4 * q + 3], p.acc16));
         if (p.c_tma) {
             ptx::fence_proxy_async_smem();
             __syncwarp();
@@ -547,7 +556,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 int32_t cls, j0;
                 a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
                 const int32_t lead_cols = p.a_shift[cls];   // columns before the rows' start
-                const uint32_t idesc = ptx::idesc_f16_f32(Cfg::TILE_M, n_mma, false, !Cfg::B_KMAJOR);
+                // D format bits 4-5: 1 = F32 accumulators, 0 = F16 (the study variant)
+                const uint32_t idesc = ptx::idesc_f16_f32(Cfg::TILE_M, n_mma, false, !Cfg::B_KMAJOR) &
+                                       ~(p.acc16 ? (3u << 4) : 0u);
                 const int buf = local % ACC_BUFS;
                 const uint32_t acc_phase = (local / ACC_BUFS) & 1;
                 if constexpr (SUBS == 1) {

@@ -71,6 +71,7 @@ struct Options {
     int32_t pair_units = 0;         // CTA pairs resident at once (0: num_sms / 2)
     int32_t test_stall = 0;
     int32_t c_store = 0;            // 0 automatic (TMA stores when possible), 1 per-lane stores
+    int32_t acc16 = 0;              // 1: FP16 accumulators (study variant)
     uint64_t wait_limit_ns = kDefaultWaitLimitNs;
 };
 
@@ -235,7 +236,9 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     // added into C. Shorter problems lose more to the extra pass over C and
     // the atomic adds than they gain from the extra SMs.
     int64_t splits = 1;
-    if (!pair && opt.split_k != 1) {
+    // (FP16 accumulators never split K: the study variant keeps the whole K
+    // range in one FP16 accumulator, as an __half accumulator type would)
+    if (!pair && opt.split_k != 1 && !opt.acc16) {
         if (opt.split_k >= 2)
             splits = opt.split_k;
         else if (p.tiles * 4 <= units && k_blocks >= 32)
@@ -754,6 +757,10 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
             if (value != 0 && value != 1) return MPGEMM_ERR_INVALID_VALUE;
             h->opt.c_store = static_cast<int32_t>(value);
             return MPGEMM_OK;
+        case MPGEMM_OPT_ACCUMULATOR:
+            if (value != 0 && value != 16 && value != 32) return MPGEMM_ERR_INVALID_VALUE;
+            h->opt.acc16 = value == 16 ? 1 : 0;
+            return MPGEMM_OK;
     }
     return MPGEMM_ERR_INVALID_VALUE;
 }
@@ -815,6 +822,7 @@ mpgemm_status_t mpgemm_run_ex(mpgemm_handle_t h, mpgemm_b_layout_t b_layout, int
     TensorMaps ta;
     if (!encode_a(plan, a_use, lda_use, M, K, &ta, &gp)) return MPGEMM_ERR_CUDA;
     encode_c(plan, C, M, N, ldc, beta, h->opt.c_store, &ta, &gp);
+    gp.acc16 = h->opt.acc16;
     if (launch_plan(plan, b_col, h->max_clusters, ta, tb, gp, stream) != cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;
