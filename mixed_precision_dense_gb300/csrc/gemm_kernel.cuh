@@ -12,13 +12,14 @@
 //               tcgen05.mma (K = 16 per instruction, FP16 x FP16 -> FP32) into
 //               one of two accumulator buffers and frees each stage with
 //               tcgen05.commit.
-//   warp 10     (256 x 512 pair tiles only) a second MMA warp: warp 1 issues
-//               the MMAs of accumulator columns 0-255, warp 10 those of
-//               256-511. The tensor pipe queues only about one MMA ahead of
-//               an issuing thread, and each barrier wait stalls that thread;
-//               with two issuers one keeps the pipe fed while the other
-//               waits (measured: full MMA rate with two issuers, about 60 %
-//               with one, for one barrier test per four MMAs).
+//   warp 6/10   (CTA-pair tiles) a second MMA warp, the one after the
+//               epilogue warps: warp 1 issues the MMAs of the first half of
+//               the accumulator's columns, this warp those of the second. The
+//               tensor pipe queues only about one MMA ahead of an issuing
+//               thread, and each barrier wait stalls that thread; with two
+//               issuers one keeps the pipe fed while the other waits
+//               (measured: full MMA rate with two issuers, about 60 % with
+//               one, for one barrier test per four MMAs).
 //   warps 2-5   epilogue (warps 2-9 for 256 x 512 pair tiles, two warps per
 //               32 accumulator rows, each taking half of the columns): each
 //               warp reads its 32 accumulator rows with
@@ -111,7 +112,7 @@ struct GemmParams {
 enum : int32_t { kRoleLoad = 1, kRoleMma = 2, kRoleEpilogue = 3 };
 enum : int32_t { kStatusTimeout = 1 };
 
-template <int BN_, int STAGES_, bool PAIR_, bool B_KMAJOR_ = false>
+template <int BN_, int STAGES_, bool PAIR_, bool B_KMAJOR_ = false, int ISSUERS_ = (BN_ == 512 ? 2 : 1)>
 struct TileConfig {
     static constexpr bool PAIR = PAIR_;
     // B column-major ([N, K] rows of K): a K-major operand like A. Its 64-row
@@ -126,17 +127,23 @@ struct TileConfig {
     static constexpr int B_COLS = BN / CTAS;           // columns of B each CTA loads
     static constexpr int BK = 64;                      // 64 halves = one 128-byte swizzle row
     static constexpr int STAGES = STAGES_;
-    // one MMA instruction covers SUB_N columns: BN, except that a pair tile
-    // 512 wide takes two instructions of 256 per K step
-    static constexpr int SUB_N = BN < 256 ? BN : 256;
+    // threads issuing MMAs: one, or two, each owning one part (a column
+    // range) of the accumulator, so the two streams of MMAs never touch the
+    // same accumulator columns
+    static constexpr int ISSUERS = ISSUERS_;
+    // one MMA instruction covers SUB_N columns: BN, except that a tile 512
+    // wide takes two instructions of 256 per K step, and a 256-wide tile with
+    // two issuers two of 128
+    static constexpr int SUB_N = BN == 512 ? 256 : (ISSUERS == 2 ? BN / 2 : BN);
     static constexpr int SUBS = BN / SUB_N;
     // two accumulator buffers (the epilogue of tile i overlaps the MMAs of
     // tile i+1) when they fit in the 512 columns of tensor memory, else one,
     // whose SUBS parts are handed back one by one
     static constexpr int ACC_BUFS = 2 * BN <= 512 ? 2 : 1;
-    // threads issuing MMAs: one per accumulator part (each owns its columns,
-    // so the two streams of MMAs never touch the same accumulator)
-    static constexpr int ISSUERS = SUBS;
+    static constexpr int RELEASE_PARTS = ACC_BUFS == 1 ? SUBS : 1;
+    // B boxes (64 columns) per part held by one CTA: a pair CTA holds half
+    // of every part's columns
+    static constexpr int ATOMS_PER_PART = SUB_N / (PAIR ? 128 : 64);
     static constexpr int A_BYTES = BM * BK * 2;        // 16 KB
     static constexpr int B_ATOM_BYTES = BK * 64 * 2;   // one 64-column box of B: 8 KB
     static constexpr int B_BYTES = BK * B_COLS * 2;
@@ -150,7 +157,7 @@ struct TileConfig {
     static constexpr int TMEM_COLS = ACC_BUFS * BN;
     // full and empty per stage; accumulator full per buffer; accumulator
     // empty per buffer and part
-    static constexpr int NUM_BARRIERS = 2 * STAGES + ACC_BUFS + ACC_BUFS * SUBS;
+    static constexpr int NUM_BARRIERS = 2 * STAGES + ACC_BUFS + ACC_BUFS * RELEASE_PARTS;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = STAGES * A_BYTES;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
@@ -160,7 +167,8 @@ struct TileConfig {
     static constexpr int THREADS = 32 * (2 + EPI_WARPS + ISSUERS - 1);
     static_assert(BN == 128 || BN == 256 || (PAIR && BN == 512), "tile width");
     static_assert(!PAIR || BN >= 256, "pair tiles are 256 x 256 or 256 x 512");
-    static_assert(SUBS == 1 || ACC_BUFS == 1, "parts only for a single accumulator buffer");
+    static_assert(ISSUERS == 1 || ISSUERS == SUBS, "one issuer, or one issuer per part");
+    static_assert(SUB_N >= (PAIR ? 128 : 64) && ATOMS_PER_PART >= 1, "parts hold whole B boxes");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment");
     static_assert(OFF_EPI % 1024 == 0, "chunk buffers are 1024-byte aligned (128-byte swizzle atoms)");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
@@ -412,9 +420,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const uint32_t bar0 = base + Cfg::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    constexpr int ACC_BUFS = Cfg::ACC_BUFS, SUBS = Cfg::SUBS;
+    constexpr int ACC_BUFS = Cfg::ACC_BUFS, SUBS = Cfg::SUBS, RELEASE_PARTS = Cfg::RELEASE_PARTS;
     auto acc_full_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-    auto acc_empty_bar = [&](int b, int h) { return bar0 + 8u * (2 * STAGES + ACC_BUFS + b * SUBS + h); };
+    auto acc_empty_bar = [&](int b, int h) { return bar0 + 8u * (2 * STAGES + ACC_BUFS + b * RELEASE_PARTS + h); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Cfg::OFF_MISC);
     volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + Cfg::OFF_MISC + 4);
 
@@ -434,7 +442,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
             ptx::mbar_init(acc_full_bar(b), Cfg::ISSUERS);
-            for (int h = 0; h < SUBS; ++h) ptx::mbar_init(acc_empty_bar(b, h), Cfg::EPI_WARPS * Cfg::CTAS);
+            for (int h = 0; h < RELEASE_PARTS; ++h) ptx::mbar_init(acc_empty_bar(b, h), Cfg::EPI_WARPS * Cfg::CTAS);
         }
         *abort_flag = 0;
         ptx::fence_barrier_init();
@@ -550,18 +558,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             for (int32_t i = first_item; ok && i < p.items; i += item_step) {
                 const WorkItem w = work_item<BN>(p, i);
                 if (w.n0 >= p.N) continue;
-                // columns per instruction and instructions per K step
-                const int32_t n_mma = PAIR ? min(w.width, Cfg::SUB_N) : 64 * min(w.width / 64, (p.N - w.n0 + 63) / 64);
-                const int32_t n_sub = PAIR ? w.width / n_mma : 1;
+                // columns the MMAs cover (a one-CTA tile skips the 64-column
+                // boxes wholly past N) and the parts (instructions per K step)
+                // they fall into: part h is columns [h SUB_N, h SUB_N + cols)
+                const int32_t n_valid = PAIR ? w.width : 64 * min(w.width / 64, (p.N - w.n0 + 63) / 64);
+                const int32_t n_parts = (n_valid + Cfg::SUB_N - 1) / Cfg::SUB_N;
                 int32_t cls, j0;
                 a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
                 const int32_t lead_cols = p.a_shift[cls];   // columns before the rows' start
-                // D format bits 4-5: 1 = F32 accumulators, 0 = F16 (the study variant)
-                const uint32_t idesc = ptx::idesc_f16_f32(Cfg::TILE_M, n_mma, false, !Cfg::B_KMAJOR) &
-                                       ~(p.acc16 ? (3u << 4) : 0u);
                 const int buf = local % ACC_BUFS;
                 const uint32_t acc_phase = (local / ACC_BUFS) & 1;
-                if constexpr (SUBS == 1) {
+                if constexpr (RELEASE_PARTS == 1) {
                     if (!waiter.wait(acc_empty_bar(buf, 0), acc_phase ^ 1u)) {
                         waiter.fail(kRoleMma, -1);
                         ok = false;
@@ -583,9 +590,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t b_base = sB + stage * Cfg::B_BYTES;
                     bool pending = false;   // MMAs issued from this stage
                     const int32_t h_begin = Cfg::ISSUERS > 1 ? me : 0;
-                    const int32_t h_end = Cfg::ISSUERS > 1 ? min(me + 1, n_sub) : n_sub;
+                    const int32_t h_end = Cfg::ISSUERS > 1 ? min(me + 1, n_parts) : n_parts;
                     for (int32_t h = h_begin; ok && h < h_end; ++h) {
-                        if constexpr (SUBS > 1) {
+                        if constexpr (RELEASE_PARTS > 1) {
                             // the first use of part h in this item: wait until the
                             // epilogue has read the previous item's part h
                             if (kb == w.kb0) {
@@ -597,10 +604,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                 ptx::tc_fence_after_sync();
                             }
                         }
-                        // part h: n_mma accumulator columns further, B atoms of
-                        // n_mma / 2 columns (this CTA's half) further
-                        const uint32_t d_part = d_tmem + static_cast<uint32_t>(h * n_mma);
-                        const uint32_t b_part = b_base + static_cast<uint32_t>(h * (n_mma / 128) * Cfg::B_ATOM_BYTES);
+                        // part h: SUB_N accumulator columns further, ATOMS_PER_PART
+                        // B boxes further (a pair CTA holds half of each part's
+                        // columns); D format bits 4-5: 1 = F32 accumulators,
+                        // 0 = F16 (the study variant)
+                        const int32_t part_cols = min(Cfg::SUB_N, n_valid - h * Cfg::SUB_N);
+                        const uint32_t idesc = ptx::idesc_f16_f32(Cfg::TILE_M, part_cols, false, !Cfg::B_KMAJOR) &
+                                               ~(p.acc16 ? (3u << 4) : 0u);
+                        const uint32_t d_part = d_tmem + static_cast<uint32_t>(h * Cfg::SUB_N);
+                        const uint32_t b_part =
+                            b_base + static_cast<uint32_t>(h * Cfg::ATOMS_PER_PART * Cfg::B_ATOM_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk) {
                             // A: K-major, 128-byte rows, 8-row groups 1024 B apart;
@@ -670,7 +683,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const int64_t row_stride = static_cast<int64_t>(p.a_classes) * p.ldc;
             float* c_tile = p.C + (cls + static_cast<int64_t>(p.a_classes) * jb) * p.ldc;
             const int32_t n0 = w.n0;
-            const int32_t part_n = SUBS > 1 ? Cfg::SUB_N : w.width;   // columns per accumulator part
+            const int32_t part_n = RELEASE_PARTS > 1 ? Cfg::SUB_N : w.width;   // columns per released part
             const int32_t my_n = part_n / COL_SPLIT;                  // of which this warp stores
             const int32_t my_off = col_half * my_n;
             // beta * C needs C's old values: the first chunk's loads go out now,
@@ -690,7 +703,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // the accumulator's parts in order (SUBS == 1: the whole item);
             // each part goes back to the MMA warp as soon as it has been read,
             // and parts past the item's width are handed back at once
-            for (int h = 0; h < SUBS; ++h) {
+            for (int h = 0; h < RELEASE_PARTS; ++h) {
                 const int32_t pn0 = n0 + h * part_n + my_off;
                 if (h * part_n < w.width) {
                     if (h > 0 && read_c) load_c_chunk(c_tile, row_stride, pn0 + lane, p.N, rows, c_cur);

@@ -42,12 +42,12 @@ constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;
 
 using Cfg256 = TileConfig<256, 4, false>;   // one CTA per 128 x 256 tile
 using Cfg128 = TileConfig<128, 6, false>;   // one CTA per 128 x 128 tile
-using CfgPair = TileConfig<256, 6, true>;   // a CTA pair per 256 x 256 tile
+using CfgPair = TileConfig<256, 6, true, false, 2>;   // a CTA pair per 256 x 256 tile, two MMA issuers
 using CfgWide = TileConfig<512, 4, true>;   // a CTA pair per 256 x 512 tile
 // the same four shapes for a column-major B (a K-major B operand)
 using Cfg256K = TileConfig<256, 4, false, true>;
 using Cfg128K = TileConfig<128, 6, false, true>;
-using CfgPairK = TileConfig<256, 6, true, true>;
+using CfgPairK = TileConfig<256, 6, true, true, 2>;
 using CfgWideK = TileConfig<512, 4, true, true>;
 // one occupancy query (max_pair_clusters) serves both pair shapes: shared
 // memory limits either to one CTA per SM, and both stay far below the SM's
