@@ -148,10 +148,12 @@ typedef enum {
     MPGEMM_OPT_L2_KEEP = 8,       /* L2 hints for the operand loads: 0 = automatic (default,
                                      keep the operand more tiles re-read), 1 = keep A,
                                      2 = keep B */
-    MPGEMM_OPT_SPLIT_K = 9,       /* 0 = automatic (default): when the output tiles cannot occupy
-                                     half of the SMs, each tile's K range is cut into slices
-                                     whose partial products are added into C (after C = beta*C),
-                                     so results may differ in the last bits from run to run;
+    MPGEMM_OPT_SPLIT_K = 9,       /* 0 = automatic (default): when the one-CTA output tiles
+                                     occupy at most a quarter of the SMs and K has 32 or more
+                                     64-wide blocks (half of the SMs and 16 blocks when
+                                     beta == 1), each tile's K range is cut into slices whose
+                                     partial products are added into C (after C = beta*C), so
+                                     results may differ in the last bits from run to run;
                                      1 = never; n in 2..64 = n slices (one-CTA tiles only) */
     MPGEMM_OPT_C_STORE = 10,      /* 0 = automatic (default): C is written with tiled TMA stores
                                      when beta == 0, K is not split, A is read as one row class,

@@ -1,17 +1,29 @@
 // The tensor-core pass of C = alpha*A*B + beta*C for sm_103a.
 //
-// Persistent CTAs walk the output in tiles. Each CTA has six warps with fixed
+// Persistent CTAs walk the output in tiles. Each CTA has warps with fixed
 // roles:
 //   warp 0      load warp: one lane issues TMA loads of A (128 x 64, K-major)
-//               and B (64 x width: N-major when B is row-major, K-major when B
-//               is column-major) into a ring of shared-memory stages; rows, columns and K past the matrix edge arrive as
-//               zeros (TMA out-of-bounds fill), which replaces the padding and
-//               guarded tail loads of "Day 80, Capstone 4: a tensor-core GEMM"
+//               and B (64 x 64 boxes: N-major when B is row-major, K-major
+//               when B is column-major) into a ring of shared-memory stages;
+//               rows, columns and K past the matrix edge arrive as zeros (TMA
+//               out-of-bounds fill), which replaces the padding and guarded
+//               tail loads of "Day 80, Capstone 4: a tensor-core GEMM"
 //               ("Faded practice", practice 3; "Common failures").
 //   warp 1      MMA warp: allocates tensor memory; one lane issues
-//               tcgen05.mma (K = 16 per instruction, FP16 x FP16 -> FP32) into
-//               one of two accumulator buffers and frees each stage with
-//               tcgen05.commit.
+//               tcgen05.mma (K = 16 per instruction, FP16 x FP16 -> FP32) and
+//               frees each stage with tcgen05.commit.
+//   warps 2-5   epilogue (warps 2-9 for 256 x 512 pair tiles: two warps per
+//               32 accumulator rows, each taking half of the columns): each
+//               warp reads its 32 accumulator rows with tcgen05.ld (32x32b:
+//               TMEM lane = row) 32 columns at a time, applies alpha in FP32
+//               and writes the 32 x 32 chunk into its own swizzled shared
+//               buffer; from there either a tiled TMA store writes it to C
+//               (beta == 0 and a TMA-addressable C), or each lane stores one
+//               column (128 contiguous bytes per warp store instruction),
+//               adding beta * C, or adding atomically for split-K; rows and
+//               columns past M and N are masked, so any M, N and ldc work.
+//               While it works on tile i, the MMAs of tile i+1 run into the
+//               other accumulator buffer (or into the parts already drained).
 //   warp 6/10   (CTA-pair tiles) a second MMA warp, the one after the
 //               epilogue warps: warp 1 issues the MMAs of the first half of
 //               the accumulator's columns, this warp those of the second. The
@@ -20,31 +32,23 @@
 //               issuers one keeps the pipe fed while the other waits
 //               (measured: full MMA rate with two issuers, about 60 % with
 //               one, for one barrier test per four MMAs).
-//   warps 2-5   epilogue (warps 2-9 for 256 x 512 pair tiles, two warps per
-//               32 accumulator rows, each taking half of the columns): each
-//               warp reads its 32 accumulator rows with
-//               tcgen05.ld (32x32b: TMEM lane = row), applies alpha in FP32,
-//               turns each 32 x 32 chunk around through shared memory so that
-//               every store instruction writes 128 contiguous bytes of one
-//               row of C, adds beta * C when beta != 0, and masks rows and
-//               columns, so any M, N and any ldc are handled. While it works
-//               on tile i, the MMA warp already accumulates tile i+1 into the
-//               other buffer.
 //
 // Two shapes of the same pipeline:
 //   single  one CTA per tile of 128 x BN (BN = 128 or 256), tcgen05.mma with
-//           cta_group::1, M = 128, N = 64 * ceil(valid columns / 64);
+//           cta_group::1, M = 128, N = 64 * ceil(valid columns / 64), two
+//           accumulator buffers;
 //   pair    a cluster of two CTAs per tile of 256 x BN (BN = 256 or 512):
-//           each CTA loads its own 128 rows of A and its own half of every
-//           256-column block of B, the even CTA issues tcgen05.mma with
-//           cta_group::2 (M = 256, N = 256, one instruction per 256-column
-//           block) over both CTAs' shared memory, and each CTA's tensor
-//           memory receives its own 128 rows of the accumulator. Per SM the
-//           256 x 256 tile moves a third less operand data per FLOP than the
-//           single shape, the 256 x 512 tile half as much. The 512-wide
-//           accumulator fills the whole tensor memory, so that shape has one
-//           accumulator buffer, released to the MMA warp in 256-column halves
-//           as the epilogue drains them.
+//           each CTA loads its own 128 rows of A and its own half of the B
+//           columns of every accumulator part; the even CTA issues
+//           tcgen05.mma with cta_group::2 (M = 256; N = 128 per part for
+//           256 x 256 tiles, 256 per part for 256 x 512 tiles) over both
+//           CTAs' shared memory, and each CTA's tensor memory receives its
+//           own 128 rows of the accumulator. Per SM the 256 x 256 tile moves
+//           a third less operand data per FLOP than the single 128 x 256
+//           shape, the 256 x 512 tile half as much. The 512-wide accumulator
+//           fills the whole tensor memory, so that shape has one accumulator
+//           buffer, whose two 256-column parts go back to their MMA threads
+//           one by one as the epilogue drains them.
 //
 // The staged-tile reuse, asynchronous copies and block rasterisation that the
 // pages build up with WMMA ("Day 80", "Worked path"; "02_mixed_precision_gemm"
