@@ -365,19 +365,65 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// Encoded tensor maps kept by a handle and reused by later calls with the
+// same arguments. A map is a pure function of them (element type, base
+// address, shape, pitch, box), so an entry never goes stale, even if the
+// memory is freed and another buffer is placed at the same address; the least
+// recently used entry is replaced. Host-side only: encoding costs a driver
+// call per map per GEMM otherwise.
+struct MapCache {
+    static constexpr int kEntries = 16;
+    struct Entry {
+        uint64_t key[6];
+        CUtensorMap map;
+        uint64_t used;
+        bool valid;
+    };
+    Entry e[kEntries] = {};
+    uint64_t clock = 0;
+
+    bool find(const uint64_t (&k)[6], CUtensorMap* out) {
+        for (Entry& x : e) {
+            if (x.valid && std::equal(k, k + 6, x.key)) {
+                x.used = ++clock;
+                *out = x.map;
+                return true;
+            }
+        }
+        return false;
+    }
+    void put(const uint64_t (&k)[6], const CUtensorMap& m) {
+        Entry* victim = &e[0];
+        for (Entry& x : e) {
+            if (!x.valid) { victim = &x; break; }
+            if (x.used < victim->used) victim = &x;
+        }
+        std::copy(k, k + 6, victim->key);
+        victim->map = m;
+        victim->used = ++clock;
+        victim->valid = true;
+    }
+};
+
 // Row-major FP16 matrix rows x cols with pitch ld (elements), boxes of
 // box_cols x box_rows, 128-byte swizzle, zeros outside the matrix.
 bool encode_f16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
-                uint32_t box_cols, uint32_t box_rows) {
+                uint32_t box_cols, uint32_t box_rows, MapCache* cache = nullptr) {
+    const uint64_t key[6] = {16, reinterpret_cast<uintptr_t>(base), static_cast<uint64_t>(rows),
+                             static_cast<uint64_t>(cols), static_cast<uint64_t>(ld),
+                             (static_cast<uint64_t>(box_cols) << 32) | box_rows};
+    if (cache && cache->find(key, map)) return true;
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const bool ok = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (ok && cache) cache->put(key, *map);
+    return ok;
 }
 
 int grid_for(int64_t work, int num_sms) {
@@ -459,7 +505,7 @@ cudaError_t prepare_kernels() {
 // The A tensor maps (one per row class) and the class fields of the kernel
 // parameters, for A as the kernel will read it (staged or not).
 bool encode_a(const mpgemm_plan_t& plan, const void* a_use, int64_t lda_use, int64_t M, int64_t K,
-              TensorMaps* maps, GemmParams* gp) {
+              TensorMaps* maps, GemmParams* gp, MapCache* cache = nullptr) {
     std::memset(maps, 0, sizeof(*maps));
     const AClassLayout L = a_class_layout(a_use, lda_use, M, plan.a_classes > 0, plan.tile_m);
     gp->a_classes = L.P;
@@ -472,7 +518,7 @@ bool encode_a(const mpgemm_plan_t& plan, const void* a_use, int64_t lda_use, int
     for (int32_t r = 0; r < L.P; ++r) {
         if (L.rows[r] == 0) continue;
         if (!encode_f16(&maps->a[r], reinterpret_cast<const void*>(L.base[r]), L.rows[r], K + L.shift[r],
-                        L.P * lda_use, 64, 128))
+                        L.P * lda_use, 64, 128, cache))
             return false;
     }
     return true;
@@ -480,16 +526,22 @@ bool encode_a(const mpgemm_plan_t& plan, const void* a_use, int64_t lda_use, int
 
 // Row-major FP32 matrix rows x cols with pitch ld (elements), 32 x 32 boxes,
 // 128-byte swizzle: the tiled TMA store of the epilogue's chunks.
-bool encode_f32_store(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+bool encode_f32_store(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
+                      MapCache* cache = nullptr) {
+    const uint64_t key[6] = {32, reinterpret_cast<uintptr_t>(base), static_cast<uint64_t>(rows),
+                             static_cast<uint64_t>(cols), static_cast<uint64_t>(ld), (32ull << 32) | 32u};
+    if (cache && cache->find(key, map)) return true;
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
     const cuuint32_t box[2] = {32, 32};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const bool ok = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (ok && cache) cache->put(key, *map);
+    return ok;
 }
 
 // Let the epilogue store C with TMA when it can: C is only written
@@ -500,11 +552,11 @@ bool encode_f32_store(CUtensorMap* map, const void* base, int64_t rows, int64_t 
 // 1025-1027 of every row (the padding of C). Otherwise, or when c_store
 // forbids it, every lane stores its own column.
 void encode_c(const mpgemm_plan_t& plan, float* C, int64_t M, int64_t N, int64_t ldc, float beta,
-              int32_t c_store, TensorMaps* maps, GemmParams* gp) {
+              int32_t c_store, TensorMaps* maps, GemmParams* gp, MapCache* cache = nullptr) {
     gp->c_tma = 0;
     if (c_store == 1 || beta != 0.0f || plan.k_splits > 1 || gp->a_classes != 1 || N % 4 != 0) return;
     if (!aligned16(C, ldc, 4)) return;
-    if (encode_f32_store(&maps->c, C, M, N, ldc)) gp->c_tma = 1;
+    if (encode_f32_store(&maps->c, C, M, N, ldc, cache)) gp->c_tma = 1;
 }
 
 GemmParams make_params(const mpgemm_plan_t& plan, int64_t M, int64_t N, int64_t K, float alpha,
@@ -581,6 +633,7 @@ SolveDevice g_solve_devices[kSolveMaxDevices];
 }  // namespace
 
 struct mpgemm_handle_st {
+    MapCache map_cache;              // tensor maps of recent calls
     int device = 0;
     int num_sms = 0;
     int max_clusters = 0;            // CTA pairs of the pair kernel resident at once
@@ -815,16 +868,16 @@ mpgemm_status_t mpgemm_run_ex(mpgemm_handle_t h, mpgemm_b_layout_t b_layout, int
     }
 
     CUtensorMap tb;
-    if (!(b_col ? encode_f16(&tb, b_use, N, K, ldb_use, 64, 64)
-                : encode_f16(&tb, b_use, K, N, ldb_use, 64, 64)))
+    if (!(b_col ? encode_f16(&tb, b_use, N, K, ldb_use, 64, 64, &h->map_cache)
+                : encode_f16(&tb, b_use, K, N, ldb_use, 64, 64, &h->map_cache)))
         return MPGEMM_ERR_CUDA;
 
     GemmParams gp = make_params(plan, M, N, K, alpha, beta, C, ldc, h->status_dev,
                                 h->opt.wait_limit_ns, h->opt.test_stall,
                                 keep_a_operand(plan, h->opt.l2_keep));
     TensorMaps ta;
-    if (!encode_a(plan, a_use, lda_use, M, K, &ta, &gp)) return MPGEMM_ERR_CUDA;
-    encode_c(plan, C, M, N, ldc, beta, h->opt.c_store, &ta, &gp);
+    if (!encode_a(plan, a_use, lda_use, M, K, &ta, &gp, &h->map_cache)) return MPGEMM_ERR_CUDA;
+    encode_c(plan, C, M, N, ldc, beta, h->opt.c_store, &ta, &gp, &h->map_cache);
     gp.acc16 = h->opt.acc16;
     if (launch_plan(plan, b_col, h->max_clusters, ta, tb, gp, stream) != cudaSuccess) {
         cudaGetLastError();

@@ -464,3 +464,15 @@ def test_tma_store_falls_back_for_unaligned_c(mp):
     with mp.Handle() as h:
         check_full(h, ops, c_offset=1)
         check_full(h, ops, c_offset=2)
+
+
+def test_tensor_map_cache_across_buffers_and_shapes(mp):
+    # one handle, 20 different operand sets (more tensor maps than the
+    # handle's 16-entry cache holds) in two rounds: every result is checked,
+    # so a map reused for the wrong buffer or shape would show
+    sets = [workloads.make_operands(64 + 32 * (i % 5), 96 + 16 * (i % 4), 64 * (1 + i % 3), seed=600 + i)
+            for i in range(20)]
+    with mp.Handle() as h:
+        for _ in range(2):
+            for ops in sets:
+                check_full(h, ops)
