@@ -329,81 +329,113 @@ __device__ __forceinline__ uint32_t chunk_off(int row, int col) {
     return static_cast<uint32_t>(row * 128 + ((((col >> 2) ^ row) & 7) << 4) + (col & 3) * 4);
 }
 
+// One 32 x 32 chunk (accumulator words r, TMEM lane = row = lane) to C,
+// without a beta * C term: alpha applied, into the warp's chunk buffer, then
+// either a tiled TMA store at C row row0, column col0 (p.c_tma; the tensor
+// map clips rows and columns outside C) or one column per lane (128
+// contiguous bytes per warp store instruction; atomic adds for split-K).
+__device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMap* tmap_c, const uint32_t (&r)[32],
+                                           float* c_tile, int64_t row_stride, int32_t rows, int32_t row0,
+                                           int32_t col0, uint32_t buf_s, int lane) {
+    const float alpha = p.alpha;
+    if (p.c_tma) {
+        // the previous chunk's TMA store must have read the buffer
+        if (lane == 0) ptx::bulk_wait_read_all();
+        __syncwarp();
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        ptx::st_shared_v4(buf_s + chunk_off(lane, 4 * q), alpha * acc_value(r[4 * q], p.acc16),
+                          alpha * acc_value(r[4 * q + 1], p.acc16), alpha * acc_value(r[4 * q + 2], p.acc16),
+                          alpha * acc_value(r[4 * q + 3], p.acc16));
+    if (p.c_tma) {
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            ptx::tma_store_2d(tmap_c, buf_s, col0, row0);
+            ptx::bulk_commit_group();
+        }
+        return;
+    }
+    __syncwarp();
+    const int32_t col = col0 + lane;
+    if (col < p.N) {
+        float* cp = c_tile + col;
+        if (p.k_splits > 1) {
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr)
+                if (rr < rows)
+                    atomicAdd(cp + static_cast<int64_t>(rr) * row_stride, ptx::ld_shared_f32(buf_s + chunk_off(rr, lane)));
+        } else {
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr)
+                if (rr < rows) cp[static_cast<int64_t>(rr) * row_stride] = ptx::ld_shared_f32(buf_s + chunk_off(rr, lane));
+        }
+    }
+    __syncwarp();
+}
+
 // The epilogue of one work item for one warp: 32 rows of C (the tensor
 // memory lanes of this warp's quarter; t_row addresses them at the
 // accumulator's first column), of which the first `rows` exist, and columns
-// n0 .. n0+width-1. Each 32 x 32 chunk goes from tensor memory through
-// registers (alpha applied) into the warp's chunk buffer (buf / buf_s, the
-// generic and shared-window addresses of the same bytes). Then either
-//  - TMA path (p.c_tma): one lane stores the chunk with a tiled TMA store at
-//    C row row0, column n0 + 32 c; the map clips rows and columns outside C;
-//  - otherwise each lane writes one column of the chunk (128 contiguous
-//    bytes per store instruction across the warp), c_tile + rr * row_stride
-//    addressing row rr, with beta * C added (c_cur: the chunk's old C values,
-//    loaded ahead of the accumulator) or, for split-K, added atomically.
+// n0 .. n0+width-1; row0 is the C row of the first of them and c_tile +
+// rr * row_stride addresses row rr. Without a beta * C term the chunks'
+// tensor-memory loads go out two at a time, and release() (which hands this
+// part of the accumulator back to the MMA warp) runs as soon as the last of
+// them has completed, before the last chunks are written. With beta != 0,
+// c_cur holds the first chunk's old C values (loaded while the MMAs still
+// ran), each later chunk's C loads go out before the previous chunk is
+// stored, and release() runs at the end.
+template <class Release>
 __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMap* tmap_c, uint32_t t_row,
                                           float* c_tile, int64_t row_stride, int32_t rows, int32_t row0,
-                                          int32_t n0, int32_t width, uint8_t* buf, uint32_t buf_s, int lane,
-                                          float (&c_cur)[32]) {
+                                          int32_t n0, int32_t width, uint32_t buf_s, int lane,
+                                          float (&c_cur)[32], Release&& release) {
     const float alpha = p.alpha, beta = p.beta;
-    const bool split = p.k_splits > 1;        // add the partial product into C
-    const bool read_c = (beta != 0.0f) && !split;
+    const bool read_c = (beta != 0.0f) && p.k_splits <= 1;
     const int32_t chunks = (min(width, p.N - n0) + 31) / 32;
+    if (!read_c) {
+        for (int32_t c = 0; c < chunks; c += 2) {
+            uint32_t r0[32], r1[32];
+            const bool two = c + 1 < chunks;
+            ptx::tmem_load_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r0);
+            if (two) ptx::tmem_load_32x32b_x32(t_row + static_cast<uint32_t>((c + 1) * 32), r1);
+            ptx::tmem_load_wait();
+            if (c + 2 >= chunks) release();
+            emit_chunk(p, tmap_c, r0, c_tile, row_stride, rows, row0, n0 + c * 32, buf_s, lane);
+            if (two) emit_chunk(p, tmap_c, r1, c_tile, row_stride, rows, row0, n0 + (c + 1) * 32, buf_s, lane);
+        }
+        if (chunks <= 0) release();
+        return;
+    }
     const float* c_rows = c_tile;
     float c_next[32];
     for (int32_t c = 0; c < chunks; ++c) {
         uint32_t r[32];
         ptx::tmem_load_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
-        if (read_c && c + 1 < chunks)
+        if (c + 1 < chunks)
             load_c_chunk(c_rows, row_stride, n0 + (c + 1) * 32 + lane, p.N, rows, c_next);
         ptx::tmem_load_wait();
-        if (p.c_tma) {
-            // the previous chunk's TMA store must have read the buffer
-            if (lane == 0) ptx::bulk_wait_read_all();
-            __syncwarp();
-        }
 #pragma unroll
         for (int q = 0; q < 8; ++q)
             ptx::st_shared_v4(buf_s + chunk_off(lane, 4 * q), alpha * acc_value(r[4 * q], p.acc16),
                               alpha * acc_value(r[4 * q + 1], p.acc16), alpha * acc_value(r[4 * q + 2], p.acc16),
                               alpha * acc_value(r[4 * q + 3], p.acc16));
-        if (p.c_tma) {
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                ptx::tma_store_2d(tmap_c, buf_s, n0 + c * 32, row0);
-                ptx::bulk_commit_group();
-            }
-            continue;
-        }
         __syncwarp();
         const int32_t col = n0 + c * 32 + lane;
         if (col < p.N) {
             float* cp = c_tile + col;
-            if (read_c) {
 #pragma unroll
-                for (int rr = 0; rr < 32; ++rr)
-                    if (rr < rows)
-                        cp[static_cast<int64_t>(rr) * row_stride] =
-                            fmaf(beta, c_cur[rr], ptx::ld_shared_f32(buf_s + chunk_off(rr, lane)));
-            } else if (split) {
-#pragma unroll
-                for (int rr = 0; rr < 32; ++rr)
-                    if (rr < rows)
-                        atomicAdd(cp + static_cast<int64_t>(rr) * row_stride, ptx::ld_shared_f32(buf_s + chunk_off(rr, lane)));
-            } else {
-#pragma unroll
-                for (int rr = 0; rr < 32; ++rr)
-                    if (rr < rows) cp[static_cast<int64_t>(rr) * row_stride] = ptx::ld_shared_f32(buf_s + chunk_off(rr, lane));
-            }
+            for (int rr = 0; rr < 32; ++rr)
+                if (rr < rows)
+                    cp[static_cast<int64_t>(rr) * row_stride] =
+                        fmaf(beta, c_cur[rr], ptx::ld_shared_f32(buf_s + chunk_off(rr, lane)));
         }
-        if (read_c) {
 #pragma unroll
-            for (int rr = 0; rr < 32; ++rr) c_cur[rr] = c_next[rr];
-        }
+        for (int rr = 0; rr < 32; ++rr) c_cur[rr] = c_next[rr];
         __syncwarp();
     }
-    (void)buf;
+    release();
 }
 
 template <class Cfg>
@@ -420,7 +452,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
     const uint32_t sA = base + Cfg::OFF_A;
     const uint32_t sB = base + Cfg::OFF_B;
-    uint8_t* epi_buf = gbase + Cfg::OFF_EPI;
     const uint32_t bar0 = base + Cfg::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -672,7 +703,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const int quarter = warp & 3;             // tensor-memory lanes 32*quarter ..
         const int col_half = (warp - 2) / 4;      // with 8 warps: which half of each part's columns
         constexpr int COL_SPLIT = Cfg::EPI_WARPS / 4;
-        uint8_t* buf = epi_buf + (warp - 2) * Cfg::EPI_CHUNK_BYTES;
         const uint32_t buf_s = base + Cfg::OFF_EPI + static_cast<uint32_t>((warp - 2) * Cfg::EPI_CHUNK_BYTES);
         const bool read_c = (p.beta != 0.0f) && p.k_splits <= 1;
         int32_t local = 0;
@@ -709,25 +739,30 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // and parts past the item's width are handed back at once
             for (int h = 0; h < RELEASE_PARTS; ++h) {
                 const int32_t pn0 = n0 + h * part_n + my_off;
+                // hand part h of the accumulator back to its MMA thread
+                auto release = [&]() {
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (PAIR)
+                            ptx::mbar_arrive_cluster(ptx::mapa_shared(acc_empty_bar(accb, h), 0));
+                        else
+                            ptx::mbar_arrive(acc_empty_bar(accb, h));
+                    }
+                };
                 if (h * part_n < w.width) {
                     if (h > 0 && read_c) load_c_chunk(c_tile, row_stride, pn0 + lane, p.N, rows, c_cur);
                     store_tile(p, &maps.c, t_row + static_cast<uint32_t>(h * part_n + my_off), c_tile, row_stride,
-                               rows, jb, pn0, my_n, buf, buf_s, lane, c_cur);
-                }
-                ptx::tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) {
-                    if constexpr (PAIR)
-                        ptx::mbar_arrive_cluster(ptx::mapa_shared(acc_empty_bar(accb, h), 0));
-                    else
-                        ptx::mbar_arrive(acc_empty_bar(accb, h));
+                               rows, jb, pn0, my_n, buf_s, lane, c_cur, release);
+                } else {
+                    release();
                 }
             }
             ++local;
         }
-        // the TMA stores must complete (and stop reading this CTA's shared
-        // memory) before the CTA exits
-        if (p.c_tma && lane == 0) ptx::bulk_wait_all();
+        // the TMA stores must have read this CTA's shared memory before the
+        // CTA exits (their global writes complete with the kernel)
+        if (p.c_tma && lane == 0) ptx::bulk_wait_read_all();
         __syncwarp();
     }
 

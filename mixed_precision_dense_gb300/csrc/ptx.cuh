@@ -86,9 +86,6 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 // shared memory (their source may be overwritten afterwards).
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
-// Wait until this thread's committed bulk stores have completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA, tensor core) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
