@@ -12,8 +12,8 @@
 //   warp 1      MMA warp: allocates tensor memory; one lane issues
 //               tcgen05.mma (K = 16 per instruction, FP16 x FP16 -> FP32) and
 //               frees each stage with tcgen05.commit.
-//   warps 2-5   epilogue (warps 2-9 for 256 x 512 pair tiles: two warps per
-//               32 accumulator rows, each taking half of the columns): each
+//   warps 2-9   epilogue, two warps per 32 accumulator rows, each taking
+//               half of the columns: each
 //               warp reads its 32 accumulator rows with tcgen05.ld (32x32b:
 //               TMEM lane = row) 32 columns at a time, applies alpha in FP32
 //               and writes the 32 x 32 chunk into its own swizzled shared
@@ -24,7 +24,7 @@
 //               columns past M and N are masked, so any M, N and ldc work.
 //               While it works on tile i, the MMAs of tile i+1 run into the
 //               other accumulator buffer (or into the parts already drained).
-//   warp 6/10   (CTA-pair tiles) a second MMA warp, the one after the
+//   warp 10     (CTA-pair tiles) a second MMA warp, the one after the
 //               epilogue warps: warp 1 issues the MMAs of the first half of
 //               the accumulator's columns, this warp those of the second. The
 //               tensor pipe queues only about one MMA ahead of an issuing
@@ -152,11 +152,13 @@ struct TileConfig {
     static constexpr int A_BYTES = BM * BK * 2;        // 16 KB
     static constexpr int B_ATOM_BYTES = BK * 64 * 2;   // one 64-column box of B: 8 KB
     static constexpr int B_BYTES = BK * B_COLS * 2;
-    // epilogue warps: 4 (one per 32 tensor-memory lanes), or 8 for the
-    // 256 x 512 tile, whose single accumulator is drained while the MMAs of
-    // the next tile wait: two warps per lane quarter, each taking half of
-    // every part's columns
-    static constexpr int EPI_WARPS = BN == 512 ? 8 : 4;
+    // epilogue warps: 8, two per 32 tensor-memory lanes, each taking half of
+    // every part's columns. The 256 x 512 tile's single accumulator is
+    // drained while the MMAs of the next tile wait, and the last tile of
+    // every CTA is drained after its MMAs end; two warps per lane quarter
+    // halve both (measured against four warps: 9-12 % less time per call
+    // for GEMMs of one or two tiles per CTA)
+    static constexpr int EPI_WARPS = 8;
     static constexpr int EPI_CHUNK_BYTES = 32 * 32 * 4;  // one warp's 32 x 32 FP32 chunk buffer
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_CHUNK_BYTES;
     static constexpr int TMEM_COLS = ACC_BUFS * BN;
@@ -402,6 +404,8 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMa
             ptx::tmem_load_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r0);
             if (two) ptx::tmem_load_32x32b_x32(t_row + static_cast<uint32_t>((c + 1) * 32), r1);
             ptx::tmem_load_wait();
+            ptx::tmem_regs_ready(r0);
+            if (two) ptx::tmem_regs_ready(r1);
             if (c + 2 >= chunks) release();
             emit_chunk(p, tmap_c, r0, c_tile, row_stride, rows, row0, n0 + c * 32, buf_s, lane);
             if (two) emit_chunk(p, tmap_c, r1, c_tile, row_stride, rows, row0, n0 + (c + 1) * 32, buf_s, lane);
@@ -417,6 +421,7 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMa
         if (c + 1 < chunks)
             load_c_chunk(c_rows, row_stride, n0 + (c + 1) * 32 + lane, p.N, rows, c_next);
         ptx::tmem_load_wait();
+        ptx::tmem_regs_ready(r);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
             ptx::st_shared_v4(buf_s + chunk_off(lane, 4 * q), alpha * acc_value(r[4 * q], p.acc16),
