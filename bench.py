@@ -486,53 +486,62 @@ def time_tc_kernel_only(handle, w, A, B, C, stream, steps, flush=None):
                       stream, steps, flush)
 
 
+# handles (and streams) the end-to-end leg rotates through
+E2E_SLOTS = 3
+
+
 def run_e2e(handle, w, ops, stream, device, args):
     """End to end through mpgemm_run_host on pinned host buffers: every step
     copies A and B (and C when beta != 0) to the device, runs the GEMM and
-    copies C back. Two handles on two streams alternate, so one step's
-    copies overlap the other's GEMM; a step's slot is reused only after its
-    stream has finished, i.e. after its result is in host memory."""
+    copies C back. Three handles on three streams rotate, so one step's
+    copy in, another's GEMM and a third's copy out can run at once (with two
+    slots a step's copy in has to wait for the copy out two steps back); a
+    step's slot is reused only after its stream has finished, i.e. after its
+    result is in host memory."""
     import torch
 
     import mixed_precision_dense_gb300 as mp
+    slots = E2E_SLOTS
     A_h = ops.A.pin_memory()
     B_h = ops.B.pin_memory()
-    C_h = [ops.C.clone().pin_memory() for _ in range(2)]
-    handles = [handle, mp.Handle()]
-    handles[1].set_option(mp.Option.TILE_M, args.tile_m)
-    handles[1].set_option(mp.Option.TILE_N, args.tile_n)
-    streams = [stream, torch.cuda.Stream(device)]
+    C_h = [ops.C.clone().pin_memory() for _ in range(slots)]
+    handles = [handle] + [mp.Handle() for _ in range(slots - 1)]
+    for h in handles[1:]:
+        h.set_option(mp.Option.TILE_M, args.tile_m)
+        h.set_option(mp.Option.TILE_N, args.tile_n)
+    streams = [stream] + [torch.cuda.Stream(device) for _ in range(slots - 1)]
     steps = max(1, min(args.steps, args.e2e_steps))
 
     def enqueue(i):
-        k = i % 2
+        k = i % slots
         handles[k].run_host(w.M, w.N, w.K, w.alpha, A_h.data_ptr(), w.lda, B_h.data_ptr(), w.ldb,
                             w.beta, C_h[k].data_ptr(), w.ldc, streams[k].cuda_stream)
 
-    for i in range(4):
+    for i in range(2 * slots):
         enqueue(i)
     torch.cuda.synchronize(device)
     barrier()
     t0 = time.perf_counter()
     for i in range(steps):
-        if i >= 2:
-            streams[i % 2].synchronize()   # step i-2's result is on the host; its slot is free
+        if i >= slots:
+            streams[i % slots].synchronize()   # step i-slots's result is on the host; its slot is free
         enqueue(i)
     for st in streams:
         st.synchronize()
     dt = time.perf_counter() - t0
-    for k in (0, 1):
+    for k in range(slots):
         st_, info = handles[k].sync_status(streams[k].cuda_stream)
         if st_ != mp.Status.OK:
             raise RuntimeError(f"device reported {st_.name} {info}")
-    handles[1].close()
+    for h in handles[1:]:
+        h.close()
     max_s, flops_all = aggregate(dt, gemm_flops(w.M, w.N, w.K) * steps, device=device)
     h2d = (w.M * w.K * 2 + w.K * w.N * 2) + (w.M * w.N * 4 if w.beta != 0 else 0)
     return {"value": round(flops_all / max_s / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": w.M * w.N * 4, "steps": steps,
             "ms_per_step": round(max_s * 1e3 / steps, 4),
-            "api": "mpgemm_run_host on pinned host buffers, two handles on two streams "
-                   "alternating, host wall clock"}
+            "api": f"mpgemm_run_host on pinned host buffers, {slots} handles on {slots} streams "
+                   "rotating, host wall clock"}
 
 
 # ----------------------------------------------------------------------------- the capstone gate
