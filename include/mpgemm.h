@@ -34,7 +34,11 @@
  *  - Every dimension must be below 2^31, and M*N*K below 2^62.
  *  - `stream` is a cudaStream_t (or CUstream) passed as void*; NULL is the
  *    legacy default stream. Device entry points are asynchronous: they
- *    enqueue work on `stream` and return without synchronising.
+ *    enqueue work on `stream` and return without synchronising. The GEMM
+ *    kernel is launched with programmatic stream serialization: its CTAs may
+ *    be scheduled and set up (barriers, tensor memory) while the previous
+ *    kernel of the stream finishes, but they read and write no global memory
+ *    before that kernel has completed, so stream order holds as usual.
  *  - The caller owns A, B, C and the stream. The handle owns its workspace
  *    (aligned staging copies, grown on demand with stream-ordered
  *    allocation), the tensor-core launch configuration and a status word

@@ -507,6 +507,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if constexpr (PAIR) ptx::cluster_sync();   // peer barriers initialised before any remote use
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // The GEMM is launched with programmatic stream serialization: it may
+    // start while the previous kernel of the stream (a staging or C-scaling
+    // pass, or the previous GEMM) is still finishing, and everything above
+    // (barriers, tensor memory, tensor-map prefetch) touches no global
+    // memory. Every thread waits here until that kernel has completed and
+    // its writes are visible; the next kernel may begin its own setup now.
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ loads
