@@ -371,6 +371,35 @@ def test_side_stream_and_back_to_back_shapes(handle):
         assert_close(got, ref, S)
 
 
+@pytest.mark.parametrize("first,second", [((2048, 2048, 2048), (2048, 2048, 64)),
+                                          ((2048, 2048, 64), (2048, 2048, 2048)),
+                                          ((512, 640, 3000), (512, 640, 17))])
+def test_back_to_back_dependent_calls(mp, handle, first, second):
+    # The GEMM is launched with programmatic dependent launch: its CTAs may be
+    # scheduled while the previous kernel still runs, and must not touch
+    # memory before it has completed. C = A1 B1, then at once C = A2 B2 + C on
+    # the same stream (the second call reads what the first writes), then
+    # C = A3 B3 - C: integer inputs make every sum exact.
+    M, N = first[0], first[1]
+    s = torch.cuda.current_stream()
+    ks = [first[2], second[2], first[2] // 2 + 1]
+    gen = torch.Generator().manual_seed(sum(ks))
+    As = [torch.randint(-3, 4, (M, k), generator=gen).half() for k in ks]
+    Bs = [torch.randint(-2, 3, (k, N), generator=gen).half() for k in ks]
+    dA = [a.cuda() for a in As]
+    dB = [b.cuda() for b in Bs]
+    C = torch.full((M, N), float("nan"), device="cuda")
+    for i, beta in enumerate([0.0, 1.0, -1.0]):
+        handle.run(M, N, ks[i], 1.0, dA[i].data_ptr(), ks[i], dB[i].data_ptr(), N, beta, C.data_ptr(), N,
+                   s.cuda_stream)
+    s.synchronize()
+    assert handle.sync_status(s.cuda_stream)[0] == mp.Status.OK
+    # (float64 products of these integers are exact)
+    prods = [a.double().numpy() @ b.double().numpy() for a, b in zip(As, Bs)]
+    ref = prods[2] - (prods[0] + prods[1])
+    assert np.array_equal(C.cpu().double().numpy(), ref)
+
+
 # --------------------------------------------------------------------------- host-buffer entry point
 
 def test_run_host_matches_oracle(handle):
