@@ -160,9 +160,11 @@ typedef enum {
                                      results may differ in the last bits from run to run;
                                      1 = never; n in 2..64 = n slices (one-CTA tiles only) */
     MPGEMM_OPT_C_STORE = 10,      /* 0 = automatic (default): C is written with tiled TMA stores
-                                     when beta == 0, K is not split, A is read as one row class,
-                                     C's base and ldc are 16-byte aligned and N is a multiple of
-                                     4; 1 = always one store per lane (the path used in every
+                                     when beta == 0 and K is not split, or added to with tiled
+                                     TMA reduce-adds when K is split (C then holds beta*C
+                                     first), provided A is read as one row class, C's base and
+                                     ldc are 16-byte aligned and N is a multiple of 4; 1 = always
+                                     one store (or atomic add) per lane (the path used in every
                                      other case) */
     MPGEMM_OPT_ACCUMULATOR = 11   /* 0 or 32 = FP32 accumulators (default, the operation defined
                                      above); 16 = FP16 accumulators, a study variant of "Day 72:

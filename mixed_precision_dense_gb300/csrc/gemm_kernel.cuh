@@ -109,8 +109,9 @@ struct GemmParams {
     int32_t test_stall;     // 1: the load warp issues nothing (timeout test)
     int32_t keep_a;         // L2 hints: 2 = keep both (evict-last), 1 = keep A (evict B first),
                             // 0 = keep B (evict A first)
-    int32_t c_tma;          // 1: C is written by TMA stores through TensorMaps::c (beta == 0,
-                            //    no split-K, one row class, C and ldc 16-byte aligned)
+    int32_t c_tma;          // 1: C is written through TensorMaps::c: TMA stores (beta == 0), or
+                            //    TMA reduce-adds of split-K slices; one row class, C and ldc
+                            //    16-byte aligned, N a multiple of 4
     int32_t acc16;          // 1: FP16 accumulators (the study variant; the product path is FP32)
 };
 
@@ -334,9 +335,10 @@ __device__ __forceinline__ uint32_t chunk_off(int row, int col) {
 
 // One 32 x 32 chunk (accumulator words r, TMEM lane = row = lane) to C,
 // without a beta * C term: alpha applied, into the warp's chunk buffer, then
-// either a tiled TMA store at C row row0, column col0 (p.c_tma; the tensor
-// map clips rows and columns outside C) or one column per lane (128
-// contiguous bytes per warp store instruction; atomic adds for split-K).
+// either a tiled TMA store (a TMA reduce-add for split-K) at C row row0,
+// column col0 (p.c_tma; the tensor map clips rows and columns outside C) or
+// one column per lane (128 contiguous bytes per warp store instruction;
+// atomic adds for split-K).
 __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMap* tmap_c, const uint32_t (&r)[32],
                                            float* c_tile, int64_t row_stride, int32_t rows, int32_t row0,
                                            int32_t col0, uint32_t buf_s, int lane) {
@@ -355,7 +357,11 @@ __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMa
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            ptx::tma_store_2d(tmap_c, buf_s, col0, row0);
+            // split-K slices add into C (which already holds beta * C)
+            if (p.k_splits > 1)
+                ptx::tma_reduce_add_2d(tmap_c, buf_s, col0, row0);
+            else
+                ptx::tma_store_2d(tmap_c, buf_s, col0, row0);
             ptx::bulk_commit_group();
         }
         return;

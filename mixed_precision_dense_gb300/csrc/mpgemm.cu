@@ -551,17 +551,18 @@ bool encode_f32_store(CUtensorMap* map, const void* base, int64_t rows, int64_t 
     return ok;
 }
 
-// Let the epilogue store C with TMA when it can: C is only written
-// (beta == 0), no split-K slices add into it, its rows are contiguous (one
-// row class), its base and pitch are 16-byte aligned, and N is a multiple of
-// 4. A TMA store clips a row only at 16-byte granularity: measured on GB300,
-// with N = 1025 the store of the chunk at column 1024 also wrote columns
-// 1025-1027 of every row (the padding of C). Otherwise, or when c_store
-// forbids it, every lane stores its own column.
+// Let the epilogue write C with TMA when it can: C is only written
+// (beta == 0), or split-K slices add into it (TMA reduce-add: C already
+// holds beta * C), its rows are contiguous (one row class), its base and
+// pitch are 16-byte aligned, and N is a multiple of 4. A TMA store clips a
+// row only at 16-byte granularity: measured on GB300, with N = 1025 the
+// store of the chunk at column 1024 also wrote columns 1025-1027 of every
+// row (the padding of C). Otherwise, or when c_store forbids it, every lane
+// stores (or atomically adds) its own column.
 void encode_c(const mpgemm_plan_t& plan, float* C, int64_t M, int64_t N, int64_t ldc, float beta,
               int32_t c_store, TensorMaps* maps, GemmParams* gp, MapCache* cache = nullptr) {
     gp->c_tma = 0;
-    if (c_store == 1 || beta != 0.0f || plan.k_splits > 1 || gp->a_classes != 1 || N % 4 != 0) return;
+    if (c_store == 1 || (beta != 0.0f && plan.k_splits <= 1) || gp->a_classes != 1 || N % 4 != 0) return;
     if (!aligned16(C, ldc, 4)) return;
     if (encode_f32_store(&maps->c, C, M, N, ldc, cache)) gp->c_tma = 1;
 }

@@ -486,6 +486,36 @@ def test_tma_store_of_c_matches_per_lane_stores(mp, M, N, K, ldc, tile_m, tile_n
     assert np.array_equal(outs[0], outs[1])
 
 
+SPLIT_REDUCE_CASES = [  # (M, N, K, lda, ldc, beta, splits): split-K slices added into C
+    (129, 68, 617, 624, 68, 0.0, 4),          # ragged rows and K: the reduce-add clips past row 129
+    (1000, 800, 1200, 1200, 804, 1.0, 2),     # beta = 1: slices add onto C as it is
+    (300, 200, 1000, 1000, 200, -0.5, 3),     # C = beta * C first, then the slices
+    (4096, 16, 4096, 4096, 16, 0.0, 0),       # the gate's skinny case (automatic split)
+]
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldc,beta,splits", SPLIT_REDUCE_CASES)
+def test_split_k_tma_reduce_matches_atomics(mp, M, N, K, lda, ldc, beta, splits):
+    # split-K slices added into C by tiled TMA reduce-adds (automatic for an
+    # aligned C) and by per-lane atomic adds: both against the oracle, and
+    # bit for bit with integer inputs, whose partial sums are exact
+    assert mp.plan(M, N, K, 1.0, 256, lda, 256, N, beta, 256, ldc)["a_classes"] == 0
+    ops = workloads.make_operands(M, N, K, lda=lda, ldc=ldc, alpha=1.5, beta=beta, c_dist="normal",
+                                  seed=M + K + 3)
+    ints = workloads.make_operands(M, N, K, lda=lda, ldc=ldc, beta=beta, dist="int3", dist_b="int2",
+                                   c_dist="int3", seed=M + K + 4)
+    outs = []
+    for c_store in (0, 1):
+        with mp.Handle() as h:
+            h.set_option(mp.Option.SPLIT_K, splits)
+            h.set_option(mp.Option.C_STORE, c_store)
+            check_full(h, ops)
+            check_full(h, ints, exact=True)
+            got, _, _ = c_result(run_gpu(h, ints), ints)
+            outs.append(got)
+    assert np.array_equal(outs[0], outs[1])
+
+
 def test_tma_store_falls_back_for_unaligned_c(mp):
     # a C base 4 bytes past a 16-byte boundary cannot be a TMA target: the
     # per-lane path writes it, guard rows and padding stay untouched
