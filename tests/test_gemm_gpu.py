@@ -400,6 +400,43 @@ def test_back_to_back_dependent_calls(mp, handle, first, second):
     assert np.array_equal(C.cpu().double().numpy(), ref)
 
 
+def test_offsets_beyond_32_bits(mp):
+    # Maximum-size addressing: A at a pitch of 32800 halves and C at a pitch
+    # of 32772 floats over 65539 rows, so their last rows start past element
+    # 2^31 (4.3 GB and 8.6 GB buffers). Sampled rows at both ends and in
+    # between are checked against the oracle, and C's padding columns of
+    # those rows must still hold the NaN poison.
+    import oracle
+    M, N, K, lda, ldc = 65539, 40, 200, 32800, 32772
+    assert M * lda > 2 ** 31 and M * ldc > 2 ** 31
+    gen = torch.Generator().manual_seed(97)
+    A = (torch.rand(M, K, generator=gen) * 2 - 1).half()
+    B = (torch.rand(K, N, generator=gen) * 2 - 1).half()
+    dA = torch.empty((M, lda), dtype=torch.float16, device="cuda")
+    dA[:, :K] = A.cuda()
+    dB = B.cuda()
+    dC = torch.empty((M, ldc), device="cuda")
+    s = torch.cuda.current_stream()
+    rows = np.array([0, 1, 127, 128, M // 2, 65409, 65535, M - 2, M - 1], dtype=np.int64)
+    I = np.repeat(rows, N)
+    J = np.tile(np.arange(N, dtype=np.int64), len(rows))
+    ref, S = oracle.elements(M, N, K, 1.0, A.reshape(-1).view(torch.int16).numpy().view(np.uint16), K,
+                             B.reshape(-1).view(torch.int16).numpy().view(np.uint16), N, 0.0, None, N, I, J)
+    for c_store in (0, 1):   # TMA stores of C, then per-lane stores
+        dC.fill_(float("nan"))
+        with mp.Handle() as h:
+            h.set_option(mp.Option.C_STORE, c_store)
+            h.run(M, N, K, 1.0, dA.data_ptr(), lda, dB.data_ptr(), N, 0.0, dC.data_ptr(), ldc, s.cuda_stream)
+            s.synchronize()
+            assert h.sync_status(s.cuda_stream)[0] == mp.Status.OK
+        got = dC[torch.from_numpy(rows).cuda()].cpu().numpy()
+        err = np.abs(got[:, :N].astype(np.float64).reshape(-1) - ref)
+        assert np.all(err <= oracle.tolerance(S)), c_store
+        assert np.isnan(got[:, N:]).all(), c_store
+    del dA, dC
+    torch.cuda.empty_cache()
+
+
 # --------------------------------------------------------------------------- host-buffer entry point
 
 def test_run_host_matches_oracle(handle):
