@@ -166,7 +166,7 @@ typedef enum {
                                      ldc are 16-byte aligned and N is a multiple of 4; 1 = always
                                      one store (or atomic add) per lane (the path used in every
                                      other case) */
-    MPGEMM_OPT_ACCUMULATOR = 11   /* 0 or 32 = FP32 accumulators (default, the operation defined
+    MPGEMM_OPT_ACCUMULATOR = 11,  /* 0 or 32 = FP32 accumulators (default, the operation defined
                                      above); 16 = FP16 accumulators, a study variant of "Day 72:
                                      Tensor cores with WMMA" (Exercise: AccT = __half): every
                                      K = 16 step is rounded to FP16, so sums lose low bits once
@@ -174,6 +174,16 @@ typedef enum {
                                      Capstone 4", "Common failures"). K is never split then: the
                                      whole K range accumulates in one FP16 accumulator. Not for
                                      production use. */
+    MPGEMM_OPT_REPRODUCIBLE = 12  /* 0 = default: a call may take a path whose FP32 summation
+                                     order can differ from run to run, so results may differ
+                                     in the last bits between identical calls (always within
+                                     the stated tolerance; exact inputs stay exact): split-K
+                                     (slices added into C in arrival order) and 256 x 256
+                                     CTA-pair tiles (two threads issue alternate k-blocks into
+                                     one accumulator, and the tensor pipe interleaves them as
+                                     they arrive); 1 = only paths with a fixed summation order:
+                                     256 x 512 pair tiles instead of 256 x 256 ones, and no
+                                     split-K, so identical calls give identical bits. */
 } mpgemm_option_t;
 
 /* Set an option. Unknown options or out-of-range values return

@@ -38,6 +38,7 @@ class Option(enum.IntEnum):
     SPLIT_K = 9
     C_STORE = 10
     ACCUMULATOR = 11
+    REPRODUCIBLE = 12
 
 
 class BLayout(enum.IntEnum):

@@ -25,13 +25,15 @@
 //               While it works on tile i, the MMAs of tile i+1 run into the
 //               other accumulator buffer (or into the parts already drained).
 //   warp 10     (CTA-pair tiles) a second MMA warp, the one after the
-//               epilogue warps: warp 1 issues the MMAs of the first half of
-//               the accumulator's columns, this warp those of the second. The
-//               tensor pipe queues only about one MMA ahead of an issuing
-//               thread, and each barrier wait stalls that thread; with two
-//               issuers one keeps the pipe fed while the other waits
-//               (measured: full MMA rate with two issuers, about 60 % with
-//               one, for one barrier test per four MMAs).
+//               epilogue warps: for 256 x 512 tiles warp 1 issues the MMAs of
+//               the first half of the accumulator's columns and this warp
+//               those of the second; for 256 x 256 tiles the two take
+//               alternate k-blocks, each at the full width. The tensor pipe
+//               queues only about one MMA ahead of an issuing thread, and
+//               each barrier wait stalls that thread; with two issuers one
+//               keeps the pipe fed while the other waits (measured: full MMA
+//               rate with two issuers, about 60 % with one, for one barrier
+//               test per four MMAs).
 //
 // Two shapes of the same pipeline:
 //   single  one CTA per tile of 128 x BN (BN = 128 or 256), tcgen05.mma with
@@ -133,14 +135,18 @@ struct TileConfig {
     static constexpr int B_COLS = BN / CTAS;           // columns of B each CTA loads
     static constexpr int BK = 64;                      // 64 halves = one 128-byte swizzle row
     static constexpr int STAGES = STAGES_;
-    // threads issuing MMAs: one, or two, each owning one part (a column
-    // range) of the accumulator, so the two streams of MMAs never touch the
-    // same accumulator columns
+    // threads issuing MMAs: one, or two. With two, a 512-wide tile gives
+    // each issuer one part (a 256-column range) of the accumulator; a
+    // 256-wide tile gives them alternate k-blocks instead (KSPLIT), each
+    // issuing the full width into the same accumulator: every stage is
+    // committed by the one issuer that used it, and the issuer of a tile's
+    // second k-block waits until the first one's MMAs (which start the
+    // accumulator) have completed
     static constexpr int ISSUERS = ISSUERS_;
+    static constexpr bool KSPLIT = ISSUERS == 2 && BN_ != 512;
     // one MMA instruction covers SUB_N columns: BN, except that a tile 512
-    // wide takes two instructions of 256 per K step, and a 256-wide tile with
-    // two issuers two of 128
-    static constexpr int SUB_N = BN == 512 ? 256 : (ISSUERS == 2 ? BN / 2 : BN);
+    // wide takes two instructions of 256 per K step
+    static constexpr int SUB_N = BN == 512 ? 256 : BN;
     static constexpr int SUBS = BN / SUB_N;
     // two accumulator buffers (the epilogue of tile i overlaps the MMAs of
     // tile i+1) when they fit in the 512 columns of tensor memory, else one,
@@ -164,8 +170,8 @@ struct TileConfig {
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_CHUNK_BYTES;
     static constexpr int TMEM_COLS = ACC_BUFS * BN;
     // full and empty per stage; accumulator full per buffer; accumulator
-    // empty per buffer and part
-    static constexpr int NUM_BARRIERS = 2 * STAGES + ACC_BUFS + ACC_BUFS * RELEASE_PARTS;
+    // empty per buffer and part; first k-block done per buffer (KSPLIT)
+    static constexpr int NUM_BARRIERS = 2 * STAGES + ACC_BUFS + ACC_BUFS * RELEASE_PARTS + ACC_BUFS;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = STAGES * A_BYTES;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
@@ -175,7 +181,7 @@ struct TileConfig {
     static constexpr int THREADS = 32 * (2 + EPI_WARPS + ISSUERS - 1);
     static_assert(BN == 128 || BN == 256 || (PAIR && BN == 512), "tile width");
     static_assert(!PAIR || BN >= 256, "pair tiles are 256 x 256 or 256 x 512");
-    static_assert(ISSUERS == 1 || ISSUERS == SUBS, "one issuer, or one issuer per part");
+    static_assert(ISSUERS == 1 || ISSUERS == SUBS || (KSPLIT && SUBS == 1), "one issuer, one per part, or two by k-block");
     static_assert(SUB_N >= (PAIR ? 128 : 64) && ATOMS_PER_PART >= 1, "parts hold whole B boxes");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment");
     static_assert(OFF_EPI % 1024 == 0, "chunk buffers are 1024-byte aligned (128-byte swizzle atoms)");
@@ -470,6 +476,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     constexpr int ACC_BUFS = Cfg::ACC_BUFS, SUBS = Cfg::SUBS, RELEASE_PARTS = Cfg::RELEASE_PARTS;
     auto acc_full_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto acc_empty_bar = [&](int b, int h) { return bar0 + 8u * (2 * STAGES + ACC_BUFS + b * RELEASE_PARTS + h); };
+    auto first_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + ACC_BUFS + ACC_BUFS * RELEASE_PARTS + b); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Cfg::OFF_MISC);
     volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + Cfg::OFF_MISC + 4);
 
@@ -485,9 +492,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full_bar(s), 1);
-            ptx::mbar_init(empty_bar(s), Cfg::ISSUERS);   // one commit per issuing thread
+            ptx::mbar_init(empty_bar(s), Cfg::KSPLIT ? 1 : Cfg::ISSUERS);   // one commit per issuer using it
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
+            ptx::mbar_init(first_bar(b), 1);
             ptx::mbar_init(acc_full_bar(b), Cfg::ISSUERS);
             for (int h = 0; h < RELEASE_PARTS; ++h) ptx::mbar_init(acc_empty_bar(b, h), Cfg::EPI_WARPS * Cfg::CTAS);
         }
@@ -605,6 +613,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // one issuer). Every issuer waits for every stage and commits it, so
         // a stage is freed only when all issuers' MMAs on it have completed;
         // an issuer with no part in an item (a half-width item) still does.
+        // KSPLIT: issuer `me` takes the k-blocks whose running count (over
+        // all items of this CTA) has parity `me`, and commits only those.
         const int me = warp == 1 ? 0 : 1;
         if (lane == 0 && rank == 0) {
             int stage = 0;
@@ -612,6 +622,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int32_t local = 0;
             bool ok = true;
             bool issued = false;
+            int64_t walked = 0;   // k-blocks of the items before this one (KSPLIT)
             for (int32_t i = first_item; ok && i < p.items; i += item_step) {
                 const WorkItem w = work_item<BN>(p, i);
                 if (w.n0 >= p.N) continue;
@@ -634,7 +645,29 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     ptx::tc_fence_after_sync();
                 }
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                // (KSPLIT) whether the item's first k-block is known to be done
+                bool started = !Cfg::KSPLIT || (walked & 1) == me;
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+                    if constexpr (Cfg::KSPLIT) {
+                        if (((walked + (kb - w.kb0)) & 1) != me) {   // the other issuer's k-block
+                            if (++stage == STAGES) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                            continue;
+                        }
+                        if (!started) {
+                            // the other issuer's MMAs on the item's first k-block
+                            // start the accumulator; these add to it
+                            if (!waiter.wait(first_bar(buf), acc_phase)) {
+                                waiter.fail(kRoleMma, kb);
+                                ok = false;
+                                break;
+                            }
+                            ptx::tc_fence_after_sync();
+                            started = true;
+                        }
+                    }
                     if (!waiter.wait(full_bar(stage), phase)) {
                         waiter.fail(kRoleMma, kb);
                         ok = false;
@@ -646,8 +679,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t a_base = sA + stage * Cfg::A_BYTES;
                     const uint32_t b_base = sB + stage * Cfg::B_BYTES;
                     bool pending = false;   // MMAs issued from this stage
-                    const int32_t h_begin = Cfg::ISSUERS > 1 ? me : 0;
-                    const int32_t h_end = Cfg::ISSUERS > 1 ? min(me + 1, n_parts) : n_parts;
+                    const int32_t h_begin = (Cfg::ISSUERS > 1 && !Cfg::KSPLIT) ? me : 0;
+                    const int32_t h_end = (Cfg::ISSUERS > 1 && !Cfg::KSPLIT) ? min(me + 1, n_parts) : n_parts;
                     for (int32_t h = h_begin; ok && h < h_end; ++h) {
                         if constexpr (RELEASE_PARTS > 1) {
                             // the first use of part h in this item: wait until the
@@ -698,6 +731,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         ptx::mma_commit_pair_multicast(empty_bar(stage), 0x3);
                     else
                         ptx::mma_commit(empty_bar(stage));
+                    if constexpr (Cfg::KSPLIT) {
+                        if (kb == w.kb0) {   // the accumulator is started once these complete
+                            if constexpr (PAIR)
+                                ptx::mma_commit_pair_multicast(first_bar(buf), 0x1);
+                            else
+                                ptx::mma_commit(first_bar(buf));
+                        }
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -710,6 +751,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     else
                         ptx::mma_commit(acc_full_bar(buf));
                 }
+                walked += w.kb1 - w.kb0;
                 ++local;
             }
             if (!ok && issued) {

@@ -43,6 +43,7 @@ constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;
 using Cfg256 = TileConfig<256, 4, false>;   // one CTA per 128 x 256 tile
 using Cfg128 = TileConfig<128, 6, false>;   // one CTA per 128 x 128 tile
 using CfgPair = TileConfig<256, 6, true, false, 2>;   // a CTA pair per 256 x 256 tile, two MMA issuers
+                                                      // taking alternate k-blocks
 using CfgWide = TileConfig<512, 4, true>;   // a CTA pair per 256 x 512 tile
 // the same four shapes for a column-major B (a K-major B operand)
 using Cfg256K = TileConfig<256, 4, false, true>;
@@ -72,6 +73,7 @@ struct Options {
     int32_t test_stall = 0;
     int32_t c_store = 0;            // 0 automatic (TMA stores when possible), 1 per-lane stores
     int32_t acc16 = 0;              // 1: FP16 accumulators (study variant)
+    int32_t reproducible = 0;       // 1: only paths whose summation order is fixed
     uint64_t wait_limit_ns = kDefaultWaitLimitNs;
 };
 
@@ -125,16 +127,16 @@ double pair_waves(int64_t tiles, int64_t units) {
 }
 
 // Pair tiles 512 wide instead of 256: each SM then receives 48 KB of operands
-// per 1024 MMA cycles instead of 32 KB per 512, and two threads issue the
-// MMAs (one per 256-column half of the accumulator), which keeps the tensor
-// pipe fed; the price is a single accumulator buffer, whose epilogue
-// overlaps the next tile only by halves, and coarser waves. The relative pipe
-// efficiencies weigh the two walks against each other (at 8192^3, with waves
-// of nearly equal cost, 512-wide tiles ran 13 % faster); below K = 2048 the
-// exposed epilogue is no longer paid for.
+// per 1024 MMA cycles instead of 32 KB per 512; the price is a single
+// accumulator buffer, whose epilogue overlaps the next tile only by halves,
+// and coarser waves. The relative efficiencies within a tile weigh the two
+// walks against each other (measured at the power cap, cycles per launch
+// corrected for the waves: 1.085 at 8192^3, 1.12 at 6144^3, 1.02 at
+// 16384 x 16384 x 4096); below K = 2048 the exposed epilogue is no longer
+// paid for.
 bool auto_wide(int64_t M, int64_t N, int64_t K, int64_t units) {
     if (K < 2048 || N < 1024) return false;
-    constexpr double kEff256 = 0.84, kEff512 = 0.84 * 1.18;
+    constexpr double kEff256 = 0.83, kEff512 = 0.83 * 1.07;
     const int64_t mt = ceil_div(M, 256);
     const double t256 = pair_waves(mt * ceil_div(N, 256), units) / kEff256;
     const double t512 = 2.0 * pair_waves(mt * ceil_div(N, 512), units) / kEff512;
@@ -198,7 +200,9 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
         if (opt.pair_units > 0) pair_units = std::min<int64_t>(pair_units, opt.pair_units);
         if (opt.max_ctas > 0) pair_units = std::min<int64_t>(pair_units, std::max<int64_t>(1, opt.max_ctas / 2));
         pair_units = std::max<int64_t>(1, pair_units);
-        const bool wide = opt.tile_n == 512 ||
+        // (256 x 256 pair tiles add alternate k-blocks from two threads, in
+        // an order that can vary: not with `reproducible`)
+        const bool wide = opt.tile_n == 512 || opt.reproducible ||
                           (!opt.tile_m && !opt.tile_n && auto_wide(M, N, K, pair_units));
         p.tile_m = 256;
         p.tile_n = wide ? 512 : 256;
@@ -241,7 +245,7 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     int64_t splits = 1;
     // (FP16 accumulators never split K: the study variant keeps the whole K
     // range in one FP16 accumulator, as an __half accumulator type would)
-    if (!pair && opt.split_k != 1 && !opt.acc16) {
+    if (!pair && opt.split_k != 1 && !opt.acc16 && !opt.reproducible) {
         if (opt.split_k >= 2)
             splits = opt.split_k;
         else if (beta == 1.0f ? (p.tiles * 2 <= units && k_blocks >= 16) : (p.tiles * 4 <= units && k_blocks >= 32))
@@ -824,6 +828,10 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
         case MPGEMM_OPT_ACCUMULATOR:
             if (value != 0 && value != 16 && value != 32) return MPGEMM_ERR_INVALID_VALUE;
             h->opt.acc16 = value == 16 ? 1 : 0;
+            return MPGEMM_OK;
+        case MPGEMM_OPT_REPRODUCIBLE:
+            if (value != 0 && value != 1) return MPGEMM_ERR_INVALID_VALUE;
+            h->opt.reproducible = static_cast<int32_t>(value);
             return MPGEMM_OK;
     }
     return MPGEMM_ERR_INVALID_VALUE;

@@ -510,7 +510,9 @@ C_STORE_CASES = [  # (M, N, K, ldc, tile_m, tile_n): beta == 0, C rows 16-byte a
 def test_tma_store_of_c_matches_per_lane_stores(mp, M, N, K, ldc, tile_m, tile_n):
     # C written by tiled TMA stores (the automatic choice here) against the
     # oracle, and bit for bit against the per-lane stores of the same sums
-    ops = workloads.make_operands(M, N, K, ldc=ldc, alpha=1.25, seed=M + N + K + 5)
+    # (integer inputs: the sums are exact whatever order a path adds in)
+    ops = workloads.make_operands(M, N, K, ldc=ldc, alpha=1.25, dist="int3", dist_b="int2",
+                                  seed=M + N + K + 5)
     outs = []
     for c_store in (0, 1):
         with mp.Handle() as h:
@@ -551,6 +553,30 @@ def test_split_k_tma_reduce_matches_atomics(mp, M, N, K, lda, ldc, beta, splits)
             got, _, _ = c_result(run_gpu(h, ints), ints)
             outs.append(got)
     assert np.array_equal(outs[0], outs[1])
+
+
+def test_reproducible_option_repeats_bits(mp):
+    # 256 x 256 CTA-pair tiles (automatic below K = 2048) add two threads'
+    # k-blocks in an order that can vary; REPRODUCIBLE = 1 takes 256 x 512
+    # tiles and no split-K, and identical calls give identical bits
+    from parity import device_operands
+    ops = workloads.make_operands(2560, 2048, 700, dist="normal", seed=98)
+    plan = mp.plan(ops.M, ops.N, ops.K, 1.0, 256, ops.lda, 256, ops.ldb, 0.0, 256, ops.ldc)
+    assert (plan["tile_m"], plan["tile_n"]) == (256, 256)
+    s = torch.cuda.current_stream()
+    with mp.Handle() as h:
+        h.set_option(mp.Option.REPRODUCIBLE, 1)
+        check_full(h, ops)
+        outs = []
+        for _ in range(3):
+            d = device_operands(ops)
+            h.run(ops.M, ops.N, ops.K, ops.alpha, d["a_ptr"], ops.lda, d["b_ptr"], ops.ldb, ops.beta,
+                  d["c_ptr"], ops.ldc, s.cuda_stream)
+            s.synchronize()
+            outs.append(d["c_buf"].cpu().numpy().view(np.uint32))
+        assert all(np.array_equal(outs[0], o) for o in outs[1:])
+        h.set_option(mp.Option.REPRODUCIBLE, 0)   # the default path: within the tolerance
+        check_full(h, ops)
 
 
 def test_tma_store_falls_back_for_unaligned_c(mp):
