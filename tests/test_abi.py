@@ -168,7 +168,10 @@ def test_tile_selection_and_grid():
     assert (p["tile_m"], p["tile_n"]) == (128, 256) and p["tiles"] == 64 * 32
     # 2048^3: 128 tiles of 128 x 256 keep 84 % of the SMs busy: wide tiles
     p = _plan(M=2048, N=2048, K=2048, lda=2048, ldb=2048, ldc=2048)
-    assert p["tile_n"] == 256 and p["tiles"] == 16 * 8 and p["grid"] == 128
+    assert p["tile_m"] == 128 and p["tile_n"] == 256 and p["tiles"] == 16 * 8 and p["grid"] == 128
+    # with K = 4096 the same square takes 64 CTA-pair tiles (84 % of the pairs)
+    p = _plan(M=2048, N=2048, K=4096, lda=4096, ldb=2048, ldc=2048)
+    assert (p["tile_m"], p["tile_n"]) == (256, 256) and p["tiles"] == 64 and p["grid"] == 128
     # 1000 x 800: 32 wide tiles would leave most SMs idle: 128 x 128
     p = _plan(M=1000, N=800, K=1200, lda=1200, ldb=800, ldc=800)
     assert p["tile_n"] == 128 and p["tiles"] == 8 * 7
