@@ -43,9 +43,12 @@
  *    (aligned staging copies, grown on demand with stream-ordered
  *    allocation), the tensor-core launch configuration and a status word
  *    that the device writes if one of its bounded waits gives up.
- *  - A handle is bound to the device that was current at mpgemm_create and
- *    may be used from one stream at a time (its workspace is reused in
- *    stream order). Use one handle per concurrently used stream.
+ *  - A handle is bound to the device that was current at mpgemm_create:
+ *    calls through it return MPGEMM_ERR_INVALID_VALUE (and enqueue nothing)
+ *    while another device is current. It may be used from one stream at a
+ *    time (its workspace is reused in stream order); use one handle per
+ *    concurrently used stream. A handle is not thread-safe: two host threads
+ *    must not call it at the same time. Any host thread may call it.
  */
 #ifndef MPGEMM_H
 #define MPGEMM_H
@@ -111,8 +114,9 @@ mpgemm_status_t mpgemm_run_ex(mpgemm_handle_t h, mpgemm_b_layout_t b_layout,
  * ldb = k, ldc = n), asynchronous on `stream`. The first call on a device
  * creates a handle for that device that lives until the process exits; all
  * calls on a device share its workspace, so calls on different streams of
- * one device must not overlap (use mpgemm_run_ex with a handle per stream
- * for that). */
+ * one device must not overlap on the GPU (use mpgemm_run_ex with a handle
+ * per stream for that). Host threads may call it concurrently: the calls
+ * on one device are serialised on the host while they are enqueued. */
 mpgemm_status_t mpgemm_solve(const void* a, const void* b, float* c,
                              size_t m, size_t n, size_t k, void* stream);
 

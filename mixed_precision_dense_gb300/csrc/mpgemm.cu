@@ -645,6 +645,7 @@ struct SolveDevice {
     std::once_flag once;
     mpgemm_status_t status = MPGEMM_ERR_CUDA;
     mpgemm_handle_st* handle = nullptr;
+    std::mutex mu;   // the handle's host state (tensor-map cache, workspace) is not thread-safe
 };
 SolveDevice g_solve_devices[kSolveMaxDevices];
 }  // namespace
@@ -677,6 +678,36 @@ mpgemm_status_t ensure_buffer(void** ptr, size_t* cap, size_t need, cudaStream_t
     }
     *cap = need;
     return MPGEMM_OK;
+}
+
+// The tensor-map encoder is a driver-API call and needs the device's
+// context current in the calling thread. The runtime binds a thread to the
+// device's primary context lazily, at its first call that needs one, so a
+// thread whose first GEMM needs no other runtime call before the encoder
+// (no staging copy, no workspace to grow) would meet it unbound. Bind it
+// here, once per thread and device; `dev` is already the current device,
+// so the caller's choice of device is not changed.
+bool bind_context(int dev) {
+    thread_local int bound = -1;
+    if (bound == dev) return true;
+    if (cudaSetDevice(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    bound = dev;
+    return true;
+}
+
+// The handle's device must be current (it owns the workspace and the launch
+// configuration of that device).
+mpgemm_status_t enter_device(const mpgemm_handle_st* h) {
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return MPGEMM_ERR_CUDA;
+    }
+    if (cur != h->device) return MPGEMM_ERR_INVALID_VALUE;
+    return bind_context(cur) ? MPGEMM_OK : MPGEMM_ERR_CUDA;
 }
 
 mpgemm_status_t take_device_report(mpgemm_handle_t h, int32_t info[4]) {
@@ -851,6 +882,7 @@ mpgemm_status_t mpgemm_run_ex(mpgemm_handle_t h, mpgemm_b_layout_t b_layout, int
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     mpgemm_plan_t plan;
     Options opt = h->opt;
+    if (mpgemm_status_t st0 = enter_device(h); st0 != MPGEMM_OK) return st0;
     opt.pair_units = h->max_clusters;
     opt.b_col_major = b_col ? 1 : 0;
     mpgemm_status_t st = make_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, h->num_sms, opt, &plan);
@@ -987,6 +1019,7 @@ mpgemm_status_t mpgemm_solve(const void* a, const void* b, float* c, size_t m, s
     std::call_once(d.once, [&d] { d.status = mpgemm_create(&d.handle); });
     if (d.status != MPGEMM_OK) return d.status;
     const int64_t M = static_cast<int64_t>(m), N = static_cast<int64_t>(n), K = static_cast<int64_t>(k);
+    std::lock_guard<std::mutex> lock(d.mu);
     return mpgemm_run_ex(d.handle, MPGEMM_B_COL_MAJOR, M, N, K, 1.0f, a, K > 1 ? K : 1, b,
                          K > 1 ? K : 1, 0.0f, c, N > 1 ? N : 1, stream);
 }
@@ -1072,6 +1105,7 @@ extern "C" mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K, f
     NoAllocDevice& d = g_noalloc_devices[dev];
     std::call_once(d.once, noalloc_setup, std::ref(d), dev);
     if (d.status != MPGEMM_OK) return d.status;
+    if (!bind_context(dev)) return MPGEMM_ERR_CUDA;
 
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     Options opt;  // defaults: automatic tile width, one CTA per SM, 4 s wait limit

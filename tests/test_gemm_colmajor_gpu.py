@@ -117,3 +117,42 @@ def test_column_major_matches_row_major_bitwise(mp):
         g1, _, _ = c_result(run_gpu(h, rm), rm)
         g2, _, _ = c_result(run_gpu(h, cm), cm)
     assert np.array_equal(g1, g2)
+
+
+def test_solve_from_several_host_threads(mp):
+    # mpgemm_solve shares one handle per device; host threads may call it at
+    # the same time (the library serialises them while it enqueues). Eight
+    # threads, three calls each, different shapes (some with a ragged K whose
+    # B needs an aligned staging copy), all on one stream; every result is
+    # checked against the oracle.
+    import threading
+    s = torch.cuda.current_stream()
+    jobs = []
+    for t in range(8):
+        for c in range(3):
+            m, n, k = 64 + 37 * t, 48 + 29 * c, 96 + 61 * (t + c) + (t % 2)
+            ops = gate_operands(m, n, k, "int", seed=500 + 10 * t + c)
+            A = ops.A.cuda()
+            B = ops.B.cuda()
+            C = torch.full((m, n), float("nan"), device="cuda")
+            jobs.append((t, ops, A, B, C))
+    errors = []
+
+    def worker(t):
+        try:
+            for (tt, ops, A, B, C) in jobs:
+                if tt == t:
+                    mp.solve(A.data_ptr(), B.data_ptr(), C.data_ptr(), ops.M, ops.N, ops.K, s.cuda_stream)
+        except Exception as e:   # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(8)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    s.synchronize()
+    for (_, ops, A, B, C) in jobs:
+        ref, _ = reference(ops)
+        assert np.array_equal(C.cpu().double().numpy(), ref)
