@@ -411,11 +411,11 @@ def run_ours(args):
     ms_per_step = max_s * 1e3 / args.steps
 
     # the dominant kernel alone: event-timed tensor-core launches (one per step
-    # when no operand needs staging; otherwise the staging launches are
-    # timed separately and subtracted)
+    # when no operand needs staging; otherwise the same kernel, same tile
+    # and same reading of A, timed on operands staged beforehand)
     kernel_ms = ms_per_step
     if launches_per_step > 1:
-        kernel_ms = time_tc_kernel_only(handle, w, A, B, C, stream, args.steps, flush)
+        kernel_ms = time_tc_kernel_only(w, A, B, C, stream, args.steps, plan, flush)
     peaks = measured_peaks()
     achieved = gemm_flops(w.M, w.N, w.K) / (kernel_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["tflops"],
@@ -469,21 +469,41 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def time_tc_kernel_only(handle, w, A, B, C, stream, steps, flush=None):
-    """Event-time the tensor-core launch on pre-staged aligned operands."""
+def time_tc_kernel_only(w, A, B, C, stream, steps, plan, flush=None):
+    """Event-time the tensor-core launch alone: the operands that the call
+    stages (plan["stage_a"], plan["stage_b"]) are copied to aligned buffers
+    first, the others are used as they are (an unaligned A that the kernel
+    reads in row classes stays so), and the tile shape is pinned to the
+    call's own, so the launch timed is the step's kernel."""
     import torch
+
+    import mixed_precision_dense_gb300 as mp
     M, N, K = w.M, w.N, w.K
-    lda, ldb = (K + 7) // 8 * 8, (N + 7) // 8 * 8
-    A2 = torch.zeros((M, lda), dtype=torch.float16, device=A.device)
-    B2 = torch.zeros((K, ldb), dtype=torch.float16, device=A.device)
-    A2[:, :K] = A[:, :K]
-    B2[:, :N] = B[:, :N]
-    for _ in range(3):
-        handle.run(M, N, K, w.alpha, A2.data_ptr(), lda, B2.data_ptr(), ldb, w.beta, C.data_ptr(),
-                   w.ldc, stream.cuda_stream)
-    return timed_loop(lambda: handle.run(M, N, K, w.alpha, A2.data_ptr(), lda, B2.data_ptr(), ldb,
-                                         w.beta, C.data_ptr(), w.ldc, stream.cuda_stream),
-                      stream, steps, flush)
+    A2, lda, B2, ldb = A, w.lda, B, w.ldb
+    if plan["stage_a"]:
+        lda = (K + 7) // 8 * 8
+        A2 = torch.zeros((M, lda), dtype=torch.float16, device=A.device)
+        A2[:, :K] = A[:, :K]
+    if plan["stage_b"]:
+        ldb = (N + 7) // 8 * 8
+        B2 = torch.zeros((K, ldb), dtype=torch.float16, device=B.device)
+        B2[:, :N] = B[:, :N]
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_M, plan["tile_m"])
+        h.set_option(mp.Option.TILE_N, plan["tile_n"])
+        run = lambda: h.run(M, N, K, w.alpha, A2.data_ptr(), lda, B2.data_ptr(), ldb, w.beta, C.data_ptr(),
+                            w.ldc, stream.cuda_stream)
+        p2 = mp.plan(M, N, K, w.alpha, A2.data_ptr(), lda, B2.data_ptr(), ldb, w.beta, C.data_ptr(), w.ldc,
+                     num_sms=torch.cuda.get_device_properties(A.device).multi_processor_count,
+                     tile_m=plan["tile_m"], tile_n=plan["tile_n"])
+        assert p2["stage_a"] == 0 and p2["stage_b"] == 0 and p2["a_classes"] == plan["a_classes"], p2
+        for _ in range(3):
+            run()
+        ms = timed_loop(run, stream, steps, flush)
+        st, info = h.sync_status(stream.cuda_stream)
+        if st != mp.Status.OK:
+            raise RuntimeError(f"device reported {st.name} {info}")
+        return ms
 
 
 # handles (and streams) the end-to-end leg rotates through

@@ -140,7 +140,10 @@ mpgemm_status_t mpgemm_sync_status(mpgemm_handle_t h, void* stream, int32_t info
 
 /* Tunables and test switches, set per handle. */
 typedef enum {
-    MPGEMM_OPT_TILE_N = 1,        /* 0 = automatic (default), or 128 or 256 columns per tile;
+    MPGEMM_OPT_TILE_N = 1,        /* 0 = automatic (default), or 128, 256 or 320 columns per
+                                     tile (320: one CTA per 128 x 320 tile, chosen
+                                     automatically when N is 257 to 320; TILE_M 256 with
+                                     TILE_N 320 makes runs return INVALID_VALUE);
                                      512 = a cluster of two CTAs per 256 x 512 tile (with
                                      TILE_M 0 or 256) */
     MPGEMM_OPT_MAX_CTAS = 2,      /* 0 = one persistent CTA per SM (default), else an upper bound */
@@ -204,7 +207,7 @@ typedef struct {
     int32_t stage_a;        /* 1 if A is copied to an aligned buffer first */
     int32_t stage_b;        /* 1 if B is copied to an aligned buffer first */
     int32_t tile_m;         /* rows per output tile: 128 (one CTA) or 256 (a CTA pair) */
-    int32_t tile_n;         /* columns per output tile (128 or 256; 256 or 512 for a pair) */
+    int32_t tile_n;         /* columns per output tile (128, 256 or 320; 256 or 512 for a pair) */
     int32_t tile_k;         /* K per pipeline stage (64) */
     int32_t stages;         /* shared-memory pipeline depth */
     int32_t m_tiles, n_tiles, k_blocks;

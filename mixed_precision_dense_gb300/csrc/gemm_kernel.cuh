@@ -38,7 +38,10 @@
 // Two shapes of the same pipeline:
 //   single  one CTA per tile of 128 x BN (BN = 128 or 256), tcgen05.mma with
 //           cta_group::1, M = 128, N = 64 * ceil(valid columns / 64), two
-//           accumulator buffers;
+//           accumulator buffers; or BN = 320 (N from 257 to 320 in one tile
+//           column, so that every row block of A is read once), two
+//           instructions per K step (N = 256 and N = 64) into one
+//           accumulator buffer whose two parts are handed back one by one;
 //   pair    a cluster of two CTAs per tile of 256 x BN (BN = 256 or 512):
 //           each CTA loads its own 128 rows of A and its own half of the B
 //           columns of every accumulator part; the even CTA issues
@@ -144,10 +147,11 @@ struct TileConfig {
     // accumulator) have completed
     static constexpr int ISSUERS = ISSUERS_;
     static constexpr bool KSPLIT = ISSUERS == 2 && BN_ != 512;
-    // one MMA instruction covers SUB_N columns: BN, except that a tile 512
-    // wide takes two instructions of 256 per K step
-    static constexpr int SUB_N = BN == 512 ? 256 : BN;
-    static constexpr int SUBS = BN / SUB_N;
+    // one MMA instruction covers SUB_N columns: BN, except that a tile wider
+    // than 256 takes two instructions per K step, of 256 columns and of the
+    // rest (256 for 512-wide pair tiles, 64 for 320-wide one-CTA tiles)
+    static constexpr int SUB_N = BN > 256 ? 256 : BN;
+    static constexpr int SUBS = (BN + SUB_N - 1) / SUB_N;
     // two accumulator buffers (the epilogue of tile i overlaps the MMAs of
     // tile i+1) when they fit in the 512 columns of tensor memory, else one,
     // whose SUBS parts are handed back one by one
@@ -168,7 +172,8 @@ struct TileConfig {
     static constexpr int EPI_WARPS = 8;
     static constexpr int EPI_CHUNK_BYTES = 32 * 32 * 4;  // one warp's 32 x 32 FP32 chunk buffer
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_CHUNK_BYTES;
-    static constexpr int TMEM_COLS = ACC_BUFS * BN;
+    // (allocations are powers of two: a 320-column accumulator takes 512)
+    static constexpr int TMEM_COLS = ACC_BUFS * BN <= 256 ? 256 : 512;
     // full and empty per stage; accumulator full per buffer; accumulator
     // empty per buffer and part; first k-block done per buffer (KSPLIT)
     static constexpr int NUM_BARRIERS = 2 * STAGES + ACC_BUFS + ACC_BUFS * RELEASE_PARTS + ACC_BUFS;
@@ -179,7 +184,8 @@ struct TileConfig {
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARRIERS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
     static constexpr int THREADS = 32 * (2 + EPI_WARPS + ISSUERS - 1);
-    static_assert(BN == 128 || BN == 256 || (PAIR && BN == 512), "tile width");
+    static_assert(BN == 128 || BN == 256 || (PAIR && BN == 512) || (!PAIR && BN == 320), "tile width");
+    static_assert(ACC_BUFS * BN <= TMEM_COLS, "accumulators fit the tensor memory allocated");
     static_assert(!PAIR || BN >= 256, "pair tiles are 256 x 256 or 256 x 512");
     static_assert(ISSUERS == 1 || ISSUERS == SUBS || (KSPLIT && SUBS == 1), "one issuer, one per part, or two by k-block");
     static_assert(SUB_N >= (PAIR ? 128 : 64) && ATOMS_PER_PART >= 1, "parts hold whole B boxes");
@@ -187,6 +193,8 @@ struct TileConfig {
     static_assert(OFF_EPI % 1024 == 0, "chunk buffers are 1024-byte aligned (128-byte swizzle atoms)");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "tensor memory allocation");
+    static_assert(BN % 64 == 0 && (BN - (SUBS - 1) * SUB_N) % (PAIR ? 128 : 64) == 0,
+                  "the last part holds whole B boxes");
 };
 
 // M-tile mb -> (row class r, first class row j0 of the tile).
@@ -815,9 +823,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                 };
                 if (h * part_n < w.width) {
-                    if (h > 0 && read_c) load_c_chunk(c_tile, row_stride, pn0 + lane, p.N, rows, c_cur);
+                    // this warp's columns of the part, within the item (the
+                    // 64-column last part of a 320-wide tile leaves the
+                    // second warp of each lane quarter none)
+                    const int32_t my_w = min(my_n, w.width - h * part_n - my_off);
+                    if (h > 0 && read_c && my_w > 0) load_c_chunk(c_tile, row_stride, pn0 + lane, p.N, rows, c_cur);
                     store_tile(p, &maps.c, t_row + static_cast<uint32_t>(h * part_n + my_off), c_tile, row_stride,
-                               rows, jb, pn0, my_n, buf_s, lane, c_cur, release);
+                               rows, jb, pn0, my_w, buf_s, lane, c_cur, release);
                 } else {
                     release();
                 }

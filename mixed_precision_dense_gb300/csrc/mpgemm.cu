@@ -42,12 +42,16 @@ constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;
 
 using Cfg256 = TileConfig<256, 4, false>;   // one CTA per 128 x 256 tile
 using Cfg128 = TileConfig<128, 6, false>;   // one CTA per 128 x 128 tile
+// one CTA per 128 x 320 tile (N from 257 to 320 in one tile column): 56 KB
+// stages, so three of them, and one accumulator buffer
+using Cfg320 = TileConfig<320, 3, false>;
 using CfgPair = TileConfig<256, 6, true, false, 2>;   // a CTA pair per 256 x 256 tile, two MMA issuers
                                                       // taking alternate k-blocks
 using CfgWide = TileConfig<512, 4, true>;   // a CTA pair per 256 x 512 tile
 // the same four shapes for a column-major B (a K-major B operand)
 using Cfg256K = TileConfig<256, 4, false, true>;
 using Cfg128K = TileConfig<128, 6, false, true>;
+using Cfg320K = TileConfig<320, 3, false, true>;
 using CfgPairK = TileConfig<256, 6, true, true, 2>;
 using CfgWideK = TileConfig<512, 4, true, true>;
 // one occupancy query (max_pair_clusters) serves both pair shapes: shared
@@ -104,10 +108,31 @@ mpgemm_status_t validate(int64_t M, int64_t N, int64_t K, float alpha, const voi
 
 // 256-wide tiles move less operand data per FLOP; they are worth it as soon
 // as they keep at least four fifths of the SMs busy.
-int32_t auto_tile_n(int64_t M, int64_t N, int32_t num_sms) {
+//
+// When N is 257 to 320, 256-wide tiles leave a second tile column of at most
+// 64 columns, whose tiles read all of A again. One 320-wide tile column
+// reads A once, but its 56 KB stages leave room for three, and at these
+// shapes a k-block takes about the load latency over the stages in flight,
+// whatever their size: a wave of 320-wide tiles costs 1.9 waves of 256-wide
+// ones when A is aligned, 1.6 when A is read in row classes (each read of an
+// unaligned row touches an extra cache line, and the 256-wide walk reads
+// every row twice). Measured on GB300 at N = 257, K = 4093, beta = 0.5, in
+// us per call, 256 -> 320 wide: M = 58368 (three waves of 320-wide tiles)
+// 181.5 -> 168.6 aligned, 229.6 -> 179.9 in row classes; M = 65536 (3.4
+// waves) 202.2 -> 221.0 and 257.5 -> 225.2; M = 77824 (four waves) 231.8 ->
+// 224.3 and 287.8 -> 237.7. The choice compares whole waves.
+int32_t auto_tile_n(int64_t M, int64_t N, int32_t num_sms, bool a_row_classes) {
     if (N <= 128) return 128;
-    const int64_t tiles256 = ceil_div(M, 128) * ceil_div(N, 256);
-    return tiles256 * 5 >= static_cast<int64_t>(num_sms) * 4 ? 256 : 128;
+    const int64_t m_tiles = ceil_div(M, 128);
+    const int64_t tiles256 = m_tiles * ceil_div(N, 256);
+    const bool wide = tiles256 * 5 >= static_cast<int64_t>(num_sms) * 4;
+    if (wide && N > 256 && N <= 320) {
+        const double wave320 = a_row_classes ? 1.6 : 1.9;   // in waves of 256-wide tiles
+        if (static_cast<double>(ceil_div(m_tiles, num_sms)) * wave320 <
+            static_cast<double>(ceil_div(tiles256, num_sms)))
+            return 320;
+    }
+    return wide ? 256 : 128;
 }
 
 // CTA pairs (256 x 256 tiles) pay off once there is at least a full wave of
@@ -184,6 +209,7 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     if (st != MPGEMM_OK) return st;
     if (num_sms <= 0) return MPGEMM_ERR_INVALID_VALUE;
     if (opt.tile_n == 512 && opt.tile_m == 128) return MPGEMM_ERR_INVALID_VALUE;   // 512 wide: pairs only
+    if (opt.tile_n == 320 && opt.tile_m == 256) return MPGEMM_ERR_INVALID_VALUE;   // 320 wide: one CTA
     mpgemm_plan_t p;
     std::memset(&p, 0, sizeof(p));
     p.tile_m = 128;
@@ -214,9 +240,13 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
         p.stages = wide ? CfgWide::STAGES : CfgPair::STAGES;
         p.smem_bytes = wide ? CfgWide::SMEM_BYTES : CfgPair::SMEM_BYTES;
     } else {
-        p.tile_n = opt.tile_n ? opt.tile_n : auto_tile_n(M, N, num_sms);
-        p.stages = (p.tile_n == 256) ? Cfg256::STAGES : Cfg128::STAGES;
-        p.smem_bytes = (p.tile_n == 256) ? Cfg256::SMEM_BYTES : Cfg128::SMEM_BYTES;
+        // (A is read in row classes below when its rows break the 16-byte rule)
+        const bool row_classes = !aligned16(A, lda, 2) && !opt.force_staging && !opt.b_col_major;
+        p.tile_n = opt.tile_n ? opt.tile_n : auto_tile_n(M, N, num_sms, row_classes);
+        p.stages = p.tile_n == 320 ? Cfg320::STAGES : (p.tile_n == 256) ? Cfg256::STAGES : Cfg128::STAGES;
+        p.smem_bytes = p.tile_n == 320   ? Cfg320::SMEM_BYTES
+                       : p.tile_n == 256 ? Cfg256::SMEM_BYTES
+                                         : Cfg128::SMEM_BYTES;
     }
     // An A whose rows break TMA's 16-byte rule is read in row classes
     // (one-CTA tiles with a row-major B), else copied to an aligned buffer.
@@ -265,11 +295,13 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     } else {
         // If the last wave of tiles would keep at most half of the CTAs (pairs)
         // busy, do those tiles as two half-width items each: the wave then
-        // finishes in half the time.
+        // finishes in half the time. (Not 320-wide tiles: a 160-column half
+        // does not follow their 256 + 64 column parts.)
         const int64_t tile_units = std::min<int64_t>(units, p.tiles);
         const int64_t rem = p.tiles % tile_units;
-        p.split_tiles =
-            (p.tiles > tile_units && rem > 0 && 2 * rem <= tile_units) ? static_cast<int32_t>(rem) : 0;
+        p.split_tiles = (p.tile_n != 320 && p.tiles > tile_units && rem > 0 && 2 * rem <= tile_units)
+                            ? static_cast<int32_t>(rem)
+                            : 0;
         p.items = p.tiles + p.split_tiles;
     }
     if (p.items > kDimLimit) return MPGEMM_ERR_INVALID_VALUE;
@@ -509,10 +541,12 @@ int32_t keep_a_operand(const mpgemm_plan_t& plan, int32_t l2_keep) {
 cudaError_t prepare_kernels() {
     cudaError_t e = set_smem_attr<Cfg256>();
     if (e == cudaSuccess) e = set_smem_attr<Cfg128>();
+    if (e == cudaSuccess) e = set_smem_attr<Cfg320>();
     if (e == cudaSuccess) e = set_smem_attr<CfgPair>();
     if (e == cudaSuccess) e = set_smem_attr<CfgWide>();
     if (e == cudaSuccess) e = set_smem_attr<Cfg256K>();
     if (e == cudaSuccess) e = set_smem_attr<Cfg128K>();
+    if (e == cudaSuccess) e = set_smem_attr<Cfg320K>();
     if (e == cudaSuccess) e = set_smem_attr<CfgPairK>();
     if (e == cudaSuccess) e = set_smem_attr<CfgWideK>();
     return e;
@@ -623,6 +657,9 @@ cudaError_t launch_plan(const mpgemm_plan_t& plan, bool b_col_major, int max_clu
         return b_col_major ? launch_tc<CfgPairK>(grid, ta, tb, gp, stream)
                            : launch_tc<CfgPair>(grid, ta, tb, gp, stream);
     }
+    if (plan.tile_n == 320)
+        return b_col_major ? launch_tc<Cfg320K>(plan.grid, ta, tb, gp, stream)
+                           : launch_tc<Cfg320>(plan.grid, ta, tb, gp, stream);
     if (plan.tile_n == 256)
         return b_col_major ? launch_tc<Cfg256K>(plan.grid, ta, tb, gp, stream)
                            : launch_tc<Cfg256>(plan.grid, ta, tb, gp, stream);
@@ -751,7 +788,8 @@ mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const 
                             mpgemm_plan_t* out) {
     if (!out) return MPGEMM_ERR_INVALID_VALUE;
     if (tile_m != 0 && tile_m != 128 && tile_m != 256) return MPGEMM_ERR_INVALID_VALUE;
-    if (tile_n != 0 && tile_n != 128 && tile_n != 256 && tile_n != 512) return MPGEMM_ERR_INVALID_VALUE;
+    if (tile_n != 0 && tile_n != 128 && tile_n != 256 && tile_n != 320 && tile_n != 512)
+        return MPGEMM_ERR_INVALID_VALUE;
     if (max_ctas < 0) return MPGEMM_ERR_INVALID_VALUE;
     Options opt;
     opt.tile_m = tile_m;
@@ -822,7 +860,8 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
     if (!h) return MPGEMM_ERR_INVALID_VALUE;
     switch (opt) {
         case MPGEMM_OPT_TILE_N:
-            if (value != 0 && value != 128 && value != 256 && value != 512) return MPGEMM_ERR_INVALID_VALUE;
+            if (value != 0 && value != 128 && value != 256 && value != 320 && value != 512)
+                return MPGEMM_ERR_INVALID_VALUE;
             h->opt.tile_n = static_cast<int32_t>(value);
             return MPGEMM_OK;
         case MPGEMM_OPT_MAX_CTAS:

@@ -156,9 +156,27 @@ def test_tile_selection_and_grid():
     assert (p["tile_m"], p["tile_n"]) == (256, 512)
     with pytest.raises(mp.MpgemmError):
         _plan(tile_m=128, tile_n=512)
-    # N = 257 would waste half of the last column band: single CTAs
+    # N = 257 would waste half of the last column band: single CTAs, one
+    # 320-wide tile column (A read once per row block, three 56 KB stages)
     p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257, beta=0.5)
-    assert (p["tile_m"], p["tile_n"]) == (128, 256)
+    assert (p["tile_m"], p["tile_n"]) == (128, 320) and p["tiles"] == 512 and p["stages"] == 3
+    assert p["split_tiles"] == 0 and p["smem_bytes"] <= 232448
+    # with A aligned, 3.4 waves of 320-wide tiles cost more than seven waves of
+    # 256-wide ones; three waves cost less than six
+    p = _plan(M=65536, N=257, K=4096, lda=4096, ldb=264, ldc=257, beta=0.5)
+    assert p["tile_n"] == 256 and p["a_classes"] == 0
+    p = _plan(M=58368, N=257, K=4096, lda=4096, ldb=264, ldc=257, beta=0.5)
+    assert p["tile_n"] == 320 and p["tiles"] == 456
+    # N = 321 needs two tile columns anyway: 256 wide; too few row blocks: not 320
+    p = _plan(M=65536, N=321, K=4093, lda=4093, ldb=321, ldc=321)
+    assert p["tile_n"] == 256
+    p = _plan(M=1000, N=300, K=1000, lda=1000, ldb=300, ldc=300)
+    assert p["tile_n"] == 128
+    # 320 wide on request (one CTA per tile only), never split in half-width items
+    p = _plan(M=5000, N=1000, K=700, lda=700, ldb=1000, ldc=1000, tile_n=320)
+    assert (p["tile_m"], p["tile_n"]) == (128, 320) and p["tiles"] == 40 * 4 and p["split_tiles"] == 0
+    with pytest.raises(mp.MpgemmError):
+        _plan(tile_m=256, tile_n=320)
     # forced pairs with a CTA cap: the grid stays even
     p = _plan(M=1000, N=800, K=64, lda=64, ldb=800, ldc=800, tile_m=256, max_ctas=5)
     assert p["tile_m"] == 256 and p["grid"] == 4 and p["tiles"] == 4 * 4

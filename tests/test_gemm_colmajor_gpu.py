@@ -69,7 +69,7 @@ CM_SHAPES = [(1, 1, 1), (17, 15, 65), (129, 257, 63), (200, 136, 617), (1000, 80
              (513, 1025, 300)]
 
 
-@pytest.mark.parametrize("tile_m,tile_n", [(0, 0), (128, 128), (128, 256), (256, 0), (256, 512)])
+@pytest.mark.parametrize("tile_m,tile_n", [(0, 0), (128, 128), (128, 256), (128, 320), (256, 0), (256, 512)])
 @pytest.mark.parametrize("M,N,K", CM_SHAPES)
 def test_run_ex_column_major(mp, tile_m, tile_n, M, N, K):
     ops = workloads.make_operands(M, N, K, alpha=1.5, beta=0.5, c_dist="normal", seed=M * 7 + N + K,

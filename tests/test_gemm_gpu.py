@@ -169,6 +169,35 @@ def test_tile_width_and_persistence(mp, tile_n, max_ctas):
         check_full(h, workloads.make_operands(700, 600, 450, beta=1.0, c_dist="normal", seed=80))
 
 
+WIDE_ONE_CTA = [  # (M, N, K, lda, ldb, ldc, beta, max_ctas): 128 x 320 tiles (parts of 256 and 64 columns)
+    (640, 257, 333, 335, 264, 257, 0.0, 0),     # odd lda (row classes), a one-column second part
+    (1000, 300, 700, 700, 300, 301, 0.5, 2),    # two CTAs walk 8 tiles: the one accumulator and the ring wrap
+    (1000, 641, 129, 129, 648, 641, 1.0, 0),    # three tile columns, the last one a single column
+    (129, 320, 65, 72, 320, 320, -0.5, 3),      # the full 256 + 64 columns, ragged rows, two k-blocks
+    (700, 1000, 450, 450, 1000, 1000, 0.0, 5),  # 320-wide tiles across a wide N
+]
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,beta,max_ctas", WIDE_ONE_CTA)
+def test_one_cta_320_wide_tiles(mp, M, N, K, lda, ldb, ldc, beta, max_ctas):
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_N, 320)
+        h.set_option(mp.Option.MAX_CTAS, max_ctas)
+        ops = workloads.make_operands(M, N, K, lda=lda, ldb=ldb, ldc=ldc, alpha=1.25, beta=beta,
+                                      c_dist="normal" if beta else "zeros", seed=M + 3 * N + K)
+        check_full(h, ops)
+
+
+@pytest.mark.parametrize("split_k", [1, 3])
+def test_one_cta_320_integer_bitwise(mp, split_k):
+    # the planner's own choice at N = 300 (one wave of 320-wide tiles), and forced split-K
+    ops = workloads.make_operands(19456, 300, 1000, dist="int3", dist_b="int2", seed=86 + split_k)
+    with mp.Handle() as h:
+        h.set_option(mp.Option.SPLIT_K, split_k)
+        assert mp.plan(19456, 300, 1000, A=1 << 20, B=1 << 30, C=1 << 34)["tile_n"] == 320
+        check_full(h, ops, exact=True)
+
+
 PAIR_SHAPES = [  # (M, N, K): one pair tile, ragged in every dimension, many tiles
     (256, 256, 64), (256, 256, 192), (200, 136, 617), (300, 500, 700), (511, 257, 129),
     (1024, 768, 1000), (257, 1025, 65), (1000, 800, 1200),
