@@ -356,6 +356,7 @@ def run_ours(args):
     handle = mp.Handle()
     handle.set_option(mp.Option.TILE_M, args.tile_m)
     handle.set_option(mp.Option.TILE_N, args.tile_n)
+    handle.set_option(mp.Option.SPLIT_K, args.split_k)
 
     def step():
         handle.run(w.M, w.N, w.K, w.alpha, A.data_ptr(), w.lda, B.data_ptr(), w.ldb, w.beta,
@@ -365,6 +366,8 @@ def run_ours(args):
                    C.data_ptr(), w.ldc, num_sms=torch.cuda.get_device_properties(device).multi_processor_count,
                    tile_m=args.tile_m, tile_n=args.tile_n)
     launches_per_step = 1 + plan["stage_a"] + plan["stage_b"]
+    if args.split_k > 1 and w.beta != 1.0:
+        launches_per_step += 1      # the pass that applies beta before the slices add into C
 
     # correctness first, on a NaN-poisoned (beta == 0) or restored (beta != 0) C
     if w.beta == 0:
@@ -415,7 +418,7 @@ def run_ours(args):
     # and same reading of A, timed on operands staged beforehand)
     kernel_ms = ms_per_step
     if launches_per_step > 1:
-        kernel_ms = time_tc_kernel_only(w, A, B, C, stream, args.steps, plan, flush)
+        kernel_ms = time_tc_kernel_only(w, A, B, C, stream, args.steps, plan, flush, args.split_k)
     peaks = measured_peaks()
     achieved = gemm_flops(w.M, w.N, w.K) / (kernel_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["tflops"],
@@ -429,7 +432,7 @@ def run_ours(args):
     cublas = None
     if not args.no_cublas:
         cublas = time_cublas_context(w, A, B, C, stream, min(args.steps, 200), flush)
-        if cublas:
+        if cublas and cublas["value"] > 0:
             cublas["ours_over_cublas"] = round(value / world / cublas["value"], 4)
 
     # end to end through the host-buffer entry point
@@ -469,7 +472,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def time_tc_kernel_only(w, A, B, C, stream, steps, plan, flush=None):
+def time_tc_kernel_only(w, A, B, C, stream, steps, plan, flush=None, split_k=0):
     """Event-time the tensor-core launch alone: the operands that the call
     stages (plan["stage_a"], plan["stage_b"]) are copied to aligned buffers
     first, the others are used as they are (an unaligned A that the kernel
@@ -491,6 +494,7 @@ def time_tc_kernel_only(w, A, B, C, stream, steps, plan, flush=None):
     with mp.Handle() as h:
         h.set_option(mp.Option.TILE_M, plan["tile_m"])
         h.set_option(mp.Option.TILE_N, plan["tile_n"])
+        h.set_option(mp.Option.SPLIT_K, split_k)
         run = lambda: h.run(M, N, K, w.alpha, A2.data_ptr(), lda, B2.data_ptr(), ldb, w.beta, C.data_ptr(),
                             w.ldc, stream.cuda_stream)
         p2 = mp.plan(M, N, K, w.alpha, A2.data_ptr(), lda, B2.data_ptr(), ldb, w.beta, C.data_ptr(), w.ldc,
@@ -529,6 +533,7 @@ def run_e2e(handle, w, ops, stream, device, args):
     for h in handles[1:]:
         h.set_option(mp.Option.TILE_M, args.tile_m)
         h.set_option(mp.Option.TILE_N, args.tile_n)
+        h.set_option(mp.Option.SPLIT_K, args.split_k)
     streams = [stream] + [torch.cuda.Stream(device) for _ in range(slots - 1)]
     steps = max(1, min(args.steps, args.e2e_steps))
 
@@ -804,8 +809,10 @@ def main(argv=None):
     ap.add_argument("--num-sms", type=int, default=152, help="SM count assumed by --record-traffic's plan")
     ap.add_argument("--tile-m", type=int, default=0, choices=[0, 128, 256],
                     help="force the tile height (0 = the library's choice)")
-    ap.add_argument("--tile-n", type=int, default=0, choices=[0, 128, 256, 512],
+    ap.add_argument("--tile-n", type=int, default=0, choices=[0, 128, 256, 320, 512],
                     help="force the tile width (0 = the library's choice)")
+    ap.add_argument("--split-k", type=int, default=0,
+                    help="slices of K per tile (0 = the library's choice, 1 = never split)")
     ap.add_argument("--acc16-study", action="store_true",
                     help="compare FP16 with FP32 accumulation and print a report instead")
     ap.add_argument("--gate", action="store_true",

@@ -205,22 +205,26 @@ __device__ __forceinline__ void a_class_of(const GemmParams& p, int32_t mb, int3
     j0 = (mb - p.a_class_first_tile[r]) * TILE_M;
 }
 
-// Zero the first d (1..7) elements of every row of a 128-row A tile in the
-// 128-byte-swizzled layout (row t's first 16 bytes sit at chunk t & 7). These
-// columns lie before the rows' first element; the matching B rows are zero,
-// but the bytes there are arbitrary and could hold NaN or Inf.
-__device__ __forceinline__ void zero_leading_columns(uint8_t* tile, int32_t d) {
-#pragma unroll 4
-    for (int t = 0; t < 128; ++t) {
-        uint4* q = reinterpret_cast<uint4*>(tile + t * 128 + ((t & 7) << 4));
-        uint4 v = *q;
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (2 * i + 1 < d) w[i] = 0u;
-            else if (2 * i < d) w[i] &= 0xFFFF0000u;
-        }
-        *q = make_uint4(w[0], w[1], w[2], w[3]);
+// Zero the first d (1..7) elements of the first `rows` rows of a 128-row A
+// tile in the 128-byte-swizzled layout (row t's first 16 bytes sit at chunk
+// t & 7). These columns lie before the rows' first element; the matching B
+// rows are zero, but the bytes there are arbitrary and could hold NaN or
+// Inf. Rows past the matrix arrived as zeros already. The 2d bytes are
+// covered by at most three plain stores (8, 4 and 2 bytes) per row, none of
+// which waits for a load: this runs on the MMA thread before the tile's
+// first instructions (a read-modify-write of every row there took about
+// 8 K cycles on GB300).
+__device__ __forceinline__ void zero_leading_columns(uint8_t* tile, int32_t d, int32_t rows) {
+    const bool s8 = d >= 4, s4 = (d & 2) != 0, s2 = (d & 1) != 0;
+    const int32_t o4 = s8 ? 8 : 0;             // offset of the 4-byte store
+    const int32_t o2 = o4 + (s4 ? 4 : 0);      // offset of the 2-byte store
+    rows = min(rows, 128);
+#pragma unroll 8
+    for (int32_t t = 0; t < rows; ++t) {
+        uint8_t* q = tile + t * 128 + ((t & 7) << 4);
+        if (s8) *reinterpret_cast<uint64_t*>(q) = 0ull;
+        if (s4) *reinterpret_cast<uint32_t*>(q + o4) = 0u;
+        if (s2) *reinterpret_cast<uint16_t*>(q + o2) = static_cast<uint16_t>(0);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -642,6 +646,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 int32_t cls, j0;
                 a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
                 const int32_t lead_cols = p.a_shift[cls];   // columns before the rows' start
+                const int32_t lead_rows = p.a_class_rows[cls] - j0;   // rows of the tile that exist
                 const int buf = local % ACC_BUFS;
                 const uint32_t acc_phase = (local / ACC_BUFS) & 1;
                 if constexpr (RELEASE_PARTS == 1) {
@@ -683,7 +688,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     ptx::tc_fence_after_sync();
                     if (kb == 0 && lead_cols > 0)
-                        zero_leading_columns(gbase + Cfg::OFF_A + stage * Cfg::A_BYTES, lead_cols);
+                        zero_leading_columns(gbase + Cfg::OFF_A + stage * Cfg::A_BYTES, lead_cols, lead_rows);
                     const uint32_t a_base = sA + stage * Cfg::A_BYTES;
                     const uint32_t b_base = sB + stage * Cfg::B_BYTES;
                     bool pending = false;   // MMAs issued from this stage

@@ -351,6 +351,8 @@ CLASS_CASES = [  # (M, N, K, lda, a_offset, tile_n, split_k): A read in row clas
     (300, 200, 256, 256, 1, 0, 0),      # aligned pitch, base 2 bytes off: 1 class, shift 1
     (3, 50, 70, 71, 0, 0, 0),           # fewer rows than classes
     (640, 128, 2049, 2049, 3, 128, 4),  # classes with split-K
+    (300, 200, 100, 109, 0, 0, 0),      # 9 NaN padding elements: every shift 1..7 lands in NaN
+    (1100, 64, 300, 311, 0, 128, 0),    # 137-138 rows per class: second tiles of 9-10 rows
 ]
 
 
