@@ -797,8 +797,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const int32_t part_n = RELEASE_PARTS > 1 ? Cfg::SUB_N : w.width;   // columns per released part
             const int32_t my_n = part_n / COL_SPLIT;                  // of which this warp stores
             const int32_t my_off = col_half * my_n;
-            // beta * C needs C's old values: the first chunk's loads go out now,
-            // while the MMAs of this tile are still running.
+            // beta * C needs C's old values: this warp's rows of the item's C
+            // are brought into L2 (one row per lane, 128-byte lines) and the
+            // first chunk's loads go out now, while the MMAs of this tile are
+            // still running.
+            // (the two warps of a lane quarter take half of the item's columns
+            // each, one bulk prefetch per row, widened to the 16-byte blocks
+            // that hold its first and last elements)
+            if (read_c && lane < rows) {
+                const int32_t cend = min(n0 + w.width, p.N);
+                const int32_t half = (cend - n0 + 1) / 2;
+                const int32_t cb = n0 + col_half * half;
+                const int32_t ce = min(cb + half, cend);
+                if (ce > cb) {
+                    const float* c_row = c_tile + static_cast<int64_t>(lane) * row_stride;
+                    const uint64_t a = reinterpret_cast<uint64_t>(c_row + cb) & ~uint64_t{15};
+                    const uint64_t e = (reinterpret_cast<uint64_t>(c_row + ce) + 15) & ~uint64_t{15};
+                    ptx::bulk_prefetch_l2(a, static_cast<uint32_t>(e - a));
+                }
+            }
             float c_cur[32];
             if (read_c) load_c_chunk(c_tile, row_stride, n0 + my_off + lane, p.N, rows, c_cur);
             const int accb = local % ACC_BUFS;

@@ -528,12 +528,15 @@ int max_pair_clusters() {
 // L2 hints of the operand loads (GemmParams::keep_a): by default both
 // operands evict-last, since every panel is re-read by the other tiles of
 // its wave (measured at 8192^3: 845 MB of DRAM reads per launch, against
-// 1224 MB when the less re-read operand was marked evict-first); the option
-// can still mark one of them evict-first.
+// 1224 MB when the less re-read operand was marked evict-first), except an
+// operand that only one tile reads: with a single tile column every panel
+// of A is read once, with a single row block every panel of B. The option
+// can still mark either one evict-first.
 int32_t keep_a_operand(const mpgemm_plan_t& plan, int32_t l2_keep) {
-    (void)plan;
     if (l2_keep == 1) return 1;
     if (l2_keep == 2) return 0;
+    if (plan.n_tiles == 1 && plan.m_tiles > 1) return 0;
+    if (plan.m_tiles == 1 && plan.n_tiles > 1) return 1;
     return 2;
 }
 

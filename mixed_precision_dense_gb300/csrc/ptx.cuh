@@ -64,6 +64,12 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 
 // ---------------------------------------------------------------- TMA
 
+// Bring `bytes` of global memory from `addr` into L2 (both multiples of 16;
+// no completion to wait for).
+__device__ __forceinline__ void bulk_prefetch_l2(uint64_t addr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
