@@ -63,7 +63,11 @@ def test_noalloc_matches_run_on_consecutive_calls(mp):
                                 c_dist="normal", seed=123),
         # aligned operands: no scratch at all
         workloads.make_operands(256, 512, 320, seed=124),
+        # N = 300 over 122 row blocks, odd lda: one 320-wide tile column, A in row classes
+        workloads.make_operands(15616, 300, 1000, lda=1001, ldc=303, alpha=1.25, beta=0.5,
+                                c_dist="normal", seed=125),
     ]
+    assert mp.plan(15616, 300, 1000, 1.25, 1 << 20, 1001, 1 << 30, 300, 0.5, 1 << 34, 303)["tile_n"] == 320
     for ops in cases:
         via_run, via_noalloc = _both(mp, ops)
         _, S = reference(ops)
