@@ -412,7 +412,8 @@ __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMa
 // them has completed, before the last chunks are written. With beta != 0,
 // c_cur holds the first chunk's old C values (loaded while the MMAs still
 // ran), each later chunk's C loads go out before the previous chunk is
-// stored, and release() runs at the end.
+// stored, and release() runs once the last chunk's tensor-memory load has
+// completed, before that chunk is stored.
 template <class Release>
 __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMap* tmap_c, uint32_t t_row,
                                           float* c_tile, int64_t row_stride, int32_t rows, int32_t row0,
@@ -446,6 +447,7 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMa
             load_c_chunk(c_rows, row_stride, n0 + (c + 1) * 32 + lane, p.N, rows, c_next);
         ptx::tmem_load_wait();
         ptx::tmem_regs_ready(r);
+        if (c + 1 >= chunks) release();   // the part's last tensor-memory load has completed
 #pragma unroll
         for (int q = 0; q < 8; ++q)
             ptx::st_shared_v4(buf_s + chunk_off(lane, 4 * q), alpha * acc_value(r[4 * q], p.acc16),
@@ -465,7 +467,7 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMa
         for (int rr = 0; rr < 32; ++rr) c_cur[rr] = c_next[rr];
         __syncwarp();
     }
-    release();
+    if (chunks <= 0) release();
 }
 
 template <class Cfg>
