@@ -156,9 +156,11 @@ typedef enum {
                                      256 = a cluster of two CTAs per 256 x 256 tile
                                      (256 x 512 when TILE_N is 512). TILE_M 128 with
                                      TILE_N 512 makes runs return INVALID_VALUE */
-    MPGEMM_OPT_L2_KEEP = 8,       /* L2 hints for the operand loads: 0 = automatic (default,
-                                     both evict-last), 1 = keep A (B evict-first), 2 = keep B
-                                     (A evict-first) */
+    MPGEMM_OPT_L2_KEEP = 8,       /* L2 hints for the operand loads: 0 = automatic (default:
+                                     both evict-last, except an operand that only one tile
+                                     reads, i.e. A when N fits one tile column or B when M
+                                     fits one row block, which is evict-first),
+                                     1 = keep A (B evict-first), 2 = keep B (A evict-first) */
     MPGEMM_OPT_SPLIT_K = 9,       /* 0 = automatic (default): when the one-CTA output tiles
                                      occupy at most a quarter of the SMs and K has 32 or more
                                      64-wide blocks (half of the SMs and 16 blocks when

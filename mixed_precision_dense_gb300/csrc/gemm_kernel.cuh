@@ -547,7 +547,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ loads
         if (lane == 0) {
-            // Both operands are loaded evict-last (C's stores are evict-first):
+            // Both operands are loaded evict-last unless only one tile reads
+            // them (keep_a, chosen by the host; C's stores are evict-first):
             // every panel is re-read by the other tiles of its wave, and
             // marking either operand evict-first cost L2 reuse (DRAM reads at
             // 8192^3: 845 MB per launch, against 1224 MB with B evict-first).
