@@ -48,7 +48,7 @@ using Cfg320 = TileConfig<320, 3, false>;
 using CfgPair = TileConfig<256, 6, true, false, 2>;   // a CTA pair per 256 x 256 tile, two MMA issuers
                                                       // taking alternate k-blocks
 using CfgWide = TileConfig<512, 4, true>;   // a CTA pair per 256 x 512 tile
-// the same four shapes for a column-major B (a K-major B operand)
+// the same five shapes for a column-major B (a K-major B operand)
 using Cfg256K = TileConfig<256, 4, false, true>;
 using Cfg128K = TileConfig<128, 6, false, true>;
 using Cfg320K = TileConfig<320, 3, false, true>;

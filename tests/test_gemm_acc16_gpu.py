@@ -57,7 +57,7 @@ def test_acc16_pages_integer_sizes_exact(mp, size):
     assert np.array_equal(run(mp, ops, 16), ref)
 
 
-@pytest.mark.parametrize("tile_m,tile_n", [(128, 128), (128, 256), (256, 256), (256, 512)])
+@pytest.mark.parametrize("tile_m,tile_n", [(128, 128), (128, 256), (128, 320), (256, 256), (256, 512)])
 def test_acc16_overflows_past_65504(mp, tile_m, tile_n):
     M = N = 256
     K = 4096
