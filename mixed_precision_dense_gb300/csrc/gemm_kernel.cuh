@@ -801,12 +801,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const int32_t my_n = part_n / COL_SPLIT;                  // of which this warp stores
             const int32_t my_off = col_half * my_n;
             // beta * C needs C's old values: this warp's rows of the item's C
-            // are brought into L2 (one row per lane, 128-byte lines) and the
-            // first chunk's loads go out now, while the MMAs of this tile are
-            // still running.
-            // (the two warps of a lane quarter take half of the item's columns
-            // each, one bulk prefetch per row, widened to the 16-byte blocks
-            // that hold its first and last elements)
+            // are brought into L2 and the first chunk's loads go out now,
+            // while the MMAs of this tile are still running (one bulk
+            // prefetch per row and lane; the two warps of a lane quarter take
+            // half of the item's columns each, widened to the 16-byte blocks
+            // that hold the first and last elements)
             if (read_c && lane < rows) {
                 const int32_t cend = min(n0 + w.width, p.N);
                 const int32_t half = (cend - n0 + 1) / 2;
