@@ -115,3 +115,34 @@ def test_reference_arm_other_ranks_exit_quietly():
                           "--workload", "0", "--steps", "3", "--warmup", "3"],
                          capture_output=True, text=True, env=env, timeout=300, check=True).stdout
     assert out.strip() == ""
+
+
+@pytest.mark.parametrize("index", [3, 4])
+def test_traffic_records_match_the_planner(index):
+    """The committed ncu traffic records (profiles/) name the tile the planner
+    picks for their workload on 152 SMs, read at least the operands once, and
+    bench.py reports a record only for its own tile and kernel sources."""
+    import mixed_precision_dense_gb300 as mp
+    import workloads
+    path = bench.traffic_path(index)
+    with open(path) as f:
+        rec = json.load(f)
+    for key in ("kernel", "workload", "tile", "dram_bytes_read_per_launch", "dram_bytes_write_per_launch",
+                "dram_bytes_per_launch", "ncu_duration_ns", "source_hash", "command"):
+        assert key in rec, key
+    w = workloads.WORKLOADS[index]
+    assert rec["workload"] == w.name
+    assert "--clock-control none" in rec["command"]
+    assert rec["dram_bytes_per_launch"] == rec["dram_bytes_read_per_launch"] + rec["dram_bytes_write_per_launch"]
+    # the same fake, 256-byte aligned addresses record_traffic plans with
+    p = mp.plan(w.M, w.N, w.K, w.alpha, 256, w.lda, 256, w.ldb, w.beta, 256, w.ldc, num_sms=152)
+    tile = f"{p['tile_m']}x{p['tile_n']}"
+    assert rec["tile"] == tile
+    assert f"TileConfig<{p['tile_n']}, {p['stages']}, {int(p['tile_m'] == 256)}" in rec["kernel"]
+    operands_once = 2 * w.M * w.K + 2 * w.K * w.N
+    assert rec["dram_bytes_read_per_launch"] >= 0.95 * operands_once
+    if rec["source_hash"] == bench.source_hash():
+        assert bench.stored_traffic(index, tile) == rec["dram_bytes_per_launch"]
+    else:
+        assert bench.stored_traffic(index, tile) is None
+    assert bench.stored_traffic(index, "0x0") is None
