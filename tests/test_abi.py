@@ -217,3 +217,19 @@ def test_tile_selection_and_grid():
         _plan(tile_n=192)
     with pytest.raises(mp.MpgemmError):
         _plan(tile_m=64)
+
+
+@pytest.mark.parametrize("N,K,lda,expect65536,expect58368", [
+    (256, 4093, 4093, 256, 256),   # one 256-wide column covers N
+    (257, 4093, 4093, 320, 320),   # row classes: 4 waves x 1.6 < 7 and 3 x 1.6 < 6
+    (320, 4093, 4093, 320, 320),
+    (257, 4096, 4096, 256, 320),   # aligned: 4 x 1.9 > 7, 3 x 1.9 < 6
+    (320, 4096, 4096, 256, 320),
+    (321, 4093, 4093, 256, 256),   # past 320: two columns either way
+])
+def test_320_wide_rule_boundaries(N, K, lda, expect65536, expect58368):
+    for M, expect in ((65536, expect65536), (58368, expect58368)):
+        p = _plan(M=M, N=N, K=K, lda=lda, ldb=N + 8, ldc=N, beta=0.5)
+        assert p["tile_n"] == expect, (M, N, lda)
+        if expect == 320:
+            assert p["tile_m"] == 128 and p["split_tiles"] == 0 and p["stages"] == 3
