@@ -285,6 +285,13 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
             splits = opt.split_k;
         else if (beta == 1.0f ? (p.tiles * 2 <= units && k_blocks >= 16) : (p.tiles * 4 <= units && k_blocks >= 32))
             splits = std::min<int64_t>(k_blocks / 8, units / p.tiles);
+        else if (beta != 1.0f && p.tiles * 8 <= units && k_blocks >= 8)
+            // very few tiles of a short K: five slices of two or more k-blocks
+            // (measured with L2 flushed: 500 x 256 x 1024, 8 tiles, 12.3 ->
+            // 10.2 us; 300 x 200 x 640, 6 tiles, 10.7 -> 10.2 us; 200 x 136 x
+            // 617, 16 tiles, 12.5 -> 11.6 us; 40 tiles of 611 x 613 x 617
+            // slowed from 14.3 to 18-20 us, so not past an eighth of the SMs)
+            splits = std::min<int64_t>(5, k_blocks / 2);
         splits = std::max<int64_t>(1, std::min<int64_t>(splits, k_blocks));
         if (splits > 1) splits = ceil_div(k_blocks, ceil_div(k_blocks, splits));  // no empty slice
     }
