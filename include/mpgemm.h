@@ -164,7 +164,9 @@ typedef enum {
     MPGEMM_OPT_SPLIT_K = 9,       /* 0 = automatic (default): when the one-CTA output tiles
                                      occupy at most a quarter of the SMs and K has 32 or more
                                      64-wide blocks (half of the SMs and 16 blocks when
-                                     beta == 1), each tile's K range is cut into slices whose
+                                     beta == 1), or at most an eighth of the SMs and K has 8
+                                     or more blocks (beta != 1; up to five slices), each
+                                     tile's K range is cut into slices whose
                                      partial products are added into C (after C = beta*C), so
                                      results may differ in the last bits from run to run;
                                      1 = never; n in 2..64 = n slices (one-CTA tiles only) */

@@ -276,7 +276,8 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     // the atomic adds than they gain from the extra SMs. With beta == 1 the
     // slices add straight onto C and no pass over C is needed, so half of the
     // CTAs idle and 16 k-blocks already pay (1000 x 800 x 1200: 21 -> 17 us
-    // with two slices).
+    // with two slices). Very few tiles (an eighth of the SMs at most) pay
+    // from eight k-blocks on (below).
     int64_t splits = 1;
     // (FP16 accumulators never split K: the study variant keeps the whole K
     // range in one FP16 accumulator, as an __half accumulator type would)
