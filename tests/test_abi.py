@@ -237,3 +237,18 @@ def test_320_wide_rule_boundaries(N, K, lda, expect65536, expect58368):
         assert p["tile_n"] == expect, (M, N, lda)
         if expect == 320:
             assert p["tile_m"] == 128 and p["split_tiles"] == 0 and p["stages"] == 3
+
+
+@pytest.mark.parametrize("M,K,beta,splits", [
+    (19 * 128, 640, 0.0, 5),   # 19 tiles: an eighth of 152 SMs, 10 k-blocks: five slices
+    (20 * 128, 640, 0.0, 1),   # 20 tiles: past an eighth
+    (128, 7 * 64, 0.0, 1),     # 7 k-blocks: too short
+    (128, 8 * 64, 0.0, 4),     # 8 k-blocks: four slices of two
+    (19 * 128, 640, 1.0, 1),   # beta == 1 keeps its own rule (16 k-blocks at least)
+    (19 * 128, 640, 0.5, 5),   # any other beta: C = beta * C first, then the slices
+])
+def test_short_k_split_rule(M, K, beta, splits):
+    p = _plan(M=M, N=128, K=K, lda=K, ldb=128, ldc=128, beta=beta)
+    assert p["tile_n"] == 128 and p["k_splits"] == splits
+    per = -(-p["k_blocks"] // p["k_splits"])
+    assert (p["k_splits"] - 1) * per < p["k_blocks"] and p["items"] == p["tiles"] * p["k_splits"]
