@@ -561,6 +561,8 @@ SPLIT_REDUCE_CASES = [  # (M, N, K, lda, ldc, beta, splits): split-K slices adde
     (1000, 800, 1200, 1200, 804, 1.0, 2),     # beta = 1: slices add onto C as it is
     (300, 200, 1000, 1000, 200, -0.5, 3),     # C = beta * C first, then the slices
     (4096, 16, 4096, 4096, 16, 0.0, 0),       # the gate's skinny case (automatic split)
+    (1000, 128, 640, 640, 128, 0.5, 0),       # 8 tiles of 10 k-blocks: five automatic slices
+    (500, 256, 1024, 1024, 256, 0.0, 0),      # 8 tiles of 16 k-blocks: four automatic slices
 ]
 
 
