@@ -185,16 +185,17 @@ typedef enum {
                                      Capstone 4", "Common failures"). K is never split then: the
                                      whole K range accumulates in one FP16 accumulator. Not for
                                      production use. */
-    MPGEMM_OPT_REPRODUCIBLE = 12  /* 0 = default: a call may take a path whose FP32 summation
-                                     order can differ from run to run, so results may differ
-                                     in the last bits between identical calls (always within
-                                     the stated tolerance; exact inputs stay exact): split-K
-                                     (slices added into C in arrival order) and 256 x 256
-                                     CTA-pair tiles (two threads issue alternate k-blocks into
-                                     one accumulator, and the tensor pipe interleaves them as
-                                     they arrive); 1 = only paths with a fixed summation order:
-                                     256 x 512 pair tiles instead of 256 x 256 ones, and no
-                                     split-K, so identical calls give identical bits. */
+    MPGEMM_OPT_REPRODUCIBLE = 12  /* 0 = default: a call may split K (see SPLIT_K), and the
+                                     slices then add into C in the order they arrive, so
+                                     results may differ in the last bits between identical
+                                     calls (always within the stated tolerance; exact inputs
+                                     stay exact); 1 = never split K, so every element is summed
+                                     by one MMA thread in one fixed order and identical calls
+                                     give identical bits (every tile shape sums in a fixed
+                                     order: the two MMA threads of a 256 x 512 CTA-pair tile
+                                     own disjoint columns of the accumulator, and those of a
+                                     256 x 256 tile hand alternate k-blocks to each other
+                                     strictly in turn). */
 } mpgemm_option_t;
 
 /* Set an option. Unknown options or out-of-range values return

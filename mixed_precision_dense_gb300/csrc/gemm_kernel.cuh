@@ -28,12 +28,14 @@
 //               epilogue warps: for 256 x 512 tiles warp 1 issues the MMAs of
 //               the first half of the accumulator's columns and this warp
 //               those of the second; for 256 x 256 tiles the two take
-//               alternate k-blocks, each at the full width. The tensor pipe
-//               queues only about one MMA ahead of an issuing thread, and
-//               each barrier wait stalls that thread; with two issuers one
-//               keeps the pipe fed while the other waits (measured: full MMA
-//               rate with two issuers, about 60 % with one, for one barrier
-//               test per four MMAs).
+//               alternate k-blocks, each at the full width, in a fixed order
+//               (each thread issues its k-block only after the other thread
+//               has issued the previous one; see TileConfig::KSPLIT). The
+//               tensor pipe queues only about one MMA ahead of an issuing
+//               thread, and each barrier wait stalls that thread; with two
+//               issuers one keeps the pipe fed while the other waits
+//               (measured: full MMA rate with two issuers, about 60 % with
+//               one, for one barrier test per four MMAs).
 //
 // Two shapes of the same pipeline:
 //   single  one CTA per tile of 128 x BN (BN = 128 or 256), tcgen05.mma with
@@ -45,8 +47,9 @@
 //   pair    a cluster of two CTAs per tile of 256 x BN (BN = 256 or 512):
 //           each CTA loads its own 128 rows of A and its own half of the B
 //           columns of every accumulator part; the even CTA issues
-//           tcgen05.mma with cta_group::2 (M = 256; N = 128 per part for
-//           256 x 256 tiles, 256 per part for 256 x 512 tiles) over both
+//           tcgen05.mma with cta_group::2 (M = 256; N = 256, the full width
+//           of a 256 x 256 tile, or per 256-column part of a 256 x 512 tile)
+//           over both
 //           CTAs' shared memory, and each CTA's tensor memory receives its
 //           own 128 rows of the accumulator. Per SM the 256 x 256 tile moves
 //           a third less operand data per FLOP than the single 128 x 256
@@ -141,10 +144,19 @@ struct TileConfig {
     // threads issuing MMAs: one, or two. With two, a 512-wide tile gives
     // each issuer one part (a 256-column range) of the accumulator; a
     // 256-wide tile gives them alternate k-blocks instead (KSPLIT), each
-    // issuing the full width into the same accumulator: every stage is
-    // committed by the one issuer that used it, and the issuer of a tile's
-    // second k-block waits until the first one's MMAs (which start the
-    // accumulator) have completed
+    // issuing the full width (N = 256 instructions, twice as long as N = 128
+    // ones, so the pipe holds twice the work ahead of each thread) into the
+    // same accumulator. Their k-blocks are handed over in a strict order:
+    // after issuing a k-block's MMAs (and committing its stage) a thread
+    // executes tcgen05.fence::before_thread_sync and arrives on the stage's
+    // hand-over barrier; the other thread waits on it, executes
+    // tcgen05.fence::after_thread_sync and only then issues the next
+    // k-block. The PTX ISA's memory consistency model for tcgen05 makes two
+    // tcgen05.mma with the same accumulator, cta_group and shape a pipelined
+    // pair, executed in the order they were issued, and the fence pair
+    // around an arrive/wait carries that order from one thread to the other,
+    // so the accumulator receives k-block 0, 1, 2, ... one after the other
+    // without either thread waiting for MMAs to complete
     static constexpr int ISSUERS = ISSUERS_;
     static constexpr bool KSPLIT = ISSUERS == 2 && BN_ != 512;
     // one MMA instruction covers SUB_N columns: BN, except that a tile wider
@@ -175,8 +187,8 @@ struct TileConfig {
     // (allocations are powers of two: a 320-column accumulator takes 512)
     static constexpr int TMEM_COLS = ACC_BUFS * BN <= 256 ? 256 : 512;
     // full and empty per stage; accumulator full per buffer; accumulator
-    // empty per buffer and part; first k-block done per buffer (KSPLIT)
-    static constexpr int NUM_BARRIERS = 2 * STAGES + ACC_BUFS + ACC_BUFS * RELEASE_PARTS + ACC_BUFS;
+    // empty per buffer and part; k-block handed over per stage (KSPLIT)
+    static constexpr int NUM_BARRIERS = 3 * STAGES + ACC_BUFS + ACC_BUFS * RELEASE_PARTS;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = STAGES * A_BYTES;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
@@ -490,7 +502,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     constexpr int ACC_BUFS = Cfg::ACC_BUFS, SUBS = Cfg::SUBS, RELEASE_PARTS = Cfg::RELEASE_PARTS;
     auto acc_full_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto acc_empty_bar = [&](int b, int h) { return bar0 + 8u * (2 * STAGES + ACC_BUFS + b * RELEASE_PARTS + h); };
-    auto first_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + ACC_BUFS + ACC_BUFS * RELEASE_PARTS + b); };
+    // (KSPLIT) arrived on once the k-block held in stage s has been issued
+    auto handed_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + ACC_BUFS + ACC_BUFS * RELEASE_PARTS + s); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Cfg::OFF_MISC);
     volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + Cfg::OFF_MISC + 4);
 
@@ -507,9 +520,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full_bar(s), 1);
             ptx::mbar_init(empty_bar(s), Cfg::KSPLIT ? 1 : Cfg::ISSUERS);   // one commit per issuer using it
+            ptx::mbar_init(handed_bar(s), 1);
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
-            ptx::mbar_init(first_bar(b), 1);
             ptx::mbar_init(acc_full_bar(b), Cfg::ISSUERS);
             for (int h = 0; h < RELEASE_PARTS; ++h) ptx::mbar_init(acc_empty_bar(b, h), Cfg::EPI_WARPS * Cfg::CTAS);
         }
@@ -628,8 +641,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // one issuer). Every issuer waits for every stage and commits it, so
         // a stage is freed only when all issuers' MMAs on it have completed;
         // an issuer with no part in an item (a half-width item) still does.
-        // KSPLIT: issuer `me` takes the k-blocks whose running count (over
-        // all items of this CTA) has parity `me`, and commits only those.
+        // KSPLIT: issuer `me` takes the k-blocks whose running count g (over
+        // all items of this CTA) has parity `me`, and commits only those;
+        // k-block g is issued only after k-block g - 1 (the other thread's,
+        // held in the previous stage) has been issued and handed over.
         const int me = warp == 1 ? 0 : 1;
         if (lane == 0 && rank == 0) {
             int stage = 0;
@@ -661,8 +676,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     ptx::tc_fence_after_sync();
                 }
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                // (KSPLIT) whether the item's first k-block is known to be done
-                bool started = !Cfg::KSPLIT || (walked & 1) == me;
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     if constexpr (Cfg::KSPLIT) {
                         if (((walked + (kb - w.kb0)) & 1) != me) {   // the other issuer's k-block
@@ -672,22 +685,28 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             }
                             continue;
                         }
-                        if (!started) {
-                            // the other issuer's MMAs on the item's first k-block
-                            // start the accumulator; these add to it
-                            if (!waiter.wait(first_bar(buf), acc_phase)) {
-                                waiter.fail(kRoleMma, kb);
-                                ok = false;
-                                break;
-                            }
-                            ptx::tc_fence_after_sync();
-                            started = true;
-                        }
                     }
                     if (!waiter.wait(full_bar(stage), phase)) {
                         waiter.fail(kRoleMma, kb);
                         ok = false;
                         break;
+                    }
+                    if constexpr (Cfg::KSPLIT) {
+                        // wait until the other thread has issued k-block g - 1
+                        // (stage g - 1 of the ring, the phase it had then). The
+                        // barrier cannot move on by a second phase meanwhile:
+                        // that thread issues k-block g - 1 + STAGES only after
+                        // this one has issued g, ..., g - 2 + STAGES.
+                        const int64_t g = walked + (kb - w.kb0);
+                        if (g > 0) {
+                            const int ps = stage == 0 ? STAGES - 1 : stage - 1;
+                            const uint32_t pph = stage == 0 ? (phase ^ 1u) : phase;
+                            if (!waiter.wait(handed_bar(ps), pph)) {
+                                waiter.fail(kRoleMma, kb);
+                                ok = false;
+                                break;
+                            }
+                        }
                     }
                     ptx::tc_fence_after_sync();
                     if (kb == 0 && lead_cols > 0)
@@ -748,12 +767,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     else
                         ptx::mma_commit(empty_bar(stage));
                     if constexpr (Cfg::KSPLIT) {
-                        if (kb == w.kb0) {   // the accumulator is started once these complete
-                            if constexpr (PAIR)
-                                ptx::mma_commit_pair_multicast(first_bar(buf), 0x1);
-                            else
-                                ptx::mma_commit(first_bar(buf));
-                        }
+                        // hand k-block g over: order this thread's MMAs so far
+                        // before the arrive that the other thread waits on
+                        ptx::tc_fence_before_sync();
+                        ptx::mbar_arrive(handed_bar(stage));
                     }
                     if (++stage == STAGES) {
                         stage = 0;

@@ -46,7 +46,7 @@ using Cfg128 = TileConfig<128, 6, false>;   // one CTA per 128 x 128 tile
 // stages, so three of them, and one accumulator buffer
 using Cfg320 = TileConfig<320, 3, false>;
 using CfgPair = TileConfig<256, 6, true, false, 2>;   // a CTA pair per 256 x 256 tile, two MMA issuers
-                                                      // taking alternate k-blocks
+                                                      // taking alternate k-blocks in a fixed order
 using CfgWide = TileConfig<512, 4, true>;   // a CTA pair per 256 x 512 tile
 // the same five shapes for a column-major B (a K-major B operand)
 using Cfg256K = TileConfig<256, 4, false, true>;
@@ -231,10 +231,7 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
         if (opt.pair_units > 0) pair_units = std::min<int64_t>(pair_units, opt.pair_units);
         if (opt.max_ctas > 0) pair_units = std::min<int64_t>(pair_units, std::max<int64_t>(1, opt.max_ctas / 2));
         pair_units = std::max<int64_t>(1, pair_units);
-        // (256 x 256 pair tiles add alternate k-blocks from two threads, in
-        // an order that can vary: not with `reproducible`)
-        const bool wide = opt.tile_n == 512 || opt.reproducible ||
-                          (!opt.tile_m && !opt.tile_n && auto_wide(M, N, K, pair_units));
+        const bool wide = opt.tile_n == 512 || (!opt.tile_m && !opt.tile_n && auto_wide(M, N, K, pair_units));
         p.tile_m = 256;
         p.tile_n = wide ? 512 : 256;
         p.stages = wide ? CfgWide::STAGES : CfgPair::STAGES;

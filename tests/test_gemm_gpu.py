@@ -588,28 +588,64 @@ def test_split_k_tma_reduce_matches_atomics(mp, M, N, K, lda, ldc, beta, splits)
     assert np.array_equal(outs[0], outs[1])
 
 
-def test_reproducible_option_repeats_bits(mp):
-    # 256 x 256 CTA-pair tiles (automatic below K = 2048) add two threads'
-    # k-blocks in an order that can vary; REPRODUCIBLE = 1 takes 256 x 512
-    # tiles and no split-K, and identical calls give identical bits
+def test_cta_pair_256_repeats_bits_and_reproducible_option(mp):
+    # The two MMA threads of a 256 x 256 CTA-pair tile take alternate
+    # k-blocks and hand each one over before the other thread issues the
+    # next, so the accumulator receives the k-blocks in one fixed order:
+    # identical calls give identical bits. REPRODUCIBLE = 1 additionally
+    # rules out split-K (whose slices add into C in arrival order).
     from parity import device_operands
-    ops = workloads.make_operands(2560, 2048, 700, dist="normal", seed=98)
-    plan = mp.plan(ops.M, ops.N, ops.K, 1.0, 256, ops.lda, 256, ops.ldb, 0.0, 256, ops.ldc)
-    assert (plan["tile_m"], plan["tile_n"]) == (256, 256)
     s = torch.cuda.current_stream()
-    with mp.Handle() as h:
-        h.set_option(mp.Option.REPRODUCIBLE, 1)
-        check_full(h, ops)
+
+    def repeat(h, ops, n=3):
         outs = []
-        for _ in range(3):
+        for _ in range(n):
             d = device_operands(ops)
             h.run(ops.M, ops.N, ops.K, ops.alpha, d["a_ptr"], ops.lda, d["b_ptr"], ops.ldb, ops.beta,
                   d["c_ptr"], ops.ldc, s.cuda_stream)
             s.synchronize()
             outs.append(d["c_buf"].cpu().numpy().view(np.uint32))
-        assert all(np.array_equal(outs[0], o) for o in outs[1:])
-        h.set_option(mp.Option.REPRODUCIBLE, 0)   # the default path: within the tolerance
+        return all(np.array_equal(outs[0], o) for o in outs[1:])
+
+    ops = workloads.make_operands(2560, 2048, 700, dist="normal", seed=98)
+    plan = mp.plan(ops.M, ops.N, ops.K, 1.0, 256, ops.lda, 256, ops.ldb, 0.0, 256, ops.ldc)
+    assert (plan["tile_m"], plan["tile_n"]) == (256, 256)
+    with mp.Handle() as h:
         check_full(h, ops)
+        assert repeat(h, ops)
+    ops = workloads.make_operands(4096, 16, 4096, dist="normal", seed=99)
+    assert mp.plan(ops.M, ops.N, ops.K, 1.0, 256, ops.lda, 256, ops.ldb, 0.0, 256, ops.ldc)["k_splits"] > 1
+    with mp.Handle() as h:
+        h.set_option(mp.Option.REPRODUCIBLE, 1)
+        check_full(h, ops)
+        assert repeat(h, ops)
+
+
+def test_cta_pair_256_long_k_integer_stress(mp):
+    # The planner's own 256 x 256 CTA-pair choice at a long K, called 30
+    # times back to back on exact small-integer inputs ("Day 72: Tensor cores
+    # with WMMA", "Why this program calls cuBLAS twice": every partial sum is
+    # an integer below 2^24, so any lost or doubled MMA shows as a mismatch):
+    # every call's C must equal the oracle's bit for bit.
+    from parity import device_operands, reference
+    M, N, K = 2560, 2048, 4096
+    ops = workloads.make_operands(M, N, K, dist="int3", dist_b="int2", seed=4242)
+    plan = mp.plan(M, N, K, 1.0, 256, K, 256, N, 0.0, 256, N)
+    assert (plan["tile_m"], plan["tile_n"]) == (256, 256)
+    ref, _ = reference(ops)
+    d = device_operands(ops)
+    s = torch.cuda.current_stream()
+    outs = []
+    with mp.Handle() as h:
+        for _ in range(30):
+            c = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+            h.run(M, N, K, 1.0, d["a_ptr"], K, d["b_ptr"], N, 0.0, c.data_ptr(), N, s.cuda_stream)
+            outs.append(c)
+        s.synchronize()
+        assert h.sync_status(s.cuda_stream)[0] == mp.Status.OK
+    for i, c in enumerate(outs):
+        got = c.cpu().double().numpy()
+        assert np.array_equal(got, ref), f"call {i}: {int((got != ref).sum())} elements differ"
 
 
 def test_tma_store_falls_back_for_unaligned_c(mp):
