@@ -13,13 +13,27 @@ independent replicas (a GEMM of this size needs no collective), so
 `value` = all ranks' FLOPs / the slowest rank's time ("weak" scaling).
 
 Extra keys:
-  roofline      the tensor-core kernel's achieved TFLOP/s (2MNK per launch over
-                its average event-timed duration) against the measured bf16
-                dense peak (the fp16 kind::f16 rate is the same);
+  roofline      the tensor-core kernel against the roof that binds it: the
+                tensor peak (2MNK per launch over its event-timed duration,
+                against the measured bf16 dense peak; the fp16 kind::f16 rate
+                is the same) when the workload's arithmetic intensity is above
+                the ridge point, else HBM (algorithmic bytes per launch over
+                the same duration, against the measured copy bandwidth);
+                roofline_alt holds the other roof;
+  peak_theoretical  SMs x FLOP per cycle per SM x maximum SM clock, the
+                per-SM factor measured on the device by the library's MMA-rate
+                probe (mpgemm_probe_mma_rate);
+  protocol      the median of 5 runs x 20 back-to-back launches and the
+                coefficient of variation of the 5 runs;
+  steady_state  alternating segments of about a second of back-to-back calls
+                of ours and of cuBLAS, clocks sampled every 50 ms: TFLOP/s, SM
+                clock, cycles per call (time x median SM clock) and power;
   e2e           the same metric through mpgemm_run_host with pinned HOST
                 buffers: every step copies A and B in and C out;
   cpu_baseline  the CPU oracle timed on a bounded sample of the same workload;
-  clocks        nvidia-smi samples taken during the timed region.
+  clocks        nvidia-smi samples taken during the timed region (or, when the
+                timed region is shorter than the sampling interval, during the
+                steady-state segments of ours, as the window key says).
 
 --impl reference times the CPU oracle (the project's correctness reference)
 on the same workload, metric and unit, one bounded sample per step.
@@ -56,6 +70,55 @@ def gemm_bytes(M: int, N: int, K: int, beta: float, a_bytes=2, b_bytes=2, c_byte
     """Algorithmic HBM bytes: A and B read once, C written once (and read once if beta != 0)."""
     c_traffic = M * N * c_bytes * (2 if beta != 0 else 1)
     return M * K * a_bytes + K * N * b_bytes + c_traffic
+
+
+def roofline_pair(M: int, N: int, K: int, beta: float, kernel_ms: float, peaks: dict, traffic=None,
+                  theoretical=None):
+    """(binding roof, the other roof) of one tensor-core launch taking
+    kernel_ms. The workload is HBM-bound when its arithmetic intensity
+    (2MNK over the algorithmic bytes) is below the ridge point of the
+    measured peaks (tensor FLOP/s over HBM bytes/s), tensor-bound otherwise
+    ("02_mixed_precision_gemm" README, "Experimental Setup": the roofline
+    against the dense tensor peak and the memory bandwidth)."""
+    flops = gemm_flops(M, N, K)
+    nbytes = gemm_bytes(M, N, K, beta)
+    secs = kernel_ms / 1e3
+    tensor_achieved = flops / secs / 1e12
+    hbm_achieved = nbytes / secs / 1e9
+    tensor = {"bound": "tensor", "achieved": round(tensor_achieved, 1), "peak": peaks["tflops"],
+              "unit": "TFLOP/s", "frac": round(tensor_achieved / peaks["tflops"], 4), "traffic": traffic,
+              "peak_kind": f"bf16 dense burst, {peaks['source']}",
+              "frac_of_sustained": (round(tensor_achieved / peaks["tflops_sustained"], 4)
+                                    if peaks.get("tflops_sustained") else None),
+              "kernel": "gemm_tc_kernel", "algorithmic_flops": flops, "algorithmic_bytes": nbytes}
+    if theoretical and theoretical.get("tflops"):
+        tensor["peak_theoretical"] = theoretical["tflops"]
+        tensor["frac_of_theoretical"] = round(tensor_achieved / theoretical["tflops"], 4)
+    hbm = {"bound": "hbm", "achieved": round(hbm_achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+           "frac": round(hbm_achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+           "peak_kind": f"HBM copy bandwidth, {peaks['source']}",
+           "kernel": "gemm_tc_kernel", "algorithmic_bytes": nbytes}
+    ridge = peaks["tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if flops / nbytes < ridge:
+        return hbm, tensor
+    return tensor, hbm
+
+
+def check_world(gpus: int, world: int):
+    """--gpus N must match the ranks actually launched: N > 1 runs as N
+    torchrun ranks (one replica per GPU), N == 1 as one process. A mismatch
+    is an error, so the line never claims GPUs it did not use."""
+    if gpus < 1:
+        raise SystemExit(f"bench.py: --gpus {gpus} is not a GPU count")
+    if gpus != world:
+        raise SystemExit(f"bench.py: --gpus {gpus} but {world} rank(s) were launched; for N > 1 run "
+                         f"python -m torch.distributed.run --nproc-per-node {gpus} bench.py --gpus {gpus}")
+
+
+def workload_config(w, world: int) -> dict:
+    """The workload as both arms report it (the same keys and values)."""
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "lda": w.lda, "ldb": w.ldb, "ldc": w.ldc,
+            "alpha": w.alpha, "beta": w.beta, "inputs": w.dist, "parallelism": f"replicas x{world}"}
 
 
 def source_hash() -> str:
@@ -163,51 +226,73 @@ def barrier():
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi clock and throttle-reason samples every 200 ms."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock, power and throttle-reason samples with timestamps,
+    every `interval_ms`; summarize() keeps the samples inside a host-time
+    window."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, interval_ms: int = 50):
         self.index = index
+        self.interval_ms = interval_ms
         self.proc = None
+        self.samples = []
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        return self
 
-    def stop(self) -> dict:
+    def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return []
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, reasons, power = [], [], set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1])); smax.append(float(parts[2]))
-                power.append(float(parts[3]))
-            except ValueError:
-                continue
-            for name, flag in zip(names, parts[5:9]):
-                if flag.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        self.samples = parse_clock_samples(out)
+        return self.samples
+
+    @staticmethod
+    def summarize(samples, t0=None, t1=None) -> dict:
+        inside = [x for x in samples if (t0 is None or x["t"] >= t0) and (t1 is None or x["t"] <= t1)]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "power_w": None, "power_w_max": None,
+                    "samples": 0, "reasons": []}
+        reasons = sorted({r for x in inside for r in x["reasons"]})
+        return {"sm_mhz": statistics.median(x["sm"] for x in inside),
+                "sm_max_mhz": max(x["smax"] for x in inside),
+                "power_w": round(statistics.median(x["power"] for x in inside), 1),
+                "power_w_max": max(x["power"] for x in inside),
+                "samples": len(inside), "reasons": reasons}
+
+
+def parse_clock_samples(text: str):
+    """Rows of the ClockSampler query -> [{t, sm, smax, power, reasons}] (t in
+    host epoch seconds; rows that do not parse are skipped)."""
+    import datetime
+    out = []
+    for line in text.splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            sm, smax, power = float(parts[2]), float(parts[3]), float(parts[4])
+        except ValueError:
+            continue
+        reasons = [n for n, flag in zip(ClockSampler.REASONS, parts[6:10]) if flag.lower().startswith("active")]
+        out.append({"t": t, "sm": sm, "smax": smax, "power": power, "reasons": reasons})
+    return out
 
 
 # ----------------------------------------------------------------------------- CPU oracle timing
@@ -268,20 +353,24 @@ def _cublas_lib():
     return None
 
 
-def time_cublas_context(w, A, B, C, stream, steps, flush=None):
+class CublasContext:
     """cublasGemmEx(FP16 A and B, FP32 C, CUBLAS_COMPUTE_32F, default algorithm)
-    on the same buffers, timed like our step. Row-major C = A*B is issued as
-    the column-major product C^T = B^T * A^T, so no copies are needed. This is
-    context measured by the harness only; the library does not use cuBLAS."""
-    import ctypes
-    import torch
-    lib = _cublas_lib()
-    if lib is None:
-        return None
-    h = ctypes.c_void_p()
-    if lib.cublasCreate_v2(ctypes.byref(h)) != 0:
-        return None
-    try:
+    on the same buffers as our step. Row-major C = A*B is issued as the
+    column-major product C^T = B^T * A^T, so no copies are needed. This is
+    context measured by the harness only; the library does not use cuBLAS.
+    `call` is None when cuBLAS cannot be loaded or refuses the problem."""
+    CALL = ("cublasGemmEx(CUDA_R_16F, CUDA_R_16F, CUDA_R_32F, CUBLAS_COMPUTE_32F, "
+            "CUBLAS_GEMM_DEFAULT), harness only")
+
+    def __init__(self, w, A, B, C, stream):
+        import ctypes
+        self.call = None
+        self._lib = _cublas_lib()
+        self._h = ctypes.c_void_p()
+        if self._lib is None or self._lib.cublasCreate_v2(ctypes.byref(self._h)) != 0:
+            self._lib = None
+            return
+        lib, h = self._lib, self._h
         lib.cublasSetStream_v2(h, ctypes.c_void_p(stream.cuda_stream))
         alpha = ctypes.c_float(w.alpha)
         beta = ctypes.c_float(w.beta)
@@ -296,14 +385,14 @@ def time_cublas_context(w, A, B, C, stream, steps, flush=None):
 
         for _ in range(3):
             if call() != 0:
-                return None
-        ms = timed_loop(call, stream, steps, flush)
-        return {"value": round(gemm_flops(w.M, w.N, w.K) / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
-                "ms_per_step": round(ms, 5),
-                "call": "cublasGemmEx(CUDA_R_16F, CUDA_R_16F, CUDA_R_32F, CUBLAS_COMPUTE_32F, "
-                        "CUBLAS_GEMM_DEFAULT), harness only"}
-    finally:
-        lib.cublasDestroy_v2(h)
+                return
+        self.call = call
+
+    def close(self):
+        if self._lib is not None:
+            self._lib.cublasDestroy_v2(self._h)
+            self._lib = None
+            self.call = None
 
 
 def timed_loop(fn, stream, steps, flush=None):
@@ -330,6 +419,104 @@ def timed_loop(fn, stream, steps, flush=None):
             ends[i].record(stream)
     ends[-1].synchronize()
     return sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
+
+
+def protocol_runs(fn, stream, flops, flush=None, runs=5, calls=20):
+    """The measurement protocol of the "02_mixed_precision_gemm" README
+    ("Results", "Reproducing"): the median of `runs` runs of `calls`
+    back-to-back launches, with each run's TFLOP/s and the coefficient of
+    variation of the runs."""
+    ms = [timed_loop(fn, stream, calls, flush) for _ in range(runs)]
+    tf = [flops / (m / 1e3) / 1e12 for m in ms]
+    return {"runs": runs, "calls_per_run": calls, "tflops_median": round(statistics.median(tf), 2),
+            "tflops_runs": [round(x, 1) for x in tf], "ms_median": round(statistics.median(ms), 5),
+            "cv": round(statistics.pstdev(ms) / statistics.mean(ms), 5)}
+
+
+def steady_state(arms: dict, stream, ms_guess: float, flops: float, device_index: int,
+                 seconds: float = 1.0, rounds: int = 2):
+    """Alternating segments of about `seconds` of back-to-back calls per arm
+    (name -> callable), `rounds` times, with clocks, power and throttle
+    reasons sampled every 50 ms. Long enough for the power cap to act (the
+    driver's short burst is not). Per arm: TFLOP/s and ms per call (median of
+    its segments), the median SM clock inside its segments and the cycles per
+    call that time x clock gives, the median power and any throttle reason."""
+    import torch
+    sampler = ClockSampler(device_index, interval_ms=50).start()
+    time.sleep(0.3)
+    segs = []
+    for _ in range(rounds):
+        for name, fn in arms.items():
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            n = max(20, int(seconds * 1e3 / max(ms_guess, 1e-3)))
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            t0 = time.time()
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+            e1.synchronize()
+            t1 = time.time()
+            segs.append((name, t0, t1, e0.elapsed_time(e1) / n, n))
+    time.sleep(0.1)
+    samples = sampler.stop()
+    out = {"seconds_per_segment": seconds, "segments_per_arm": rounds, "clock_interval_ms": 50}
+    for name in arms:
+        mine = [x for x in segs if x[0] == name]
+        ms = statistics.median(x[3] for x in mine)
+        # skip the first 50 ms of a segment: the clock takes a moment to settle
+        inside = [x for seg in mine for x in samples if seg[1] + 0.05 <= x["t"] <= seg[2]]
+        clk = ClockSampler.summarize(inside)
+        mhz = clk["sm_mhz"]
+        out[name] = {"tflops": round(flops / (ms / 1e3) / 1e12, 1), "ms_per_call": round(ms, 5),
+                     "calls_per_segment": mine[0][4], "sm_mhz": mhz,
+                     "cycles_per_call": round(ms * 1e-3 * mhz * 1e6) if mhz else None,
+                     "power_w": clk["power_w"], "clock_samples": clk["samples"], "reasons": clk["reasons"]}
+    if "ours" in out and "cublas" in out:
+        out["ours_over_cublas"] = round(out["ours"]["tflops"] / out["cublas"]["tflops"], 4)
+        if out["ours"]["cycles_per_call"] and out["cublas"]["cycles_per_call"]:
+            out["cycles_cublas_over_ours"] = round(out["cublas"]["cycles_per_call"] / out["ours"]["cycles_per_call"], 4)
+    out["_samples"] = samples
+    out["_segments"] = segs
+    return out
+
+
+def theoretical_peak(device, max_mhz=None):
+    """SMs x FLOP per cycle per SM x maximum SM clock, the per-SM factor
+    measured by the library's MMA-rate probe (one CTA per SM issuing 16384
+    back-to-back 128 x 256 x 16 MMAs) and the maximum clock as nvidia-smi
+    reports it (else MEASURED_PEAKS.json's)."""
+    import torch
+
+    import mixed_precision_dense_gb300 as mp
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    mmas = 1 << 14
+    out = torch.zeros(2 * sms, dtype=torch.int64, device=device)
+    stream = torch.cuda.current_stream(device)
+    mp.probe_mma_rate(sms, mmas, out.data_ptr(), stream.cuda_stream)
+    stream.synchronize()
+    res = out.cpu().tolist()
+    cycles = [res[2 * i] for i in range(sms) if res[2 * i + 1] == 1]
+    if not cycles:
+        return None
+    per_sm = statistics.median(mp.PROBE_FLOP_PER_MMA * mmas / c for c in cycles)
+    if max_mhz is None:
+        try:
+            q = subprocess.run(["nvidia-smi", f"--id={device.index or 0}", "--query-gpu=clocks.max.sm",
+                                "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20)
+            max_mhz = float(q.stdout.strip().splitlines()[0])
+        except (OSError, ValueError, IndexError, subprocess.TimeoutExpired):
+            path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+            max_mhz = json.load(open(path)).get("sm_max_mhz") if os.path.exists(path) else None
+    if not max_mhz:
+        return None
+    return {"tflops": round(sms * per_sm * max_mhz * 1e6 / 1e12, 1), "sms": sms,
+            "flop_per_clk_per_sm": round(per_sm, 1), "sm_max_mhz": max_mhz,
+            "how": "mpgemm_probe_mma_rate: one CTA per SM, 16384 back-to-back kind::f16 "
+                   "128 x 256 x 16 MMAs, %clock64 cycles; x SMs x max SM clock"}
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -395,21 +582,22 @@ def run_ours(args):
 
     small = gemm_bytes(w.M, w.N, w.K, w.beta) < L2_BYTES
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=device) if small else None
-    sampler = ClockSampler(local)
-    sampler.start()
+    sampler = ClockSampler(local, interval_ms=20).start()
     time.sleep(0.3)
     barrier()
     torch.cuda.synchronize(device)
+    t_begin = time.time()
     local_ms = timed_loop(step, stream, args.steps, flush)
     torch.cuda.synchronize(device)
+    t_end = time.time()
     barrier()
-    clocks = sampler.stop()
+    timed_clocks = ClockSampler.summarize(sampler.stop(), t_begin, t_end)
     st, info = handle.sync_status(stream.cuda_stream)
     if st != mp.Status.OK:
         raise RuntimeError(f"device reported {st.name} {info}")
     local_s = local_ms * args.steps / 1e3
-    flops_local = gemm_flops(w.M, w.N, w.K) * args.steps
-    max_s, flops_all = aggregate(local_s, flops_local, device=device)
+    flops = gemm_flops(w.M, w.N, w.K)
+    max_s, flops_all = aggregate(local_s, flops * args.steps, device=device)
     value = flops_all / max_s / 1e12
     ms_per_step = max_s * 1e3 / args.steps
 
@@ -421,20 +609,42 @@ def run_ours(args):
     if plan["stage_a"] or plan["stage_b"]:
         kernel_ms = time_tc_kernel_only(w, A, B, C, stream, args.steps, plan, flush, args.split_k)
     peaks = measured_peaks()
-    achieved = gemm_flops(w.M, w.N, w.K) / (kernel_ms / 1e3) / 1e12
-    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["tflops"], 4),
-                "traffic": None if args.shape else stored_traffic(args.workload, f"{plan['tile_m']}x{plan['tile_n']}"),
-                "peak_kind": f"bf16 dense burst, {peaks['source']}",
-                "frac_of_sustained": (round(achieved / peaks["tflops_sustained"], 4)
-                                      if peaks["tflops_sustained"] else None),
-                "kernel": "gemm_tc_kernel", "algorithmic_bytes": gemm_bytes(w.M, w.N, w.K, w.beta)}
+    theory = None if args.no_probe else theoretical_peak(device)
+    traffic = None if args.shape else stored_traffic(args.workload, f"{plan['tile_m']}x{plan['tile_n']}")
+    roofline, roofline_alt = roofline_pair(w.M, w.N, w.K, w.beta, kernel_ms, peaks, traffic, theory)
 
-    cublas = None
-    if not args.no_cublas:
-        cublas = time_cublas_context(w, A, B, C, stream, min(args.steps, 200), flush)
-        if cublas and cublas["value"] > 0:
-            cublas["ours_over_cublas"] = round(value / world / cublas["value"], 4)
+    protocol = protocol_runs(step, stream, flops, flush)
+    cublas, steady = None, None
+    cub = None if args.no_cublas else CublasContext(w, A, B, C, stream)
+    if cub is not None and cub.call is not None:
+        cub_ms = timed_loop(cub.call, stream, args.steps, flush)
+        cublas = {"value": round(flops / (cub_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                  "ms_per_step": round(cub_ms, 5), "call": CublasContext.CALL,
+                  "ours_over_cublas": round(value / world / (flops / (cub_ms / 1e3) / 1e12), 4),
+                  "protocol": protocol_runs(cub.call, stream, flops, flush)}
+    if args.steady_seconds > 0:
+        arms = {"ours": step}
+        if cub is not None and cub.call is not None:
+            arms["cublas"] = cub.call
+        steady = steady_state(arms, stream, local_ms, flops, local, seconds=args.steady_seconds)
+        steady["l2"] = "back to back on the same operands, no L2 flush"
+    if cub is not None:
+        cub.close()
+    if timed_clocks["samples"] > 0 and (steady is None or t_end - t_begin >= 0.5):
+        clocks = dict(timed_clocks, window="the timed region")
+    elif steady is not None:
+        segs = [x for x in steady["_segments"] if x[0] == "ours"]
+        inside = [x for seg in segs for x in steady["_samples"] if seg[1] + 0.05 <= x["t"] <= seg[2]]
+        clocks = dict(ClockSampler.summarize(inside),
+                      window=(f"the steady-state segments of ours (the timed region, {args.steps} calls in "
+                              f"{local_s * 1e3:.1f} ms, is too short for nvidia-smi's samples, which lag "
+                              "by tens of ms)"),
+                      timed_region=timed_clocks)
+    else:
+        clocks = dict(timed_clocks, window="the timed region")
+    if steady is not None:
+        steady.pop("_samples")
+        steady.pop("_segments")
 
     # end to end through the host-buffer entry point
     e2e = None
@@ -454,16 +664,19 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16 inputs, f32 accumulate", "data": "synthetic (seeded)",
-            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "lda": w.lda,
-                       "ldb": w.ldb, "ldc": w.ldc, "alpha": w.alpha, "beta": w.beta,
-                       "inputs": w.dist, "tile": f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}",
-                       "grid": plan["grid"], "parallelism": f"replicas x{world}",
-                       "l2": (f"L2 flushed between steps (a {2 * L2_BYTES // 2**20} MiB write before each "
-                              "step, outside the timed calls)" if small else
-                              f"inputs larger than L2 ({gemm_bytes(w.M, w.N, w.K, w.beta) / 2**20:.0f} MiB "
-                              f"> {L2_BYTES // 2**20} MiB): no flush")},
+            "config": workload_config(w, world),
+            "l2": (f"L2 flushed between steps (a {2 * L2_BYTES // 2**20} MiB write before each "
+                   "step, outside the timed calls)" if small else
+                   f"inputs larger than L2 ({gemm_bytes(w.M, w.N, w.K, w.beta) / 2**20:.0f} MiB "
+                   f"> {L2_BYTES // 2**20} MiB): no flush"),
+            "launch": {"tile": f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}", "grid": plan["grid"],
+                       "k_splits": plan["k_splits"], "a_row_classes": plan["a_classes"],
+                       "staged": {"A": plan["stage_a"], "B": plan["stage_b"]}},
             "pct_of_peak": round(100 * value / world / peaks["tflops"], 2),
-            "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
+            "pct_of_theoretical_peak": round(100 * value / world / theory["tflops"], 2) if theory else None,
+            "peak_theoretical": theory,
+            "roofline": roofline, "roofline_alt": roofline_alt, "protocol": protocol,
+            "steady_state": steady, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
             "context_cublas": cublas,
             "gpu_launches": launches_per_step * args.steps, "check_max_err_over_tol": check,
         }
@@ -780,7 +993,7 @@ def run_reference(args):
         "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle: FP16 decoded, double sums)",
         "data": "synthetic (seeded)",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "parallelism": "host cores"},
+        "config": workload_config(w, world),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -800,6 +1013,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--steady-seconds", type=float, default=1.0,
+                    help="length of each steady-state segment (two per arm); 0 = none")
+    ap.add_argument("--no-probe", action="store_true", help="skip the MMA-rate probe (theoretical peak)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-check", action="store_true")
@@ -820,6 +1036,8 @@ def main(argv=None):
                     help="run the capstone gate's eight cases and print a report instead")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least three warm-up steps, whatever was asked
+    if not (args.record_traffic or args.acc16_study or args.gate):
+        check_world(args.gpus, dist_env()[0])
     if args.record_traffic:
         record_traffic(args)
     elif args.acc16_study:

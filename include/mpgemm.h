@@ -270,6 +270,23 @@ mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K,
                                    const void* B, int64_t ldb,
                                    float beta, float* C, int64_t ldc, void* stream);
 
+/* Measurement utility behind the theoretical tensor peak. The roofline of
+ * "02_mixed_precision_gemm" README ("Experimental Setup") takes the dense
+ * tensor peak as MACs per SM per clock x SMs x 2 x clock; this pins the per-SM
+ * factor on the current device. `ctas` CTAs (use the SM count: each CTA
+ * takes more than half an SM's shared memory, so one runs per SM) each issue
+ * `mmas` back-to-back kind::f16 MMAs of M = 128, N = 256, K = 16 (FP16 x FP16
+ * -> FP32, 1,048,576 FLOP each) from one thread, with no loads, and time them
+ * with the SM cycle counter. `out` is a device array of 2 * ctas uint64_t:
+ * out[2c] = cycles from the first issue to the last completion in CTA c,
+ * out[2c + 1] = 1, or 0 if that CTA's bounded wait for the completion gave
+ * up. FLOP per cycle per SM = 1048576 * mmas / out[2c]. Asynchronous on
+ * `stream`; synchronise before reading `out`. Needs no handle and allocates
+ * nothing. ctas in 1..65535, mmas in 4..4194304, `out` 8-byte aligned, else
+ * MPGEMM_ERR_INVALID_VALUE; MPGEMM_ERR_UNSUPPORTED_DEVICE unless the
+ * current device is compute capability 10.3. */
+mpgemm_status_t mpgemm_probe_mma_rate(int32_t ctas, int32_t mmas, uint64_t* out, void* stream);
+
 /* A static description of a status code. Never NULL. */
 const char* mpgemm_status_string(mpgemm_status_t s);
 

@@ -6,10 +6,10 @@ The computation lives in the CUDA library ``libmpgemm.so`` (C ABI in
 ctypes (``binding``). PyTorch is only used for device memory and streams.
 """
 from .binding import (BLayout, Handle, MpgemmError, Option, Plan, Status, default_handle, gemm,
-                      header_functions, load, plan, run_noalloc, solve, status_string,
-                      NOALLOC_SCRATCH_BYTES)
+                      header_functions, load, plan, probe_mma_rate, run_noalloc, solve,
+                      status_string, NOALLOC_SCRATCH_BYTES, PROBE_FLOP_PER_MMA)
 from .build import LIB_PATH, build
 
 __all__ = ["BLayout", "Handle", "MpgemmError", "Option", "Plan", "Status", "default_handle", "gemm",
-           "header_functions", "load", "plan", "run_noalloc", "solve", "status_string",
-           "NOALLOC_SCRATCH_BYTES", "LIB_PATH", "build"]
+           "header_functions", "load", "plan", "probe_mma_rate", "run_noalloc", "solve", "status_string",
+           "NOALLOC_SCRATCH_BYTES", "PROBE_FLOP_PER_MMA", "LIB_PATH", "build"]

@@ -99,11 +99,12 @@ def load(path: str = LIB_PATH):
         lib.mpgemm_set_option.argtypes = [p, ctypes.c_int, i64]
         lib.mpgemm_plan.argtypes = [i64, i64, i64, f32, p, i64, p, i64, f32, p, i64,
                                     i32, i32, i32, i32, i32, i32, ctypes.POINTER(Plan)]
+        lib.mpgemm_probe_mma_rate.argtypes = [i32, i32, p, p]
         lib.mpgemm_status_string.restype = ctypes.c_char_p
         lib.mpgemm_status_string.argtypes = [ctypes.c_int]
         for name in ("mpgemm_create", "mpgemm_destroy", "mpgemm_run", "mpgemm_run_ex", "mpgemm_solve",
                      "mpgemm_run_host", "mpgemm_run_noalloc",
-                     "mpgemm_sync_status", "mpgemm_set_option", "mpgemm_plan"):
+                     "mpgemm_sync_status", "mpgemm_set_option", "mpgemm_plan", "mpgemm_probe_mma_rate"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -143,6 +144,14 @@ def run_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> Statu
 
 
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+
+PROBE_FLOP_PER_MMA = 2 * 128 * 256 * 16
+
+
+def probe_mma_rate(ctas, mmas, out, stream=0):
+    """mpgemm_probe_mma_rate: `out` is the device address (int) of 2 * ctas
+    uint64 values; see the header for their meaning."""
+    _check(load().mpgemm_probe_mma_rate(ctas, mmas, out or None, stream or None), "mpgemm_probe_mma_rate")
 
 
 def solve(a, b, c, m, n, k, stream=0):

@@ -33,6 +33,7 @@
 
 #include "../../include/mpgemm.h"
 #include "gemm_kernel.cuh"
+#include "peak_probe.cuh"
 
 namespace mpgemm {
 namespace {
@@ -1069,6 +1070,29 @@ mpgemm_status_t mpgemm_solve(const void* a, const void* b, float* c, size_t m, s
     std::lock_guard<std::mutex> lock(d.mu);
     return mpgemm_run_ex(d.handle, MPGEMM_B_COL_MAJOR, M, N, K, 1.0f, a, K > 1 ? K : 1, b,
                          K > 1 ? K : 1, 0.0f, c, N > 1 ? N : 1, stream);
+}
+
+mpgemm_status_t mpgemm_probe_mma_rate(int32_t ctas, int32_t mmas, uint64_t* out, void* stream) {
+    if (ctas < 1 || ctas > 65535 || mmas < 4 || mmas > (1 << 22) || !out ||
+        reinterpret_cast<uintptr_t>(out) % 8 != 0)
+        return MPGEMM_ERR_INVALID_VALUE;
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MPGEMM_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return MPGEMM_ERR_UNSUPPORTED_DEVICE;
+    if (cudaFuncSetAttribute(mma_rate_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, kProbeSmemBytes) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return MPGEMM_ERR_CUDA;
+    }
+    mma_rate_probe<<<ctas, 32, kProbeSmemBytes, static_cast<cudaStream_t>(stream)>>>(
+        mmas, kDefaultWaitLimitNs, reinterpret_cast<unsigned long long*>(out));
+    if (cudaGetLastError() != cudaSuccess) return MPGEMM_ERR_LAUNCH;
+    return MPGEMM_OK;
 }
 
 mpgemm_status_t mpgemm_sync_status(mpgemm_handle_t h, void* stream, int32_t info[4]) {

@@ -48,6 +48,13 @@ def test_null_handle_is_rejected(lib):
     assert lib.mpgemm_create(None) == Status.ERR_INVALID_VALUE
 
 
+@pytest.mark.parametrize("ctas,mmas,out", [(0, 64, 256), (65536, 64, 256), (1, 3, 256), (1, 1 << 23, 256),
+                                           (1, 64, 0), (1, 64, 260)])
+def test_probe_rejects_bad_arguments(lib, ctas, mmas, out):
+    # checked before any CUDA call, so this runs without a GPU
+    assert lib.mpgemm_probe_mma_rate(ctas, mmas, out or None, None) == Status.ERR_INVALID_VALUE
+
+
 def test_create_without_gpu_fails_cleanly(lib):
     import torch
     if torch.cuda.is_available():

@@ -112,7 +112,7 @@ def test_reference_arm_prints_one_json_line():
 def test_reference_arm_other_ranks_exit_quietly():
     env = dict(os.environ, WORLD_SIZE="2", RANK="1")
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                          "--workload", "0", "--steps", "3", "--warmup", "3"],
+                          "--gpus", "2", "--workload", "0", "--steps", "3", "--warmup", "3"],
                          capture_output=True, text=True, env=env, timeout=300, check=True).stdout
     assert out.strip() == ""
 
@@ -146,3 +146,78 @@ def test_traffic_records_match_the_planner(index):
     else:
         assert bench.stored_traffic(index, tile) is None
     assert bench.stored_traffic(index, "0x0") is None
+
+
+def test_check_world_rejects_a_mismatch():
+    bench.check_world(1, 1)
+    bench.check_world(4, 4)
+    for gpus, world in [(2, 1), (1, 2), (8, 4), (0, 1)]:
+        with pytest.raises(SystemExit):
+            bench.check_world(gpus, world)
+
+
+def test_gpus_flag_without_ranks_exits_nonzero():
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0")
+    proc = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "3"],
+                          capture_output=True, text=True, env=env, timeout=300)
+    assert proc.returncode != 0 and "--gpus 2" in proc.stderr and proc.stdout.strip() == ""
+
+
+def _world_rank_main(rank, world, port, out):
+    # two gloo ranks launched for --gpus 3: every rank refuses before any GPU work
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world), RANK=str(rank))
+    try:
+        bench.check_world(3, bench.dist_env()[0])
+        out[rank] = "ran"
+    except SystemExit:
+        out[rank] = "refused"
+
+
+def test_check_world_on_two_gloo_ranks():
+    mgr = tmp.Manager()
+    out = mgr.dict()
+    tmp.spawn(_world_rank_main, args=(2, _free_port(), out), nprocs=2, join=True)
+    assert dict(out) == {0: "refused", 1: "refused"}
+
+
+PEAKS = {"tflops": 1927.1, "tflops_sustained": 1710.6, "hbm_gbs": 6775.9, "source": "measured"}
+
+
+def test_roofline_picks_hbm_for_the_tall_skinny_workload():
+    # 65536 x 257 x 4093 with beta != 0: 2MNK / bytes = 204.8 flop/B, below
+    # the ridge 1927.1e12 / 6775.9e9 = 284 flop/B -> HBM-bound
+    w = __import__("workloads").WORKLOADS[4]
+    nbytes = bench.gemm_bytes(w.M, w.N, w.K, w.beta)
+    assert nbytes == 2 * w.M * w.K + 2 * w.K * w.N + 2 * 4 * w.M * w.N
+    main, alt = bench.roofline_pair(w.M, w.N, w.K, w.beta, 0.2, PEAKS)
+    assert main["bound"] == "hbm" and alt["bound"] == "tensor"
+    assert main["unit"] == "GB/s" and main["achieved"] == pytest.approx(nbytes / 0.2e-3 / 1e9, rel=1e-3)
+    assert main["frac"] == pytest.approx(main["achieved"] / 6775.9, rel=1e-3)
+
+
+def test_roofline_picks_tensor_for_the_square_workload():
+    theory = {"tflops": 2577.6}
+    main, alt = bench.roofline_pair(8192, 8192, 8192, 0.0, 0.6, PEAKS, traffic=123, theoretical=theory)
+    assert main["bound"] == "tensor" and alt["bound"] == "hbm"
+    assert main["achieved"] == pytest.approx(2 * 8192 ** 3 / 0.6e-3 / 1e12, rel=1e-3)
+    assert main["frac_of_theoretical"] == pytest.approx(main["achieved"] / 2577.6, rel=1e-3)
+    assert main["traffic"] == 123 == alt["traffic"]
+
+
+def test_clock_samples_parse_and_window():
+    text = ("2026/12/02 11:20:01.000, 0, 1500, 2070, 1350.5, 0x4, Not Active, Not Active, Not Active, Active\n"
+            "2026/12/02 11:20:01.050, 0, 1600, 2070, 1360.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+            "garbage line\n"
+            "2026/12/02 11:20:02.000, 0, 2070, 2070, 200.0, 0x0, Not Active, Not Active, Not Active, Not Active\n")
+    samples = bench.parse_clock_samples(text)
+    assert len(samples) == 3 and samples[0]["reasons"] == ["sw_power_cap"]
+    t0 = samples[0]["t"]
+    s = bench.ClockSampler.summarize(samples, t0, t0 + 0.1)
+    assert s["samples"] == 2 and s["sm_mhz"] == 1550 and s["reasons"] == ["sw_power_cap"]
+    assert bench.ClockSampler.summarize(samples, t0 + 5, None)["samples"] == 0
+
+
+def test_both_arms_report_the_same_config():
+    w = __import__("workloads").WORKLOADS[3]
+    assert bench.workload_config(w, 1) == bench.workload_config(w, 1)
+    assert bench.workload_config(w, 2)["parallelism"] == "replicas x2"

@@ -468,6 +468,30 @@ def test_offsets_beyond_32_bits(mp):
     torch.cuda.empty_cache()
 
 
+# --------------------------------------------------------------------------- tensor-core rate probe
+
+def test_mma_rate_probe_pins_the_per_sm_rate(mp):
+    # One probe CTA per SM issues back-to-back M = 128, N = 256, K = 16
+    # kind::f16 MMAs: the per-SM dense FP16 rate is 1,048,576 FLOP over the
+    # cycles each takes. Every CTA must finish, and the rate must be one
+    # value for all SMs (the factor of the "02_mixed_precision_gemm" README's
+    # peak = MACs/SM/clk x SMs x 2 x clock, measured rather than assumed).
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    mmas = 1 << 14
+    out = torch.zeros(2 * sms, dtype=torch.int64, device="cuda")
+    s = torch.cuda.current_stream()
+    mp.probe_mma_rate(sms, mmas, out.data_ptr(), s.cuda_stream)
+    s.synchronize()
+    res = out.cpu().numpy().reshape(sms, 2)
+    assert np.all(res[:, 1] == 1)
+    flop_per_clk = mp.PROBE_FLOP_PER_MMA * mmas / res[:, 0]
+    # (a data-sheet figure would be 8192; allow the issue overhead of the
+    # first and last instruction, and nothing above the cycle count of one
+    # 128 x 256 x 16 MMA per 128 cycles)
+    assert 7000 < float(np.median(flop_per_clk)) <= 8192 * 1.001
+    assert float(flop_per_clk.max() / flop_per_clk.min()) < 1.05
+
+
 # --------------------------------------------------------------------------- host-buffer entry point
 
 def test_run_host_matches_oracle(handle):
