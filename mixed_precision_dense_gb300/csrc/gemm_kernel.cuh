@@ -158,10 +158,11 @@ struct TileConfig {
     // so the accumulator receives k-block 0, 1, 2, ... one after the other
     // without either thread waiting for MMAs to complete
     static constexpr int ISSUERS = ISSUERS_;
-    static constexpr bool KSPLIT = ISSUERS == 2 && BN_ != 512;
+    static constexpr bool KSPLIT = ISSUERS == 2 && BN_ <= 256;
     // one MMA instruction covers SUB_N columns: BN, except that a tile wider
     // than 256 takes two instructions per K step, of 256 columns and of the
-    // rest (256 for 512-wide pair tiles, 64 for 320-wide one-CTA tiles)
+    // rest (256 for 512-wide pair tiles, 128 for 384-wide ones, 64 for
+    // 320-wide one-CTA tiles)
     static constexpr int SUB_N = BN > 256 ? 256 : BN;
     static constexpr int SUBS = (BN + SUB_N - 1) / SUB_N;
     // two accumulator buffers (the epilogue of tile i overlaps the MMAs of
@@ -196,9 +197,10 @@ struct TileConfig {
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARRIERS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
     static constexpr int THREADS = 32 * (2 + EPI_WARPS + ISSUERS - 1);
-    static_assert(BN == 128 || BN == 256 || (PAIR && BN == 512) || (!PAIR && BN == 320), "tile width");
+    static_assert(BN == 128 || BN == 256 || (PAIR && (BN == 384 || BN == 512)) || (!PAIR && BN == 320),
+                  "tile width");
     static_assert(ACC_BUFS * BN <= TMEM_COLS, "accumulators fit the tensor memory allocated");
-    static_assert(!PAIR || BN >= 256, "pair tiles are 256 x 256 or 256 x 512");
+    static_assert(!PAIR || BN >= 256, "pair tiles are 256 x 256, 256 x 384 or 256 x 512");
     static_assert(ISSUERS == 1 || ISSUERS == SUBS || (KSPLIT && SUBS == 1), "one issuer, one per part, or two by k-block");
     static_assert(SUB_N >= (PAIR ? 128 : 64) && ATOMS_PER_PART >= 1, "parts hold whole B boxes");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment");
@@ -239,6 +241,24 @@ __device__ __forceinline__ void zero_leading_columns(uint8_t* tile, int32_t d, i
         if (s2) *reinterpret_cast<uint16_t*>(q + o2) = static_cast<uint16_t>(0);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// The same for the A tile of the other CTA of a pair, written through
+// distributed shared memory (tile_c: the tile's cluster address), then
+// ordered before this thread's later tensor-core reads of it.
+__device__ __forceinline__ void zero_leading_columns_peer(uint32_t tile_c, int32_t d, int32_t rows) {
+    const bool s8 = d >= 4, s4 = (d & 2) != 0, s2 = (d & 1) != 0;
+    const uint32_t o4 = s8 ? 8u : 0u;
+    const uint32_t o2 = o4 + (s4 ? 4u : 0u);
+    rows = min(rows, 128);
+#pragma unroll 8
+    for (int32_t t = 0; t < rows; ++t) {
+        const uint32_t q = tile_c + static_cast<uint32_t>(t * 128 + ((t & 7) << 4));
+        if (s8) ptx::st_cluster_u64(q, 0ull);
+        if (s4) ptx::st_cluster_u32(q + o4, 0u);
+        if (s2) ptx::st_cluster_u16(q + o2, static_cast<uint16_t>(0));
+    }
+    ptx::fence_proxy_async_cluster();
 }
 
 // Tile t of the persistent walk -> (m block, n block). Tiles are visited in
@@ -297,6 +317,15 @@ __device__ __forceinline__ WorkItem work_item(const GemmParams& p, int32_t i) {
     w.kb0 = 0;
     w.kb1 = p.k_blocks;
     return w;
+}
+
+// Columns of item w that the MMAs cover: the item's width cut down to the
+// 64-column boxes (one CTA) or 128-column units (a pair: each CTA holds half
+// of every part) that hold columns below N.
+template <class Cfg>
+__device__ __forceinline__ int32_t item_cols(const GemmParams& p, const WorkItem& w) {
+    constexpr int32_t unit = 64 * Cfg::CTAS;
+    return unit * min(w.width / unit, (p.N - w.n0 + unit - 1) / unit);
 }
 
 struct Waiter {
@@ -580,16 +609,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     // item, and this CTA loads sub_n / 2 of them (its half) for
                     // each instruction, in 64-column boxes ("atoms"); atom a
                     // belongs to instruction a / per_sub.
-                    const int32_t sub_n = PAIR ? min(w.width, Cfg::SUB_N) : w.width;
-                    const int32_t per_sub = PAIR ? sub_n / 128 : 0;
-                    const int32_t n0 = w.n0 + (PAIR ? static_cast<int32_t>(rank) * (sub_n / 2) : 0);
+                    const int32_t n_valid = item_cols<Cfg>(p, w);
                     int32_t cls, j0;
                     a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
                     const CUtensorMap* map_a = &maps.a[cls];
                     const int32_t a_row = j0 + static_cast<int32_t>(rank) * BM;   // class row
                     const int32_t b_shift = p.a_shift[cls];
-                    // single: only the boxes that hold valid columns; pair: all boxes
-                    const int32_t n_atoms = PAIR ? w.width / 128 : min(w.width / 64, (p.N - w.n0 + 63) / 64);
+                    // only the boxes that hold valid columns (a pair CTA holds
+                    // half of every part's columns)
+                    const int32_t n_atoms = n_valid / (64 * Cfg::CTAS);
                     const uint32_t bytes = (Cfg::A_BYTES + n_atoms * Cfg::B_ATOM_BYTES) * Cfg::CTAS;
                     for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                         if (!waiter.wait(empty_bar(stage), phase ^ 1u)) {
@@ -602,11 +630,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
                             ptx::tma_load_2d_pair(sA + stage * Cfg::A_BYTES, map_a, lead_full, kb * BK,
                                                   a_row, pol_a);
-                            for (int j = 0; j < n_atoms; ++j) {
-                                const int32_t col = n0 + (j / per_sub) * sub_n + (j % per_sub) * 64;
-                                ptx::tma_load_2d_pair(sB + stage * Cfg::B_BYTES + j * Cfg::B_ATOM_BYTES,
-                                                      &tmap_b, lead_full, Cfg::B_KMAJOR ? kb * BK : col,
-                                                      Cfg::B_KMAJOR ? col : kb * BK - b_shift, pol_b);
+                            // part h (an MMA instruction's columns): this CTA loads
+                            // its half of them, in 64-column boxes from box h *
+                            // ATOMS_PER_PART on
+                            for (int32_t h = 0; h * Cfg::SUB_N < n_valid; ++h) {
+                                const int32_t half = min(Cfg::SUB_N, n_valid - h * Cfg::SUB_N) / 2;
+                                const int32_t c0 = w.n0 + h * Cfg::SUB_N + static_cast<int32_t>(rank) * half;
+                                for (int32_t a = 0; a * 64 < half; ++a) {
+                                    const int32_t col = c0 + a * 64;
+                                    ptx::tma_load_2d_pair(
+                                        sB + stage * Cfg::B_BYTES + (h * Cfg::ATOMS_PER_PART + a) * Cfg::B_ATOM_BYTES,
+                                        &tmap_b, lead_full, Cfg::B_KMAJOR ? kb * BK : col,
+                                        Cfg::B_KMAJOR ? col : kb * BK - b_shift, pol_b);
+                                }
                             }
                         } else {
                             ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
@@ -614,8 +650,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                              a_row, pol_a);
                             for (int j = 0; j < n_atoms; ++j)
                                 ptx::tma_load_2d(sB + stage * Cfg::B_BYTES + j * Cfg::B_ATOM_BYTES,
-                                                 &tmap_b, full_bar(stage), Cfg::B_KMAJOR ? kb * BK : n0 + j * 64,
-                                                 Cfg::B_KMAJOR ? n0 + j * 64 : kb * BK - b_shift, pol_b);
+                                                 &tmap_b, full_bar(stage), Cfg::B_KMAJOR ? kb * BK : w.n0 + j * 64,
+                                                 Cfg::B_KMAJOR ? w.n0 + j * 64 : kb * BK - b_shift, pol_b);
                         }
                         if (rank == 0) {
                             armed |= 1u << stage;
@@ -656,10 +692,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             for (int32_t i = first_item; ok && i < p.items; i += item_step) {
                 const WorkItem w = work_item<BN>(p, i);
                 if (w.n0 >= p.N) continue;
-                // columns the MMAs cover (a one-CTA tile skips the 64-column
-                // boxes wholly past N) and the parts (instructions per K step)
-                // they fall into: part h is columns [h SUB_N, h SUB_N + cols)
-                const int32_t n_valid = PAIR ? w.width : 64 * min(w.width / 64, (p.N - w.n0 + 63) / 64);
+                // columns the MMAs cover (the boxes wholly past N are skipped)
+                // and the parts (instructions per K step) they fall into: part
+                // h is columns [h SUB_N, h SUB_N + cols)
+                const int32_t n_valid = item_cols<Cfg>(p, w);
                 const int32_t n_parts = (n_valid + Cfg::SUB_N - 1) / Cfg::SUB_N;
                 int32_t cls, j0;
                 a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
@@ -709,8 +745,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         }
                     }
                     ptx::tc_fence_after_sync();
-                    if (kb == 0 && lead_cols > 0)
+                    if (kb == 0 && lead_cols > 0) {
                         zero_leading_columns(gbase + Cfg::OFF_A + stage * Cfg::A_BYTES, lead_cols, lead_rows);
+                        // the other CTA of a pair holds the tile's next 128 rows
+                        if constexpr (PAIR)
+                            zero_leading_columns_peer(ptx::mapa_shared(sA + stage * Cfg::A_BYTES, 1), lead_cols,
+                                                      lead_rows - BM);
+                    }
                     const uint32_t a_base = sA + stage * Cfg::A_BYTES;
                     const uint32_t b_base = sB + stage * Cfg::B_BYTES;
                     bool pending = false;   // MMAs issued from this stage

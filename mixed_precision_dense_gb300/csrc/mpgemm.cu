@@ -49,17 +49,22 @@ using Cfg320 = TileConfig<320, 3, false>;
 using CfgPair = TileConfig<256, 6, true, false, 2>;   // a CTA pair per 256 x 256 tile, two MMA issuers
                                                       // taking alternate k-blocks in a fixed order
 using CfgWide = TileConfig<512, 4, true>;   // a CTA pair per 256 x 512 tile
+// a CTA pair per 256 x 384 tile (parts of 256 and 128 columns, one MMA
+// thread each; N from 257 to 384 in one tile column)
+using CfgPair384 = TileConfig<384, 4, true, false, 2>;
 // the same five shapes for a column-major B (a K-major B operand)
 using Cfg256K = TileConfig<256, 4, false, true>;
 using Cfg128K = TileConfig<128, 6, false, true>;
 using Cfg320K = TileConfig<320, 3, false, true>;
 using CfgPairK = TileConfig<256, 6, true, true, 2>;
 using CfgWideK = TileConfig<512, 4, true, true>;
+using CfgPair384K = TileConfig<384, 4, true, true, 2>;
 // one occupancy query (max_pair_clusters) serves both pair shapes: shared
 // memory limits either to one CTA per SM, and both stay far below the SM's
 // thread and register limits at that occupancy
 static_assert(CfgWide::SMEM_BYTES > 232448 / 2 && CfgPair::SMEM_BYTES > 232448 / 2 &&
-                  CfgWide::THREADS <= 384 && CfgPair::THREADS <= 384,
+                  CfgPair384::SMEM_BYTES > 232448 / 2 && CfgWide::THREADS <= 384 && CfgPair::THREADS <= 384 &&
+                  CfgPair384::THREADS <= 384,
               "the wide pair kernel fits wherever the 256 x 256 pair kernel fits");
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -211,6 +216,7 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     if (num_sms <= 0) return MPGEMM_ERR_INVALID_VALUE;
     if (opt.tile_n == 512 && opt.tile_m == 128) return MPGEMM_ERR_INVALID_VALUE;   // 512 wide: pairs only
     if (opt.tile_n == 320 && opt.tile_m == 256) return MPGEMM_ERR_INVALID_VALUE;   // 320 wide: one CTA
+    if (opt.tile_n == 384 && opt.tile_m == 128) return MPGEMM_ERR_INVALID_VALUE;   // 384 wide: pairs only
     mpgemm_plan_t p;
     std::memset(&p, 0, sizeof(p));
     p.tile_m = 128;
@@ -225,7 +231,7 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
         return MPGEMM_OK;
     }
     p.stage_b = (opt.force_staging || !aligned16(B, ldb, 2)) ? 1 : 0;
-    const bool pair = opt.tile_n == 512 ||
+    const bool pair = opt.tile_n == 512 || opt.tile_n == 384 ||
                       (opt.tile_m ? (opt.tile_m == 256) : (!opt.tile_n && auto_pair(M, N, K, num_sms)));
     if (pair) {
         int64_t pair_units = num_sms / 2;
@@ -234,9 +240,9 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
         pair_units = std::max<int64_t>(1, pair_units);
         const bool wide = opt.tile_n == 512 || (!opt.tile_m && !opt.tile_n && auto_wide(M, N, K, pair_units));
         p.tile_m = 256;
-        p.tile_n = wide ? 512 : 256;
-        p.stages = wide ? CfgWide::STAGES : CfgPair::STAGES;
-        p.smem_bytes = wide ? CfgWide::SMEM_BYTES : CfgPair::SMEM_BYTES;
+        p.tile_n = opt.tile_n == 384 ? 384 : (wide ? 512 : 256);
+        p.stages = p.tile_n == 384 ? CfgPair384::STAGES : (wide ? CfgWide::STAGES : CfgPair::STAGES);
+        p.smem_bytes = p.tile_n == 384 ? CfgPair384::SMEM_BYTES : (wide ? CfgWide::SMEM_BYTES : CfgPair::SMEM_BYTES);
     } else {
         // (A is read in row classes below when its rows break the 16-byte rule)
         const bool row_classes = !aligned16(A, lda, 2) && !opt.force_staging && !opt.b_col_major;
@@ -247,9 +253,9 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
                                          : Cfg128::SMEM_BYTES;
     }
     // An A whose rows break TMA's 16-byte rule is read in row classes
-    // (one-CTA tiles with a row-major B), else copied to an aligned buffer.
+    // (row-major B), else copied to an aligned buffer.
     const bool a_aligned = aligned16(A, lda, 2);
-    const bool a_classes = !a_aligned && !opt.force_staging && !pair && !opt.b_col_major;
+    const bool a_classes = !a_aligned && !opt.force_staging && !opt.b_col_major;
     p.stage_a = (opt.force_staging || (!a_aligned && !a_classes)) ? 1 : 0;
     const AClassLayout L = a_class_layout(A, lda, M, a_classes, p.tile_m);
     p.a_classes = a_classes ? L.P : 0;
@@ -301,11 +307,13 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     } else {
         // If the last wave of tiles would keep at most half of the CTAs (pairs)
         // busy, do those tiles as two half-width items each: the wave then
-        // finishes in half the time. (Not 320-wide tiles: a 160-column half
-        // does not follow their 256 + 64 column parts.)
+        // finishes in half the time. (Not 320- or 384-wide tiles: a 160- or
+        // 192-column half does not follow their 256 + 64 or 256 + 128 column
+        // parts.)
         const int64_t tile_units = std::min<int64_t>(units, p.tiles);
         const int64_t rem = p.tiles % tile_units;
-        p.split_tiles = (p.tile_n != 320 && p.tiles > tile_units && rem > 0 && 2 * rem <= tile_units)
+        p.split_tiles = (p.tile_n != 320 && p.tile_n != 384 && p.tiles > tile_units && rem > 0 &&
+                         2 * rem <= tile_units)
                             ? static_cast<int32_t>(rem)
                             : 0;
         p.items = p.tiles + p.split_tiles;
@@ -558,6 +566,8 @@ cudaError_t prepare_kernels() {
     if (e == cudaSuccess) e = set_smem_attr<Cfg320K>();
     if (e == cudaSuccess) e = set_smem_attr<CfgPairK>();
     if (e == cudaSuccess) e = set_smem_attr<CfgWideK>();
+    if (e == cudaSuccess) e = set_smem_attr<CfgPair384>();
+    if (e == cudaSuccess) e = set_smem_attr<CfgPair384K>();
     return e;
 }
 
@@ -663,6 +673,9 @@ cudaError_t launch_plan(const mpgemm_plan_t& plan, bool b_col_major, int max_clu
         if (plan.tile_n == 512)
             return b_col_major ? launch_tc<CfgWideK>(grid, ta, tb, gp, stream)
                                : launch_tc<CfgWide>(grid, ta, tb, gp, stream);
+        if (plan.tile_n == 384)
+            return b_col_major ? launch_tc<CfgPair384K>(grid, ta, tb, gp, stream)
+                               : launch_tc<CfgPair384>(grid, ta, tb, gp, stream);
         return b_col_major ? launch_tc<CfgPairK>(grid, ta, tb, gp, stream)
                            : launch_tc<CfgPair>(grid, ta, tb, gp, stream);
     }
@@ -797,7 +810,7 @@ mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const 
                             mpgemm_plan_t* out) {
     if (!out) return MPGEMM_ERR_INVALID_VALUE;
     if (tile_m != 0 && tile_m != 128 && tile_m != 256) return MPGEMM_ERR_INVALID_VALUE;
-    if (tile_n != 0 && tile_n != 128 && tile_n != 256 && tile_n != 320 && tile_n != 512)
+    if (tile_n != 0 && tile_n != 128 && tile_n != 256 && tile_n != 320 && tile_n != 384 && tile_n != 512)
         return MPGEMM_ERR_INVALID_VALUE;
     if (max_ctas < 0) return MPGEMM_ERR_INVALID_VALUE;
     Options opt;
@@ -869,7 +882,7 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
     if (!h) return MPGEMM_ERR_INVALID_VALUE;
     switch (opt) {
         case MPGEMM_OPT_TILE_N:
-            if (value != 0 && value != 128 && value != 256 && value != 320 && value != 512)
+            if (value != 0 && value != 128 && value != 256 && value != 320 && value != 384 && value != 512)
                 return MPGEMM_ERR_INVALID_VALUE;
             h->opt.tile_n = static_cast<int32_t>(value);
             return MPGEMM_OK;

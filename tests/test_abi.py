@@ -126,9 +126,16 @@ def test_alignment_classification():
     p = _plan(M=128, N=128, K=128, lda=128, ldb=128, ldc=128, A=256 + 2)
     assert (p["stage_a"], p["stage_b"], p["a_classes"]) == (0, 0, 1)
     assert p["k_blocks"] == 3                      # K + 1 view columns
-    # CTA pairs read A through one plain map: an unaligned A is staged
+    # CTA pairs read an unaligned A in row classes too, with 256-row class
+    # tiles: ceil(1024 / 256) tiles in each of the 8 classes
     p = _plan(M=8192, N=8192, K=8192, lda=8193, ldb=8192, ldc=8192)
-    assert p["tile_m"] == 256 and p["stage_a"] == 1 and p["a_classes"] == 0
+    assert p["tile_m"] == 256 and p["stage_a"] == 0 and p["a_classes"] == 8
+    assert p["m_tiles"] == 8 * 4
+    # 256 x 384 pair tiles: pairs only, never split into half-width items
+    p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257, tile_n=384)
+    assert (p["tile_m"], p["tile_n"], p["a_classes"], p["split_tiles"]) == (256, 384, 8, 0)
+    with pytest.raises(mp.MpgemmError):
+        _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257, tile_m=128, tile_n=384)
     p = _plan(M=128, N=128, K=128, lda=128, ldb=128, ldc=128, force_staging=True)
     assert (p["stage_a"], p["stage_b"]) == (1, 1)
 

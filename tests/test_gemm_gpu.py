@@ -293,9 +293,9 @@ def test_wide_pair_large_sampled(mp):
 SPLIT_CASES = [  # (tile_m, tile_n, max_ctas, M, N, K): the last partial wave is split in halves
     (128, 256, 5, 1000, 800, 200),     # half tiles wholly past column 800 are skipped
     (128, 128, 7, 700, 600, 336),
-    (256, 256, 8, 1300, 1100, 150),
+    (256, 256, 8, 1300, 1100, 152),
     (256, 256, 10, 768, 1024, 320),
-    (256, 512, 8, 1300, 1100, 150),    # 256-wide halves; the half past column 1100 is skipped
+    (256, 512, 8, 1300, 1100, 152),    # 256-wide halves; the half past column 1100 is skipped
 ]
 
 
@@ -375,6 +375,85 @@ def test_a_row_classes_integer_bitwise(mp):
     ops = workloads.make_operands(777, 260, 1021, lda=1021, dist="int3", dist_b="int2", seed=88)
     with mp.Handle() as h:
         check_full(h, ops, exact=True)
+
+
+PAIR_CLASS_CASES = [  # (M, N, K, lda, a_offset, tile_n): A read in row classes by CTA pairs
+    (600, 300, 500, 503, 0, 256),    # NaN padding between rows: both CTAs' leading columns zeroed
+    (1100, 520, 333, 340, 0, 256),   # 2 classes
+    (700, 257, 1000, 1002, 0, 384),  # 4 classes, 256 x 384 tiles
+    (513, 700, 129, 131, 0, 512),    # 8 classes, 256 x 512 tiles, the odd CTA with few rows
+    (300, 200, 256, 256, 1, 256),    # aligned pitch, base 2 bytes off: 1 class, shift 1
+    (40, 300, 70, 71, 0, 256),       # 5 rows per class: the odd CTA of every pair has none
+]
+
+
+@pytest.mark.parametrize("M,N,K,lda,a_offset,tile_n", PAIR_CLASS_CASES)
+def test_a_row_classes_cta_pairs(mp, M, N, K, lda, a_offset, tile_n):
+    plan = mp.plan(M, N, K, 1.0, 256 + 2 * a_offset, lda, 256, N, 0.5, 256, N, tile_m=256,
+                   tile_n=0 if tile_n == 256 else tile_n)
+    assert plan["tile_m"] == 256 and plan["tile_n"] == tile_n
+    assert plan["a_classes"] >= 1 and plan["stage_a"] == 0
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_M, 256)
+        h.set_option(mp.Option.TILE_N, 0 if tile_n == 256 else tile_n)
+        ops = workloads.make_operands(M, N, K, lda=lda, alpha=1.25, beta=0.5, c_dist="normal",
+                                      seed=M + lda + tile_n)
+        check_full(h, ops, a_offset=a_offset)
+        h.set_option(mp.Option.FORCE_STAGING, 1)
+        check_full(h, ops, a_offset=a_offset)
+
+
+@pytest.mark.parametrize("tile_n", [256, 384, 512])
+def test_a_row_classes_cta_pairs_integer_bitwise(mp, tile_n):
+    ops = workloads.make_operands(777, 520, 1021, lda=1021, dist="int3", dist_b="int2", seed=89 + tile_n)
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_M, 256)
+        h.set_option(mp.Option.TILE_N, 0 if tile_n == 256 else tile_n)
+        check_full(h, ops, exact=True)
+
+
+PAIR384_SHAPES = [  # (M, N, K, lda, ldb, ldc, beta, max_ctas): 256 x 384 CTA-pair tiles
+    (256, 384, 64, 64, 384, 384, 0.0, 0),       # one full tile
+    (256, 257, 617, 617, 257, 257, 0.5, 0),     # one column past 256: the 128-column part
+    (1000, 300, 700, 700, 300, 301, 1.0, 4),    # two pairs walk 4 tiles through the one accumulator
+    (511, 600, 129, 129, 600, 600, -0.5, 0),    # second tile column 216 wide: trimmed to 256
+    (1300, 1100, 333, 335, 1103, 1101, 0.75, 6),  # unaligned A (row classes), B and C staged / per lane
+]
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,beta,max_ctas", PAIR384_SHAPES)
+def test_cta_pair_384_wide_tiles(mp, M, N, K, lda, ldb, ldc, beta, max_ctas):
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_N, 384)
+        h.set_option(mp.Option.MAX_CTAS, max_ctas)
+        ops = workloads.make_operands(M, N, K, lda=lda, ldb=ldb, ldc=ldc, alpha=1.5, beta=beta,
+                                      c_dist="normal" if beta else "zeros", seed=M + 5 * N + K)
+        check_full(h, ops)
+        ops = workloads.make_operands(M, N, K, lda=lda, ldb=K + 3, ldc=ldc, alpha=1.5, beta=beta,
+                                      c_dist="normal" if beta else "zeros", seed=M + 5 * N + K + 1,
+                                      b_col_major=True)
+        check_full(h, ops)
+
+
+@pytest.mark.parametrize("M,N,K", [(600, 100, 300), (600, 640, 300), (700, 129, 129)])
+def test_cta_pair_tiles_trimmed_to_valid_columns(mp, M, N, K):
+    # a pair tile's columns are cut to the 128-column units below N (N = 128
+    # instructions for a 256-wide tile with at most 128 valid columns)
+    for tile_n in (0, 512):
+        with mp.Handle() as h:
+            h.set_option(mp.Option.TILE_M, 256)
+            h.set_option(mp.Option.TILE_N, tile_n)
+            check_full(h, workloads.make_operands(M, N, K, beta=0.5, c_dist="normal", seed=M + N + tile_n))
+            check_full(h, workloads.make_operands(M, N, K, dist="int3", dist_b="int2", seed=M + N + tile_n + 1),
+                       exact=True)
+
+
+def test_tall_skinny_workload_in_256x384_pairs(mp):
+    ops = workloads.workload_operands(4)
+    I, J = workloads.workload_sample(4)
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_N, 384)
+        check_sampled(h, ops, I, J)
 
 
 def test_forced_staging_matches(mp):
