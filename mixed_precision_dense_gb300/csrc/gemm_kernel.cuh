@@ -89,11 +89,13 @@ namespace mpgemm {
 // rows earlier (rows before 0 arrive as zeros).
 constexpr int kMaxAClasses = 8;
 
-// The tensor maps of A (one per row class) and of C (FP32, 32 x 32 boxes,
-// 128-byte swizzle; used only when GemmParams::c_tma is set).
+// The tensor maps of A (one per row class), of C (FP32, 32 x 32 boxes,
+// 128-byte swizzle; used only when GemmParams::c_tma is set) and of B in
+// narrow boxes (used only by 256 x 320 pair tiles).
 struct TensorMaps {
     CUtensorMap a[kMaxAClasses];
     CUtensorMap c;
+    CUtensorMap b_tail;   // B in 32-column boxes, 64-byte swizzle (the narrow last part of a 320-wide pair)
 };
 
 struct GemmParams {
@@ -165,6 +167,11 @@ struct TileConfig {
     // 320-wide one-CTA tiles)
     static constexpr int SUB_N = BN > 256 ? 256 : BN;
     static constexpr int SUBS = (BN + SUB_N - 1) / SUB_N;
+    // columns of the last part; a pair CTA holds half of them. A 320-wide
+    // pair's last part is 64 columns: each CTA loads its 32 of them as one
+    // 4 KB box in the 64-byte swizzle (row-major B only)
+    static constexpr int TAIL_N = BN - (SUBS - 1) * SUB_N;
+    static constexpr bool NARROW_TAIL = PAIR && TAIL_N == 64;
     // two accumulator buffers (the epilogue of tile i overlaps the MMAs of
     // tile i+1) when they fit in the 512 columns of tensor memory, else one,
     // whose SUBS parts are handed back one by one
@@ -176,6 +183,7 @@ struct TileConfig {
     static constexpr int A_BYTES = BM * BK * 2;        // 16 KB
     static constexpr int B_ATOM_BYTES = BK * 64 * 2;   // one 64-column box of B: 8 KB
     static constexpr int B_BYTES = BK * B_COLS * 2;
+    static constexpr int B_TAIL_BYTES = BK * 32 * 2;   // one narrow box: 32 columns of 64 K-rows
     // epilogue warps: 8, two per 32 tensor-memory lanes, each taking half of
     // every part's columns. The 256 x 512 tile's single accumulator is
     // drained while the MMAs of the next tile wait, and the last tile of
@@ -197,17 +205,17 @@ struct TileConfig {
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARRIERS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
     static constexpr int THREADS = 32 * (2 + EPI_WARPS + ISSUERS - 1);
-    static_assert(BN == 128 || BN == 256 || (PAIR && (BN == 384 || BN == 512)) || (!PAIR && BN == 320),
-                  "tile width");
+    static_assert(BN == 128 || BN == 256 || BN == 320 || (PAIR && (BN == 384 || BN == 512)), "tile width");
+    static_assert(!NARROW_TAIL || (!B_KMAJOR && ISSUERS == 2), "narrow last part: row-major B, one issuer per part");
     static_assert(ACC_BUFS * BN <= TMEM_COLS, "accumulators fit the tensor memory allocated");
-    static_assert(!PAIR || BN >= 256, "pair tiles are 256 x 256, 256 x 384 or 256 x 512");
+    static_assert(!PAIR || BN >= 256, "pair tiles are 256 x 256, 256 x 320, 256 x 384 or 256 x 512");
     static_assert(ISSUERS == 1 || ISSUERS == SUBS || (KSPLIT && SUBS == 1), "one issuer, one per part, or two by k-block");
     static_assert(SUB_N >= (PAIR ? 128 : 64) && ATOMS_PER_PART >= 1, "parts hold whole B boxes");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment");
     static_assert(OFF_EPI % 1024 == 0, "chunk buffers are 1024-byte aligned (128-byte swizzle atoms)");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "tensor memory allocation");
-    static_assert(BN % 64 == 0 && (BN - (SUBS - 1) * SUB_N) % (PAIR ? 128 : 64) == 0,
+    static_assert(BN % 64 == 0 && (TAIL_N % (PAIR ? 128 : 64) == 0 || NARROW_TAIL),
                   "the last part holds whole B boxes");
 };
 
@@ -321,11 +329,12 @@ __device__ __forceinline__ WorkItem work_item(const GemmParams& p, int32_t i) {
 
 // Columns of item w that the MMAs cover: the item's width cut down to the
 // 64-column boxes (one CTA) or 128-column units (a pair: each CTA holds half
-// of every part) that hold columns below N.
+// of every part) that hold columns below N (a 320-wide pair's 64-column last
+// part counts whole).
 template <class Cfg>
 __device__ __forceinline__ int32_t item_cols(const GemmParams& p, const WorkItem& w) {
     constexpr int32_t unit = 64 * Cfg::CTAS;
-    return unit * min(w.width / unit, (p.N - w.n0 + unit - 1) / unit);
+    return min(w.width, unit * ((p.N - w.n0 + unit - 1) / unit));
 }
 
 struct Waiter {
@@ -561,6 +570,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (warp == 0 && lane == 0) {
         for (int r = 0; r < p.a_classes; ++r) ptx::prefetch_tensormap(&maps.a[r]);
         if (p.c_tma) ptx::prefetch_tensormap(&maps.c);
+        if constexpr (Cfg::NARROW_TAIL) ptx::prefetch_tensormap(&maps.b_tail);
         ptx::prefetch_tensormap(&tmap_b);
     }
     if (warp == 1) {
@@ -618,7 +628,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     // only the boxes that hold valid columns (a pair CTA holds
                     // half of every part's columns)
                     const int32_t n_atoms = n_valid / (64 * Cfg::CTAS);
-                    const uint32_t bytes = (Cfg::A_BYTES + n_atoms * Cfg::B_ATOM_BYTES) * Cfg::CTAS;
+                    const uint32_t bytes = (Cfg::A_BYTES + (n_valid / Cfg::CTAS) * BK * 2) * Cfg::CTAS;
                     for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                         if (!waiter.wait(empty_bar(stage), phase ^ 1u)) {
                             waiter.fail(kRoleLoad, kb);
@@ -636,12 +646,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             for (int32_t h = 0; h * Cfg::SUB_N < n_valid; ++h) {
                                 const int32_t half = min(Cfg::SUB_N, n_valid - h * Cfg::SUB_N) / 2;
                                 const int32_t c0 = w.n0 + h * Cfg::SUB_N + static_cast<int32_t>(rank) * half;
+                                const uint32_t dst = sB + stage * Cfg::B_BYTES + h * Cfg::ATOMS_PER_PART * Cfg::B_ATOM_BYTES;
+                                if (Cfg::NARROW_TAIL && half == 32) {
+                                    ptx::tma_load_2d_pair(dst, &maps.b_tail, lead_full, c0, kb * BK - b_shift, pol_b);
+                                    continue;
+                                }
                                 for (int32_t a = 0; a * 64 < half; ++a) {
                                     const int32_t col = c0 + a * 64;
-                                    ptx::tma_load_2d_pair(
-                                        sB + stage * Cfg::B_BYTES + (h * Cfg::ATOMS_PER_PART + a) * Cfg::B_ATOM_BYTES,
-                                        &tmap_b, lead_full, Cfg::B_KMAJOR ? kb * BK : col,
-                                        Cfg::B_KMAJOR ? col : kb * BK - b_shift, pol_b);
+                                    ptx::tma_load_2d_pair(dst + a * Cfg::B_ATOM_BYTES, &tmap_b, lead_full,
+                                                          Cfg::B_KMAJOR ? kb * BK : col,
+                                                          Cfg::B_KMAJOR ? col : kb * BK - b_shift, pol_b);
                                 }
                             }
                         } else {
@@ -789,9 +803,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             //    (leading offset), 8 K-rows of 128 B per group (stride
                             //    offset); the k-th 16-row slice starts 16 * 128 bytes
                             //    further. B column-major: K-major like A.
+                            // A narrow last part (32 columns per CTA): 64-byte rows,
+                            //    64-byte swizzle, 8 K-rows of 64 B per group, the
+                            //    k-th 16-row slice 16 * 64 bytes further.
                             const uint64_t b_desc =
                                 Cfg::B_KMAJOR ? ptx::smem_desc_sw128(b_part + kk * 32, 16, 1024)
-                                              : ptx::smem_desc_sw128(b_part + kk * 2048, Cfg::B_ATOM_BYTES, 1024);
+                                : (Cfg::NARROW_TAIL && part_cols == 64)
+                                    ? ptx::smem_desc(b_part + kk * 1024, Cfg::B_TAIL_BYTES, 512, ptx::kLayoutSw64)
+                                    : ptx::smem_desc_sw128(b_part + kk * 2048, Cfg::B_ATOM_BYTES, 1024);
                             if constexpr (PAIR)
                                 ptx::mma_f16_pair(d_part, a_desc, b_desc, idesc, (kb != w.kb0) || kk != 0);
                             else

@@ -52,6 +52,10 @@ using CfgWide = TileConfig<512, 4, true>;   // a CTA pair per 256 x 512 tile
 // a CTA pair per 256 x 384 tile (parts of 256 and 128 columns, one MMA
 // thread each; N from 257 to 384 in one tile column)
 using CfgPair384 = TileConfig<384, 4, true, false, 2>;
+// a CTA pair per 256 x 320 tile: parts of 256 and 64 columns, the 64-column
+// part read in 32-column boxes per CTA (4 KB, 64-byte swizzle), so five 36 KB
+// stages fit (N from 257 to 320, row-major B)
+using CfgPair320 = TileConfig<320, 5, true, false, 2>;
 // the same five shapes for a column-major B (a K-major B operand)
 using Cfg256K = TileConfig<256, 4, false, true>;
 using Cfg128K = TileConfig<128, 6, false, true>;
@@ -63,8 +67,9 @@ using CfgPair384K = TileConfig<384, 4, true, true, 2>;
 // memory limits either to one CTA per SM, and both stay far below the SM's
 // thread and register limits at that occupancy
 static_assert(CfgWide::SMEM_BYTES > 232448 / 2 && CfgPair::SMEM_BYTES > 232448 / 2 &&
-                  CfgPair384::SMEM_BYTES > 232448 / 2 && CfgWide::THREADS <= 384 && CfgPair::THREADS <= 384 &&
-                  CfgPair384::THREADS <= 384,
+                  CfgPair384::SMEM_BYTES > 232448 / 2 && CfgPair320::SMEM_BYTES > 232448 / 2 &&
+                  CfgWide::THREADS <= 384 && CfgPair::THREADS <= 384 && CfgPair384::THREADS <= 384 &&
+                  CfgPair320::THREADS <= 384,
               "the wide pair kernel fits wherever the 256 x 256 pair kernel fits");
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -141,6 +146,16 @@ int32_t auto_tile_n(int64_t M, int64_t N, int32_t num_sms, bool a_row_classes) {
     return wide ? 256 : 128;
 }
 
+// N from 257 to 384 in one tile column of CTA pairs (256 x 320 tiles, or
+// 256 x 384 past 320 columns or for a column-major B) once those tiles fill
+// every pair: A is read once, and each SM receives half of B per k-block.
+// Measured on GB300 at 65536 x 257 x 4093 (lda 4093, beta = 0.5): 182 us in
+// 256 x 320 pairs, 185 us in 256 x 384 pairs, 218 us in one-CTA 128 x 320
+// tiles; with A aligned at 58368 rows, 135 against 169 us.
+bool auto_narrow_pair(int64_t M, int64_t N, int32_t num_sms) {
+    return N > 256 && N <= 384 && ceil_div(M, 256) >= num_sms / 2;
+}
+
 // CTA pairs (256 x 256 tiles) pay off once there is at least a full wave of
 // pair tiles and the last column band wastes at most a fifth of its width;
 // with a long K (3072 or more), also when the pair tiles keep four fifths
@@ -215,7 +230,8 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     if (st != MPGEMM_OK) return st;
     if (num_sms <= 0) return MPGEMM_ERR_INVALID_VALUE;
     if (opt.tile_n == 512 && opt.tile_m == 128) return MPGEMM_ERR_INVALID_VALUE;   // 512 wide: pairs only
-    if (opt.tile_n == 320 && opt.tile_m == 256) return MPGEMM_ERR_INVALID_VALUE;   // 320 wide: one CTA
+    // 256 x 320 pairs read B in narrow row-major boxes
+    if (opt.tile_n == 320 && opt.tile_m == 256 && opt.b_col_major) return MPGEMM_ERR_INVALID_VALUE;
     if (opt.tile_n == 384 && opt.tile_m == 128) return MPGEMM_ERR_INVALID_VALUE;   // 384 wide: pairs only
     mpgemm_plan_t p;
     std::memset(&p, 0, sizeof(p));
@@ -231,7 +247,8 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
         return MPGEMM_OK;
     }
     p.stage_b = (opt.force_staging || !aligned16(B, ldb, 2)) ? 1 : 0;
-    const bool pair = opt.tile_n == 512 || opt.tile_n == 384 ||
+    const bool narrow_pair = !opt.tile_m && !opt.tile_n && auto_narrow_pair(M, N, num_sms);
+    const bool pair = opt.tile_n == 512 || opt.tile_n == 384 || narrow_pair ||
                       (opt.tile_m ? (opt.tile_m == 256) : (!opt.tile_n && auto_pair(M, N, K, num_sms)));
     if (pair) {
         int64_t pair_units = num_sms / 2;
@@ -240,9 +257,14 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
         pair_units = std::max<int64_t>(1, pair_units);
         const bool wide = opt.tile_n == 512 || (!opt.tile_m && !opt.tile_n && auto_wide(M, N, K, pair_units));
         p.tile_m = 256;
-        p.tile_n = opt.tile_n == 384 ? 384 : (wide ? 512 : 256);
-        p.stages = p.tile_n == 384 ? CfgPair384::STAGES : (wide ? CfgWide::STAGES : CfgPair::STAGES);
-        p.smem_bytes = p.tile_n == 384 ? CfgPair384::SMEM_BYTES : (wide ? CfgWide::SMEM_BYTES : CfgPair::SMEM_BYTES);
+        p.tile_n = (opt.tile_n == 384 || opt.tile_n == 320) ? opt.tile_n : (wide ? 512 : 256);
+        if (narrow_pair) p.tile_n = (N <= 320 && !opt.b_col_major) ? 320 : 384;
+        p.stages = p.tile_n == 384   ? CfgPair384::STAGES
+                   : p.tile_n == 320 ? CfgPair320::STAGES
+                                     : (wide ? CfgWide::STAGES : CfgPair::STAGES);
+        p.smem_bytes = p.tile_n == 384   ? CfgPair384::SMEM_BYTES
+                       : p.tile_n == 320 ? CfgPair320::SMEM_BYTES
+                                         : (wide ? CfgWide::SMEM_BYTES : CfgPair::SMEM_BYTES);
     } else {
         // (A is read in row classes below when its rows break the 16-byte rule)
         const bool row_classes = !aligned16(A, lda, 2) && !opt.force_staging && !opt.b_col_major;
@@ -461,12 +483,14 @@ struct MapCache {
 };
 
 // Row-major FP16 matrix rows x cols with pitch ld (elements), boxes of
-// box_cols x box_rows, 128-byte swizzle, zeros outside the matrix, 128-byte
+// box_cols x box_rows, 128-byte swizzle (or `swizzle`), zeros outside the matrix, 128-byte
 // L2 promotion (the box rows are 128 bytes; 256-byte promotion was 8 % slower
 // on 65536 x 257 x 4093 and made no difference on square shapes).
 bool encode_f16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
-                uint32_t box_cols, uint32_t box_rows, MapCache* cache = nullptr) {
-    const uint64_t key[6] = {16, reinterpret_cast<uintptr_t>(base), static_cast<uint64_t>(rows),
+                uint32_t box_cols, uint32_t box_rows, MapCache* cache = nullptr,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+    const uint64_t key[6] = {16 | (static_cast<uint64_t>(swizzle) << 8), reinterpret_cast<uintptr_t>(base),
+                             static_cast<uint64_t>(rows),
                              static_cast<uint64_t>(cols), static_cast<uint64_t>(ld),
                              (static_cast<uint64_t>(box_cols) << 32) | box_rows};
     if (cache && cache->find(key, map)) return true;
@@ -477,7 +501,7 @@ bool encode_f16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, 
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const bool ok = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     if (ok && cache) cache->put(key, *map);
     return ok;
@@ -568,6 +592,7 @@ cudaError_t prepare_kernels() {
     if (e == cudaSuccess) e = set_smem_attr<CfgWideK>();
     if (e == cudaSuccess) e = set_smem_attr<CfgPair384>();
     if (e == cudaSuccess) e = set_smem_attr<CfgPair384K>();
+    if (e == cudaSuccess) e = set_smem_attr<CfgPair320>();
     return e;
 }
 
@@ -629,6 +654,14 @@ void encode_c(const mpgemm_plan_t& plan, float* C, int64_t M, int64_t N, int64_t
     if (encode_f32_store(&maps->c, C, M, N, ldc, cache)) gp->c_tma = 1;
 }
 
+// The narrow B boxes of 256 x 320 pair tiles (32 columns of 64 K-rows, 64-byte
+// swizzle: the last 64-column part, half per CTA); nothing for other tiles.
+bool encode_b_tail(const mpgemm_plan_t& plan, const void* b_use, int64_t K, int64_t N, int64_t ldb_use,
+                   TensorMaps* maps, MapCache* cache = nullptr) {
+    if (plan.tile_m != 256 || plan.tile_n != 320) return true;
+    return encode_f16(&maps->b_tail, b_use, K, N, ldb_use, 32, 64, cache, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 GemmParams make_params(const mpgemm_plan_t& plan, int64_t M, int64_t N, int64_t K, float alpha,
                        float beta, float* C, int64_t ldc, int32_t* status, uint64_t wait_limit_ns,
                        int32_t test_stall, int32_t keep_a) {
@@ -676,6 +709,7 @@ cudaError_t launch_plan(const mpgemm_plan_t& plan, bool b_col_major, int max_clu
         if (plan.tile_n == 384)
             return b_col_major ? launch_tc<CfgPair384K>(grid, ta, tb, gp, stream)
                                : launch_tc<CfgPair384>(grid, ta, tb, gp, stream);
+        if (plan.tile_n == 320) return launch_tc<CfgPair320>(grid, ta, tb, gp, stream);
         return b_col_major ? launch_tc<CfgPairK>(grid, ta, tb, gp, stream)
                            : launch_tc<CfgPair>(grid, ta, tb, gp, stream);
     }
@@ -991,6 +1025,7 @@ mpgemm_status_t mpgemm_run_ex(mpgemm_handle_t h, mpgemm_b_layout_t b_layout, int
                                 keep_a_operand(plan, h->opt.l2_keep));
     TensorMaps ta;
     if (!encode_a(plan, a_use, lda_use, M, K, &ta, &gp, &h->map_cache)) return MPGEMM_ERR_CUDA;
+    if (!encode_b_tail(plan, b_use, K, N, ldb_use, &ta, &h->map_cache)) return MPGEMM_ERR_CUDA;
     encode_c(plan, C, M, N, ldc, beta, h->opt.c_store, &ta, &gp, &h->map_cache);
     gp.acc16 = h->opt.acc16;
     if (launch_plan(plan, b_col, h->max_clusters, ta, tb, gp, stream) != cudaSuccess) {
@@ -1236,6 +1271,7 @@ extern "C" mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K, f
                                 keep_a_operand(plan, 0));
     TensorMaps ta;
     if (!encode_a(plan, a_use, lda_use, M, K, &ta, &gp)) return MPGEMM_ERR_CUDA;
+    if (!encode_b_tail(plan, b_use, K, N, ldb_use, &ta)) return MPGEMM_ERR_CUDA;
     encode_c(plan, C, M, N, ldc, beta, 0, &ta, &gp);
     if (launch_plan(plan, false, d.max_clusters, ta, tb, gp, stream) != cudaSuccess) {
         cudaGetLastError();

@@ -170,27 +170,36 @@ def test_tile_selection_and_grid():
     assert (p["tile_m"], p["tile_n"]) == (256, 512)
     with pytest.raises(mp.MpgemmError):
         _plan(tile_m=128, tile_n=512)
-    # N = 257 would waste half of the last column band: single CTAs, one
-    # 320-wide tile column (A read once per row block, three 56 KB stages)
+    # N = 257 would waste half of the last column band: one tile column of
+    # 256 x 320 CTA pairs (A read once per row block, five 36 KB stages, A in
+    # 8 row classes of 32 pair tiles each)
     p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257, beta=0.5)
-    assert (p["tile_m"], p["tile_n"]) == (128, 320) and p["tiles"] == 512 and p["stages"] == 3
-    assert p["split_tiles"] == 0 and p["smem_bytes"] <= 232448
-    # with A aligned, 3.4 waves of 320-wide tiles cost more than seven waves of
-    # 256-wide ones; three waves cost less than six
-    p = _plan(M=65536, N=257, K=4096, lda=4096, ldb=264, ldc=257, beta=0.5)
-    assert p["tile_n"] == 256 and p["a_classes"] == 0
+    assert (p["tile_m"], p["tile_n"]) == (256, 320) and p["tiles"] == 256 and p["stages"] == 5
+    assert p["a_classes"] == 8 and p["split_tiles"] == 0 and p["smem_bytes"] <= 232448
     p = _plan(M=58368, N=257, K=4096, lda=4096, ldb=264, ldc=257, beta=0.5)
-    assert p["tile_n"] == 320 and p["tiles"] == 456
-    # N = 321 needs two tile columns anyway: 256 wide; too few row blocks: not 320
+    assert (p["tile_m"], p["tile_n"]) == (256, 320) and p["tiles"] == 228
+    # fewer rows than one full wave of pair tiles: one-CTA tiles; with A
+    # aligned, a wave of 320-wide tiles (1.9 waves of 256-wide ones) costs
+    # more than one wave of 256-wide tiles, and less than two
+    p = _plan(M=9600, N=257, K=4096, lda=4096, ldb=264, ldc=257, beta=0.5)
+    assert (p["tile_m"], p["tile_n"]) == (128, 256) and p["a_classes"] == 0
+    p = _plan(M=19200, N=257, K=4096, lda=4096, ldb=264, ldc=257, beta=0.5)
+    assert (p["tile_m"], p["tile_n"], p["stages"]) == (128, 320, 3) and p["tiles"] == 150
+    # N = 321: one tile column of 256 x 384 pairs; too few row blocks: not 320
     p = _plan(M=65536, N=321, K=4093, lda=4093, ldb=321, ldc=321)
-    assert p["tile_n"] == 256
+    assert (p["tile_m"], p["tile_n"]) == (256, 384)
     p = _plan(M=1000, N=300, K=1000, lda=1000, ldb=300, ldc=300)
     assert p["tile_n"] == 128
-    # 320 wide on request (one CTA per tile only), never split in half-width items
+    # 320 wide on request (one CTA per tile, or a pair with tile_m 256), never
+    # split in half-width items
     p = _plan(M=5000, N=1000, K=700, lda=700, ldb=1000, ldc=1000, tile_n=320)
     assert (p["tile_m"], p["tile_n"]) == (128, 320) and p["tiles"] == 40 * 4 and p["split_tiles"] == 0
+    p = _plan(M=5000, N=1000, K=700, lda=700, ldb=1000, ldc=1000, tile_m=256, tile_n=320)
+    assert (p["tile_m"], p["tile_n"], p["stages"]) == (256, 320, 5) and p["tiles"] == 20 * 4
+    assert p["split_tiles"] == 0
+    # the 256 x 320 pair reads B in narrow row-major boxes: not for a column-major B
     with pytest.raises(mp.MpgemmError):
-        _plan(tile_m=256, tile_n=320)
+        _plan(tile_m=256, tile_n=320, ldb=617, b_col_major=True)
     # forced pairs with a CTA cap: the grid stays even
     p = _plan(M=1000, N=800, K=64, lda=64, ldb=800, ldc=800, tile_m=256, max_ctas=5)
     assert p["tile_m"] == 256 and p["grid"] == 4 and p["tiles"] == 4 * 4
@@ -237,20 +246,23 @@ def test_tile_selection_and_grid():
         _plan(tile_m=64)
 
 
-@pytest.mark.parametrize("N,K,lda,expect65536,expect58368", [
-    (256, 4093, 4093, 256, 256),   # one 256-wide column covers N
-    (257, 4093, 4093, 320, 320),   # row classes: 4 waves x 1.6 < 7 and 3 x 1.6 < 6
-    (320, 4093, 4093, 320, 320),
-    (257, 4096, 4096, 256, 320),   # aligned: 4 x 1.9 > 7, 3 x 1.9 < 6
-    (320, 4096, 4096, 256, 320),
-    (321, 4093, 4093, 256, 256),   # past 320: two columns either way
+@pytest.mark.parametrize("M,N,lda,b_col,expect", [
+    (65536, 256, 4093, False, (128, 256)),   # one 256-wide column covers N: one-CTA tiles
+    (65536, 257, 4093, False, (256, 320)),   # the tall-skinny workload: 256 x 320 pairs
+    (58368, 320, 4096, False, (256, 320)),
+    (65536, 321, 4096, False, (256, 384)),   # past 320: 256 x 384 pairs
+    (65536, 384, 4096, False, (256, 384)),
+    (65536, 300, 4096, True, (256, 384)),    # column-major B: the 384-wide pair
+    (65536, 385, 4093, False, (128, 256)),   # past 384: two 256-wide columns of one-CTA tiles
+    (19456, 257, 4093, False, (256, 320)),   # 76 pair tiles: every pair busy
+    (19200, 257, 4093, False, (128, 320)),   # 75: the one-CTA rule (row classes: 1.6 waves of 320 < 2)
+    (9600, 257, 4096, False, (128, 256)),    # aligned A: 1.9 waves of 320 against one wave of 256
 ])
-def test_320_wide_rule_boundaries(N, K, lda, expect65536, expect58368):
-    for M, expect in ((65536, expect65536), (58368, expect58368)):
-        p = _plan(M=M, N=N, K=K, lda=lda, ldb=N + 8, ldc=N, beta=0.5)
-        assert p["tile_n"] == expect, (M, N, lda)
-        if expect == 320:
-            assert p["tile_m"] == 128 and p["split_tiles"] == 0 and p["stages"] == 3
+def test_narrow_tile_column_rules(M, N, lda, b_col, expect):
+    p = _plan(M=M, N=N, K=4093, lda=lda, ldb=4093 if b_col else N + 8, ldc=N, beta=0.5, b_col_major=b_col)
+    assert (p["tile_m"], p["tile_n"]) == expect, (M, N, lda)
+    if expect[1] in (320, 384):
+        assert p["split_tiles"] == 0 and p["n_tiles"] == 1
 
 
 @pytest.mark.parametrize("M,K,beta,splits", [

@@ -435,6 +435,36 @@ def test_cta_pair_384_wide_tiles(mp, M, N, K, lda, ldb, ldc, beta, max_ctas):
         check_full(h, ops)
 
 
+PAIR320_SHAPES = [  # (M, N, K, lda, ldb, ldc, beta, max_ctas): 256 x 320 pair tiles, narrow last part
+    (256, 320, 64, 64, 320, 320, 0.0, 0),       # one full tile
+    (256, 257, 617, 617, 257, 257, 0.5, 0),     # one column past 256: the 64-column part
+    (1000, 300, 700, 700, 300, 301, 1.0, 4),    # two pairs walk 4 tiles through the one accumulator
+    (511, 700, 129, 129, 700, 700, -0.5, 0),    # three tile columns, the last 60 wide (one 128 unit)
+    (1300, 1100, 333, 335, 1103, 1101, 0.75, 6),  # A in row classes, B staged, C per lane
+    (700, 290, 1000, 1002, 290, 290, 0.0, 0),   # 4 row classes, columns 256..289 in the narrow part
+]
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,beta,max_ctas", PAIR320_SHAPES)
+def test_cta_pair_320_wide_tiles(mp, M, N, K, lda, ldb, ldc, beta, max_ctas):
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_M, 256)
+        h.set_option(mp.Option.TILE_N, 320)
+        h.set_option(mp.Option.MAX_CTAS, max_ctas)
+        ops = workloads.make_operands(M, N, K, lda=lda, ldb=ldb, ldc=ldc, alpha=1.5, beta=beta,
+                                      c_dist="normal" if beta else "zeros", seed=M + 7 * N + K)
+        check_full(h, ops)
+
+
+def test_cta_pair_320_integer_bitwise(mp):
+    # every column of the narrow part exact: 288 columns, A in 8 row classes
+    ops = workloads.make_operands(777, 288, 1021, lda=1021, dist="int3", dist_b="int2", seed=90)
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_M, 256)
+        h.set_option(mp.Option.TILE_N, 320)
+        check_full(h, ops, exact=True)
+
+
 @pytest.mark.parametrize("M,N,K", [(600, 100, 300), (600, 640, 300), (700, 129, 129)])
 def test_cta_pair_tiles_trimmed_to_valid_columns(mp, M, N, K):
     # a pair tile's columns are cut to the 128-column units below N (N = 128
@@ -448,11 +478,13 @@ def test_cta_pair_tiles_trimmed_to_valid_columns(mp, M, N, K):
                        exact=True)
 
 
-def test_tall_skinny_workload_in_256x384_pairs(mp):
+@pytest.mark.parametrize("tile_n", [320, 384])
+def test_tall_skinny_workload_in_pairs(mp, tile_n):
     ops = workloads.workload_operands(4)
     I, J = workloads.workload_sample(4)
     with mp.Handle() as h:
-        h.set_option(mp.Option.TILE_N, 384)
+        h.set_option(mp.Option.TILE_M, 256)
+        h.set_option(mp.Option.TILE_N, tile_n)
         check_sampled(h, ops, I, J)
 
 
