@@ -297,6 +297,25 @@ def parse_clock_samples(text: str):
 
 # ----------------------------------------------------------------------------- CPU oracle timing
 
+def cpu_model() -> str:
+    """The host CPU as the OS names it (lscpu's model name, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def time_oracle_sample(w, ops, target_seconds: float, max_elements: int, seed: int):
     """Time the oracle on seeded sampled elements of the workload; returns
     (TFLOP/s-equivalent, seconds, elements, threads)."""
@@ -655,6 +674,7 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         v, dt, n, threads = time_oracle_sample(w, ops, args.cpu_seconds, 1 << 20, w.seed_base + 5)
         cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "cpu_model": cpu_model(),
                "sample": f"{n} seeded elements of C (K = {w.K} MACs each) in {dt:.2f} s"}
 
     handle.close()
@@ -995,7 +1015,7 @@ def run_reference(args):
         "data": "synthetic (seeded)",
         "config": workload_config(w, world),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "cpu_model": cpu_model(), "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,

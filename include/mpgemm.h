@@ -76,11 +76,15 @@ typedef enum {
 
 /* Create a handle bound to the current CUDA device. Fails with
  * MPGEMM_ERR_UNSUPPORTED_DEVICE unless that device is compute capability
- * 10.3 (GB300). *out is set to NULL on failure. */
+ * 10.3 (GB300). *out is set to NULL on failure. (No page defines this call:
+ * the pages' gate entry point takes no handle. The handle holds the
+ * stream-ordered workspace, the encoded tensor maps and the device status
+ * word.) */
 mpgemm_status_t mpgemm_create(mpgemm_handle_t* out);
 
 /* Release the handle and its workspace. NULL is accepted. Work enqueued
- * with the handle must have completed (synchronise its stream first). */
+ * with the handle must have completed (synchronise its stream first). (No
+ * page defines this call: it ends the lifetime mpgemm_create starts.) */
 mpgemm_status_t mpgemm_destroy(mpgemm_handle_t h);
 
 /* C = alpha*A*B + beta*C on device memory (see the conventions above).
@@ -131,7 +135,8 @@ mpgemm_status_t mpgemm_run_host(mpgemm_handle_t h, int64_t M, int64_t N, int64_t
                                 float beta, float* C, int64_t ldc, void* stream);
 
 /* Synchronise `stream`, then report the state of the handle's device status
- * word: MPGEMM_OK, or MPGEMM_ERR_DEVICE_TIMEOUT if a bounded device wait gave
+ * word (no page defines this call: it reports the bounded device waits this
+ * library adds): MPGEMM_OK, or MPGEMM_ERR_DEVICE_TIMEOUT if a bounded device wait gave
  * up since the last report (the report is cleared), or MPGEMM_ERR_CUDA if
  * the synchronisation itself failed. If info is not NULL it receives four
  * integers describing the last timeout: {code, role, block, detail}
@@ -287,7 +292,8 @@ mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K,
  * current device is compute capability 10.3. */
 mpgemm_status_t mpgemm_probe_mma_rate(int32_t ctas, int32_t mmas, uint64_t* out, void* stream);
 
-/* A static description of a status code. Never NULL. */
+/* A static description of a status code. Never NULL. (No page defines this
+ * call: it names the codes above.) */
 const char* mpgemm_status_string(mpgemm_status_t s);
 
 #ifdef __cplusplus
