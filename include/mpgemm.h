@@ -170,7 +170,7 @@ typedef enum {
                                      occupy at most a quarter of the SMs and K has 32 or more
                                      64-wide blocks (half of the SMs and 16 blocks when
                                      beta == 1), or at most an eighth of the SMs and K has 8
-                                     or more blocks (beta != 1; up to five slices), each
+                                     or more blocks (up to five slices), each
                                      tile's K range is cut into slices whose
                                      partial products are added into C (after C = beta*C), so
                                      results may differ in the last bits from run to run;
@@ -251,18 +251,21 @@ mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha,
  * allocation would fail), and code that cannot own a handle's lifetime. The pages have no counterpart of this
  * entry point: it exists for those callers only.
  *
- * Operands that need an aligned staging copy (see the conventions above:
- * an unaligned B, or an unaligned A that cannot be read in row classes) are
+ * B is row-major, so an unaligned A is always read in row classes and never
+ * copied. A B whose base or row pitch is not a multiple of 16 bytes is
  * staged into one fixed, file-scope device array of
  * MPGEMM_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU which loads this
- * library holds until the process exits. If the staged copies of
- * A and B together need more than that, the call returns
- * MPGEMM_ERR_SCRATCH_LIMIT and enqueues nothing; aligned operands need no
- * scratch and have no size limit beyond mpgemm_run's.
+ * library holds until the process exits: K rows of round_up(N, 8) halves,
+ * rounded up to 256 bytes, at most 16 MiB (e.g. K = 8192 with N up to 1024).
+ * Beyond that the call returns MPGEMM_ERR_SCRATCH_LIMIT and enqueues
+ * nothing; an aligned B needs no scratch and has no size limit beyond
+ * mpgemm_run's.
  *
  * The first call on each device (with that device current) looks up the
  * array's device address and sets the kernels' shared-memory limits; make
- * that first call before any stream capture. All calls share the one array
+ * that first call before any stream capture. If that set-up fails (for
+ * example on a CUDA error left pending by other code), the call returns the
+ * error and the next call tries the set-up again. All calls share the one array
  * and the work is stream-ordered only: calls whose work overlaps on the GPU
  * (different streams, or several host threads) race on the scratch and must
  * be serialised by the caller. A bounded device wait that gives up is

@@ -312,12 +312,14 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
             splits = opt.split_k;
         else if (beta == 1.0f ? (p.tiles * 2 <= units && k_blocks >= 16) : (p.tiles * 4 <= units && k_blocks >= 32))
             splits = std::min<int64_t>(k_blocks / 8, units / p.tiles);
-        else if (beta != 1.0f && p.tiles * 8 <= units && k_blocks >= 8)
+        else if (p.tiles * 8 <= units && k_blocks >= 8)
             // very few tiles of a short K: five slices of two or more k-blocks
-            // (measured with L2 flushed: 500 x 256 x 1024, 8 tiles, 12.3 ->
-            // 10.2 us; 300 x 200 x 640, 6 tiles, 10.7 -> 10.2 us; 200 x 136 x
-            // 617, 16 tiles, 12.5 -> 11.6 us; 40 tiles of 611 x 613 x 617
-            // slowed from 14.3 to 18-20 us, so not past an eighth of the SMs)
+            // (measured with L2 flushed and beta != 1: 500 x 256 x 1024, 8
+            // tiles, 12.3 -> 10.2 us; 300 x 200 x 640, 6 tiles, 10.7 -> 10.2
+            // us; 200 x 136 x 617, 16 tiles, 12.5 -> 11.6 us; 40 tiles of 611 x
+            // 613 x 617 slowed from 14.3 to 18-20 us, so not past an eighth of
+            // the SMs). With beta == 1 the slices need no pass over C first,
+            // so the split only costs less.
             splits = std::min<int64_t>(5, k_blocks / 2);
         splits = std::max<int64_t>(1, std::min<int64_t>(splits, k_blocks));
         if (splits > 1) splits = ceil_div(k_blocks, ceil_div(k_blocks, splits));  // no empty slice
@@ -1173,8 +1175,8 @@ constexpr int kNoAllocMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocStatusBytes + kNoAllocScratchBytes];
 
 struct NoAllocDevice {
-    std::once_flag once;
-    mpgemm_status_t status = MPGEMM_ERR_CUDA;
+    std::mutex mu;
+    bool ready = false;                // set once a set-up has succeeded
     unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
     int num_sms = 0;
     int max_clusters = 0;
@@ -1182,31 +1184,32 @@ struct NoAllocDevice {
 
 NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];
 
-// Runs once per device, with that device current.
-void noalloc_setup(NoAllocDevice& d, int dev) {
+// With that device current: look up the scratch array's device address and
+// set the kernels' attributes. Called until it succeeds once per device (a
+// failure, e.g. an error another component left pending, is returned and
+// the next call tries again).
+mpgemm_status_t noalloc_setup(NoAllocDevice& d, int dev) {
+    std::lock_guard<std::mutex> lock(d.mu);
+    if (d.ready) return MPGEMM_OK;
     int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         cudaGetLastError();
-        d.status = MPGEMM_ERR_CUDA;
-        return;
+        return MPGEMM_ERR_CUDA;
     }
-    if (major != 10 || minor != 3) {
-        d.status = MPGEMM_ERR_UNSUPPORTED_DEVICE;
-        return;
-    }
+    if (major != 10 || minor != 3) return MPGEMM_ERR_UNSUPPORTED_DEVICE;
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr ||
         !encode_fn() || prepare_kernels() != cudaSuccess) {
         cudaGetLastError();
-        d.status = MPGEMM_ERR_CUDA;
-        return;
+        return MPGEMM_ERR_CUDA;
     }
     d.scratch = static_cast<unsigned char*>(ptr);
     d.num_sms = sms;
     d.max_clusters = max_pair_clusters();
-    d.status = MPGEMM_OK;
+    d.ready = true;
+    return MPGEMM_OK;
 }
 
 }  // namespace
@@ -1222,8 +1225,7 @@ extern "C" mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K, f
     }
     if (dev < 0 || dev >= kNoAllocMaxDevices) return MPGEMM_ERR_CUDA;
     NoAllocDevice& d = g_noalloc_devices[dev];
-    std::call_once(d.once, noalloc_setup, std::ref(d), dev);
-    if (d.status != MPGEMM_OK) return d.status;
+    if (mpgemm_status_t s0 = noalloc_setup(d, dev); s0 != MPGEMM_OK) return s0;
     if (!bind_context(dev)) return MPGEMM_ERR_CUDA;
 
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
@@ -1246,17 +1248,14 @@ extern "C" mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K, f
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;
     }
+    // (B is row-major here, so an unaligned A is read in row classes and
+    // never staged: only B's copy uses the scratch)
+    if (plan.stage_a) return MPGEMM_ERR_INVALID_VALUE;
     const void* a_use = A;
     const void* b_use = B;
-    int64_t lda_use = lda, ldb_use = ldb;
+    const int64_t lda_use = lda;
+    int64_t ldb_use = ldb;
     unsigned char* ws = d.scratch + kNoAllocStatusBytes;
-    if (plan.stage_a) {
-        lda_use = round_up(K, 8);
-        stage_rows_u16<<<grid_for(M * ceil_div(K, 8), d.num_sms), 256, 0, stream>>>(
-            static_cast<const uint16_t*>(A), lda, reinterpret_cast<uint16_t*>(ws), lda_use, M, K);
-        a_use = ws;
-        ws += round_up(M * lda_use * 2, 256);
-    }
     if (plan.stage_b) {
         ldb_use = round_up(N, 8);
         stage_rows_u16<<<grid_for(K * ceil_div(N, 8), d.num_sms), 256, 0, stream>>>(

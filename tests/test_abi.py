@@ -270,7 +270,7 @@ def test_narrow_tile_column_rules(M, N, lda, b_col, expect):
     (20 * 128, 640, 0.0, 1),   # 20 tiles: past an eighth
     (128, 7 * 64, 0.0, 1),     # 7 k-blocks: too short
     (128, 8 * 64, 0.0, 4),     # 8 k-blocks: four slices of two
-    (19 * 128, 640, 1.0, 1),   # beta == 1 keeps its own rule (16 k-blocks at least)
+    (19 * 128, 640, 1.0, 5),   # beta == 1: no pass over C first, the same short-K rule
     (19 * 128, 640, 0.5, 5),   # any other beta: C = beta * C first, then the slices
 ])
 def test_short_k_split_rule(M, K, beta, splits):

@@ -84,6 +84,10 @@ def _draw(gen: torch.Generator, shape, dist: str) -> torch.Tensor:
         return torch.ones(shape, dtype=torch.float32)
     if dist == "zeros":
         return torch.zeros(shape, dtype=torch.float32)
+    if dist == "subnormal":          # integers in [-1023, 1023] times 2^-24: FP16 subnormals (or 0)
+        return torch.randint(-1023, 1024, shape, generator=gen).to(torch.float32) * 2.0 ** -24
+    if dist == "int3_x8192":         # integers in [-3, 3] times 2^13
+        return torch.randint(-3, 4, shape, generator=gen).to(torch.float32) * 8192.0
     if dist == "edge":               # magnitudes near the top of the FP16 range
         mag = 32768.0 + torch.rand(shape, generator=gen, dtype=torch.float32) * 32736.0
         sign = torch.randint(0, 2, shape, generator=gen).to(torch.float32) * 2.0 - 1.0
