@@ -123,6 +123,9 @@ struct GemmParams {
                             //    TMA reduce-adds of split-K slices; one row class, C and ldc
                             //    16-byte aligned, N a multiple of 4
     int32_t acc16;          // 1: FP16 accumulators (the study variant; the product path is FP32)
+    int32_t overlap_prepass;  // 1: launched right after this library's pass over C (C = beta * C
+                              //    before split-K slices add into it): only the epilogue warps,
+                              //    which write C, wait for it; the loads and MMAs start at once
 };
 
 enum : int32_t { kRoleLoad = 1, kRoleMma = 2, kRoleEpilogue = 3 };
@@ -594,7 +597,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // memory. Every thread waits here until that kernel has completed and
     // its writes are visible; the next kernel may begin its own setup now.
     ptx::griddep_launch_dependents();
-    ptx::griddep_wait();
+    // (after the library's own pass over C, which itself started only once
+    // everything before it in the stream had completed, A and B are ready:
+    // only C has to wait for that pass)
+    if (!p.overlap_prepass || (warp >= 2 && warp < 2 + Cfg::EPI_WARPS)) ptx::griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ loads

@@ -411,7 +411,10 @@ __global__ void stage_rows_u16(const uint16_t* __restrict__ src, int64_t lds,
 }
 
 // C = beta * C over M x N (beta == 0 writes zeros without reading C).
+// The GEMM launched after it (programmatic dependent launch) may start its
+// loads and MMAs at once; its epilogue waits for this pass to complete.
 __global__ void scale_c(float* __restrict__ C, int64_t ldc, int64_t M, int64_t N, float beta) {
+    ptx::griddep_launch_dependents();
     const int64_t total = M * N;
     for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -689,6 +692,8 @@ GemmParams make_params(const mpgemm_plan_t& plan, int64_t M, int64_t N, int64_t 
     gp.wait_limit_ns = wait_limit_ns;
     gp.test_stall = test_stall;
     gp.keep_a = keep_a;
+    // split-K slices after the pass that applies beta (launch_plan)
+    gp.overlap_prepass = (plan.k_splits > 1 && beta != 1.0f) ? 1 : 0;
     return gp;
 }
 
