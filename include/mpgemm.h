@@ -190,7 +190,7 @@ typedef enum {
                                      Capstone 4", "Common failures"). K is never split then: the
                                      whole K range accumulates in one FP16 accumulator. Not for
                                      production use. */
-    MPGEMM_OPT_REPRODUCIBLE = 12  /* 0 = default: a call may split K (see SPLIT_K), and the
+    MPGEMM_OPT_REPRODUCIBLE = 12, /* 0 = default: a call may split K (see SPLIT_K), and the
                                      slices then add into C in the order they arrive, so
                                      results may differ in the last bits between identical
                                      calls (always within the stated tolerance; exact inputs
@@ -200,7 +200,20 @@ typedef enum {
                                      order: the two MMA threads of a 256 x 512 CTA-pair tile
                                      own disjoint columns of the accumulator, and those of a
                                      256 x 256 tile hand alternate k-blocks to each other
-                                     strictly in turn). */
+                                     strictly in turn). The stream-K walk (STREAM_K) is
+                                     allowed: it, too, sums in a fixed order. */
+    MPGEMM_OPT_STREAM_K = 13      /* 0 = automatic (default): CTA-pair tiles of 320 or 384
+                                     columns (N from 257 to 384) that leave the last wave of
+                                     pairs partly idle walk the problem as one contiguous range
+                                     of k-blocks per pair instead of whole tiles (stream-K,
+                                     Osama et al., 2023): every pair gets the same number of
+                                     k-blocks, and a tile cut between two ranges is written
+                                     twice in a fixed order (the later k-blocks with beta * C
+                                     first, then the earlier ones added on), so identical calls
+                                     still give identical bits; 1 = never; 2 = whenever the
+                                     call runs on CTA pairs of 256 to 384 columns with at least
+                                     one tile per pair (not with FP16 accumulators, nor in
+                                     mpgemm_run_noalloc) */
 } mpgemm_option_t;
 
 /* Set an option. Unknown options or out-of-range values return
@@ -234,6 +247,8 @@ typedef struct {
     int32_t a_classes;      /* 0: A is read through one plain tensor map (aligned, or staged);
                                P >= 1: A's rows are not 16-byte aligned and are read in P
                                classes of rows i = r (mod P) instead of being copied */
+    int32_t sk_ranges;      /* 0, or the stream-K walk's ranges of k-blocks (one per CTA pair;
+                               see MPGEMM_OPT_STREAM_K) */
 } mpgemm_plan_t;
 
 mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha,

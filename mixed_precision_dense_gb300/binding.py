@@ -39,6 +39,7 @@ class Option(enum.IntEnum):
     C_STORE = 10
     ACCUMULATOR = 11
     REPRODUCIBLE = 12
+    STREAM_K = 13
 
 
 class BLayout(enum.IntEnum):
@@ -60,7 +61,7 @@ class Plan(ctypes.Structure):
                 ("raster_group", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("last_k_valid", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
                 ("split_tiles", ctypes.c_int32), ("items", ctypes.c_int64),
-                ("k_splits", ctypes.c_int32), ("a_classes", ctypes.c_int32)]
+                ("k_splits", ctypes.c_int32), ("a_classes", ctypes.c_int32), ("sk_ranges", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -126,6 +126,21 @@ struct GemmParams {
     int32_t overlap_prepass;  // 1: launched right after this library's pass over C (C = beta * C
                               //    before split-K slices add into it): only the epilogue warps,
                               //    which write C, wait for it; the loads and MMAs start at once
+    // Stream-K walk (sk_units > 0): the tiles' k-blocks, tile after tile in
+    // raster order, are cut into sk_ranges contiguous ranges of equal length
+    // (at least one tile's k-blocks each), one per persistent CTA (pair).
+    // A tile cut between ranges r and r + 1 is written twice, in a fixed
+    // order: range r + 1 does the tile's last k-blocks first and writes
+    // C = alpha * (their sum) + beta * C, then publishes sk_epoch in its
+    // flags; range r, whose last item holds the tile's first k-blocks, adds
+    // alpha * (their sum) onto that C after it has seen the flag.
+    int32_t sk_units;       // tiles * k_blocks (below 2^31), or 0
+    int32_t sk_ranges;
+    int32_t sk_len;         // sk_units / sk_ranges: ranges r < sk_units % sk_ranges hold one more
+    int32_t sk_rem;
+    int32_t sk_epoch;       // this call's flag value (never 0)
+    int32_t* sk_flags;      // [sk_ranges][CTAS][epilogue warps]: each epilogue warp publishes
+                            // its own rows and columns of the tile
 };
 
 enum : int32_t { kRoleLoad = 1, kRoleMma = 2, kRoleEpilogue = 3 };
@@ -177,9 +192,20 @@ struct TileConfig {
     static constexpr bool NARROW_TAIL = PAIR && TAIL_N == 64;
     // two accumulator buffers (the epilogue of tile i overlaps the MMAs of
     // tile i+1) when they fit in the 512 columns of tensor memory, else one,
-    // whose SUBS parts are handed back one by one
-    static constexpr int ACC_BUFS = 2 * BN <= 512 ? 2 : 1;
-    static constexpr int RELEASE_PARTS = ACC_BUFS == 1 ? SUBS : 1;
+    // whose SUBS parts are handed back one by one. A 320-wide pair tile
+    // (STAGGER) alternates between two layouts of its 256- and 64-column
+    // parts in the 512 columns, which overlap only by 64 columns each way:
+    //   even items: 256-column part at column 0,   64-column part at 256
+    //   odd items:  256-column part at column 256, 64-column part at 0
+    // Its epilogue hands back three parts in this order: the 64-column part,
+    // the first 64 columns of the 256-column part, and the other 192. The
+    // next item's 256-column MMAs wait only for the first of them, its
+    // 64-column MMAs for the second; the 192 columns are drained while the
+    // next item's MMAs run (one buffer of 320 columns made them wait for the
+    // whole 256-column part).
+    static constexpr bool STAGGER = NARROW_TAIL;
+    static constexpr int ACC_BUFS = (STAGGER || 2 * BN <= 512) ? 2 : 1;
+    static constexpr int RELEASE_PARTS = STAGGER ? 3 : (ACC_BUFS == 1 ? SUBS : 1);
     // B boxes (64 columns) per part held by one CTA: a pair CTA holds half
     // of every part's columns
     static constexpr int ATOMS_PER_PART = SUB_N / (PAIR ? 128 : 64);
@@ -194,10 +220,14 @@ struct TileConfig {
     // halve both (measured against four warps: 9-12 % less time per call
     // for GEMMs of one or two tiles per CTA)
     static constexpr int EPI_WARPS = 8;
+    // the stream-K walk (GemmParams::sk_units) is built into the CTA-pair
+    // shapes of at most 384 columns, those that run tall-skinny problems of
+    // a few waves of tiles
+    static constexpr bool STREAM_K = PAIR && BN <= 384;
     static constexpr int EPI_CHUNK_BYTES = 32 * 32 * 4;  // one warp's 32 x 32 FP32 chunk buffer
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_CHUNK_BYTES;
     // (allocations are powers of two: a 320-column accumulator takes 512)
-    static constexpr int TMEM_COLS = ACC_BUFS * BN <= 256 ? 256 : 512;
+    static constexpr int TMEM_COLS = (STAGGER || ACC_BUFS * BN > 256) ? 512 : 256;
     // full and empty per stage; accumulator full per buffer; accumulator
     // empty per buffer and part; k-block handed over per stage (KSPLIT)
     static constexpr int NUM_BARRIERS = 3 * STAGES + ACC_BUFS + ACC_BUFS * RELEASE_PARTS;
@@ -210,7 +240,8 @@ struct TileConfig {
     static constexpr int THREADS = 32 * (2 + EPI_WARPS + ISSUERS - 1);
     static_assert(BN == 128 || BN == 256 || BN == 320 || (PAIR && (BN == 384 || BN == 512)), "tile width");
     static_assert(!NARROW_TAIL || (!B_KMAJOR && ISSUERS == 2), "narrow last part: row-major B, one issuer per part");
-    static_assert(ACC_BUFS * BN <= TMEM_COLS, "accumulators fit the tensor memory allocated");
+    static_assert(STAGGER ? (BN == 320 && SUB_N == 256) : ACC_BUFS * BN <= TMEM_COLS,
+                  "accumulators fit the tensor memory allocated");
     static_assert(!PAIR || BN >= 256, "pair tiles are 256 x 256, 256 x 320, 256 x 384 or 256 x 512");
     static_assert(ISSUERS == 1 || ISSUERS == SUBS || (KSPLIT && SUBS == 1), "one issuer, one per part, or two by k-block");
     static_assert(SUB_N >= (PAIR ? 128 : 64) && ATOMS_PER_PART >= 1, "parts hold whole B boxes");
@@ -296,10 +327,50 @@ struct WorkItem {
     int32_t n0;      // first column
     int32_t width;   // columns: BN or BN / 2
     int32_t kb0, kb1;  // k-blocks [kb0, kb1)
+    int32_t sk;      // stream-K: kSkWhole, or kSkFirst (the tile's first k-blocks: added
+                     // onto C after the next range has written it) or kSkRest (its
+                     // other k-blocks, written first)
+    int32_t range;   // stream-K: the range the item belongs to
 };
+enum : int32_t { kSkWhole = 0, kSkFirst = 1, kSkRest = 2 };
 
-template <int BN>
+template <int BN, bool STREAM_K>
 __device__ __forceinline__ WorkItem work_item(const GemmParams& p, int32_t i) {
+    if (STREAM_K && p.sk_units > 0) {
+        // item j of range r (i = r + j * sk_ranges, as the CTAs walk)
+        const int32_t r = i % p.sk_ranges, j = i / p.sk_ranges;
+        const int32_t u0 = r * p.sk_len + min(r, p.sk_rem);
+        const int32_t u1 = u0 + p.sk_len + (r < p.sk_rem ? 1 : 0);
+        const int32_t t0 = u0 / p.k_blocks;
+        const int32_t t_last = (u1 - 1) / p.k_blocks;
+        // The range's tiles in order, except that a last piece holding a
+        // tile's first k-blocks (kSkFirst) goes before the range's last
+        // whole tile: its epilogue then runs while that tile's MMAs do, and
+        // every range ends on a whole tile's epilogue.
+        const int32_t n = t_last - t0 + 1;
+        const bool first_last = u1 - t_last * p.k_blocks < p.k_blocks;
+        const bool swap = first_last && (n >= 3 || (n == 2 && u0 == t0 * p.k_blocks));
+        const int32_t jn = (swap && j >= n - 2 && j < n) ? (2 * n - 3 - j) : j;
+        const int32_t t = t0 + jn;
+        WorkItem w;
+        w.range = r;
+        w.width = BN;
+        w.sk = kSkWhole;
+        if (t > t_last) {   // none: past the last column, skipped by every role
+            w.mb = 0;
+            w.n0 = p.N;
+            w.kb0 = w.kb1 = 0;
+            return w;
+        }
+        int32_t mb, nb;
+        tile_coords(p, t, mb, nb);
+        w.mb = mb;
+        w.n0 = nb * BN;
+        w.kb0 = t == t0 ? u0 - t0 * p.k_blocks : 0;
+        w.kb1 = t == t_last ? u1 - t_last * p.k_blocks : p.k_blocks;
+        w.sk = w.kb0 > 0 ? kSkRest : (w.kb1 < p.k_blocks ? kSkFirst : kSkWhole);
+        return w;
+    }
     if (p.k_splits > 1) {
         const int32_t t = i / p.k_splits;
         const int32_t slice = i - t * p.k_splits;
@@ -311,6 +382,8 @@ __device__ __forceinline__ WorkItem work_item(const GemmParams& p, int32_t i) {
         w.width = BN;
         w.kb0 = slice * p.kb_per_split;
         w.kb1 = min(w.kb0 + p.kb_per_split, p.k_blocks);
+        w.sk = kSkWhole;
+        w.range = 0;
         return w;
     }
     int32_t t = i, half = -1;
@@ -327,6 +400,8 @@ __device__ __forceinline__ WorkItem work_item(const GemmParams& p, int32_t i) {
     w.width = half < 0 ? BN : BN / 2;
     w.kb0 = 0;
     w.kb1 = p.k_blocks;
+    w.sk = kSkWhole;
+    w.range = 0;
     return w;
 }
 
@@ -338,6 +413,26 @@ template <class Cfg>
 __device__ __forceinline__ int32_t item_cols(const GemmParams& p, const WorkItem& w) {
     constexpr int32_t unit = 64 * Cfg::CTAS;
     return min(w.width, unit * ((p.N - w.n0 + unit - 1) / unit));
+}
+
+// Part h (in the order the epilogue hands parts back) of the accumulator of
+// an item using buffer buf: its first tensor-memory column, its first column
+// within the item, and its width (item_width when the whole accumulator is
+// one part).
+struct AccPart {
+    int32_t tmem_col, out_col, width;
+};
+
+template <class Cfg>
+__device__ __forceinline__ AccPart acc_part(int h, int buf, int32_t item_width) {
+    if constexpr (Cfg::STAGGER) {
+        const int32_t main = buf ? 256 : 0, narrow = buf ? 0 : 256;
+        if (h == 0) return {narrow, 256, 64};
+        if (h == 1) return {main, 0, 64};
+        return {main + 64, 64, 192};
+    } else {
+        return {buf * Cfg::BN + h * Cfg::SUB_N, h * Cfg::SUB_N, Cfg::RELEASE_PARTS > 1 ? Cfg::SUB_N : item_width};
+    }
 }
 
 struct Waiter {
@@ -410,11 +505,24 @@ __device__ __forceinline__ uint32_t chunk_off(int row, int col) {
 // column col0 (p.c_tma; the tensor map clips rows and columns outside C) or
 // one column per lane (128 contiguous bytes per warp store instruction;
 // atomic adds for split-K).
+// Stream-K (SK): items of a tile cut between two ranges are written
+// through per-lane stores, and the tile's first k-blocks (sk == kSkFirst)
+// add onto C.
+template <bool SK>
+__device__ __forceinline__ bool chunk_tma(const GemmParams& p, int32_t sk) {
+    return p.c_tma && (!SK || sk == kSkWhole);
+}
+template <bool SK>
+__device__ __forceinline__ bool chunk_accumulate(const GemmParams& p, int32_t sk) {
+    return p.k_splits > 1 || (SK && sk == kSkFirst);
+}
+
+template <bool SK>
 __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMap* tmap_c, const uint32_t (&r)[32],
                                            float* c_tile, int64_t row_stride, int32_t rows, int32_t row0,
-                                           int32_t col0, uint32_t buf_s, int lane) {
+                                           int32_t col0, uint32_t buf_s, int lane, int32_t sk) {
     const float alpha = p.alpha;
-    if (p.c_tma) {
+    if (chunk_tma<SK>(p, sk)) {
         // the previous chunk's TMA store must have read the buffer
         if (lane == 0) ptx::bulk_wait_read_all();
         __syncwarp();
@@ -424,12 +532,12 @@ __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMa
         ptx::st_shared_v4(buf_s + chunk_off(lane, 4 * q), alpha * acc_value(r[4 * q], p.acc16),
                           alpha * acc_value(r[4 * q + 1], p.acc16), alpha * acc_value(r[4 * q + 2], p.acc16),
                           alpha * acc_value(r[4 * q + 3], p.acc16));
-    if (p.c_tma) {
+    if (chunk_tma<SK>(p, sk)) {
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
             // split-K slices add into C (which already holds beta * C)
-            if (p.k_splits > 1)
+            if (chunk_accumulate<SK>(p, sk))
                 ptx::tma_reduce_add_2d(tmap_c, buf_s, col0, row0);
             else
                 ptx::tma_store_2d(tmap_c, buf_s, col0, row0);
@@ -441,7 +549,7 @@ __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMa
     const int32_t col = col0 + lane;
     if (col < p.N) {
         float* cp = c_tile + col;
-        if (p.k_splits > 1) {
+        if (chunk_accumulate<SK>(p, sk)) {
 #pragma unroll
             for (int rr = 0; rr < 32; ++rr)
                 if (rr < rows)
@@ -467,13 +575,14 @@ __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMa
 // ran), each later chunk's C loads go out before the previous chunk is
 // stored, and release() runs once the last chunk's tensor-memory load has
 // completed, before that chunk is stored.
-template <class Release>
+template <bool SK, class Release>
 __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMap* tmap_c, uint32_t t_row,
                                           float* c_tile, int64_t row_stride, int32_t rows, int32_t row0,
                                           int32_t n0, int32_t width, uint32_t buf_s, int lane,
-                                          float (&c_cur)[32], Release&& release) {
+                                          float (&c_cur)[32], int32_t sk, Release&& release) {
     const float alpha = p.alpha, beta = p.beta;
-    const bool read_c = (beta != 0.0f) && p.k_splits <= 1;
+    // (stream-K: the tile's first k-blocks add onto C without reading it)
+    const bool read_c = beta != 0.0f && p.k_splits <= 1 && (!SK || sk != kSkFirst);
     const int32_t chunks = (min(width, p.N - n0) + 31) / 32;
     if (!read_c) {
         for (int32_t c = 0; c < chunks; c += 2) {
@@ -485,8 +594,8 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMa
             ptx::tmem_regs_ready(r0);
             if (two) ptx::tmem_regs_ready(r1);
             if (c + 2 >= chunks) release();
-            emit_chunk(p, tmap_c, r0, c_tile, row_stride, rows, row0, n0 + c * 32, buf_s, lane);
-            if (two) emit_chunk(p, tmap_c, r1, c_tile, row_stride, rows, row0, n0 + (c + 1) * 32, buf_s, lane);
+            emit_chunk<SK>(p, tmap_c, r0, c_tile, row_stride, rows, row0, n0 + c * 32, buf_s, lane, sk);
+            if (two) emit_chunk<SK>(p, tmap_c, r1, c_tile, row_stride, rows, row0, n0 + (c + 1) * 32, buf_s, lane, sk);
         }
         if (chunks <= 0) release();
         return;
@@ -619,7 +728,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             bool ok = true;
             if (!p.test_stall) {
                 for (int32_t i = first_item; ok && i < p.items; i += item_step) {
-                    const WorkItem w = work_item<BN>(p, i);
+                    const WorkItem w = work_item<BN, Cfg::STREAM_K>(p, i);
                     if (w.n0 >= p.N) continue;   // a half tile wholly past the last column
                     // Pair: each MMA instruction covers sub_n columns of the
                     // item, and this CTA loads sub_n / 2 of them (its half) for
@@ -705,12 +814,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (lane == 0 && rank == 0) {
             int stage = 0;
             uint32_t phase = 0;
+            auto next_stage = [&]() {
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            };
             int32_t local = 0;
             bool ok = true;
             bool issued = false;
             int64_t walked = 0;   // k-blocks of the items before this one (KSPLIT)
             for (int32_t i = first_item; ok && i < p.items; i += item_step) {
-                const WorkItem w = work_item<BN>(p, i);
+                const WorkItem w = work_item<BN, Cfg::STREAM_K>(p, i);
                 if (w.n0 >= p.N) continue;
                 // columns the MMAs cover (the boxes wholly past N are skipped)
                 // and the parts (instructions per K step) they fall into: part
@@ -731,14 +846,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     ptx::tc_fence_after_sync();
                 }
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(Cfg::STAGGER ? 0 : buf * BN);
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     if constexpr (Cfg::KSPLIT) {
                         if (((walked + (kb - w.kb0)) & 1) != me) {   // the other issuer's k-block
-                            if (++stage == STAGES) {
-                                stage = 0;
-                                phase ^= 1u;
-                            }
+                            next_stage();
                             continue;
                         }
                     }
@@ -778,7 +890,29 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const int32_t h_begin = (Cfg::ISSUERS > 1 && !Cfg::KSPLIT) ? me : 0;
                     const int32_t h_end = (Cfg::ISSUERS > 1 && !Cfg::KSPLIT) ? min(me + 1, n_parts) : n_parts;
                     for (int32_t h = h_begin; ok && h < h_end; ++h) {
-                        if constexpr (RELEASE_PARTS > 1) {
+                        if constexpr (Cfg::STAGGER) {
+                            // the first use of part h in this item: wait until the
+                            // epilogue has read what overlaps it: the same part of
+                            // the item before last (same layout; for the 256-column
+                            // part its last-released third implies the others), and
+                            // of the previous item (other layout) the 64 columns
+                            // handed back first (256-column part) or second
+                            // (64-column part)
+                            if (kb == w.kb0) {
+                                bool fine = true;
+#pragma unroll 1
+                                for (int q = 0; fine && q < (local > 0 ? 2 : 1); ++q)
+                                    fine = q == 0 ? waiter.wait(acc_empty_bar(buf, h == 0 ? 2 : 0), acc_phase ^ 1u)
+                                                  : waiter.wait(acc_empty_bar(buf ^ 1, h == 0 ? 0 : 1),
+                                                                static_cast<uint32_t>((local - 1) / 2) & 1u);
+                                if (!fine) {
+                                    waiter.fail(kRoleMma, -1);
+                                    ok = false;
+                                    break;
+                                }
+                                ptx::tc_fence_after_sync();
+                            }
+                        } else if constexpr (RELEASE_PARTS > 1) {
                             // the first use of part h in this item: wait until the
                             // epilogue has read the previous item's part h
                             if (kb == w.kb0) {
@@ -797,7 +931,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         const int32_t part_cols = min(Cfg::SUB_N, n_valid - h * Cfg::SUB_N);
                         const uint32_t idesc = ptx::idesc_f16_f32(Cfg::TILE_M, part_cols, false, !Cfg::B_KMAJOR) &
                                                ~(p.acc16 ? (3u << 4) : 0u);
-                        const uint32_t d_part = d_tmem + static_cast<uint32_t>(h * Cfg::SUB_N);
+                        const uint32_t d_part =
+                            d_tmem + static_cast<uint32_t>(Cfg::STAGGER ? ((h == 0) == (buf == 0) ? 0 : 256) : h * Cfg::SUB_N);
                         const uint32_t b_part =
                             b_base + static_cast<uint32_t>(h * Cfg::ATOMS_PER_PART * Cfg::B_ATOM_BYTES);
 #pragma unroll
@@ -838,10 +973,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         ptx::tc_fence_before_sync();
                         ptx::mbar_arrive(handed_bar(stage));
                     }
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    next_stage();
                     if (!ok) break;
                 }
                 if (ok) {
@@ -870,7 +1002,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const bool read_c = (p.beta != 0.0f) && p.k_splits <= 1;
         int32_t local = 0;
         for (int32_t i = first_item; i < p.items; i += item_step) {
-            const WorkItem w = work_item<BN>(p, i);
+            const WorkItem w = work_item<BN, Cfg::STREAM_K>(p, i);
             if (w.n0 >= p.N) continue;
             int32_t cls, j0;
             a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
@@ -880,16 +1012,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const int64_t row_stride = static_cast<int64_t>(p.a_classes) * p.ldc;
             float* c_tile = p.C + (cls + static_cast<int64_t>(p.a_classes) * jb) * p.ldc;
             const int32_t n0 = w.n0;
-            const int32_t part_n = RELEASE_PARTS > 1 ? Cfg::SUB_N : w.width;   // columns per released part
-            const int32_t my_n = part_n / COL_SPLIT;                  // of which this warp stores
-            const int32_t my_off = col_half * my_n;
+            const int accb = local % ACC_BUFS;
+            const uint32_t acc_phase = (local / ACC_BUFS) & 1;
+            // (stream-K: the tile's first k-blocks add onto C without reading it)
+            const int32_t sk = Cfg::STREAM_K ? w.sk : kSkWhole;
+            const bool item_read_c = read_c && sk != kSkFirst;
             // beta * C needs C's old values: this warp's rows of the item's C
             // are brought into L2 and the first chunk's loads go out now,
             // while the MMAs of this tile are still running (one bulk
             // prefetch per row and lane; the two warps of a lane quarter take
             // half of the item's columns each, widened to the 16-byte blocks
             // that hold the first and last elements)
-            if (read_c && lane < rows) {
+            if (item_read_c && lane < rows) {
                 const int32_t cend = min(n0 + w.width, p.N);
                 const int32_t half = (cend - n0 + 1) / 2;
                 const int32_t cb = n0 + col_half * half;
@@ -902,22 +1036,45 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
             }
             float c_cur[32];
-            if (read_c) load_c_chunk(c_tile, row_stride, n0 + my_off + lane, p.N, rows, c_cur);
-            const int accb = local % ACC_BUFS;
-            const uint32_t acc_phase = (local / ACC_BUFS) & 1;
+            if (item_read_c) {
+                // (this warp's first columns of the first part handed back)
+                const AccPart g0 = acc_part<Cfg>(0, accb, w.width);
+                load_c_chunk(c_tile, row_stride, n0 + g0.out_col + col_half * (g0.width / COL_SPLIT) + lane, p.N,
+                             rows, c_cur);
+            }
             const bool ready = waiter.wait(acc_full_bar(accb), acc_phase);
             if (!__all_sync(0xffffffffu, ready)) {
                 if (lane == 0) waiter.fail(kRoleEpilogue, i);
                 break;
             }
             ptx::tc_fence_after_sync();
-            const uint32_t t_row =
-                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(accb * BN);
-            // the accumulator's parts in order (SUBS == 1: the whole item);
+            // Stream-K: wait until the warp holding the same rows and columns
+            // in the next range has written them and published this call's
+            // epoch in its flag
+            if (sk == kSkFirst) {
+                const int32_t* flag = p.sk_flags + ((w.range + 1) * Cfg::CTAS + static_cast<int32_t>(rank)) *
+                                                       Cfg::EPI_WARPS + (warp - 2);
+                bool got = ptx::ld_acquire_gpu(flag) == p.sk_epoch;
+                if (!got) {
+                    const uint64_t t0 = ptx::globaltimer_ns();
+                    while (!(got = ptx::ld_acquire_gpu(flag) == p.sk_epoch) && !*abort_flag &&
+                           ptx::globaltimer_ns() - t0 <= p.wait_limit_ns) {
+                    }
+                }
+                if (!__all_sync(0xffffffffu, got)) {
+                    if (lane == 0) waiter.fail(kRoleEpilogue, i);
+                    break;
+                }
+            }
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+            // the accumulator's parts in order (one part: the whole item);
             // each part goes back to the MMA warp as soon as it has been read,
             // and parts past the item's width are handed back at once
             for (int h = 0; h < RELEASE_PARTS; ++h) {
-                const int32_t pn0 = n0 + h * part_n + my_off;
+                const AccPart g = acc_part<Cfg>(h, accb, w.width);
+                const int32_t my_n = g.width / COL_SPLIT;   // columns of the part this warp stores
+                const int32_t my_off = col_half * my_n;
+                const int32_t pn0 = n0 + g.out_col + my_off;
                 // hand part h of the accumulator back to its MMA thread
                 auto release = [&]() {
                     ptx::tc_fence_before_sync();
@@ -929,17 +1086,24 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             ptx::mbar_arrive(acc_empty_bar(accb, h));
                     }
                 };
-                if (h * part_n < w.width) {
-                    // this warp's columns of the part, within the item (the
-                    // 64-column last part of a 320-wide tile leaves the
-                    // second warp of each lane quarter none)
-                    const int32_t my_w = min(my_n, w.width - h * part_n - my_off);
-                    if (h > 0 && read_c && my_w > 0) load_c_chunk(c_tile, row_stride, pn0 + lane, p.N, rows, c_cur);
-                    store_tile(p, &maps.c, t_row + static_cast<uint32_t>(h * part_n + my_off), c_tile, row_stride,
-                               rows, jb, pn0, my_w, buf_s, lane, c_cur, release);
+                if (g.out_col < w.width) {
+                    // this warp's columns of the part, within the item
+                    const int32_t my_w = min(my_n, w.width - g.out_col - my_off);
+                    if (h > 0 && item_read_c && my_w > 0) load_c_chunk(c_tile, row_stride, pn0 + lane, p.N, rows, c_cur);
+                    store_tile<Cfg::STREAM_K>(p, &maps.c, t_row + static_cast<uint32_t>(g.tmem_col + my_off), c_tile, row_stride,
+                               rows, jb, pn0, my_w, buf_s, lane, c_cur, sk, release);
                 } else {
                     release();
                 }
+            }
+            if (sk == kSkRest) {
+                // every lane's stores of C visible at GPU scope before the flag
+                __threadfence();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::st_release_gpu(
+                        p.sk_flags + (w.range * Cfg::CTAS + static_cast<int32_t>(rank)) * Cfg::EPI_WARPS + (warp - 2),
+                        p.sk_epoch);
             }
             ++local;
         }

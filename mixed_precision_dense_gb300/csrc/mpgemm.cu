@@ -63,6 +63,11 @@ using Cfg320K = TileConfig<320, 3, false, true>;
 using CfgPairK = TileConfig<256, 6, true, true, 2>;
 using CfgWideK = TileConfig<512, 4, true, true>;
 using CfgPair384K = TileConfig<384, 4, true, true, 2>;
+// stream-K flags per range: one per CTA of the pair and epilogue warp
+constexpr int kSkFlagsPerRange = 2 * CfgPair::EPI_WARPS;
+static_assert(CfgPair::STREAM_K && CfgPair320::STREAM_K && CfgPair384::STREAM_K && !CfgWide::STREAM_K &&
+                  CfgPair320::EPI_WARPS == CfgPair::EPI_WARPS && CfgPair384::EPI_WARPS == CfgPair::EPI_WARPS,
+              "stream-K shapes");
 // one occupancy query (max_pair_clusters) serves both pair shapes: shared
 // memory limits either to one CTA per SM, and both stay far below the SM's
 // thread and register limits at that occupancy
@@ -89,6 +94,7 @@ struct Options {
     int32_t c_store = 0;            // 0 automatic (TMA stores when possible), 1 per-lane stores
     int32_t acc16 = 0;              // 1: FP16 accumulators (study variant)
     int32_t reproducible = 0;       // 1: only paths whose summation order is fixed
+    int32_t stream_k = 0;           // 0 automatic, 1 never, 2 whenever the tile shape allows
     uint64_t wait_limit_ns = kDefaultWaitLimitNs;
 };
 
@@ -341,6 +347,24 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
                             ? static_cast<int32_t>(rem)
                             : 0;
         p.items = p.tiles + p.split_tiles;
+    }
+    // Stream-K (MPGEMM_OPT_STREAM_K): CTA pairs of 256 to 384 columns with at
+    // least one tile per pair may walk one contiguous range of k-blocks each
+    // instead of whole tiles. Automatic for the 320- and 384-wide pairs of
+    // tall-skinny problems when the last wave of tiles leaves pairs idle:
+    // 65536 x 257 x 4093 (256 tiles on 76 pairs, 3.37 waves) ran four waves
+    // of tiles whose epilogues all fell together.
+    p.sk_ranges = 0;
+    if (pair && splits == 1 && !opt.acc16 && opt.stream_k != 1 && p.tile_n <= 384 && p.tiles >= units) {
+        const int64_t sk_units = p.tiles * k_blocks;
+        const bool want = opt.stream_k == 2 || (p.tile_n >= 320 && p.tiles % units != 0);
+        if (want && sk_units < (int64_t{1} << 31)) {
+            p.sk_ranges = static_cast<int32_t>(units);
+            p.split_tiles = 0;
+            // a range of len (+1) k-blocks touches at most ceil((len + 1) / k_blocks) + 1 tiles
+            const int64_t len = sk_units / units;
+            p.items = units * (ceil_div(len + 1, k_blocks) + 1);
+        }
     }
     if (p.items > kDimLimit) return MPGEMM_ERR_INVALID_VALUE;
     units = std::min<int64_t>(units, p.items);
@@ -694,6 +718,12 @@ GemmParams make_params(const mpgemm_plan_t& plan, int64_t M, int64_t N, int64_t 
     gp.keep_a = keep_a;
     // split-K slices after the pass that applies beta (launch_plan)
     gp.overlap_prepass = (plan.k_splits > 1 && beta != 1.0f) ? 1 : 0;
+    if (plan.sk_ranges > 0) {   // (the caller sets sk_flags and sk_epoch)
+        gp.sk_units = static_cast<int32_t>(plan.tiles * plan.k_blocks);
+        gp.sk_ranges = plan.sk_ranges;
+        gp.sk_len = gp.sk_units / gp.sk_ranges;
+        gp.sk_rem = gp.sk_units % gp.sk_ranges;
+    }
     return gp;
 }
 
@@ -710,6 +740,9 @@ cudaError_t launch_plan(const mpgemm_plan_t& plan, bool b_col_major, int max_clu
     if (plan.tile_m == 256) {
         int grid = plan.grid;
         if (max_clusters > 0 && grid > 2 * max_clusters) grid = 2 * max_clusters;
+        // every stream-K range needs its own pair, all resident together
+        if (plan.sk_ranges > 0 && (grid != 2 * plan.sk_ranges || !gp.sk_flags || gp.sk_epoch == 0))
+            return cudaErrorInvalidValue;
         if (plan.tile_n == 512)
             return b_col_major ? launch_tc<CfgWideK>(grid, ta, tb, gp, stream)
                                : launch_tc<CfgWide>(grid, ta, tb, gp, stream);
@@ -762,6 +795,9 @@ struct mpgemm_handle_st {
     size_t ws_bytes = 0;
     void* host_ws = nullptr;         // device copies for mpgemm_run_host
     size_t host_ws_bytes = 0;
+    int32_t* sk_flags = nullptr;     // stream-K flags (zeroed when allocated), and the epoch of
+    size_t sk_flags_bytes = 0;       // the last call that used them
+    int32_t sk_epoch = 0;
 };
 
 namespace {
@@ -913,6 +949,7 @@ mpgemm_status_t mpgemm_destroy(mpgemm_handle_t h) {
     if (!h) return MPGEMM_OK;
     if (h->ws) cudaFree(h->ws);
     if (h->host_ws) cudaFree(h->host_ws);
+    if (h->sk_flags) cudaFree(h->sk_flags);
     if (h->status_host) cudaFreeHost(h->status_host);
     cudaGetLastError();
     delete h;
@@ -970,6 +1007,10 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
         case MPGEMM_OPT_REPRODUCIBLE:
             if (value != 0 && value != 1) return MPGEMM_ERR_INVALID_VALUE;
             h->opt.reproducible = static_cast<int32_t>(value);
+            return MPGEMM_OK;
+        case MPGEMM_OPT_STREAM_K:
+            if (value < 0 || value > 2) return MPGEMM_ERR_INVALID_VALUE;
+            h->opt.stream_k = static_cast<int32_t>(value);
             return MPGEMM_OK;
     }
     return MPGEMM_ERR_INVALID_VALUE;
@@ -1035,6 +1076,27 @@ mpgemm_status_t mpgemm_run_ex(mpgemm_handle_t h, mpgemm_b_layout_t b_layout, int
     if (!encode_b_tail(plan, b_use, K, N, ldb_use, &ta, &h->map_cache)) return MPGEMM_ERR_CUDA;
     encode_c(plan, C, M, N, ldc, beta, h->opt.c_store, &ta, &gp, &h->map_cache);
     gp.acc16 = h->opt.acc16;
+    if (plan.sk_ranges > 0) {
+        // Stream-K flags: one per range, CTA and epilogue warp. A new buffer
+        // starts at zero, which no call's epoch is; each call publishes a
+        // new epoch, so flags left by earlier calls never match.
+        const size_t need = static_cast<size_t>(plan.sk_ranges) * kSkFlagsPerRange * sizeof(int32_t);
+        if (need > h->sk_flags_bytes || h->sk_epoch == INT32_MAX) {
+            void* buf = h->sk_flags;
+            size_t cap = h->sk_flags_bytes;
+            st = ensure_buffer(&buf, &cap, need, stream);
+            h->sk_flags = static_cast<int32_t*>(buf);
+            h->sk_flags_bytes = cap;
+            if (st != MPGEMM_OK) return st;
+            if (cudaMemsetAsync(h->sk_flags, 0, h->sk_flags_bytes, stream) != cudaSuccess) {
+                cudaGetLastError();
+                return MPGEMM_ERR_LAUNCH;
+            }
+            h->sk_epoch = 0;
+        }
+        gp.sk_flags = h->sk_flags;
+        gp.sk_epoch = ++h->sk_epoch;
+    }
     if (launch_plan(plan, b_col, h->max_clusters, ta, tb, gp, stream) != cudaSuccess) {
         cudaGetLastError();
         return MPGEMM_ERR_LAUNCH;
@@ -1236,6 +1298,7 @@ extern "C" mpgemm_status_t mpgemm_run_noalloc(int64_t M, int64_t N, int64_t K, f
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     Options opt;  // defaults: automatic tile width, one CTA per SM, 4 s wait limit
     opt.pair_units = d.max_clusters;
+    opt.stream_k = 1;   // (its flags would need memory of their own)
     mpgemm_plan_t plan;
     mpgemm_status_t st =
         make_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d.num_sms, opt, &plan);

@@ -118,6 +118,38 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA, tensor core) accesses.
+// Flag hand-over between CTAs through global memory: a release store
+// publishes everything the thread (and, after a CTA barrier, the threads
+// that fenced before it) wrote; an acquire load makes it visible.
+__device__ __forceinline__ void st_release_gpu(int32_t* addr, int32_t v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* addr) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
+// Named barrier `id` (1-15) over `threads` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// 16-byte global store and load that keep the line out of L1 (the partial
+// sums one CTA writes and another reads).
+__device__ __forceinline__ void st_global_cg_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("st.global.cg.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+__device__ __forceinline__ float4 ld_global_cg_v4(const float* addr) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

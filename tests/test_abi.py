@@ -229,9 +229,10 @@ def test_tile_selection_and_grid():
         p = _plan(M=256, N=128, K=K, lda=K, ldb=128, ldc=128)
         per = -(-p["k_blocks"] // p["k_splits"])
         assert (p["k_splits"] - 1) * per < p["k_blocks"]
-    # a last wave more than half full is not split
+    # a last wave more than half full is not split in halves; the 320-wide
+    # pairs of this tall-skinny problem walk stream-K ranges instead
     p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257)
-    assert p["split_tiles"] == 0 and p["items"] == p["tiles"]
+    assert p["split_tiles"] == 0 and p["sk_ranges"] == 76
     p = _plan()
     assert p["a_classes"] == 8 and p["tiles"] == 8 * 2                      # 8 classes of 25 rows
     # 16 tiles of 10 k-blocks (at most an eighth of the SMs): five K slices
@@ -278,3 +279,40 @@ def test_short_k_split_rule(M, K, beta, splits):
     assert p["tile_n"] == 128 and p["k_splits"] == splits
     per = -(-p["k_blocks"] // p["k_splits"])
     assert (p["k_splits"] - 1) * per < p["k_blocks"] and p["items"] == p["tiles"] * p["k_splits"]
+
+
+def test_stream_k_planning():
+    """The stream-K walk: automatic for 320- and 384-wide CTA-pair tiles whose
+    last wave leaves pairs idle; one range of equal length per pair; the
+    items cover the tiles every range touches."""
+    p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257)
+    assert (p["tile_m"], p["tile_n"], p["tiles"], p["k_blocks"]) == (256, 320, 256, 65)   # (row-class shift)
+    ranges, kb = p["sk_ranges"], p["k_blocks"]
+    assert ranges == 76 and p["grid"] == 2 * ranges
+    length = p["tiles"] * kb // ranges                  # 218 k-blocks, 72 ranges hold 219
+    assert length >= kb
+    per_range = -(-(length + 1) // kb) + 1
+    assert p["items"] == ranges * per_range
+    # every range touches at most per_range tiles: brute force over the ranges
+    units, rem = p["tiles"] * kb, p["tiles"] * kb % ranges
+    for r in range(ranges):
+        u0 = r * length + min(r, rem)
+        u1 = u0 + length + (1 if r < rem else 0)
+        assert (u1 - 1) // kb - u0 // kb + 1 <= per_range
+        if r == ranges - 1:
+            assert u1 == units
+    # 384-wide pairs (N from 321 on), and the K-major B variant
+    p = _plan(M=65536, N=384, K=4096, lda=4096, ldb=384, ldc=384)
+    assert p["tile_n"] == 384 and p["sk_ranges"] == 76
+    p = _plan(M=65536, N=300, K=4096, lda=4096, ldb=4096, ldc=300, b_col_major=True)
+    assert p["tile_n"] == 384 and p["sk_ranges"] == 76
+    # exactly three waves of tiles: nothing to balance
+    p = _plan(M=58368, N=257, K=4096, lda=4096, ldb=257, ldc=257)
+    assert p["tiles"] == 3 * 76 and p["sk_ranges"] == 0 and p["items"] == p["tiles"]
+    # 256-wide pairs, single CTAs and fewer tiles than pairs: never automatic
+    assert _plan(M=65536, N=256, K=4096, lda=4096, ldb=256, ldc=256)["sk_ranges"] == 0
+    assert _plan(M=8192, N=300, K=4096, lda=4096, ldb=300, ldc=300)["sk_ranges"] == 0
+    assert _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192)["sk_ranges"] == 0
+    # a smaller grid: ranges follow the pairs launched
+    p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257, max_ctas=100)
+    assert p["sk_ranges"] == 50 and p["grid"] == 100

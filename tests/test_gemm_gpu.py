@@ -802,3 +802,98 @@ def test_tensor_map_cache_across_buffers_and_shapes(mp):
         for _ in range(2):
             for ops in sets:
                 check_full(h, ops)
+
+
+# --------------------------------------------------------------------------- stream-K walk
+
+STREAM_K_CASES = [  # (tile_m, tile_n, max_ctas, M, N, K, lda, ldb, ldc, beta, b_col_major)
+    # 256 x 256 pairs, 10 tiles on 3 pairs: TMA stores for whole tiles, per-lane for cut ones
+    (256, 256, 6, 1280, 512, 1000, 1000, 512, 512, 0.0, False),
+    # 256 x 320 pairs, A in row classes, beta * C on the later k-blocks
+    (256, 320, 6, 1900, 257, 617, 617, 257, 257, 0.5, False),
+    # 256 x 384 pairs, beta == 1, unaligned A and C, 6 tiles on 5 pairs
+    (256, 384, 10, 1300, 380, 333, 335, 380, 383, 1.0, False),
+    # 256 x 384 pairs with a column-major B, 4 tiles on 2 pairs (one range = two tiles)
+    (256, 384, 4, 1024, 300, 500, 500, 503, 300, -0.5, True),
+    # ranges of 1.3 tiles: every pair cuts two tiles
+    (256, 256, 14, 2304, 256, 1536, 1536, 256, 256, 0.25, False),
+]
+
+
+@pytest.mark.parametrize("tile_m,tile_n,max_ctas,M,N,K,lda,ldb,ldc,beta,b_col", STREAM_K_CASES)
+def test_stream_k_walk(mp, tile_m, tile_n, max_ctas, M, N, K, lda, ldb, ldc, beta, b_col):
+    # Every pair walks one contiguous range of k-blocks; a tile cut between
+    # two ranges is written by the later k-blocks (with beta * C) and then
+    # added to by the earlier ones. Against the oracle, element by element,
+    # NaN-poisoned C when beta == 0; then on exact integers bit for bit.
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_M, tile_m)
+        h.set_option(mp.Option.TILE_N, tile_n)
+        h.set_option(mp.Option.MAX_CTAS, max_ctas)
+        h.set_option(mp.Option.STREAM_K, 2)
+        ops = workloads.make_operands(M, N, K, lda=lda, ldb=ldb, ldc=ldc, alpha=1.25, beta=beta,
+                                      c_dist="normal" if beta else "zeros", seed=M + 3 * N + K,
+                                      b_col_major=b_col)
+        check_full(h, ops)
+        ints = workloads.make_operands(M, N, K, lda=lda, ldb=ldb, ldc=ldc, beta=beta, dist="int3",
+                                       dist_b="int2", c_dist="int3" if beta else "zeros",
+                                       seed=M + 3 * N + K + 1, b_col_major=b_col)
+        check_full(h, ints, exact=True)
+
+
+def test_stream_k_plan_reaches_the_kernel(mp):
+    # the planner's ranges for the cases above (the kernel reads them the same way)
+    for tile_m, tile_n, max_ctas, M, N, K, lda, ldb, ldc, beta, b_col in STREAM_K_CASES:
+        del tile_m, beta
+        p = mp.plan(M, N, K, 1.0, 256, lda, 256, ldb, 0.0, 256, ldc, tile_m=256, tile_n=tile_n,
+                    max_ctas=max_ctas, b_col_major=b_col)
+        assert p["tiles"] >= max_ctas // 2
+
+
+def test_stream_k_identical_bits_on_repeat_and_against_the_whole_tile_walk(mp):
+    # The tall-skinny shape the planner walks in stream-K ranges by itself
+    # (256 tiles of 256 x 320 on 76 pairs): identical calls give identical
+    # bits, and the whole-tile walk (STREAM_K = 1) agrees within the
+    # tolerance; on integers both equal the oracle.
+    from parity import device_operands, reference, assert_close
+    s = torch.cuda.current_stream()
+    M, N, K = 65536, 257, 1021
+    plan = mp.plan(M, N, K, 1.0, 256, K, 256, N, 0.5, 256, N)
+    if plan["grid"] != 152:
+        pytest.skip("written for 76 CTA pairs")
+    assert plan["tile_n"] == 320 and plan["sk_ranges"] == 76
+
+    def run(h, ops, n):
+        outs = []
+        for _ in range(n):
+            d = device_operands(ops)
+            h.run(ops.M, ops.N, ops.K, ops.alpha, d["a_ptr"], ops.lda, d["b_ptr"], ops.ldb, ops.beta,
+                  d["c_ptr"], ops.ldc, s.cuda_stream)
+            s.synchronize()
+            assert h.sync_status(s.cuda_stream)[0] == mp.Status.OK
+            outs.append(c_result(d, ops)[0])
+        return outs
+
+    ops = workloads.make_operands(M, N, K, alpha=0.75, beta=0.5, c_dist="normal", seed=77)
+    rows = np.arange(0, M, 97)
+    I, J = np.repeat(rows, N), np.tile(np.arange(N), rows.size)
+
+    def sampled(ops):
+        ref, S = reference(ops, I, J)
+        return ref.reshape(rows.size, N), S.reshape(rows.size, N)
+
+    ref, S = sampled(ops)
+    with mp.Handle() as h:
+        outs = run(h, ops, 3)
+    assert all(np.array_equal(outs[0].view(np.uint64), o.view(np.uint64)) for o in outs[1:])
+    assert_close(outs[0][rows], ref, S, "stream-K")
+    with mp.Handle() as h:
+        h.set_option(mp.Option.STREAM_K, 1)
+        whole = run(h, ops, 1)[0]
+    assert_close(whole[rows], ref, S, "whole tiles")
+    ints = workloads.make_operands(M, N, K, beta=0.5, dist="int3", dist_b="int2", c_dist="int3", seed=78)
+    ref, _ = sampled(ints)
+    with mp.Handle() as h:
+        got = run(h, ints, 2)
+    for g in got:
+        assert np.array_equal(g[rows], ref)
