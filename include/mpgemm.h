@@ -203,7 +203,8 @@ typedef enum {
                                      strictly in turn). The stream-K walk (STREAM_K) is
                                      allowed: it, too, sums in a fixed order. */
     MPGEMM_OPT_STREAM_K = 13      /* 0 = automatic (default): CTA-pair tiles of 320 or 384
-                                     columns (N from 257 to 384) that leave the last wave of
+                                     columns (N from 257 to 384), or a single column of
+                                     256-wide pair tiles, that leave the last wave of
                                      pairs partly idle walk the problem as one contiguous range
                                      of k-blocks per pair instead of whole tiles (stream-K,
                                      Osama et al., 2023): every pair gets the same number of

@@ -350,14 +350,19 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     }
     // Stream-K (MPGEMM_OPT_STREAM_K): CTA pairs of 256 to 384 columns with at
     // least one tile per pair may walk one contiguous range of k-blocks each
-    // instead of whole tiles. Automatic for the 320- and 384-wide pairs of
-    // tall-skinny problems when the last wave of tiles leaves pairs idle:
-    // 65536 x 257 x 4093 (256 tiles on 76 pairs, 3.37 waves) ran four waves
-    // of tiles whose epilogues all fell together.
+    // instead of whole tiles. Automatic for tall-skinny problems (the 320-
+    // and 384-wide pairs, or one column of 256-wide tiles) when the last wave
+    // of tiles leaves pairs idle. Measured on GB300 with L2 flushed, us:
+    //   65536 x 257 x 4093, beta 0.5 (256 tiles on 76 pairs): 186 -> 172;
+    //   65536 x 256 x 4096: 121 -> 112 (beta 0), 135 -> 130 (beta 0.5);
+    // and slower for square and wide problems on 256 x 256 pairs (6144^3:
+    // 311 -> 361; 20480 x 1024 x 4096: 159 -> 171), whose cut tiles cost a
+    // second pass over C while their pairs still drain whole tiles.
     p.sk_ranges = 0;
     if (pair && splits == 1 && !opt.acc16 && opt.stream_k != 1 && p.tile_n <= 384 && p.tiles >= units) {
         const int64_t sk_units = p.tiles * k_blocks;
-        const bool want = opt.stream_k == 2 || (p.tile_n >= 320 && p.tiles % units != 0);
+        const bool want =
+            opt.stream_k == 2 || ((p.tile_n >= 320 || p.n_tiles == 1) && p.tiles % units != 0);
         if (want && sk_units < (int64_t{1} << 31)) {
             p.sk_ranges = static_cast<int32_t>(units);
             p.split_tiles = 0;

@@ -309,8 +309,11 @@ def test_stream_k_planning():
     # exactly three waves of tiles: nothing to balance
     p = _plan(M=58368, N=257, K=4096, lda=4096, ldb=257, ldc=257)
     assert p["tiles"] == 3 * 76 and p["sk_ranges"] == 0 and p["items"] == p["tiles"]
-    # 256-wide pairs, single CTAs and fewer tiles than pairs: never automatic
-    assert _plan(M=65536, N=256, K=4096, lda=4096, ldb=256, ldc=256)["sk_ranges"] == 0
+    # one column of 256-wide pair tiles (3.37 waves); more columns, single
+    # CTAs and fewer tiles than pairs: never automatic
+    p = _plan(M=65536, N=256, K=4096, lda=4096, ldb=256, ldc=256, tile_m=256)
+    assert (p["tile_n"], p["n_tiles"], p["sk_ranges"], p["split_tiles"]) == (256, 1, 76, 0)
+    assert _plan(M=20480, N=1024, K=4096, lda=4096, ldb=1024, ldc=1024, tile_m=256)["sk_ranges"] == 0
     assert _plan(M=8192, N=300, K=4096, lda=4096, ldb=300, ldc=300)["sk_ranges"] == 0
     assert _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192)["sk_ranges"] == 0
     # a smaller grid: ranges follow the pairs launched
