@@ -89,6 +89,9 @@ namespace mpgemm {
 // rows earlier (rows before 0 arrive as zeros).
 constexpr int kMaxAClasses = 8;
 
+// Most ranges of a stream-K walk (one per CTA pair).
+constexpr int kMaxSkRanges = 128;
+
 // The tensor maps of A (one per row class), of C (FP32, 32 x 32 boxes,
 // 128-byte swizzle; used only when GemmParams::c_tma is set) and of B in
 // narrow boxes (used only by 256 x 320 pair tiles).
@@ -127,8 +130,9 @@ struct GemmParams {
                               //    before split-K slices add into it): only the epilogue warps,
                               //    which write C, wait for it; the loads and MMAs start at once
     // Stream-K walk (sk_units > 0): the tiles' k-blocks, tile after tile in
-    // raster order, are cut into sk_ranges contiguous ranges of equal length
-    // (at least one tile's k-blocks each), one per persistent CTA (pair).
+    // raster order, are cut into sk_ranges contiguous ranges, range r being
+    // [sk_start[r], sk_start[r + 1]) (at least one tile's k-blocks each), one
+    // per persistent CTA (pair).
     // A tile cut between ranges r and r + 1 is written twice, in a fixed
     // order: range r + 1 does the tile's last k-blocks first and writes
     // C = alpha * (their sum) + beta * C, then publishes sk_epoch in its
@@ -136,11 +140,10 @@ struct GemmParams {
     // alpha * (their sum) onto that C after it has seen the flag.
     int32_t sk_units;       // tiles * k_blocks (below 2^31), or 0
     int32_t sk_ranges;
-    int32_t sk_len;         // sk_units / sk_ranges: ranges r < sk_units % sk_ranges hold one more
-    int32_t sk_rem;
     int32_t sk_epoch;       // this call's flag value (never 0)
     int32_t* sk_flags;      // [sk_ranges][CTAS][epilogue warps]: each epilogue warp publishes
                             // its own rows and columns of the tile
+    int32_t sk_start[kMaxSkRanges + 1];
 };
 
 enum : int32_t { kRoleLoad = 1, kRoleMma = 2, kRoleEpilogue = 3 };
@@ -224,6 +227,10 @@ struct TileConfig {
     // shapes of at most 384 columns, those that run tall-skinny problems of
     // a few waves of tiles
     static constexpr bool STREAM_K = PAIR && BN <= 384;
+    // the beta * C epilogue reads a chunk's 32 rows from shared memory
+    // before storing any (not in 256 x 384 pairs, whose registers it spills:
+    // 100 bytes, 65536 x 384 x 4096 200.0 -> 203.9 us)
+    static constexpr bool EPI_BATCH_LOADS = BN != 384;
     static constexpr int EPI_CHUNK_BYTES = 32 * 32 * 4;  // one warp's 32 x 32 FP32 chunk buffer
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_CHUNK_BYTES;
     // (allocations are powers of two: a 320-column accumulator takes 512)
@@ -339,8 +346,7 @@ __device__ __forceinline__ WorkItem work_item(const GemmParams& p, int32_t i) {
     if (STREAM_K && p.sk_units > 0) {
         // item j of range r (i = r + j * sk_ranges, as the CTAs walk)
         const int32_t r = i % p.sk_ranges, j = i / p.sk_ranges;
-        const int32_t u0 = r * p.sk_len + min(r, p.sk_rem);
-        const int32_t u1 = u0 + p.sk_len + (r < p.sk_rem ? 1 : 0);
+        const int32_t u0 = p.sk_start[r], u1 = p.sk_start[r + 1];
         const int32_t t0 = u0 / p.k_blocks;
         const int32_t t_last = (u1 - 1) / p.k_blocks;
         // The range's tiles in order, except that a last piece holding a
@@ -575,7 +581,7 @@ __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMa
 // ran), each later chunk's C loads go out before the previous chunk is
 // stored, and release() runs once the last chunk's tensor-memory load has
 // completed, before that chunk is stored.
-template <bool SK, class Release>
+template <bool SK, bool BATCH, class Release>
 __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMap* tmap_c, uint32_t t_row,
                                           float* c_tile, int64_t row_stride, int32_t rows, int32_t row0,
                                           int32_t n0, int32_t width, uint32_t buf_s, int lane,
@@ -619,11 +625,26 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMa
         const int32_t col = n0 + c * 32 + lane;
         if (col < p.N) {
             float* cp = c_tile + col;
+            if constexpr (BATCH) {
+                // the lane's 32 rows read from shared memory first, into the
+                // registers that held the accumulator words: the loads issue
+                // back to back instead of each waiting behind the previous
+                // row's global store (65536 x 257 x 4093, beta 0.5: 171.7 ->
+                // 169.3 us)
 #pragma unroll
-            for (int rr = 0; rr < 32; ++rr)
-                if (rr < rows)
-                    cp[static_cast<int64_t>(rr) * row_stride] =
-                        fmaf(beta, c_cur[rr], ptx::ld_shared_f32(buf_s + chunk_off(rr, lane)));
+                for (int rr = 0; rr < 32; ++rr)
+                    r[rr] = __float_as_uint(ptx::ld_shared_f32(buf_s + chunk_off(rr, lane)));
+#pragma unroll
+                for (int rr = 0; rr < 32; ++rr)
+                    if (rr < rows)
+                        cp[static_cast<int64_t>(rr) * row_stride] = fmaf(beta, c_cur[rr], __uint_as_float(r[rr]));
+            } else {
+#pragma unroll
+                for (int rr = 0; rr < 32; ++rr)
+                    if (rr < rows)
+                        cp[static_cast<int64_t>(rr) * row_stride] =
+                            fmaf(beta, c_cur[rr], ptx::ld_shared_f32(buf_s + chunk_off(rr, lane)));
+            }
         }
 #pragma unroll
         for (int rr = 0; rr < 32; ++rr) c_cur[rr] = c_next[rr];
@@ -1090,7 +1111,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     // this warp's columns of the part, within the item
                     const int32_t my_w = min(my_n, w.width - g.out_col - my_off);
                     if (h > 0 && item_read_c && my_w > 0) load_c_chunk(c_tile, row_stride, pn0 + lane, p.N, rows, c_cur);
-                    store_tile<Cfg::STREAM_K>(p, &maps.c, t_row + static_cast<uint32_t>(g.tmem_col + my_off), c_tile, row_stride,
+                    store_tile<Cfg::STREAM_K, Cfg::EPI_BATCH_LOADS>(p, &maps.c, t_row + static_cast<uint32_t>(g.tmem_col + my_off), c_tile, row_stride,
                                rows, jb, pn0, my_w, buf_s, lane, c_cur, sk, release);
                 } else {
                     release();

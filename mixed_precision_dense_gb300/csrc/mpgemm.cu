@@ -30,6 +30,7 @@
 #include <functional>
 #include <numeric>
 #include <mutex>
+#include <vector>
 
 #include "../../include/mpgemm.h"
 #include "gemm_kernel.cuh"
@@ -229,6 +230,35 @@ AClassLayout a_class_layout(const void* A, int64_t lda, int64_t M, bool classes,
     return L;
 }
 
+// The stream-K ranges: range r is [start[r], start[r + 1]) of the tiles'
+// k-blocks (units = tiles * k_blocks), R ranges of about equal length. A
+// boundary that would leave a piece of a tile of an eighth of its k-blocks
+// or fewer on either side moves to the tile's edge: such a piece costs a
+// whole epilogue (and, inside a range, stalls the next tile's MMAs behind
+// the drain) for a few k-blocks of work. Without the moves when they would
+// leave a range shorter than one tile's k-blocks. Measured on GB300, L2
+// flushed, us, equal ranges / moved / ranges balanced on k-blocks plus a
+// cost per tile touched (eighth or quarter of a tile):
+//   65536 x 257 x 4093, beta 0.5: 171.4 / 169.2 / 169.9, 167.6
+//   65536 x 257 x 4093, beta 0:   158.5 / 158.6 / 167.7, 167.4
+//   65536 x 300 x 4096, beta 0:   -     / 140.8 / 150.9, 150.4
+std::vector<int32_t> sk_range_starts(int64_t units, int64_t k_blocks, int64_t R) {
+    std::vector<int32_t> start(static_cast<size_t>(R + 1));
+    const int64_t len = units / R, rem = units % R, snap = std::max<int64_t>(1, k_blocks / 8);
+    for (int64_t r = 0; r <= R; ++r) start[r] = static_cast<int32_t>(r * len + std::min(r, rem));
+    std::vector<int32_t> moved = start;
+    for (int64_t r = 1; r < R; ++r) {
+        const int64_t off = moved[r] % k_blocks;
+        if (off != 0 && off <= snap)
+            moved[r] = static_cast<int32_t>(moved[r] - off);
+        else if (off != 0 && k_blocks - off <= snap)
+            moved[r] = static_cast<int32_t>(moved[r] + (k_blocks - off));
+    }
+    for (int64_t r = 0; r < R; ++r)
+        if (moved[r + 1] - moved[r] < k_blocks) return start;
+    return moved;
+}
+
 mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                           const void* B, int64_t ldb, float beta, const void* C, int64_t ldc,
                           int32_t num_sms, const Options& opt, mpgemm_plan_t* out) {
@@ -363,12 +393,15 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
         const int64_t sk_units = p.tiles * k_blocks;
         const bool want =
             opt.stream_k == 2 || ((p.tile_n >= 320 || p.n_tiles == 1) && p.tiles % units != 0);
-        if (want && sk_units < (int64_t{1} << 31)) {
+        if (want && sk_units < (int64_t{1} << 31) && units <= kMaxSkRanges) {
             p.sk_ranges = static_cast<int32_t>(units);
             p.split_tiles = 0;
-            // a range of len (+1) k-blocks touches at most ceil((len + 1) / k_blocks) + 1 tiles
-            const int64_t len = sk_units / units;
-            p.items = units * (ceil_div(len + 1, k_blocks) + 1);
+            // items: every range walks as many as the range touching most tiles
+            const std::vector<int32_t> start = sk_range_starts(sk_units, k_blocks, units);
+            int64_t most = 1;
+            for (int64_t r = 0; r < units; ++r)
+                most = std::max<int64_t>(most, (start[r + 1] - 1) / k_blocks - start[r] / k_blocks + 1);
+            p.items = units * most;
         }
     }
     if (p.items > kDimLimit) return MPGEMM_ERR_INVALID_VALUE;
@@ -726,8 +759,8 @@ GemmParams make_params(const mpgemm_plan_t& plan, int64_t M, int64_t N, int64_t 
     if (plan.sk_ranges > 0) {   // (the caller sets sk_flags and sk_epoch)
         gp.sk_units = static_cast<int32_t>(plan.tiles * plan.k_blocks);
         gp.sk_ranges = plan.sk_ranges;
-        gp.sk_len = gp.sk_units / gp.sk_ranges;
-        gp.sk_rem = gp.sk_units % gp.sk_ranges;
+        const std::vector<int32_t> start = sk_range_starts(gp.sk_units, plan.k_blocks, plan.sk_ranges);
+        std::copy(start.begin(), start.end(), gp.sk_start);
     }
     return gp;
 }

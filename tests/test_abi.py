@@ -281,26 +281,41 @@ def test_short_k_split_rule(M, K, beta, splits):
     assert (p["k_splits"] - 1) * per < p["k_blocks"] and p["items"] == p["tiles"] * p["k_splits"]
 
 
+def _sk_starts(units, kb, R):
+    """The planner's stream-K boundaries, restated: equal ranges, then each
+    inner boundary within an eighth of a tile's k-blocks of a tile edge moved
+    onto that edge, unless a range would become shorter than one tile."""
+    length, rem, snap = units // R, units % R, max(1, kb // 8)
+    start = [r * length + min(r, rem) for r in range(R + 1)]
+    moved = list(start)
+    for r in range(1, R):
+        off = moved[r] % kb
+        if off and off <= snap:
+            moved[r] -= off
+        elif off and kb - off <= snap:
+            moved[r] += kb - off
+    return moved if all(moved[r + 1] - moved[r] >= kb for r in range(R)) else start
+
+
 def test_stream_k_planning():
     """The stream-K walk: automatic for 320- and 384-wide CTA-pair tiles whose
-    last wave leaves pairs idle; one range of equal length per pair; the
-    items cover the tiles every range touches."""
+    last wave leaves pairs idle; one range of about equal length per pair;
+    the items cover the tiles every range touches."""
     p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257)
     assert (p["tile_m"], p["tile_n"], p["tiles"], p["k_blocks"]) == (256, 320, 256, 65)   # (row-class shift)
     ranges, kb = p["sk_ranges"], p["k_blocks"]
     assert ranges == 76 and p["grid"] == 2 * ranges
-    length = p["tiles"] * kb // ranges                  # 218 k-blocks, 72 ranges hold 219
-    assert length >= kb
-    per_range = -(-(length + 1) // kb) + 1
-    assert p["items"] == ranges * per_range
-    # every range touches at most per_range tiles: brute force over the ranges
-    units, rem = p["tiles"] * kb, p["tiles"] * kb % ranges
-    for r in range(ranges):
-        u0 = r * length + min(r, rem)
-        u1 = u0 + length + (1 if r < rem else 0)
-        assert (u1 - 1) // kb - u0 // kb + 1 <= per_range
-        if r == ranges - 1:
-            assert u1 == units
+    units = p["tiles"] * kb
+    start = _sk_starts(units, kb, ranges)
+    assert start[0] == 0 and start[-1] == units
+    lengths = [start[r + 1] - start[r] for r in range(ranges)]
+    assert min(lengths) >= kb and sum(lengths) == units
+    # no piece of a tile shorter than an eighth of its k-blocks at any boundary
+    assert all(s_ % kb == 0 or kb // 8 < s_ % kb < kb - kb // 8 for s_ in start)
+    # lengths within two eighths of a tile of each other
+    assert max(lengths) - min(lengths) <= 2 * (kb // 8) + 1
+    touched = max((start[r + 1] - 1) // kb - start[r] // kb + 1 for r in range(ranges))
+    assert p["items"] == ranges * touched
     # 384-wide pairs (N from 321 on), and the K-major B variant
     p = _plan(M=65536, N=384, K=4096, lda=4096, ldb=384, ldc=384)
     assert p["tile_n"] == 384 and p["sk_ranges"] == 76
