@@ -232,7 +232,8 @@ typedef struct {
     int32_t stage_b;        /* 1 if B is copied to an aligned buffer first */
     int32_t tile_m;         /* rows per output tile: 128 (one CTA) or 256 (a CTA pair) */
     int32_t tile_n;         /* columns per output tile (128, 256 or 320; 256 or 512 for a pair) */
-    int32_t tile_k;         /* K per pipeline stage (64) */
+    int32_t tile_k;         /* K per pipeline stage (64, or 128 for tiles that stage two
+                               64-wide k-blocks at once); k_blocks counts these stages */
     int32_t stages;         /* shared-memory pipeline depth */
     int32_t m_tiles, n_tiles, k_blocks;
     int64_t tiles;          /* m_tiles * n_tiles */

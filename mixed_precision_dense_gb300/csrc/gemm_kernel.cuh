@@ -149,7 +149,7 @@ struct GemmParams {
 enum : int32_t { kRoleLoad = 1, kRoleMma = 2, kRoleEpilogue = 3 };
 enum : int32_t { kStatusTimeout = 1 };
 
-template <int BN_, int STAGES_, bool PAIR_, bool B_KMAJOR_ = false, int ISSUERS_ = (BN_ == 512 ? 2 : 1)>
+template <int BN_, int STAGES_, bool PAIR_, bool B_KMAJOR_ = false, int ISSUERS_ = (BN_ == 512 ? 2 : 1), int KPS_ = 1>
 struct TileConfig {
     static constexpr bool PAIR = PAIR_;
     // B column-major ([N, K] rows of K): a K-major operand like A. Its 64-row
@@ -163,6 +163,15 @@ struct TileConfig {
     static constexpr int BN = BN_;                     // columns per output tile
     static constexpr int B_COLS = BN / CTAS;           // columns of B each CTA loads
     static constexpr int BK = 64;                      // 64 halves = one 128-byte swizzle row
+    // 64-wide k-blocks per pipeline stage: each stage holds KPS of them, A's
+    // and B's boxes for each one after the other, and the kernel's k-block
+    // unit (k_blocks, split-K slices, stream-K ranges) is a whole stage, SK
+    // wide. Two per stage: one barrier round trip per 128 k, and each row of
+    // A read 256 contiguous bytes at a time (a probe streaming the
+    // tall-skinny pattern, no MMA: A from DRAM 4.2-4.6 TB/s with one per
+    // stage, 5.3-5.5 TB/s with two)
+    static constexpr int KPS = KPS_;
+    static constexpr int SK = BK * KPS;
     static constexpr int STAGES = STAGES_;
     // threads issuing MMAs: one, or two. With two, a 512-wide tile gives
     // each issuer one part (a 256-column range) of the accumulator; a
@@ -212,9 +221,11 @@ struct TileConfig {
     // B boxes (64 columns) per part held by one CTA: a pair CTA holds half
     // of every part's columns
     static constexpr int ATOMS_PER_PART = SUB_N / (PAIR ? 128 : 64);
-    static constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+    static constexpr int A_SUB_BYTES = BM * BK * 2;    // one 64-wide k-block of A: 16 KB
+    static constexpr int A_BYTES = A_SUB_BYTES * KPS;
     static constexpr int B_ATOM_BYTES = BK * 64 * 2;   // one 64-column box of B: 8 KB
-    static constexpr int B_BYTES = BK * B_COLS * 2;
+    static constexpr int B_SUB_BYTES = BK * B_COLS * 2;   // B of one 64-wide k-block
+    static constexpr int B_BYTES = B_SUB_BYTES * KPS;
     static constexpr int B_TAIL_BYTES = BK * 32 * 2;   // one narrow box: 32 columns of 64 K-rows
     // epilogue warps: 8, two per 32 tensor-memory lanes, each taking half of
     // every part's columns. The 256 x 512 tile's single accumulator is
@@ -252,7 +263,8 @@ struct TileConfig {
     static_assert(!PAIR || BN >= 256, "pair tiles are 256 x 256, 256 x 320, 256 x 384 or 256 x 512");
     static_assert(ISSUERS == 1 || ISSUERS == SUBS || (KSPLIT && SUBS == 1), "one issuer, one per part, or two by k-block");
     static_assert(SUB_N >= (PAIR ? 128 : 64) && ATOMS_PER_PART >= 1, "parts hold whole B boxes");
-    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment");
+    static_assert(A_SUB_BYTES % 1024 == 0 && B_SUB_BYTES % 1024 == 0, "stage alignment");
+    static_assert(KPS == 1 || KPS == 2, "k-blocks per stage");
     static_assert(OFF_EPI % 1024 == 0, "chunk buffers are 1024-byte aligned (128-byte swizzle atoms)");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "tensor memory allocation");
@@ -764,7 +776,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     // only the boxes that hold valid columns (a pair CTA holds
                     // half of every part's columns)
                     const int32_t n_atoms = n_valid / (64 * Cfg::CTAS);
-                    const uint32_t bytes = (Cfg::A_BYTES + (n_valid / Cfg::CTAS) * BK * 2) * Cfg::CTAS;
+                    const uint32_t bytes = (Cfg::A_BYTES + (n_valid / Cfg::CTAS) * Cfg::SK * 2) * Cfg::CTAS;
                     for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                         if (!waiter.wait(empty_bar(stage), phase ^ 1u)) {
                             waiter.fail(kRoleLoad, kb);
@@ -774,34 +786,49 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         if constexpr (PAIR) {
                             const uint32_t lead_full = ptx::mapa_shared(full_bar(stage), 0);
                             if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
-                            ptx::tma_load_2d_pair(sA + stage * Cfg::A_BYTES, map_a, lead_full, kb * BK,
-                                                  a_row, pol_a);
-                            // part h (an MMA instruction's columns): this CTA loads
-                            // its half of them, in 64-column boxes from box h *
-                            // ATOMS_PER_PART on
-                            for (int32_t h = 0; h * Cfg::SUB_N < n_valid; ++h) {
-                                const int32_t half = min(Cfg::SUB_N, n_valid - h * Cfg::SUB_N) / 2;
-                                const int32_t c0 = w.n0 + h * Cfg::SUB_N + static_cast<int32_t>(rank) * half;
-                                const uint32_t dst = sB + stage * Cfg::B_BYTES + h * Cfg::ATOMS_PER_PART * Cfg::B_ATOM_BYTES;
-                                if (Cfg::NARROW_TAIL && half == 32) {
-                                    ptx::tma_load_2d_pair(dst, &maps.b_tail, lead_full, c0, kb * BK - b_shift, pol_b);
-                                    continue;
-                                }
-                                for (int32_t a = 0; a * 64 < half; ++a) {
-                                    const int32_t col = c0 + a * 64;
-                                    ptx::tma_load_2d_pair(dst + a * Cfg::B_ATOM_BYTES, &tmap_b, lead_full,
-                                                          Cfg::B_KMAJOR ? kb * BK : col,
-                                                          Cfg::B_KMAJOR ? col : kb * BK - b_shift, pol_b);
+                            // the stage's KPS k-blocks of A first (back to back: 64 * KPS
+                            // contiguous halves of every row), then their B
+#pragma unroll
+                            for (int q = 0; q < Cfg::KPS; ++q)
+                                ptx::tma_load_2d_pair(sA + stage * Cfg::A_BYTES + q * Cfg::A_SUB_BYTES, map_a, lead_full,
+                                                      kb * Cfg::SK + q * BK, a_row, pol_a);
+#pragma unroll
+                            for (int q = 0; q < Cfg::KPS; ++q) {
+                                const int32_t k0 = kb * Cfg::SK + q * BK;
+                                // part h (an MMA instruction's columns): this CTA loads
+                                // its half of them, in 64-column boxes from box h *
+                                // ATOMS_PER_PART on
+                                for (int32_t h = 0; h * Cfg::SUB_N < n_valid; ++h) {
+                                    const int32_t half = min(Cfg::SUB_N, n_valid - h * Cfg::SUB_N) / 2;
+                                    const int32_t c0 = w.n0 + h * Cfg::SUB_N + static_cast<int32_t>(rank) * half;
+                                    const uint32_t dst = sB + stage * Cfg::B_BYTES + q * Cfg::B_SUB_BYTES +
+                                                         h * Cfg::ATOMS_PER_PART * Cfg::B_ATOM_BYTES;
+                                    if (Cfg::NARROW_TAIL && half == 32) {
+                                        ptx::tma_load_2d_pair(dst, &maps.b_tail, lead_full, c0, k0 - b_shift, pol_b);
+                                        continue;
+                                    }
+                                    for (int32_t a = 0; a * 64 < half; ++a) {
+                                        const int32_t col = c0 + a * 64;
+                                        ptx::tma_load_2d_pair(dst + a * Cfg::B_ATOM_BYTES, &tmap_b, lead_full,
+                                                              Cfg::B_KMAJOR ? k0 : col, Cfg::B_KMAJOR ? col : k0 - b_shift,
+                                                              pol_b);
+                                    }
                                 }
                             }
                         } else {
                             ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
-                            ptx::tma_load_2d(sA + stage * Cfg::A_BYTES, map_a, full_bar(stage), kb * BK,
-                                             a_row, pol_a);
-                            for (int j = 0; j < n_atoms; ++j)
-                                ptx::tma_load_2d(sB + stage * Cfg::B_BYTES + j * Cfg::B_ATOM_BYTES,
-                                                 &tmap_b, full_bar(stage), Cfg::B_KMAJOR ? kb * BK : w.n0 + j * 64,
-                                                 Cfg::B_KMAJOR ? w.n0 + j * 64 : kb * BK - b_shift, pol_b);
+#pragma unroll
+                            for (int q = 0; q < Cfg::KPS; ++q)
+                                ptx::tma_load_2d(sA + stage * Cfg::A_BYTES + q * Cfg::A_SUB_BYTES, map_a, full_bar(stage),
+                                                 kb * Cfg::SK + q * BK, a_row, pol_a);
+#pragma unroll
+                            for (int q = 0; q < Cfg::KPS; ++q) {
+                                const int32_t k0 = kb * Cfg::SK + q * BK;
+                                for (int j = 0; j < n_atoms; ++j)
+                                    ptx::tma_load_2d(sB + stage * Cfg::B_BYTES + q * Cfg::B_SUB_BYTES + j * Cfg::B_ATOM_BYTES,
+                                                     &tmap_b, full_bar(stage), Cfg::B_KMAJOR ? k0 : w.n0 + j * 64,
+                                                     Cfg::B_KMAJOR ? w.n0 + j * 64 : k0 - b_shift, pol_b);
+                            }
                         }
                         if (rank == 0) {
                             armed |= 1u << stage;
@@ -957,10 +984,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         const uint32_t b_part =
                             b_base + static_cast<uint32_t>(h * Cfg::ATOMS_PER_PART * Cfg::B_ATOM_BYTES);
 #pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk) {
+                        for (int k16 = 0; k16 < Cfg::SK / 16; ++k16) {
+                            // (64-wide k-block q of the stage, its 16-wide slice kk)
+                            const int q = k16 / (BK / 16), kk = k16 % (BK / 16);
+                            const uint32_t b_q = b_part + static_cast<uint32_t>(q * Cfg::B_SUB_BYTES);
                             // A: K-major, 128-byte rows, 8-row groups 1024 B apart;
                             //    the k-th 16-wide slice starts 32 bytes further.
-                            const uint64_t a_desc = ptx::smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                            const uint64_t a_desc =
+                                ptx::smem_desc_sw128(a_base + q * Cfg::A_SUB_BYTES + kk * 32, 16, 1024);
                             // B row-major: N-major, 64-column boxes B_ATOM_BYTES apart
                             //    (leading offset), 8 K-rows of 128 B per group (stride
                             //    offset); the k-th 16-row slice starts 16 * 128 bytes
@@ -969,14 +1000,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             //    64-byte swizzle, 8 K-rows of 64 B per group, the
                             //    k-th 16-row slice 16 * 64 bytes further.
                             const uint64_t b_desc =
-                                Cfg::B_KMAJOR ? ptx::smem_desc_sw128(b_part + kk * 32, 16, 1024)
+                                Cfg::B_KMAJOR ? ptx::smem_desc_sw128(b_q + kk * 32, 16, 1024)
                                 : (Cfg::NARROW_TAIL && part_cols == 64)
-                                    ? ptx::smem_desc(b_part + kk * 1024, Cfg::B_TAIL_BYTES, 512, ptx::kLayoutSw64)
-                                    : ptx::smem_desc_sw128(b_part + kk * 2048, Cfg::B_ATOM_BYTES, 1024);
+                                    ? ptx::smem_desc(b_q + kk * 1024, Cfg::B_TAIL_BYTES, 512, ptx::kLayoutSw64)
+                                    : ptx::smem_desc_sw128(b_q + kk * 2048, Cfg::B_ATOM_BYTES, 1024);
                             if constexpr (PAIR)
-                                ptx::mma_f16_pair(d_part, a_desc, b_desc, idesc, (kb != w.kb0) || kk != 0);
+                                ptx::mma_f16_pair(d_part, a_desc, b_desc, idesc, (kb != w.kb0) || k16 != 0);
                             else
-                                ptx::mma_f16(d_part, a_desc, b_desc, idesc, (kb != w.kb0) || kk != 0);
+                                ptx::mma_f16(d_part, a_desc, b_desc, idesc, (kb != w.kb0) || k16 != 0);
                         }
                         pending = true;
                     }

@@ -47,7 +47,7 @@ using Cfg128 = TileConfig<128, 6, false>;   // one CTA per 128 x 128 tile
 // one CTA per 128 x 320 tile (N from 257 to 320 in one tile column): 56 KB
 // stages, so three of them, and one accumulator buffer
 using Cfg320 = TileConfig<320, 3, false>;
-using CfgPair = TileConfig<256, 6, true, false, 2>;   // a CTA pair per 256 x 256 tile, two MMA issuers
+using CfgPair = TileConfig<256, 3, true, false, 2, 2>;   // a CTA pair per 256 x 256 tile, two MMA issuers
                                                       // taking alternate k-blocks in a fixed order
 using CfgWide = TileConfig<512, 4, true>;   // a CTA pair per 256 x 512 tile
 // a CTA pair per 256 x 384 tile (parts of 256 and 128 columns, one MMA
@@ -259,6 +259,19 @@ std::vector<int32_t> sk_range_starts(int64_t units, int64_t k_blocks, int64_t R)
     return moved;
 }
 
+// 64-wide k-blocks per pipeline stage of the kernel a plan launches.
+int32_t plan_kps(int32_t tile_m, int32_t tile_n, bool b_col_major) {
+    if (tile_m == 256) {
+        if (tile_n == 512) return b_col_major ? CfgWideK::KPS : CfgWide::KPS;
+        if (tile_n == 384) return b_col_major ? CfgPair384K::KPS : CfgPair384::KPS;
+        if (tile_n == 320) return CfgPair320::KPS;
+        return b_col_major ? CfgPairK::KPS : CfgPair::KPS;
+    }
+    if (tile_n == 320) return b_col_major ? Cfg320K::KPS : Cfg320::KPS;
+    if (tile_n == 256) return b_col_major ? Cfg256K::KPS : Cfg256::KPS;
+    return b_col_major ? Cfg128K::KPS : Cfg128::KPS;
+}
+
 mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                           const void* B, int64_t ldb, float beta, const void* C, int64_t ldc,
                           int32_t num_sms, const Options& opt, mpgemm_plan_t* out) {
@@ -318,13 +331,14 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     const AClassLayout L = a_class_layout(A, lda, M, a_classes, p.tile_m);
     p.a_classes = a_classes ? L.P : 0;
     const int64_t m_tiles = L.first_tile[L.P], n_tiles = ceil_div(N, p.tile_n);
-    const int64_t k_blocks = ceil_div(K + L.max_shift, 64);
+    p.tile_k = 64 * plan_kps(p.tile_m, p.tile_n, opt.b_col_major != 0);
+    const int64_t k_blocks = ceil_div(K + L.max_shift, p.tile_k);
     if (m_tiles * n_tiles > kDimLimit / 2) return MPGEMM_ERR_INVALID_VALUE;
     p.m_tiles = static_cast<int32_t>(m_tiles);
     p.n_tiles = static_cast<int32_t>(n_tiles);
     p.k_blocks = static_cast<int32_t>(k_blocks);
     p.tiles = m_tiles * n_tiles;
-    p.last_k_valid = static_cast<int32_t>(K - (k_blocks - 1) * 64);
+    p.last_k_valid = static_cast<int32_t>(K - (k_blocks - 1) * p.tile_k);
     // persistent grid: one CTA (single) or one CTA pair (pair) per SM or SM pair
     const int64_t per_unit = pair ? 2 : 1;
     int64_t units = num_sms / per_unit;

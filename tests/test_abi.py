@@ -162,7 +162,7 @@ def test_tile_selection_and_grid():
     assert p["split_tiles"] == 0 and p["items"] == 512
     # the same square with a short K keeps 256 x 256 pair tiles
     p = _plan(M=8192, N=8192, K=1024, lda=1024, ldb=8192, ldc=8192)
-    assert (p["tile_m"], p["tile_n"]) == (256, 256) and p["stages"] == 6
+    assert (p["tile_m"], p["tile_n"]) == (256, 256) and p["stages"] == 3 and p["tile_k"] == 128   # two 64-wide k-blocks per stage
     # 512-wide tiles on request, also for small or ragged shapes; never with one CTA per tile
     p = _plan(M=300, N=700, K=200, lda=200, ldb=700, ldc=700, tile_n=512)
     assert (p["tile_m"], p["tile_n"]) == (256, 512) and p["tiles"] == 2 * 2 and p["grid"] == 8
