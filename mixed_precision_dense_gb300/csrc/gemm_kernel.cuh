@@ -44,20 +44,25 @@
 //           column, so that every row block of A is read once), two
 //           instructions per K step (N = 256 and N = 64) into one
 //           accumulator buffer whose two parts are handed back one by one;
-//   pair    a cluster of two CTAs per tile of 256 x BN (BN = 256 or 512):
-//           each CTA loads its own 128 rows of A and its own half of the B
-//           columns of every accumulator part; the even CTA issues
+//   pair    a cluster of two CTAs per tile of 256 x BN (BN = 256, 320, 384
+//           or 512): each CTA loads its own 128 rows of A and its own half of
+//           the B columns of every accumulator part; the even CTA issues
 //           tcgen05.mma with cta_group::2 (M = 256; N = 256, the full width
-//           of a 256 x 256 tile, or per 256-column part of a 256 x 512 tile)
-//           over both
-//           CTAs' shared memory, and each CTA's tensor memory receives its
-//           own 128 rows of the accumulator. Per SM the 256 x 256 tile moves
-//           a third less operand data per FLOP than the single 128 x 256
-//           shape, the 256 x 512 tile half as much. The 512-wide accumulator
-//           fills the whole tensor memory, so that shape has one accumulator
-//           buffer, whose two 256-column parts go back to their MMA threads
-//           one by one as the epilogue drains them.
+//           of a 256 x 256 tile, or per part of a wider tile: 256 + 64, 256
+//           + 128, 256 + 256) over both CTAs' shared memory, and each CTA's
+//           tensor memory receives its own 128 rows of the accumulator. Per
+//           SM the 256 x 256 tile moves a third less operand data per FLOP
+//           than the single 128 x 256 shape, the 256 x 512 tile half as
+//           much. The 384- and 512-wide accumulators leave room for one
+//           buffer, whose parts go back to their MMA threads one by one as
+//           the epilogue drains them; the 320-wide one alternates two
+//           staggered layouts (TileConfig::STAGGER).
 //
+// A stage holds one or two 64-wide k-blocks (TileConfig::KPS). The pairs of
+// 256 to 384 columns can also walk the problem in stream-K ranges (one
+// contiguous range of k-blocks per pair, GemmParams::sk_units) instead of
+// whole tiles.
+
 // The staged-tile reuse, asynchronous copies and block rasterisation that the
 // pages build up with WMMA ("Day 80", "Worked path"; "02_mixed_precision_gemm"
 // README, "Summary": cp.async double buffering and cross-block L2 reuse) map
