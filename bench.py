@@ -42,6 +42,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -121,19 +122,28 @@ def workload_config(w, world: int) -> dict:
             "alpha": w.alpha, "beta": w.beta, "inputs": w.dist, "parallelism": f"replicas x{world}"}
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments and blank space (string literals in
+    these files hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_hash() -> str:
     """Hash of what fixes the tensor-core kernel's memory traffic: its device
-    sources and the tile configurations it is instantiated with. A stored ncu
-    traffic figure is only reported while this hash matches."""
+    code (comments and layout aside) and the tile configurations it is
+    instantiated with. A stored ncu traffic figure is only reported while
+    this hash matches."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mixed_precision_dense_gb300", "csrc")
     for name in ("gemm_kernel.cuh", "ptx.cuh"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name)) as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
     with open(os.path.join(csrc, "mpgemm.cu")) as f:
         for line in f:
             if line.startswith("using Cfg"):
-                h.update(line.encode())
+                h.update(_code_only(line).encode())
     return h.hexdigest()[:16]
 
 
