@@ -86,32 +86,56 @@ namespace mpgemm {
 
 // A is read through one tensor map per "row class". Usually there is one
 // class holding every row. When A's rows do not start on 16-byte boundaries
-// (an odd lda, say), the rows whose start addresses agree modulo 16 form a
-// class: rows i = r (mod P), P <= 8, have a row stride of P * lda * 2 bytes,
-// a multiple of 16, so TMA can read them from the aligned address just below
-// row r, where they sit shifted right by a_shift[r] elements. A tile then
-// holds 128 rows of one class, and the matching B rows are fetched a_shift[r]
-// rows earlier (rows before 0 arrive as zeros).
-constexpr int kMaxAClasses = 8;
+// (an odd lda, say), the rows whose start addresses agree modulo U (U = 16,
+// or U = 128: one L2 line) form a class: rows i = r (mod P), with P * lda * 2
+// a multiple of U, so TMA can read them from the U-aligned address at or
+// below row r, where they sit shifted right by a_shift(r) elements (up to 7,
+// or up to 63). A tile then holds 128 rows of one class, and the matching B
+// rows are fetched a_shift(r) rows earlier (rows before 0 arrive as zeros).
+// With U = 128 every box row of A is one whole L2 line (measured on GB300,
+// 65536 x 257 x 4093: rows starting mid-line cost 7 % at this size).
+// P <= 8 for U = 16; U = 128 takes up to 64 classes, whose 8 KB of tensor
+// maps only the tall-skinny kernels carry (TileConfig::A_CLASSES): larger
+// kernel parameters cost the small calls about 0.2-0.5 us per launch.
+constexpr int kMaxAClasses = 64;
+// The kernels with room for 8 classes read each class's geometry from
+// tables of 8 (the 64-class ones compute it: GemmParams; tables of 64, or
+// the closed form in the 8-class kernels, cost the 256 x 384 pair 60 more
+// bytes of spilled registers).
+constexpr int kTableAClasses = 8;
 
 // Most ranges of a stream-K walk (one per CTA pair).
 constexpr int kMaxSkRanges = 128;
 
-// The tensor maps of A (one per row class), of C (FP32, 32 x 32 boxes,
-// 128-byte swizzle; used only when GemmParams::c_tma is set) and of B in
-// narrow boxes (used only by 256 x 320 pair tiles).
-struct TensorMaps {
-    CUtensorMap a[kMaxAClasses];
+// The tensor maps of A (one per row class, room for NC classes), of C
+// (FP32, 32 x 32 boxes, 128-byte swizzle; used only when GemmParams::c_tma
+// is set) and of B in narrow boxes (used only by 256 x 288 and 256 x 320
+// pair tiles).
+template <int NC>
+struct TensorMapsT {
+    CUtensorMap a[NC];
     CUtensorMap c;
-    CUtensorMap b_tail;   // B in 32-column boxes, 64-byte swizzle (the narrow last part of a 320-wide pair)
+    CUtensorMap b_tail;   // B in 16- or 32-column boxes (32- or 64-byte swizzle): the narrow last part
 };
+using TensorMaps = TensorMapsT<kMaxAClasses>;
 
 struct GemmParams {
     int32_t M, N, K;
-    int32_t a_classes;                               // P >= 1
-    int32_t a_shift[kMaxAClasses];                   // elements left of each class's rows
-    int32_t a_class_rows[kMaxAClasses];              // rows in class r: ceil((M - r) / P)
-    int32_t a_class_first_tile[kMaxAClasses + 1];    // first M-tile of each class
+    // Row classes of A (P of them; P = 1: every row, no shift). With M = P q
+    // + m, classes r < m hold q + 1 rows (a_tiles_hi M-tiles), the others q
+    // (a_tiles_lo); the M-tiles of class 0 come first, then those of class
+    // 1, and so on. Class r's rows sit a_shift(r) = ((a_off0 + r a_step) mod
+    // a_unit) / 2 elements right of the aligned address its tensor map
+    // starts at (a_off0: A's address mod a_unit; a_step: 2 lda mod a_unit).
+    int32_t a_classes;                  // P >= 1
+    int32_t a_unit, a_off0, a_step;
+    int32_t a_rem;                      // m
+    int32_t a_rows_hi, a_rows_lo;       // q + 1, q
+    int32_t a_tiles_hi, a_tiles_lo;
+    // the same as tables, for P <= 8: shift, rows and first M-tile of class r
+    int32_t a_shift[kTableAClasses];
+    int32_t a_class_rows[kTableAClasses];
+    int32_t a_class_first_tile[kTableAClasses + 1];
     int32_t m_tiles, n_tiles, k_blocks;   // tiles counted in units of the kernel's tile
     int32_t tiles;
     int32_t tail_start;     // tiles from here on (raster order) are done as two half-width items
@@ -198,28 +222,32 @@ struct TileConfig {
     static constexpr bool KSPLIT = ISSUERS == 2 && BN_ <= 256;
     // one MMA instruction covers SUB_N columns: BN, except that a tile wider
     // than 256 takes two instructions per K step, of 256 columns and of the
-    // rest (256 for 512-wide pair tiles, 128 for 384-wide ones, 64 for
-    // 320-wide one-CTA tiles)
+    // rest (256 for 512-wide pair tiles, 128 for 384-wide ones, 64 or 32 for
+    // 320- or 288-wide ones)
     static constexpr int SUB_N = BN > 256 ? 256 : BN;
     static constexpr int SUBS = (BN + SUB_N - 1) / SUB_N;
-    // columns of the last part; a pair CTA holds half of them. A 320-wide
-    // pair's last part is 64 columns: each CTA loads its 32 of them as one
-    // 4 KB box in the 64-byte swizzle (row-major B only)
+    // columns of the last part; a pair CTA holds half of them. The last part
+    // of a 320-wide pair is 64 columns, each CTA loading its 32 as one 4 KB
+    // box in the 64-byte swizzle; that of a 288-wide pair 32 columns, 16 per
+    // CTA in a 2 KB box in the 32-byte swizzle (row-major B only). For N =
+    // 257 (one valid column there) the narrower part took 2 % off 65536 x 257
+    // x 4093 and makes room for three stages of two k-blocks.
     static constexpr int TAIL_N = BN - (SUBS - 1) * SUB_N;
-    static constexpr bool NARROW_TAIL = PAIR && TAIL_N == 64;
+    static constexpr bool NARROW_TAIL = PAIR && (TAIL_N == 64 || TAIL_N == 32);
     // two accumulator buffers (the epilogue of tile i overlaps the MMAs of
     // tile i+1) when they fit in the 512 columns of tensor memory, else one,
-    // whose SUBS parts are handed back one by one. A 320-wide pair tile
-    // (STAGGER) alternates between two layouts of its 256- and 64-column
-    // parts in the 512 columns, which overlap only by 64 columns each way:
-    //   even items: 256-column part at column 0,   64-column part at 256
-    //   odd items:  256-column part at column 256, 64-column part at 0
-    // Its epilogue hands back three parts in this order: the 64-column part,
-    // the first 64 columns of the 256-column part, and the other 192. The
-    // next item's 256-column MMAs wait only for the first of them, its
-    // 64-column MMAs for the second; the 192 columns are drained while the
-    // next item's MMAs run (one buffer of 320 columns made them wait for the
-    // whole 256-column part).
+    // whose SUBS parts are handed back one by one. A 320- or 288-wide pair
+    // tile (STAGGER) alternates between two layouts of its 256-column part
+    // and its last part (64 or 32 columns, in a 64-column slot) in the 512
+    // columns, which overlap only by 64 columns each way:
+    //   even items: 256-column part at column 0,   last part at 256
+    //   odd items:  256-column part at column 256, last part at 0
+    // Its epilogue hands back three parts in this order: the last part, the
+    // first 64 columns of the 256-column part, and the other 192. The next
+    // item's 256-column MMAs wait only for the first of them, its last-part
+    // MMAs for the second; the 192 columns are drained while the next item's
+    // MMAs run (one buffer of 320 columns made them wait for the whole
+    // 256-column part).
     static constexpr bool STAGGER = NARROW_TAIL;
     static constexpr int ACC_BUFS = (STAGGER || 2 * BN <= 512) ? 2 : 1;
     static constexpr int RELEASE_PARTS = STAGGER ? 3 : (ACC_BUFS == 1 ? SUBS : 1);
@@ -231,7 +259,7 @@ struct TileConfig {
     static constexpr int B_ATOM_BYTES = BK * 64 * 2;   // one 64-column box of B: 8 KB
     static constexpr int B_SUB_BYTES = BK * B_COLS * 2;   // B of one 64-wide k-block
     static constexpr int B_BYTES = B_SUB_BYTES * KPS;
-    static constexpr int B_TAIL_BYTES = BK * 32 * 2;   // one narrow box: 32 columns of 64 K-rows
+    static constexpr int B_TAIL_BYTES = BK * (TAIL_N / 2) * 2;   // one narrow box: a CTA's tail columns, 64 K-rows
     // epilogue warps: 8, two per 32 tensor-memory lanes, each taking half of
     // every part's columns. The 256 x 512 tile's single accumulator is
     // drained while the MMAs of the next tile wait, and the last tile of
@@ -249,6 +277,10 @@ struct TileConfig {
     static constexpr bool EPI_BATCH_LOADS = BN != 384;
     static constexpr int EPI_CHUNK_BYTES = 32 * 32 * 4;  // one warp's 32 x 32 FP32 chunk buffer
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_CHUNK_BYTES;
+    // row classes of A the kernel's parameters hold room for (see
+    // kMaxAClasses): 64 for the row-major pairs of 288 and 320 columns,
+    // which run the tall-skinny, memory-bound problems, 8 for the rest
+    static constexpr int A_CLASSES = (PAIR && !B_KMAJOR && (BN == 288 || BN == 320)) ? kMaxAClasses : 8;
     // (allocations are powers of two: a 320-column accumulator takes 512)
     static constexpr int TMEM_COLS = (STAGGER || ACC_BUFS * BN > 256) ? 512 : 256;
     // full and empty per stage; accumulator full per buffer; accumulator
@@ -261,11 +293,11 @@ struct TileConfig {
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARRIERS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
     static constexpr int THREADS = 32 * (2 + EPI_WARPS + ISSUERS - 1);
-    static_assert(BN == 128 || BN == 256 || BN == 320 || (PAIR && (BN == 384 || BN == 512)), "tile width");
+    static_assert(BN == 128 || BN == 256 || BN == 320 || (PAIR && (BN == 288 || BN == 384 || BN == 512)), "tile width");
     static_assert(!NARROW_TAIL || (!B_KMAJOR && ISSUERS == 2), "narrow last part: row-major B, one issuer per part");
-    static_assert(STAGGER ? (BN == 320 && SUB_N == 256) : ACC_BUFS * BN <= TMEM_COLS,
+    static_assert(STAGGER ? ((BN == 320 || BN == 288) && SUB_N == 256) : ACC_BUFS * BN <= TMEM_COLS,
                   "accumulators fit the tensor memory allocated");
-    static_assert(!PAIR || BN >= 256, "pair tiles are 256 x 256, 256 x 320, 256 x 384 or 256 x 512");
+    static_assert(!PAIR || BN >= 256, "pair tiles are 256 x 256, 256 x 288, 256 x 320, 256 x 384 or 256 x 512");
     static_assert(ISSUERS == 1 || ISSUERS == SUBS || (KSPLIT && SUBS == 1), "one issuer, one per part, or two by k-block");
     static_assert(SUB_N >= (PAIR ? 128 : 64) && ATOMS_PER_PART >= 1, "parts hold whole B boxes");
     static_assert(A_SUB_BYTES % 1024 == 0 && B_SUB_BYTES % 1024 == 0, "stage alignment");
@@ -273,38 +305,85 @@ struct TileConfig {
     static_assert(OFF_EPI % 1024 == 0, "chunk buffers are 1024-byte aligned (128-byte swizzle atoms)");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "tensor memory allocation");
-    static_assert(BN % 64 == 0 && (TAIL_N % (PAIR ? 128 : 64) == 0 || NARROW_TAIL),
+    static_assert((BN % 64 == 0 || NARROW_TAIL) && (TAIL_N % (PAIR ? 128 : 64) == 0 || NARROW_TAIL),
                   "the last part holds whole B boxes");
+    static_assert(A_CLASSES == 8 || A_CLASSES == kMaxAClasses, "row-class capacities");
 };
 
-// M-tile mb -> (row class r, first class row j0 of the tile).
-template <int TILE_M>
+// M-tile mb -> (row class r, first class row j0 of the tile), in a kernel
+// with room for NC classes.
+template <int TILE_M, int NC>
 __device__ __forceinline__ void a_class_of(const GemmParams& p, int32_t mb, int32_t& r, int32_t& j0) {
-    r = 0;
-    while (r + 1 < p.a_classes && mb >= p.a_class_first_tile[r + 1]) ++r;
-    j0 = (mb - p.a_class_first_tile[r]) * TILE_M;
+    if constexpr (NC <= kTableAClasses) {
+        r = 0;
+        while (r + 1 < p.a_classes && mb >= p.a_class_first_tile[r + 1]) ++r;
+        j0 = (mb - p.a_class_first_tile[r]) * TILE_M;
+        return;
+    }
+    const int32_t hi_tiles = p.a_rem * p.a_tiles_hi;
+    int32_t t;
+    if (mb < hi_tiles) {
+        r = mb / p.a_tiles_hi;
+        t = mb - r * p.a_tiles_hi;
+    } else {
+        const int32_t q = (mb - hi_tiles) / p.a_tiles_lo;
+        r = p.a_rem + q;
+        t = mb - hi_tiles - q * p.a_tiles_lo;
+    }
+    j0 = t * TILE_M;
+}
+// elements before the rows of class r, and the rows it holds
+template <int NC>
+__device__ __forceinline__ int32_t a_shift_of(const GemmParams& p, int32_t r) {
+    if constexpr (NC <= kTableAClasses) return p.a_shift[r];
+    return ((p.a_off0 + r * p.a_step) & (p.a_unit - 1)) >> 1;   // a_unit: 16 or 128
+}
+template <int NC>
+__device__ __forceinline__ int32_t a_rows_of(const GemmParams& p, int32_t r) {
+    if constexpr (NC <= kTableAClasses) return p.a_class_rows[r];
+    return r < p.a_rem ? p.a_rows_hi : p.a_rows_lo;
 }
 
-// Zero the first d (1..7) elements of the first `rows` rows of a 128-row A
-// tile in the 128-byte-swizzled layout (row t's first 16 bytes sit at chunk
-// t & 7). These columns lie before the rows' first element; the matching B
-// rows are zero, but the bytes there are arbitrary and could hold NaN or
-// Inf. Rows past the matrix arrived as zeros already. The 2d bytes are
-// covered by at most three plain stores (8, 4 and 2 bytes) per row, none of
-// which waits for a load: this runs on the MMA thread before the tile's
-// first instructions (a read-modify-write of every row there took about
-// 8 K cycles on GB300).
-__device__ __forceinline__ void zero_leading_columns(uint8_t* tile, int32_t d, int32_t rows) {
-    const bool s8 = d >= 4, s4 = (d & 2) != 0, s2 = (d & 1) != 0;
-    const int32_t o4 = s8 ? 8 : 0;             // offset of the 4-byte store
-    const int32_t o2 = o4 + (s4 ? 4 : 0);      // offset of the 2-byte store
+// Zero elements [16 j, 16 j + d) (d = 1..15) of the first `rows` rows of a
+// 128-row A tile in the 128-byte-swizzled layout (16-byte chunk c of row t
+// sits at chunk c ^ (t & 7)). These are the last of the a_shift = 16 j + d
+// columns that lie before the rows' first element; the MMAs skip the
+// 16-wide K slices below 16 j altogether. The matching B rows are zero, but
+// the bytes there are arbitrary and could hold NaN or Inf. Rows past the
+// matrix arrived as zeros already. At most four plain stores (16, 8, 4 and
+// 2 bytes) per row, none of which waits for a load: this runs on the MMA
+// thread before the tile's first instructions (a read-modify-write of every
+// row there took about 8 K cycles on GB300).
+struct LeadStores {
+    int32_t c16, c;          // chunk of the 16-byte store (if s16), chunk of the partial stores
+    bool s16, s8, s4, s2;
+    int32_t o4, o2;          // offsets of the 4- and 2-byte stores within chunk c
+};
+__device__ __forceinline__ LeadStores lead_stores(int32_t j, int32_t d) {
+    LeadStores z;
+    z.s16 = d >= 8;
+    z.c16 = 2 * j;
+    z.c = 2 * j + (z.s16 ? 1 : 0);
+    const int32_t part = d & 7;
+    z.s8 = part >= 4;
+    z.s4 = (part & 2) != 0;
+    z.s2 = (part & 1) != 0;
+    z.o4 = z.s8 ? 8 : 0;
+    z.o2 = z.o4 + (z.s4 ? 4 : 0);
+    return z;
+}
+
+__device__ __forceinline__ void zero_leading_columns(uint8_t* tile, int32_t j, int32_t d, int32_t rows) {
+    const LeadStores z = lead_stores(j, d);
     rows = min(rows, 128);
 #pragma unroll 8
     for (int32_t t = 0; t < rows; ++t) {
-        uint8_t* q = tile + t * 128 + ((t & 7) << 4);
-        if (s8) *reinterpret_cast<uint64_t*>(q) = 0ull;
-        if (s4) *reinterpret_cast<uint32_t*>(q + o4) = 0u;
-        if (s2) *reinterpret_cast<uint16_t*>(q + o2) = static_cast<uint16_t>(0);
+        uint8_t* row = tile + t * 128;
+        if (z.s16) *reinterpret_cast<uint4*>(row + ((z.c16 ^ (t & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+        uint8_t* q = row + ((z.c ^ (t & 7)) << 4);
+        if (z.s8) *reinterpret_cast<uint64_t*>(q) = 0ull;
+        if (z.s4) *reinterpret_cast<uint32_t*>(q + z.o4) = 0u;
+        if (z.s2) *reinterpret_cast<uint16_t*>(q + z.o2) = static_cast<uint16_t>(0);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -312,17 +391,21 @@ __device__ __forceinline__ void zero_leading_columns(uint8_t* tile, int32_t d, i
 // The same for the A tile of the other CTA of a pair, written through
 // distributed shared memory (tile_c: the tile's cluster address), then
 // ordered before this thread's later tensor-core reads of it.
-__device__ __forceinline__ void zero_leading_columns_peer(uint32_t tile_c, int32_t d, int32_t rows) {
-    const bool s8 = d >= 4, s4 = (d & 2) != 0, s2 = (d & 1) != 0;
-    const uint32_t o4 = s8 ? 8u : 0u;
-    const uint32_t o2 = o4 + (s4 ? 4u : 0u);
+__device__ __forceinline__ void zero_leading_columns_peer(uint32_t tile_c, int32_t j, int32_t d, int32_t rows) {
+    const LeadStores z = lead_stores(j, d);
     rows = min(rows, 128);
 #pragma unroll 8
     for (int32_t t = 0; t < rows; ++t) {
-        const uint32_t q = tile_c + static_cast<uint32_t>(t * 128 + ((t & 7) << 4));
-        if (s8) ptx::st_cluster_u64(q, 0ull);
-        if (s4) ptx::st_cluster_u32(q + o4, 0u);
-        if (s2) ptx::st_cluster_u16(q + o2, static_cast<uint16_t>(0));
+        const uint32_t row = tile_c + static_cast<uint32_t>(t * 128);
+        if (z.s16) {
+            const uint32_t q16 = row + static_cast<uint32_t>((z.c16 ^ (t & 7)) << 4);
+            ptx::st_cluster_u64(q16, 0ull);
+            ptx::st_cluster_u64(q16 + 8, 0ull);
+        }
+        const uint32_t q = row + static_cast<uint32_t>((z.c ^ (t & 7)) << 4);
+        if (z.s8) ptx::st_cluster_u64(q, 0ull);
+        if (z.s4) ptx::st_cluster_u32(q + static_cast<uint32_t>(z.o4), 0u);
+        if (z.s2) ptx::st_cluster_u16(q + static_cast<uint32_t>(z.o2), static_cast<uint16_t>(0));
     }
     ptx::fence_proxy_async_cluster();
 }
@@ -672,8 +755,8 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMa
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ TensorMaps maps, const __grid_constant__ CUtensorMap tmap_b,
-                   const GemmParams p) {
+    gemm_tc_kernel(const __grid_constant__ TensorMapsT<Cfg::A_CLASSES> maps,
+                   const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr bool PAIR = Cfg::PAIR;
 
@@ -687,7 +770,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const uint32_t bar0 = base + Cfg::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    constexpr int ACC_BUFS = Cfg::ACC_BUFS, SUBS = Cfg::SUBS, RELEASE_PARTS = Cfg::RELEASE_PARTS;
+    constexpr int ACC_BUFS = Cfg::ACC_BUFS, RELEASE_PARTS = Cfg::RELEASE_PARTS;
     auto acc_full_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto acc_empty_bar = [&](int b, int h) { return bar0 + 8u * (2 * STAGES + ACC_BUFS + b * RELEASE_PARTS + h); };
     // (KSPLIT) arrived on once the k-block held in stage s has been issued
@@ -718,7 +801,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         ptx::fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        for (int r = 0; r < p.a_classes; ++r) ptx::prefetch_tensormap(&maps.a[r]);
+        for (int r = 0; r < min(p.a_classes, Cfg::A_CLASSES); ++r) ptx::prefetch_tensormap(&maps.a[r]);
         if (p.c_tma) ptx::prefetch_tensormap(&maps.c);
         if constexpr (Cfg::NARROW_TAIL) ptx::prefetch_tensormap(&maps.b_tail);
         ptx::prefetch_tensormap(&tmap_b);
@@ -774,10 +857,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     // belongs to instruction a / per_sub.
                     const int32_t n_valid = item_cols<Cfg>(p, w);
                     int32_t cls, j0;
-                    a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
+                    a_class_of<Cfg::TILE_M, Cfg::A_CLASSES>(p, w.mb, cls, j0);
                     const CUtensorMap* map_a = &maps.a[cls];
                     const int32_t a_row = j0 + static_cast<int32_t>(rank) * BM;   // class row
-                    const int32_t b_shift = p.a_shift[cls];
+                    const int32_t b_shift = a_shift_of<Cfg::A_CLASSES>(p, cls);
                     // only the boxes that hold valid columns (a pair CTA holds
                     // half of every part's columns)
                     const int32_t n_atoms = n_valid / (64 * Cfg::CTAS);
@@ -808,7 +891,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                     const int32_t c0 = w.n0 + h * Cfg::SUB_N + static_cast<int32_t>(rank) * half;
                                     const uint32_t dst = sB + stage * Cfg::B_BYTES + q * Cfg::B_SUB_BYTES +
                                                          h * Cfg::ATOMS_PER_PART * Cfg::B_ATOM_BYTES;
-                                    if (Cfg::NARROW_TAIL && half == 32) {
+                                    if (Cfg::NARROW_TAIL && half == Cfg::TAIL_N / 2) {
                                         ptx::tma_load_2d_pair(dst, &maps.b_tail, lead_full, c0, k0 - b_shift, pol_b);
                                         continue;
                                     }
@@ -886,9 +969,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const int32_t n_valid = item_cols<Cfg>(p, w);
                 const int32_t n_parts = (n_valid + Cfg::SUB_N - 1) / Cfg::SUB_N;
                 int32_t cls, j0;
-                a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
-                const int32_t lead_cols = p.a_shift[cls];   // columns before the rows' start
-                const int32_t lead_rows = p.a_class_rows[cls] - j0;   // rows of the tile that exist
+                a_class_of<Cfg::TILE_M, Cfg::A_CLASSES>(p, w.mb, cls, j0);
+                const int32_t lead_cols = a_shift_of<Cfg::A_CLASSES>(p, cls);   // columns before the rows' start
+                const int32_t lead_rows = a_rows_of<Cfg::A_CLASSES>(p, cls) - j0;   // rows of the tile that exist
+                // k-block 0 of the tile: its first lead_cols / 16 slices of 16
+                // lie wholly before the rows' start and are not issued; the
+                // rest of those columns are zeroed in shared memory
+                const int32_t lead_k16 = lead_cols >> 4, lead_part = lead_cols & 15;
                 const int buf = local % ACC_BUFS;
                 const uint32_t acc_phase = (local / ACC_BUFS) & 1;
                 if constexpr (RELEASE_PARTS == 1) {
@@ -930,13 +1017,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         }
                     }
                     ptx::tc_fence_after_sync();
-                    if (kb == 0 && lead_cols > 0) {
-                        zero_leading_columns(gbase + Cfg::OFF_A + stage * Cfg::A_BYTES, lead_cols, lead_rows);
+                    if (kb == 0 && lead_part > 0) {
+                        zero_leading_columns(gbase + Cfg::OFF_A + stage * Cfg::A_BYTES, lead_k16, lead_part, lead_rows);
                         // the other CTA of a pair holds the tile's next 128 rows
                         if constexpr (PAIR)
-                            zero_leading_columns_peer(ptx::mapa_shared(sA + stage * Cfg::A_BYTES, 1), lead_cols,
-                                                      lead_rows - BM);
+                            zero_leading_columns_peer(ptx::mapa_shared(sA + stage * Cfg::A_BYTES, 1), lead_k16,
+                                                      lead_part, lead_rows - BM);
                     }
+                    const int32_t skip16 = kb == 0 ? lead_k16 : 0;   // slices not issued
                     const uint32_t a_base = sA + stage * Cfg::A_BYTES;
                     const uint32_t b_base = sB + stage * Cfg::B_BYTES;
                     bool pending = false;   // MMAs issued from this stage
@@ -990,6 +1078,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             b_base + static_cast<uint32_t>(h * Cfg::ATOMS_PER_PART * Cfg::B_ATOM_BYTES);
 #pragma unroll
                         for (int k16 = 0; k16 < Cfg::SK / 16; ++k16) {
+                            if (k16 < skip16) continue;
                             // (64-wide k-block q of the stage, its 16-wide slice kk)
                             const int q = k16 / (BK / 16), kk = k16 % (BK / 16);
                             const uint32_t b_q = b_part + static_cast<uint32_t>(q * Cfg::B_SUB_BYTES);
@@ -1001,18 +1090,22 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             //    (leading offset), 8 K-rows of 128 B per group (stride
                             //    offset); the k-th 16-row slice starts 16 * 128 bytes
                             //    further. B column-major: K-major like A.
-                            // A narrow last part (32 columns per CTA): 64-byte rows,
-                            //    64-byte swizzle, 8 K-rows of 64 B per group, the
-                            //    k-th 16-row slice 16 * 64 bytes further.
+                            // A narrow last part (32 or 16 columns per CTA): rows of
+                            //    64 or 32 bytes in the swizzle of that width, 8
+                            //    K-rows per group, the k-th 16-row slice 16 rows
+                            //    further.
+                            constexpr int TAIL_ROW = Cfg::TAIL_N;   // bytes per K-row of a CTA's tail box
                             const uint64_t b_desc =
                                 Cfg::B_KMAJOR ? ptx::smem_desc_sw128(b_q + kk * 32, 16, 1024)
-                                : (Cfg::NARROW_TAIL && part_cols == 64)
-                                    ? ptx::smem_desc(b_q + kk * 1024, Cfg::B_TAIL_BYTES, 512, ptx::kLayoutSw64)
+                                : (Cfg::NARROW_TAIL && part_cols == Cfg::TAIL_N)
+                                    ? ptx::smem_desc(b_q + kk * 16 * TAIL_ROW, Cfg::B_TAIL_BYTES, 8 * TAIL_ROW,
+                                                     TAIL_ROW == 64 ? ptx::kLayoutSw64 : ptx::kLayoutSw32)
                                     : ptx::smem_desc_sw128(b_q + kk * 2048, Cfg::B_ATOM_BYTES, 1024);
+                            const bool acc = (kb != w.kb0) || k16 != skip16;
                             if constexpr (PAIR)
-                                ptx::mma_f16_pair(d_part, a_desc, b_desc, idesc, (kb != w.kb0) || k16 != 0);
+                                ptx::mma_f16_pair(d_part, a_desc, b_desc, idesc, acc);
                             else
-                                ptx::mma_f16(d_part, a_desc, b_desc, idesc, (kb != w.kb0) || k16 != 0);
+                                ptx::mma_f16(d_part, a_desc, b_desc, idesc, acc);
                         }
                         pending = true;
                     }
@@ -1062,9 +1155,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const WorkItem w = work_item<BN, Cfg::STREAM_K>(p, i);
             if (w.n0 >= p.N) continue;
             int32_t cls, j0;
-            a_class_of<Cfg::TILE_M>(p, w.mb, cls, j0);
+            a_class_of<Cfg::TILE_M, Cfg::A_CLASSES>(p, w.mb, cls, j0);
             const int32_t jb = j0 + static_cast<int32_t>(rank) * BM + quarter * 32;  // class row
-            const int32_t rows = min(32, p.a_class_rows[cls] - jb);
+            const int32_t rows = min(32, a_rows_of<Cfg::A_CLASSES>(p, cls) - jb);
             // C rows of class cls are cls, cls + P, cls + 2P, ...
             const int64_t row_stride = static_cast<int64_t>(p.a_classes) * p.ldc;
             float* c_tile = p.C + (cls + static_cast<int64_t>(p.a_classes) * jb) * p.ldc;

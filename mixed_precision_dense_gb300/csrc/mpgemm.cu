@@ -55,8 +55,21 @@ using CfgWide = TileConfig<512, 4, true>;   // a CTA pair per 256 x 512 tile
 using CfgPair384 = TileConfig<384, 4, true, false, 2>;
 // a CTA pair per 256 x 320 tile: parts of 256 and 64 columns, the 64-column
 // part read in 32-column boxes per CTA (4 KB, 64-byte swizzle), so five 36 KB
-// stages fit (N from 257 to 320, row-major B)
+// stages fit (N from 289 to 320, row-major B)
 using CfgPair320 = TileConfig<320, 5, true, false, 2>;
+// a CTA pair per 256 x 288 tile: parts of 256 and 32 columns, the 32-column
+// part read in 16-column boxes per CTA (2 KB, 32-byte swizzle), so five 34 KB
+// stages fit (N from 257 to 288, row-major B). Measured on GB300 at 65536 x
+// 257 x 4093 with lda 4093 (L2 flushed, us, beta 0.5 / 0): 256 x 320 pairs
+// 169.2 / 159.8; 256 x 288 pairs 164.2 / 151.6 (A in 128-byte row classes).
+// Three stages of two k-blocks would be faster still (160.5 / 147.3 with
+// the epilogue's chunk buffers shared, wrongly, by two warps each), but
+// leave 22 KB for the 32 KB of chunk buffers: with 16-row buffers the
+// epilogue took 9 us more; with 32 x 16 ones it spilled 276 bytes of
+// registers; with four epilogue warps beta = 0.5 took 169.4 us (the last
+// item's epilogue, exposed, runs at half the rate); two stages of two
+// k-blocks 181.6 us.
+using CfgPair288 = TileConfig<288, 5, true, false, 2>;
 // the same five shapes for a column-major B (a K-major B operand)
 using Cfg256K = TileConfig<256, 4, false, true>;
 using Cfg128K = TileConfig<128, 6, false, true>;
@@ -66,16 +79,22 @@ using CfgWideK = TileConfig<512, 4, true, true>;
 using CfgPair384K = TileConfig<384, 4, true, true, 2>;
 // stream-K flags per range: one per CTA of the pair and epilogue warp
 constexpr int kSkFlagsPerRange = 2 * CfgPair::EPI_WARPS;
-static_assert(CfgPair::STREAM_K && CfgPair320::STREAM_K && CfgPair384::STREAM_K && !CfgWide::STREAM_K &&
+static_assert(CfgPair::STREAM_K && CfgPair288::STREAM_K && CfgPair320::STREAM_K && CfgPair384::STREAM_K &&
+                  !CfgWide::STREAM_K && CfgPair288::EPI_WARPS == CfgPair::EPI_WARPS &&
                   CfgPair320::EPI_WARPS == CfgPair::EPI_WARPS && CfgPair384::EPI_WARPS == CfgPair::EPI_WARPS,
               "stream-K shapes");
+// the kernels whose parameters hold 64 row classes of A (the rest hold 8)
+static_assert(CfgPair288::A_CLASSES == kMaxAClasses && CfgPair320::A_CLASSES == kMaxAClasses &&
+                  CfgPair384::A_CLASSES == kTableAClasses && CfgPair::A_CLASSES == kTableAClasses &&
+                  CfgWide::A_CLASSES == kTableAClasses && Cfg320::A_CLASSES == kTableAClasses,
+              "row-class capacities");
 // one occupancy query (max_pair_clusters) serves both pair shapes: shared
 // memory limits either to one CTA per SM, and both stay far below the SM's
 // thread and register limits at that occupancy
 static_assert(CfgWide::SMEM_BYTES > 232448 / 2 && CfgPair::SMEM_BYTES > 232448 / 2 &&
                   CfgPair384::SMEM_BYTES > 232448 / 2 && CfgPair320::SMEM_BYTES > 232448 / 2 &&
-                  CfgWide::THREADS <= 384 && CfgPair::THREADS <= 384 && CfgPair384::THREADS <= 384 &&
-                  CfgPair320::THREADS <= 384,
+                  CfgPair288::SMEM_BYTES > 232448 / 2 && CfgWide::THREADS <= 384 && CfgPair::THREADS <= 384 &&
+                  CfgPair384::THREADS <= 384 && CfgPair320::THREADS <= 384 && CfgPair288::THREADS <= 384,
               "the wide pair kernel fits wherever the 256 x 256 pair kernel fits");
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -201,12 +220,35 @@ bool auto_wide(int64_t M, int64_t N, int64_t K, int64_t units) {
     return t512 < t256;
 }
 
-// How the tensor-core pass reads A (see TensorMaps in gemm_kernel.cuh): one row
-// class when A's rows start on 16-byte boundaries (or A was staged), else
-// P = 16 / gcd(2 * lda, 16) classes of rows i = r (mod P), each read from the
-// aligned address at or below row r with a shift of a few elements.
+// How the tensor-core pass reads A (see kMaxAClasses in gemm_kernel.cuh): one
+// row class when A's rows start on 16-byte boundaries (or A was staged), else
+// P classes of rows i = r (mod P), each read from the U-aligned address at or
+// below row r with a shift of (address mod U) / 2 elements, where U = 128
+// when P * lda * 2 is a multiple of 128 (every row of a class then starts at
+// the same offset in its L2 line, and every box row of A is one whole line),
+// else 16. The planner takes P = 16 / gcd(2 lda, 16), or P = 128 / gcd(2 lda,
+// 128) (up to 64) when the kernel has room for that many classes and they
+// cost at most 1/32 more tiles.
+int32_t a_class_unit(int64_t P, int64_t lda) { return (P * 2 * lda) % 128 == 0 ? 128 : 16; }
+
+int64_t a_class_tiles(int64_t M, int64_t P, int64_t tile_m) {
+    int64_t tiles = 0;
+    for (int64_t r = 0; r < P && r < M; ++r) tiles += ceil_div((M - r + P - 1) / P, tile_m);
+    return tiles;
+}
+
+int32_t choose_a_classes(int64_t lda, int64_t M, int64_t tile_m, int32_t capacity) {
+    const int64_t p16 = 16 / std::gcd<int64_t>(2 * lda, 16);
+    const int64_t p128 = 128 / std::gcd<int64_t>(2 * lda, 128);
+    if (p128 > p16 && p128 <= capacity &&
+        a_class_tiles(M, p128, tile_m) * 32 <= a_class_tiles(M, p16, tile_m) * 33)
+        return static_cast<int32_t>(p128);
+    return static_cast<int32_t>(p16);
+}
+
 struct AClassLayout {
     int32_t P = 1;
+    int32_t unit = 16;   // U
     int32_t max_shift = 0;
     int32_t shift[kMaxAClasses] = {};
     int64_t rows[kMaxAClasses] = {};
@@ -214,13 +256,15 @@ struct AClassLayout {
     uintptr_t base[kMaxAClasses] = {};
 };
 
-AClassLayout a_class_layout(const void* A, int64_t lda, int64_t M, bool classes, int64_t tile_m) {
+// classes: the P chosen by the planner, or 0 (one class, no shift)
+AClassLayout a_class_layout(const void* A, int64_t lda, int64_t M, int32_t classes, int64_t tile_m) {
     AClassLayout L;
     const uintptr_t a = reinterpret_cast<uintptr_t>(A);
-    L.P = classes ? static_cast<int32_t>(16 / std::gcd<int64_t>(2 * lda, 16)) : 1;
+    L.P = classes > 0 ? std::min(classes, kMaxAClasses) : 1;
+    L.unit = classes > 0 ? a_class_unit(L.P, lda) : 16;
     for (int32_t r = 0; r < L.P; ++r) {
         const uintptr_t addr = a + static_cast<uintptr_t>(r) * static_cast<uintptr_t>(lda) * 2;
-        const int32_t off = classes ? static_cast<int32_t>(addr % 16) : 0;
+        const int32_t off = classes > 0 ? static_cast<int32_t>(addr % static_cast<uintptr_t>(L.unit)) : 0;
         L.shift[r] = off / 2;
         L.max_shift = std::max(L.max_shift, L.shift[r]);
         L.base[r] = addr - off;
@@ -265,6 +309,7 @@ int32_t plan_kps(int32_t tile_m, int32_t tile_n, bool b_col_major) {
         if (tile_n == 512) return b_col_major ? CfgWideK::KPS : CfgWide::KPS;
         if (tile_n == 384) return b_col_major ? CfgPair384K::KPS : CfgPair384::KPS;
         if (tile_n == 320) return CfgPair320::KPS;
+        if (tile_n == 288) return CfgPair288::KPS;
         return b_col_major ? CfgPairK::KPS : CfgPair::KPS;
     }
     if (tile_n == 320) return b_col_major ? Cfg320K::KPS : Cfg320::KPS;
@@ -279,8 +324,9 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     if (st != MPGEMM_OK) return st;
     if (num_sms <= 0) return MPGEMM_ERR_INVALID_VALUE;
     if (opt.tile_n == 512 && opt.tile_m == 128) return MPGEMM_ERR_INVALID_VALUE;   // 512 wide: pairs only
-    // 256 x 320 pairs read B in narrow row-major boxes
+    // 256 x 320 and 256 x 288 pairs read B in narrow row-major boxes; 288 wide: pairs only
     if (opt.tile_n == 320 && opt.tile_m == 256 && opt.b_col_major) return MPGEMM_ERR_INVALID_VALUE;
+    if (opt.tile_n == 288 && (opt.tile_m == 128 || opt.b_col_major)) return MPGEMM_ERR_INVALID_VALUE;
     if (opt.tile_n == 384 && opt.tile_m == 128) return MPGEMM_ERR_INVALID_VALUE;   // 384 wide: pairs only
     mpgemm_plan_t p;
     std::memset(&p, 0, sizeof(p));
@@ -297,7 +343,7 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     }
     p.stage_b = (opt.force_staging || !aligned16(B, ldb, 2)) ? 1 : 0;
     const bool narrow_pair = !opt.tile_m && !opt.tile_n && auto_narrow_pair(M, N, num_sms);
-    const bool pair = opt.tile_n == 512 || opt.tile_n == 384 || narrow_pair ||
+    const bool pair = opt.tile_n == 512 || opt.tile_n == 384 || opt.tile_n == 288 || narrow_pair ||
                       (opt.tile_m ? (opt.tile_m == 256) : (!opt.tile_n && auto_pair(M, N, K, num_sms)));
     if (pair) {
         int64_t pair_units = num_sms / 2;
@@ -306,13 +352,15 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
         pair_units = std::max<int64_t>(1, pair_units);
         const bool wide = opt.tile_n == 512 || (!opt.tile_m && !opt.tile_n && auto_wide(M, N, K, pair_units));
         p.tile_m = 256;
-        p.tile_n = (opt.tile_n == 384 || opt.tile_n == 320) ? opt.tile_n : (wide ? 512 : 256);
-        if (narrow_pair) p.tile_n = (N <= 320 && !opt.b_col_major) ? 320 : 384;
+        p.tile_n = (opt.tile_n == 384 || opt.tile_n == 320 || opt.tile_n == 288) ? opt.tile_n : (wide ? 512 : 256);
+        if (narrow_pair) p.tile_n = opt.b_col_major ? 384 : N <= 288 ? 288 : N <= 320 ? 320 : 384;
         p.stages = p.tile_n == 384   ? CfgPair384::STAGES
                    : p.tile_n == 320 ? CfgPair320::STAGES
+                   : p.tile_n == 288 ? CfgPair288::STAGES
                                      : (wide ? CfgWide::STAGES : CfgPair::STAGES);
         p.smem_bytes = p.tile_n == 384   ? CfgPair384::SMEM_BYTES
                        : p.tile_n == 320 ? CfgPair320::SMEM_BYTES
+                       : p.tile_n == 288 ? CfgPair288::SMEM_BYTES
                                          : (wide ? CfgWide::SMEM_BYTES : CfgPair::SMEM_BYTES);
     } else {
         // (A is read in row classes below when its rows break the 16-byte rule)
@@ -328,8 +376,12 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     const bool a_aligned = aligned16(A, lda, 2);
     const bool a_classes = !a_aligned && !opt.force_staging && !opt.b_col_major;
     p.stage_a = (opt.force_staging || (!a_aligned && !a_classes)) ? 1 : 0;
-    const AClassLayout L = a_class_layout(A, lda, M, a_classes, p.tile_m);
-    p.a_classes = a_classes ? L.P : 0;
+    // room for 64 classes in the row-major pairs of 288 and 320 columns
+    const int32_t class_room = (pair && !opt.b_col_major && (p.tile_n == 288 || p.tile_n == 320))
+                                   ? CfgPair320::A_CLASSES
+                                   : kTableAClasses;
+    p.a_classes = a_classes ? choose_a_classes(lda, M, p.tile_m, class_room) : 0;
+    const AClassLayout L = a_class_layout(A, lda, M, p.a_classes, p.tile_m);
     const int64_t m_tiles = L.first_tile[L.P], n_tiles = ceil_div(N, p.tile_n);
     p.tile_k = 64 * plan_kps(p.tile_m, p.tile_n, opt.b_col_major != 0);
     const int64_t k_blocks = ceil_div(K + L.max_shift, p.tile_k);
@@ -381,12 +433,12 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     } else {
         // If the last wave of tiles would keep at most half of the CTAs (pairs)
         // busy, do those tiles as two half-width items each: the wave then
-        // finishes in half the time. (Not 320- or 384-wide tiles: a 160- or
-        // 192-column half does not follow their 256 + 64 or 256 + 128 column
+        // finishes in half the time. (Not 288-, 320- or 384-wide tiles: a
+        // half does not follow their 256 + 32, 256 + 64 or 256 + 128 column
         // parts.)
         const int64_t tile_units = std::min<int64_t>(units, p.tiles);
         const int64_t rem = p.tiles % tile_units;
-        p.split_tiles = (p.tile_n != 320 && p.tile_n != 384 && p.tiles > tile_units && rem > 0 &&
+        p.split_tiles = (p.tile_n != 288 && p.tile_n != 320 && p.tile_n != 384 && p.tiles > tile_units && rem > 0 &&
                          2 * rem <= tile_units)
                             ? static_cast<int32_t>(rem)
                             : 0;
@@ -394,8 +446,8 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     }
     // Stream-K (MPGEMM_OPT_STREAM_K): CTA pairs of 256 to 384 columns with at
     // least one tile per pair may walk one contiguous range of k-blocks each
-    // instead of whole tiles. Automatic for tall-skinny problems (the 320-
-    // and 384-wide pairs, or one column of 256-wide tiles) when the last wave
+    // instead of whole tiles. Automatic for tall-skinny problems (the 288-,
+    // 320- and 384-wide pairs, or one column of 256-wide tiles) when the last wave
     // of tiles leaves pairs idle. Measured on GB300 with L2 flushed, us:
     //   65536 x 257 x 4093, beta 0.5 (256 tiles on 76 pairs): 186 -> 172;
     //   65536 x 256 x 4096: 121 -> 112 (beta 0), 135 -> 130 (beta 0.5);
@@ -406,7 +458,7 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     if (pair && splits == 1 && !opt.acc16 && opt.stream_k != 1 && p.tile_n <= 384 && p.tiles >= units) {
         const int64_t sk_units = p.tiles * k_blocks;
         const bool want =
-            opt.stream_k == 2 || ((p.tile_n >= 320 || p.n_tiles == 1) && p.tiles % units != 0);
+            opt.stream_k == 2 || ((p.tile_n > 256 || p.n_tiles == 1) && p.tiles % units != 0);
         if (want && sk_units < (int64_t{1} << 31) && units <= kMaxSkRanges) {
             p.sk_ranges = static_cast<int32_t>(units);
             p.split_tiles = 0;
@@ -561,6 +613,38 @@ struct MapCache {
         victim->used = ++clock;
         victim->valid = true;
     }
+
+    // Whole sets of A's class maps when there are more classes than the
+    // entries above hold (up to 64 for one call): keyed by the call's A
+    // (address, pitch, rows, K, classes), two sets kept.
+    struct ClassSet {
+        uint64_t key[6];
+        int32_t n;
+        CUtensorMap a[kMaxAClasses];
+        uint64_t used;
+        bool valid;
+    };
+    ClassSet sets[2] = {};
+
+    bool find_set(const uint64_t (&k)[6], CUtensorMap* out) {
+        for (ClassSet& x : sets) {
+            if (x.valid && std::equal(k, k + 6, x.key)) {
+                x.used = ++clock;
+                std::copy(x.a, x.a + x.n, out);
+                return true;
+            }
+        }
+        return false;
+    }
+    void put_set(const uint64_t (&k)[6], const CUtensorMap* a, int32_t n) {
+        ClassSet* victim = !sets[0].valid ? &sets[0] : !sets[1].valid ? &sets[1]
+                           : (sets[0].used <= sets[1].used ? &sets[0] : &sets[1]);
+        std::copy(k, k + 6, victim->key);
+        victim->n = n;
+        std::copy(a, a + n, victim->a);
+        victim->used = ++clock;
+        victim->valid = true;
+    }
 };
 
 // Row-major FP16 matrix rows x cols with pitch ld (elements), boxes of
@@ -600,9 +684,26 @@ cudaError_t set_smem_attr() {
                                 Cfg::SMEM_BYTES);
 }
 
+// The kernel's tensor maps, cut down to the row classes it has room for
+// (the planner never gives it more).
+template <int NC>
+TensorMapsT<NC> maps_for(const TensorMaps& ta) {
+    if constexpr (NC == kMaxAClasses) {
+        return ta;
+    } else {
+        TensorMapsT<NC> t;
+        std::copy(ta.a, ta.a + NC, t.a);
+        t.c = ta.c;
+        t.b_tail = ta.b_tail;
+        return t;
+    }
+}
+
 template <class Cfg>
 cudaError_t launch_tc(int grid, const TensorMaps& ta, const CUtensorMap& tb, const GemmParams& gp,
                       cudaStream_t stream) {
+    if (gp.a_classes > Cfg::A_CLASSES) return cudaErrorInvalidValue;
+    const TensorMapsT<Cfg::A_CLASSES> maps = maps_for<Cfg::A_CLASSES>(ta);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -620,7 +721,7 @@ cudaError_t launch_tc(int grid, const TensorMaps& ta, const CUtensorMap& tb, con
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<Cfg>, ta, tb, gp);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<Cfg>, maps, tb, gp);
 }
 
 // Clusters of two CTAs of the pair kernel that fit on the device at once.
@@ -674,6 +775,7 @@ cudaError_t prepare_kernels() {
     if (e == cudaSuccess) e = set_smem_attr<CfgPair384>();
     if (e == cudaSuccess) e = set_smem_attr<CfgPair384K>();
     if (e == cudaSuccess) e = set_smem_attr<CfgPair320>();
+    if (e == cudaSuccess) e = set_smem_attr<CfgPair288>();
     return e;
 }
 
@@ -681,21 +783,43 @@ cudaError_t prepare_kernels() {
 // parameters, for A as the kernel will read it (staged or not).
 bool encode_a(const mpgemm_plan_t& plan, const void* a_use, int64_t lda_use, int64_t M, int64_t K,
               TensorMaps* maps, GemmParams* gp, MapCache* cache = nullptr) {
-    std::memset(maps, 0, sizeof(*maps));
-    const AClassLayout L = a_class_layout(a_use, lda_use, M, plan.a_classes > 0, plan.tile_m);
+    const AClassLayout L = a_class_layout(a_use, lda_use, M, plan.a_classes, plan.tile_m);
+    // the classes' geometry in closed form (see GemmParams)
     gp->a_classes = L.P;
-    for (int32_t r = 0; r < kMaxAClasses; ++r) {
-        gp->a_shift[r] = L.shift[r];
-        gp->a_class_rows[r] = static_cast<int32_t>(L.rows[r]);
-        gp->a_class_first_tile[r] = static_cast<int32_t>(L.first_tile[r < L.P ? r : L.P]);
+    gp->a_unit = L.unit;
+    gp->a_off0 = static_cast<int32_t>(reinterpret_cast<uintptr_t>(a_use) % static_cast<uintptr_t>(L.unit));
+    gp->a_step = static_cast<int32_t>((2 * lda_use) % L.unit);
+    gp->a_rem = static_cast<int32_t>(M % L.P);
+    gp->a_rows_lo = static_cast<int32_t>(M / L.P);
+    gp->a_rows_hi = gp->a_rows_lo + 1;
+    gp->a_tiles_lo = static_cast<int32_t>(ceil_div(gp->a_rows_lo, plan.tile_m));
+    gp->a_tiles_hi = static_cast<int32_t>(ceil_div(gp->a_rows_hi, plan.tile_m));
+    if (plan.a_classes == 0) gp->a_off0 = gp->a_step = 0;   // read in place: no shift
+    // (and as tables, for the kernels with room for 8 classes)
+    for (int32_t r = 0; r < kTableAClasses; ++r) {
+        gp->a_shift[r] = r < L.P ? L.shift[r] : 0;
+        gp->a_class_rows[r] = r < L.P ? static_cast<int32_t>(L.rows[r]) : 0;
+        gp->a_class_first_tile[r] = static_cast<int32_t>(L.first_tile[std::min(r, L.P)]);
     }
-    gp->a_class_first_tile[kMaxAClasses] = static_cast<int32_t>(L.first_tile[L.P]);
+    gp->a_class_first_tile[kTableAClasses] = static_cast<int32_t>(L.first_tile[std::min(kTableAClasses, L.P)]);
+    // (every map a kernel receives is defined: the first 8, or all when
+    // there are more classes; C's and B's narrow maps are set later if used)
+    std::memset(maps->a, 0, sizeof(maps->a[0]) * static_cast<size_t>(L.P > 8 ? kMaxAClasses : 8));
+    std::memset(&maps->c, 0, sizeof(maps->c));
+    std::memset(&maps->b_tail, 0, sizeof(maps->b_tail));
+    // more classes than the per-map entries hold: the whole set at once
+    const bool as_set = cache && L.P > MapCache::kEntries / 2;
+    const uint64_t set_key[6] = {static_cast<uint64_t>(L.P), reinterpret_cast<uintptr_t>(a_use),
+                                 static_cast<uint64_t>(lda_use), static_cast<uint64_t>(M),
+                                 static_cast<uint64_t>(K), 0};
+    if (as_set && cache->find_set(set_key, maps->a)) return true;
     for (int32_t r = 0; r < L.P; ++r) {
         if (L.rows[r] == 0) continue;
         if (!encode_f16(&maps->a[r], reinterpret_cast<const void*>(L.base[r]), L.rows[r], K + L.shift[r],
-                        L.P * lda_use, 64, 128, cache))
+                        L.P * lda_use, 64, 128, as_set ? nullptr : cache))
             return false;
     }
+    if (as_set) cache->put_set(set_key, maps->a, L.P);
     return true;
 }
 
@@ -735,11 +859,14 @@ void encode_c(const mpgemm_plan_t& plan, float* C, int64_t M, int64_t N, int64_t
     if (encode_f32_store(&maps->c, C, M, N, ldc, cache)) gp->c_tma = 1;
 }
 
-// The narrow B boxes of 256 x 320 pair tiles (32 columns of 64 K-rows, 64-byte
-// swizzle: the last 64-column part, half per CTA); nothing for other tiles.
+// The narrow B boxes of 256 x 320 and 256 x 288 pair tiles (32 or 16 columns
+// of 64 K-rows, 64- or 32-byte swizzle: the last 64- or 32-column part, half
+// per CTA); nothing for other tiles.
 bool encode_b_tail(const mpgemm_plan_t& plan, const void* b_use, int64_t K, int64_t N, int64_t ldb_use,
                    TensorMaps* maps, MapCache* cache = nullptr) {
-    if (plan.tile_m != 256 || plan.tile_n != 320) return true;
+    if (plan.tile_m != 256 || (plan.tile_n != 320 && plan.tile_n != 288)) return true;
+    if (plan.tile_n == 288)
+        return encode_f16(&maps->b_tail, b_use, K, N, ldb_use, 16, 64, cache, CU_TENSOR_MAP_SWIZZLE_32B);
     return encode_f16(&maps->b_tail, b_use, K, N, ldb_use, 32, 64, cache, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
@@ -802,6 +929,7 @@ cudaError_t launch_plan(const mpgemm_plan_t& plan, bool b_col_major, int max_clu
             return b_col_major ? launch_tc<CfgPair384K>(grid, ta, tb, gp, stream)
                                : launch_tc<CfgPair384>(grid, ta, tb, gp, stream);
         if (plan.tile_n == 320) return launch_tc<CfgPair320>(grid, ta, tb, gp, stream);
+        if (plan.tile_n == 288) return launch_tc<CfgPair288>(grid, ta, tb, gp, stream);
         return b_col_major ? launch_tc<CfgPairK>(grid, ta, tb, gp, stream)
                            : launch_tc<CfgPair>(grid, ta, tb, gp, stream);
     }
@@ -939,7 +1067,8 @@ mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha, const 
                             mpgemm_plan_t* out) {
     if (!out) return MPGEMM_ERR_INVALID_VALUE;
     if (tile_m != 0 && tile_m != 128 && tile_m != 256) return MPGEMM_ERR_INVALID_VALUE;
-    if (tile_n != 0 && tile_n != 128 && tile_n != 256 && tile_n != 320 && tile_n != 384 && tile_n != 512)
+    if (tile_n != 0 && tile_n != 128 && tile_n != 256 && tile_n != 288 && tile_n != 320 && tile_n != 384 &&
+        tile_n != 512)
         return MPGEMM_ERR_INVALID_VALUE;
     if (max_ctas < 0) return MPGEMM_ERR_INVALID_VALUE;
     Options opt;
@@ -1012,7 +1141,8 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
     if (!h) return MPGEMM_ERR_INVALID_VALUE;
     switch (opt) {
         case MPGEMM_OPT_TILE_N:
-            if (value != 0 && value != 128 && value != 256 && value != 320 && value != 384 && value != 512)
+            if (value != 0 && value != 128 && value != 256 && value != 288 && value != 320 && value != 384 &&
+                value != 512)
                 return MPGEMM_ERR_INVALID_VALUE;
             h->opt.tile_n = static_cast<int32_t>(value);
             return MPGEMM_OK;

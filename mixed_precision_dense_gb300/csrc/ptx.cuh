@@ -363,7 +363,7 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t m, uint32_t n, boo
 // tcgen05): bits 0-13 start address >> 4, 16-29 leading-dimension byte
 // offset >> 4, 32-45 stride-dimension byte offset >> 4, 46-48 fixed 0b001,
 // 49-51 base offset (0: tiles are 1024-byte aligned), 61-63 swizzle mode
-// (2 = 128-byte swizzle, 4 = 64-byte swizzle).
+// (2 = 128-byte swizzle, 4 = 64-byte swizzle, 6 = 32-byte swizzle).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
                                               uint32_t layout) {
     return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
@@ -375,6 +375,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 // swizzle modes of the descriptor's layout field
 constexpr uint32_t kLayoutSw128 = 2;   // 128-byte swizzle
 constexpr uint32_t kLayoutSw64 = 4;    // 64-byte swizzle
+constexpr uint32_t kLayoutSw32 = 6;    // 32-byte swizzle
 
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
     return smem_desc(saddr, lbo_bytes, sbo_bytes, kLayoutSw128);

@@ -116,8 +116,10 @@ def test_alignment_classification():
     assert p["workspace_bytes"] == 200 * 624 * 2 + 136 * 624 * 2
     p = _plan(M=2048, N=2048, K=2048, lda=2048, ldb=2048, ldc=2048)
     assert (p["stage_a"], p["stage_b"]) == (0, 0) and p["workspace_bytes"] == 0
+    # the tall-skinny pairs take classes of rows that start at the same offset
+    # in a 128-byte line: 8186-byte rows start at 64 offsets
     p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257, beta=0.5)
-    assert (p["stage_a"], p["stage_b"], p["a_classes"]) == (0, 1, 8)
+    assert (p["stage_a"], p["stage_b"], p["a_classes"]) == (0, 1, 64)
     # lda = 4094: rows start at four offsets; lda = 4100: two
     assert _plan(M=4096, N=257, K=4093, lda=4094, ldb=257, ldc=257)["a_classes"] == 4
     assert _plan(M=4096, N=257, K=4093, lda=4100, ldb=257, ldc=257)["a_classes"] == 2
@@ -131,7 +133,8 @@ def test_alignment_classification():
     p = _plan(M=8192, N=8192, K=8192, lda=8193, ldb=8192, ldc=8192)
     assert p["tile_m"] == 256 and p["stage_a"] == 0 and p["a_classes"] == 8
     assert p["m_tiles"] == 8 * 4
-    # 256 x 384 pair tiles: pairs only, never split into half-width items
+    # 256 x 384 pair tiles (room for 8 row classes): pairs only, never split
+    # into half-width items
     p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257, tile_n=384)
     assert (p["tile_m"], p["tile_n"], p["a_classes"], p["split_tiles"]) == (256, 384, 8, 0)
     with pytest.raises(mp.MpgemmError):
@@ -171,13 +174,17 @@ def test_tile_selection_and_grid():
     with pytest.raises(mp.MpgemmError):
         _plan(tile_m=128, tile_n=512)
     # N = 257 would waste half of the last column band: one tile column of
-    # 256 x 320 CTA pairs (A read once per row block, five 36 KB stages, A in
-    # 8 row classes of 32 pair tiles each)
+    # 256 x 288 CTA pairs (A read once per row block, five 34 KB stages, A in
+    # 64 row classes of 4 pair tiles each)
     p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257, beta=0.5)
-    assert (p["tile_m"], p["tile_n"]) == (256, 320) and p["tiles"] == 256 and p["stages"] == 5
-    assert p["a_classes"] == 8 and p["split_tiles"] == 0 and p["smem_bytes"] <= 232448
+    assert (p["tile_m"], p["tile_n"]) == (256, 288) and p["tiles"] == 256 and p["stages"] == 5
+    assert p["tile_k"] == 64 and p["a_classes"] == 64 and p["split_tiles"] == 0
+    assert 200 * 1024 < p["smem_bytes"] <= 232448
     p = _plan(M=58368, N=257, K=4096, lda=4096, ldb=264, ldc=257, beta=0.5)
-    assert (p["tile_m"], p["tile_n"]) == (256, 320) and p["tiles"] == 228
+    assert (p["tile_m"], p["tile_n"]) == (256, 288) and p["tiles"] == 228
+    # N from 289 to 320: 256 x 320 pairs (five 36 KB stages)
+    p = _plan(M=58368, N=300, K=4096, lda=4096, ldb=304, ldc=300, beta=0.5)
+    assert (p["tile_m"], p["tile_n"], p["stages"], p["tile_k"]) == (256, 320, 5, 64) and p["tiles"] == 228
     # fewer rows than one full wave of pair tiles: one-CTA tiles; with A
     # aligned, a wave of 320-wide tiles (1.9 waves of 256-wide ones) costs
     # more than one wave of 256-wide tiles, and less than two
@@ -197,9 +204,17 @@ def test_tile_selection_and_grid():
     p = _plan(M=5000, N=1000, K=700, lda=700, ldb=1000, ldc=1000, tile_m=256, tile_n=320)
     assert (p["tile_m"], p["tile_n"], p["stages"]) == (256, 320, 5) and p["tiles"] == 20 * 4
     assert p["split_tiles"] == 0
-    # the 256 x 320 pair reads B in narrow row-major boxes: not for a column-major B
+    # the 256 x 320 and 256 x 288 pairs read B in narrow row-major boxes: not
+    # for a column-major B; 288 wide: pairs only
     with pytest.raises(mp.MpgemmError):
         _plan(tile_m=256, tile_n=320, ldb=617, b_col_major=True)
+    with pytest.raises(mp.MpgemmError):
+        _plan(tile_n=288, ldb=617, b_col_major=True)
+    with pytest.raises(mp.MpgemmError):
+        _plan(tile_m=128, tile_n=288)
+    p = _plan(M=5000, N=1000, K=700, lda=700, ldb=1000, ldc=1000, tile_n=288)
+    assert (p["tile_m"], p["tile_n"], p["stages"]) == (256, 288, 5) and p["tiles"] == 20 * 4
+    assert p["split_tiles"] == 0
     # forced pairs with a CTA cap: the grid stays even
     p = _plan(M=1000, N=800, K=64, lda=64, ldb=800, ldc=800, tile_m=256, max_ctas=5)
     assert p["tile_m"] == 256 and p["grid"] == 4 and p["tiles"] == 4 * 4
@@ -229,7 +244,7 @@ def test_tile_selection_and_grid():
         p = _plan(M=256, N=128, K=K, lda=K, ldb=128, ldc=128)
         per = -(-p["k_blocks"] // p["k_splits"])
         assert (p["k_splits"] - 1) * per < p["k_blocks"]
-    # a last wave more than half full is not split in halves; the 320-wide
+    # a last wave more than half full is not split in halves; the 288-wide
     # pairs of this tall-skinny problem walk stream-K ranges instead
     p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257)
     assert p["split_tiles"] == 0 and p["sk_ranges"] == 76
@@ -247,22 +262,61 @@ def test_tile_selection_and_grid():
         _plan(tile_m=64)
 
 
+def _row_classes(lda, M, tile_m, room):
+    """The planner's row classes of an A whose rows are not 16-byte aligned,
+    restated: P16 = 16 / gcd(2 lda, 16) classes (rows at the same offset
+    modulo 16), or P128 = 128 / gcd(2 lda, 128) (the same offset in a 128-byte
+    line) when the kernel has room for them and they cost at most 1/32 more
+    M-tiles."""
+    from math import gcd
+    p16, p128 = 16 // gcd(2 * lda, 16), 128 // gcd(2 * lda, 128)
+    tiles = lambda P: sum(-(-((M - r + P - 1) // P) // tile_m) for r in range(min(P, M)))
+    return p128 if p128 > p16 and p128 <= room and tiles(p128) * 32 <= tiles(p16) * 33 else p16
+
+
+@pytest.mark.parametrize("M,N,K,lda,A,expect", [
+    (65536, 257, 4093, 4093, 256, 64),    # 8186-byte rows: 64 line offsets, 4 pair tiles per class
+    (65536, 257, 4093, 4094, 256, 32),
+    (65536, 257, 4092, 4092, 256, 16),
+    (65536, 300, 4093, 4093, 256, 64),    # the 320-wide pairs too
+    (65536, 384, 4093, 4093, 256, 8),     # the 384-wide ones have room for 8
+    (19456, 257, 4093, 4093, 256, 8),     # 64 classes of 304 rows: 128 pair tiles against 80
+    (19200, 257, 4093, 4093, 256, 8),     # one-CTA tiles: room for 8 classes
+    (8192, 8192, 8192, 8193, 256, 8),     # 256 x 256 pairs: room for 8
+    (4096, 4096, 4096, 4096, 258, 1),     # one class (aligned pitch), shifted by (A mod 128) / 2
+])
+def test_line_aligned_row_classes(M, N, K, lda, A, expect):
+    p = _plan(M=M, N=N, K=K, lda=lda, ldb=N, ldc=N, A=A)
+    assert p["stage_a"] == 0 and p["a_classes"] == expect
+    room = 64 if (p["tile_m"], p["tile_n"]) in ((256, 288), (256, 320)) else 8
+    if lda * 2 % 16:
+        assert expect == _row_classes(lda, M, p["tile_m"], room)
+    P = expect
+    unit = 128 if P * 2 * lda % 128 == 0 else 16
+    shifts = [((A + r * 2 * lda) % unit) // 2 for r in range(P)]
+    rows = [(M - r + P - 1) // P for r in range(P)]
+    assert p["m_tiles"] == sum(-(-n // p["tile_m"]) for n in rows)
+    assert p["k_blocks"] == -(-(K + max(shifts)) // p["tile_k"])
+
+
 @pytest.mark.parametrize("M,N,lda,b_col,expect", [
     (65536, 256, 4093, False, (128, 256)),   # one 256-wide column covers N: one-CTA tiles
-    (65536, 257, 4093, False, (256, 320)),   # the tall-skinny workload: 256 x 320 pairs
+    (65536, 257, 4093, False, (256, 288)),   # the tall-skinny workload: 256 x 288 pairs
+    (58368, 288, 4096, False, (256, 288)),
+    (58368, 289, 4096, False, (256, 320)),   # past 288: 256 x 320 pairs
     (58368, 320, 4096, False, (256, 320)),
     (65536, 321, 4096, False, (256, 384)),   # past 320: 256 x 384 pairs
     (65536, 384, 4096, False, (256, 384)),
     (65536, 300, 4096, True, (256, 384)),    # column-major B: the 384-wide pair
     (65536, 385, 4093, False, (128, 256)),   # past 384: two 256-wide columns of one-CTA tiles
-    (19456, 257, 4093, False, (256, 320)),   # 76 pair tiles: every pair busy
+    (19456, 257, 4093, False, (256, 288)),   # 76 pair tiles: every pair busy
     (19200, 257, 4093, False, (128, 320)),   # 75: the one-CTA rule (row classes: 1.6 waves of 320 < 2)
     (9600, 257, 4096, False, (128, 256)),    # aligned A: 1.9 waves of 320 against one wave of 256
 ])
 def test_narrow_tile_column_rules(M, N, lda, b_col, expect):
     p = _plan(M=M, N=N, K=4093, lda=lda, ldb=4093 if b_col else N + 8, ldc=N, beta=0.5, b_col_major=b_col)
     assert (p["tile_m"], p["tile_n"]) == expect, (M, N, lda)
-    if expect[1] in (320, 384):
+    if expect[1] in (288, 320, 384):
         assert p["split_tiles"] == 0 and p["n_tiles"] == 1
 
 
@@ -298,11 +352,12 @@ def _sk_starts(units, kb, R):
 
 
 def test_stream_k_planning():
-    """The stream-K walk: automatic for 320- and 384-wide CTA-pair tiles whose
-    last wave leaves pairs idle; one range of about equal length per pair;
-    the items cover the tiles every range touches."""
+    """The stream-K walk: automatic for 288-, 320- and 384-wide CTA-pair tiles
+    whose last wave leaves pairs idle; one range of about equal length per
+    pair; the items cover the tiles every range touches."""
     p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257)
-    assert (p["tile_m"], p["tile_n"], p["tiles"], p["k_blocks"]) == (256, 320, 256, 65)   # (row-class shift)
+    # k-blocks over K plus the largest row-class shift (63)
+    assert (p["tile_m"], p["tile_n"], p["tiles"], p["k_blocks"]) == (256, 288, 256, 65)
     ranges, kb = p["sk_ranges"], p["k_blocks"]
     assert ranges == 76 and p["grid"] == 2 * ranges
     units = p["tiles"] * kb
@@ -316,7 +371,9 @@ def test_stream_k_planning():
     assert max(lengths) - min(lengths) <= 2 * (kb // 8) + 1
     touched = max((start[r + 1] - 1) // kb - start[r] // kb + 1 for r in range(ranges))
     assert p["items"] == ranges * touched
-    # 384-wide pairs (N from 321 on), and the K-major B variant
+    # 320- and 384-wide pairs (N from 289 and 321 on), and the K-major B variant
+    p = _plan(M=65536, N=300, K=4096, lda=4096, ldb=304, ldc=300)
+    assert p["tile_n"] == 320 and p["sk_ranges"] == 76
     p = _plan(M=65536, N=384, K=4096, lda=4096, ldb=384, ldc=384)
     assert p["tile_n"] == 384 and p["sk_ranges"] == 76
     p = _plan(M=65536, N=300, K=4096, lda=4096, ldb=4096, ldc=300, b_col_major=True)

@@ -353,6 +353,12 @@ CLASS_CASES = [  # (M, N, K, lda, a_offset, tile_n, split_k): A read in row clas
     (640, 128, 2049, 2049, 3, 128, 4),  # classes with split-K
     (300, 200, 100, 109, 0, 0, 0),      # 9 NaN padding elements: every shift 1..7 lands in NaN
     (1100, 64, 300, 311, 0, 128, 0),    # 137-138 rows per class: second tiles of 9-10 rows
+    # aligned pitch (a multiple of 128 bytes), base off a 16-byte boundary: one
+    # class read from the 128-byte line below, shifted 40 or 63 elements (the
+    # first two or three 16-wide K slices of k-block 0 not issued, 8 or 15
+    # columns zeroed)
+    (300, 200, 256, 256, 40 + 1, 0, 0),
+    (300, 200, 256, 256, 63, 256, 0),
 ]
 
 
@@ -360,6 +366,8 @@ CLASS_CASES = [  # (M, N, K, lda, a_offset, tile_n, split_k): A read in row clas
 def test_a_row_classes(mp, M, N, K, lda, a_offset, tile_n, split_k):
     plan = mp.plan(M, N, K, 1.0, 256 + 2 * a_offset, lda, 256, N, 0.5, 256, N, tile_n=tile_n)
     assert plan["a_classes"] >= 1 and plan["stage_a"] == 0
+    if lda == 256:
+        assert plan["a_classes"] == 1 and plan["k_blocks"] == -(-(K + (2 * a_offset + 256) % 128 // 2) // 64)
     with mp.Handle() as h:
         h.set_option(mp.Option.TILE_N, tile_n)
         h.set_option(mp.Option.SPLIT_K, split_k)
@@ -465,6 +473,53 @@ def test_cta_pair_320_integer_bitwise(mp):
         check_full(h, ops, exact=True)
 
 
+PAIR288_SHAPES = [  # (M, N, K, lda, ldb, ldc, beta, max_ctas): 256 x 288 pair tiles, 32-column last part
+    (256, 288, 64, 64, 288, 288, 0.0, 0),       # one full tile (TMA stores)
+    (256, 257, 617, 617, 257, 257, 0.5, 0),     # one column past 256: the 32-column part, 8 row classes
+    (1000, 280, 700, 700, 280, 281, 1.0, 4),    # two pairs walk 4 tiles through the staggered layouts
+    (511, 700, 129, 129, 700, 700, -0.5, 0),    # three tile columns, the last 124 wide (one 128 unit)
+    (1300, 1100, 333, 335, 1103, 1101, 0.75, 6),  # A in row classes, B staged, C per lane
+    (16384, 270, 300, 365, 270, 270, 0.5, 0),   # A in 64 line-aligned row classes; 65 NaN halves
+                                                 # between rows: every shift (up to 63) starts in NaN
+]
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,beta,max_ctas", PAIR288_SHAPES)
+def test_cta_pair_288_wide_tiles(mp, M, N, K, lda, ldb, ldc, beta, max_ctas):
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_M, 256)
+        h.set_option(mp.Option.TILE_N, 288)
+        h.set_option(mp.Option.MAX_CTAS, max_ctas)
+        ops = workloads.make_operands(M, N, K, lda=lda, ldb=ldb, ldc=ldc, alpha=1.5, beta=beta,
+                                      c_dist="normal" if beta else "zeros", seed=M + 11 * N + K)
+        check_full(h, ops)
+
+
+@pytest.mark.parametrize("M,N,K,lda,classes", [(777, 288, 1021, 1021, 8), (16384, 272, 515, 515, 64)])
+def test_cta_pair_288_integer_bitwise(mp, M, N, K, lda, classes):
+    # every column of the 32-column part exact; A in 16-byte or line-aligned row classes
+    plan = mp.plan(M, N, K, 1.0, 256, lda, 256, N, 0.0, 256, N, tile_m=256, tile_n=288)
+    assert plan["a_classes"] == classes
+    ops = workloads.make_operands(M, N, K, lda=lda, dist="int3", dist_b="int2", seed=91 + classes)
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_M, 256)
+        h.set_option(mp.Option.TILE_N, 288)
+        check_full(h, ops, exact=True)
+
+
+def test_line_aligned_classes_in_320_pairs(mp):
+    # 64 row classes in 256 x 320 pairs, NaN between rows, beta * C
+    plan = mp.plan(16384, 300, 300, 1.0, 256, 365, 256, 300, 0.5, 256, 300, tile_m=256, tile_n=320)
+    assert plan["a_classes"] == 64
+    with mp.Handle() as h:
+        h.set_option(mp.Option.TILE_M, 256)
+        h.set_option(mp.Option.TILE_N, 320)
+        check_full(h, workloads.make_operands(16384, 300, 300, lda=365, alpha=0.75, beta=0.5, c_dist="normal",
+                                              seed=92))
+        check_full(h, workloads.make_operands(16384, 300, 300, lda=365, dist="int3", dist_b="int2", seed=93),
+                   exact=True)
+
+
 @pytest.mark.parametrize("M,N,K", [(600, 100, 300), (600, 640, 300), (700, 129, 129)])
 def test_cta_pair_tiles_trimmed_to_valid_columns(mp, M, N, K):
     # a pair tile's columns are cut to the 128-column units below N (N = 128
@@ -478,7 +533,7 @@ def test_cta_pair_tiles_trimmed_to_valid_columns(mp, M, N, K):
                        exact=True)
 
 
-@pytest.mark.parametrize("tile_n", [320, 384])
+@pytest.mark.parametrize("tile_n", [288, 320, 384])
 def test_tall_skinny_workload_in_pairs(mp, tile_n):
     ops = workloads.workload_operands(4)
     I, J = workloads.workload_sample(4)
@@ -810,7 +865,11 @@ STREAM_K_CASES = [  # (tile_m, tile_n, max_ctas, M, N, K, lda, ldb, ldc, beta, b
     # 256 x 256 pairs, 10 tiles on 3 pairs: TMA stores for whole tiles, per-lane for cut ones
     (256, 256, 6, 1280, 512, 1000, 1000, 512, 512, 0.0, False),
     # 256 x 320 pairs, A in row classes, beta * C on the later k-blocks
-    (256, 320, 6, 1900, 257, 617, 617, 257, 257, 0.5, False),
+    (256, 320, 6, 1900, 300, 617, 617, 300, 300, 0.5, False),
+    # 256 x 288 pairs, A in row classes (16-byte), beta * C on the later k-blocks
+    (256, 288, 6, 1900, 257, 617, 617, 257, 257, 0.5, False),
+    # 256 x 288 pairs, A in 64 line-aligned classes (the walk crosses classes)
+    (256, 288, 20, 16384, 260, 300, 301, 260, 260, 0.5, False),
     # 256 x 384 pairs, beta == 1, unaligned A and C, 6 tiles on 5 pairs
     (256, 384, 10, 1300, 380, 333, 335, 380, 383, 1.0, False),
     # 256 x 384 pairs with a column-major B, 4 tiles on 2 pairs (one range = two tiles)
@@ -852,7 +911,7 @@ def test_stream_k_plan_reaches_the_kernel(mp):
 
 def test_stream_k_identical_bits_on_repeat_and_against_the_whole_tile_walk(mp):
     # The tall-skinny shape the planner walks in stream-K ranges by itself
-    # (256 tiles of 256 x 320 on 76 pairs): identical calls give identical
+    # (256 tiles of 256 x 288 on 76 pairs): identical calls give identical
     # bits, and the whole-tile walk (STREAM_K = 1) agrees within the
     # tolerance; on integers both equal the oracle.
     from parity import device_operands, reference, assert_close
@@ -861,7 +920,7 @@ def test_stream_k_identical_bits_on_repeat_and_against_the_whole_tile_walk(mp):
     plan = mp.plan(M, N, K, 1.0, 256, K, 256, N, 0.5, 256, N)
     if plan["grid"] != 152:
         pytest.skip("written for 76 CTA pairs")
-    assert plan["tile_n"] == 320 and plan["sk_ranges"] == 76
+    assert plan["tile_n"] == 288 and plan["sk_ranges"] == 76
 
     def run(h, ops, n):
         outs = []
