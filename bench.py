@@ -1056,7 +1056,7 @@ def main(argv=None):
     ap.add_argument("--num-sms", type=int, default=152, help="SM count assumed by --record-traffic's plan")
     ap.add_argument("--tile-m", type=int, default=0, choices=[0, 128, 256],
                     help="force the tile height (0 = the library's choice)")
-    ap.add_argument("--tile-n", type=int, default=0, choices=[0, 128, 256, 320, 384, 512],
+    ap.add_argument("--tile-n", type=int, default=0, choices=[0, 128, 256, 288, 320, 384, 512],
                     help="force the tile width (0 = the library's choice)")
     ap.add_argument("--split-k", type=int, default=0,
                     help="slices of K per tile (0 = the library's choice, 1 = never split)")

@@ -23,9 +23,13 @@
  *    ldc >= max(1, N). Any leading dimension is accepted. When A's rows do
  *    not start on 16-byte boundaries (an odd lda, say) and B is row-major,
  *    the tensor-core pass reads A directly in classes of rows that share a
- *    misalignment; otherwise an operand whose base address or row pitch is
- *    not a multiple of 16 bytes is staged through an aligned copy on the
- *    device first.
+ *    misalignment (their offset modulo 16 bytes, or, in the 256 x 288 and
+ *    256 x 320 CTA-pair tiles, their offset in a 128-byte line); otherwise
+ *    an operand whose base address or row pitch is not a multiple of 16
+ *    bytes is staged through an aligned copy on the device first. A class
+ *    is read from the aligned address at or below its first row, up to 126
+ *    bytes before A: A's allocation must begin on a 128-byte boundary, as
+ *    every CUDA device allocation does (those bytes are read, never used).
  *  - A and B must be aligned to 2 bytes and C to 4 bytes (their element
  *    sizes); otherwise MPGEMM_ERR_INVALID_VALUE.
  *  - beta == 0: C is only written, never read, so it may hold NaN on entry.
@@ -145,12 +149,15 @@ mpgemm_status_t mpgemm_sync_status(mpgemm_handle_t h, void* stream, int32_t info
 
 /* Tunables and test switches, set per handle. */
 typedef enum {
-    MPGEMM_OPT_TILE_N = 1,        /* 0 = automatic (default), or 128, 256 or 320 columns per
-                                     tile (320: one CTA per 128 x 320 tile, chosen
-                                     automatically when N is 257 to 320; TILE_M 256 with
-                                     TILE_N 320 makes runs return INVALID_VALUE);
-                                     512 = a cluster of two CTAs per 256 x 512 tile (with
-                                     TILE_M 0 or 256) */
+    MPGEMM_OPT_TILE_N = 1,        /* 0 = automatic (default), or columns per tile: 128 or 256
+                                     (one CTA, or a pair with TILE_M 256); 320 (one CTA per
+                                     128 x 320 tile, or with TILE_M 256 a pair per 256 x 320
+                                     tile, row-major B only); 288, 384 and 512 (a cluster of
+                                     two CTAs per 256-row tile; 288 with row-major B only).
+                                     A combination not listed makes runs return
+                                     INVALID_VALUE. Automatically, N from 257 to 288, 320 or
+                                     384 in one column of 288-, 320- or 384-wide pairs when
+                                     those fill every pair */
     MPGEMM_OPT_MAX_CTAS = 2,      /* 0 = one persistent CTA per SM (default), else an upper bound */
     MPGEMM_OPT_FORCE_STAGING = 3, /* 1 = stage A and B through aligned copies even when aligned */
     MPGEMM_OPT_WAIT_LIMIT_US = 4, /* limit of every bounded device wait, microseconds (default 4e6) */
@@ -202,7 +209,7 @@ typedef enum {
                                      256 x 256 tile hand alternate k-blocks to each other
                                      strictly in turn). The stream-K walk (STREAM_K) is
                                      allowed: it, too, sums in a fixed order. */
-    MPGEMM_OPT_STREAM_K = 13      /* 0 = automatic (default): CTA-pair tiles of 320 or 384
+    MPGEMM_OPT_STREAM_K = 13      /* 0 = automatic (default): CTA-pair tiles of 288, 320 or 384
                                      columns (N from 257 to 384), or a single column of
                                      256-wide pair tiles, that leave the last wave of
                                      pairs partly idle walk the problem as one contiguous range
@@ -231,7 +238,8 @@ typedef struct {
     int32_t stage_a;        /* 1 if A is copied to an aligned buffer first */
     int32_t stage_b;        /* 1 if B is copied to an aligned buffer first */
     int32_t tile_m;         /* rows per output tile: 128 (one CTA) or 256 (a CTA pair) */
-    int32_t tile_n;         /* columns per output tile (128, 256 or 320; 256 or 512 for a pair) */
+    int32_t tile_n;         /* columns per output tile (128, 256 or 320; 256, 288, 320, 384 or
+                               512 for a pair) */
     int32_t tile_k;         /* K per pipeline stage (64, or 128 for tiles that stage two
                                64-wide k-blocks at once); k_blocks counts these stages */
     int32_t stages;         /* shared-memory pipeline depth */
@@ -248,7 +256,10 @@ typedef struct {
     int32_t k_splits;       /* slices of K per tile (1 = no split-K) */
     int32_t a_classes;      /* 0: A is read through one plain tensor map (aligned, or staged);
                                P >= 1: A's rows are not 16-byte aligned and are read in P
-                               classes of rows i = r (mod P) instead of being copied */
+                               classes of rows i = r (mod P) instead of being copied: rows
+                               at the same offset modulo 16 bytes (P <= 8), or, in the
+                               256 x 288 and 256 x 320 pairs when that adds at most 1/32
+                               more tiles, in the same 128-byte line (P <= 64) */
     int32_t sk_ranges;      /* 0, or the stream-K walk's ranges of k-blocks (one per CTA pair;
                                see MPGEMM_OPT_STREAM_K) */
 } mpgemm_plan_t;
