@@ -179,8 +179,8 @@ typedef enum {
                                      beta == 1), or at most an eighth of the SMs and K has 8
                                      or more blocks (up to five slices), each
                                      tile's K range is cut into slices whose
-                                     partial products are added into C (after C = beta*C), so
-                                     results may differ in the last bits from run to run;
+                                     partial products are summed: in clusters (see
+                                     SPLIT_REDUCE) or added into C after C = beta*C;
                                      1 = never; n in 2..64 = n slices (one-CTA tiles only) */
     MPGEMM_OPT_C_STORE = 10,      /* 0 = automatic (default): C is written with tiled TMA stores
                                      when beta == 0 and K is not split, or added to with tiled
@@ -197,19 +197,19 @@ typedef enum {
                                      Capstone 4", "Common failures"). K is never split then: the
                                      whole K range accumulates in one FP16 accumulator. Not for
                                      production use. */
-    MPGEMM_OPT_REPRODUCIBLE = 12, /* 0 = default: a call may split K (see SPLIT_K), and the
-                                     slices then add into C in the order they arrive, so
+    MPGEMM_OPT_REPRODUCIBLE = 12, /* 0 = default: a call may split K (see SPLIT_K), and slices
+                                     that add into C do so in the order they arrive, so
                                      results may differ in the last bits between identical
                                      calls (always within the stated tolerance; exact inputs
-                                     stay exact); 1 = never split K, so every element is summed
-                                     by one MMA thread in one fixed order and identical calls
-                                     give identical bits (every tile shape sums in a fixed
+                                     stay exact); 1 = K is split only where the slices are
+                                     summed in clusters (SPLIT_REDUCE), in a fixed order, so
+                                     identical calls give identical bits (every tile shape sums in a fixed
                                      order: the two MMA threads of a 256 x 512 CTA-pair tile
                                      own disjoint columns of the accumulator, and those of a
                                      256 x 256 tile hand alternate k-blocks to each other
                                      strictly in turn). The stream-K walk (STREAM_K) is
                                      allowed: it, too, sums in a fixed order. */
-    MPGEMM_OPT_STREAM_K = 13      /* 0 = automatic (default): CTA-pair tiles of 288, 320 or 384
+    MPGEMM_OPT_STREAM_K = 13,     /* 0 = automatic (default): CTA-pair tiles of 288, 320 or 384
                                      columns (N from 257 to 384), or a single column of
                                      256-wide pair tiles, that leave the last wave of
                                      pairs partly idle walk the problem as one contiguous range
@@ -222,18 +222,40 @@ typedef enum {
                                      call runs on CTA pairs of 256 to 384 columns with at least
                                      one tile per pair (not with FP16 accumulators, nor in
                                      mpgemm_run_noalloc) */
+    MPGEMM_OPT_SPLIT_REDUCE = 14  /* how split-K slices are summed. 1 = they add into C with
+                                     TMA reduce-adds or atomic adds, after a pass that applies
+                                     beta (unless beta == 1), in the order they finish.
+                                     2 = in clusters, where the tiles are 128 x 128 with at
+                                     most 8 slices (more are cut to 8) and every slice fits
+                                     the device at once: the slices of a tile run as one
+                                     cluster of CTAs; each writes its partial accumulator to
+                                     its shared memory and, after a cluster barrier, sums its
+                                     share of the tile's rows over the partials (through
+                                     distributed shared memory, in CTA order) and writes C
+                                     once, with no pass over C first and no atomics, so
+                                     identical calls give identical bits; else as 1. About
+                                     1.3-4 us slower per call than 1 on GB300.
+                                     0 = automatic (default): 2 when REPRODUCIBLE is set, else 1 */
 } mpgemm_option_t;
 
 /* Set an option. Unknown options or out-of-range values return
  * MPGEMM_ERR_INVALID_VALUE and leave the handle unchanged. */
 mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_t value);
 
+/* What mpgemm_run_ex would do for these arguments with this handle's options
+ * and device (host work only; the handle's device must be current). Same
+ * argument checks and status codes as mpgemm_run_ex. */
+typedef struct mpgemm_plan_s mpgemm_plan_t;
+mpgemm_status_t mpgemm_plan_call(mpgemm_handle_t h, mpgemm_b_layout_t b_layout, int64_t M, int64_t N,
+                                 int64_t K, float alpha, const void* A, int64_t lda, const void* B,
+                                 int64_t ldb, float beta, const float* C, int64_t ldc, mpgemm_plan_t* out);
+
 /* What mpgemm_run would do for these arguments, computed on the host only
  * (no device work; usable without a GPU). `num_sms` stands in for the
  * device's SM count; tile_m, tile_n, max_ctas and force_staging mirror the
  * options above; b_col_major selects the layout of B (ldb >= K when set). The grid of the CTA-pair kernel is further capped at run
  * time by the number of two-CTA clusters the device can hold at once. */
-typedef struct {
+struct mpgemm_plan_s {
     int32_t quick;          /* 0 = tensor-core path, 1 = nothing to do, 2 = C = beta*C only */
     int32_t stage_a;        /* 1 if A is copied to an aligned buffer first */
     int32_t stage_b;        /* 1 if B is copied to an aligned buffer first */
@@ -262,7 +284,10 @@ typedef struct {
                                more tiles, in the same 128-byte line (P <= 64) */
     int32_t sk_ranges;      /* 0, or the stream-K walk's ranges of k-blocks (one per CTA pair;
                                see MPGEMM_OPT_STREAM_K) */
-} mpgemm_plan_t;
+    int32_t split_reduce;   /* k_splits > 1: 1 = a tile's slices run as one cluster and are
+                               summed through distributed shared memory; 0 = they add into C
+                               (see MPGEMM_OPT_SPLIT_REDUCE) */
+};
 
 mpgemm_status_t mpgemm_plan(int64_t M, int64_t N, int64_t K, float alpha,
                             const void* A, int64_t lda, const void* B, int64_t ldb,

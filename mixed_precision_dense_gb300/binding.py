@@ -40,6 +40,7 @@ class Option(enum.IntEnum):
     ACCUMULATOR = 11
     REPRODUCIBLE = 12
     STREAM_K = 13
+    SPLIT_REDUCE = 14
 
 
 class BLayout(enum.IntEnum):
@@ -61,7 +62,8 @@ class Plan(ctypes.Structure):
                 ("raster_group", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("last_k_valid", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
                 ("split_tiles", ctypes.c_int32), ("items", ctypes.c_int64),
-                ("k_splits", ctypes.c_int32), ("a_classes", ctypes.c_int32), ("sk_ranges", ctypes.c_int32)]
+                ("k_splits", ctypes.c_int32), ("a_classes", ctypes.c_int32), ("sk_ranges", ctypes.c_int32),
+                ("split_reduce", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -100,12 +102,15 @@ def load(path: str = LIB_PATH):
         lib.mpgemm_set_option.argtypes = [p, ctypes.c_int, i64]
         lib.mpgemm_plan.argtypes = [i64, i64, i64, f32, p, i64, p, i64, f32, p, i64,
                                     i32, i32, i32, i32, i32, i32, ctypes.POINTER(Plan)]
+        lib.mpgemm_plan_call.argtypes = [p, ctypes.c_int, i64, i64, i64, f32, p, i64, p, i64, f32, p, i64,
+                                         ctypes.POINTER(Plan)]
         lib.mpgemm_probe_mma_rate.argtypes = [i32, i32, p, p]
         lib.mpgemm_status_string.restype = ctypes.c_char_p
         lib.mpgemm_status_string.argtypes = [ctypes.c_int]
         for name in ("mpgemm_create", "mpgemm_destroy", "mpgemm_run", "mpgemm_run_ex", "mpgemm_solve",
                      "mpgemm_run_host", "mpgemm_run_noalloc",
-                     "mpgemm_sync_status", "mpgemm_set_option", "mpgemm_plan", "mpgemm_probe_mma_rate"):
+                     "mpgemm_sync_status", "mpgemm_set_option", "mpgemm_plan", "mpgemm_plan_call",
+                     "mpgemm_probe_mma_rate"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -189,6 +194,14 @@ class Handle:
 
     def set_option(self, option: Option, value: int):
         _check(self._lib.mpgemm_set_option(self._h, int(option), int(value)), "mpgemm_set_option")
+
+    def plan(self, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, b_layout=0) -> dict:
+        """mpgemm_plan_call: what run_ex would do with this handle's options."""
+        out = Plan()
+        st = self._lib.mpgemm_plan_call(self._h, int(b_layout), M, N, K, alpha, A or None, lda, B or None,
+                                        ldb, beta, C or None, ldc, ctypes.byref(out))
+        _check(st, "mpgemm_plan_call")
+        return out.as_dict()
 
     def run(self, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0):
         """mpgemm_run on device addresses (ints); raises MpgemmError on a bad status."""

@@ -107,6 +107,10 @@ constexpr int kTableAClasses = 8;
 // Most ranges of a stream-K walk (one per CTA pair).
 constexpr int kMaxSkRanges = 128;
 
+// Most CTAs (K slices) of a tile's cluster in the cluster split-K (the
+// portable cluster size).
+constexpr int kMaxClusterSlices = 8;
+
 // The tensor maps of A (one per row class, room for NC classes), of C
 // (FP32, 32 x 32 boxes, 128-byte swizzle; used only when GemmParams::c_tma
 // is set) and of B in narrow boxes (used only by 256 x 288 and 256 x 320
@@ -178,9 +182,18 @@ struct GemmParams {
 enum : int32_t { kRoleLoad = 1, kRoleMma = 2, kRoleEpilogue = 3 };
 enum : int32_t { kStatusTimeout = 1 };
 
-template <int BN_, int STAGES_, bool PAIR_, bool B_KMAJOR_ = false, int ISSUERS_ = (BN_ == 512 ? 2 : 1), int KPS_ = 1>
+template <int BN_, int STAGES_, bool PAIR_, bool B_KMAJOR_ = false, int ISSUERS_ = (BN_ == 512 ? 2 : 1), int KPS_ = 1,
+          bool CSPLIT_ = false>
 struct TileConfig {
     static constexpr bool PAIR = PAIR_;
+    // Split-K in clusters (one-CTA 128 x 128 tiles): the k_splits CTAs of a
+    // cluster (GemmParams::k_splits of them, launched as one cluster per
+    // tile) each sum one slice of K into their own accumulator, write it to
+    // shared memory (over the idle ring) and, after a cluster barrier, each
+    // sums its share of the tile's rows over every CTA's partial through
+    // distributed shared memory, in CTA order, and writes C once: no pass
+    // over C first, no atomics, the same bits on every call.
+    static constexpr bool CSPLIT = CSPLIT_;
     // B column-major ([N, K] rows of K): a K-major operand like A. Its 64-row
     // boxes stack in shared memory exactly like the 64-column boxes of a
     // row-major B, so the ring layout is the same; only the box coordinates,
@@ -308,6 +321,8 @@ struct TileConfig {
     static_assert((BN % 64 == 0 || NARROW_TAIL) && (TAIL_N % (PAIR ? 128 : 64) == 0 || NARROW_TAIL),
                   "the last part holds whole B boxes");
     static_assert(A_CLASSES == 8 || A_CLASSES == kMaxAClasses, "row-class capacities");
+    static_assert(!CSPLIT || (!PAIR && BN == 128 && STAGES * (A_BYTES + B_BYTES) >= 128 * 128 * 4),
+                  "cluster split-K: one-CTA 128 x 128 tiles, the partial accumulator fits the ring");
 };
 
 // M-tile mb -> (row class r, first class row j0 of the tile), in a kernel
@@ -605,6 +620,16 @@ __device__ __forceinline__ uint32_t chunk_off(int row, int col) {
     return static_cast<uint32_t>(row * 128 + ((((col >> 2) ^ row) & 7) << 4) + (col & 3) * 4);
 }
 
+// Byte offset of accumulator element (row, col) of a 128 x 128 FP32 partial
+// (cluster split-K): 512-byte rows, each 128-byte segment swizzled like a
+// chunk buffer, so that a lane writing 32 columns of its row as eight
+// 16-byte stores, and 32 lanes reading 32 consecutive columns of a row, both
+// touch every bank once.
+__device__ __forceinline__ uint32_t partial_off(int row, int col) {
+    return static_cast<uint32_t>(row * 512 + (col >> 5) * 128 + (((((col & 31) >> 2) ^ row) & 7) << 4) +
+                                 (col & 3) * 4);
+}
+
 // One 32 x 32 chunk (accumulator words r, TMEM lane = row = lane) to C,
 // without a beta * C term: alpha applied, into the warp's chunk buffer, then
 // either a tiled TMA store (a TMA reduce-add for split-K) at C row row0,
@@ -751,6 +776,92 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMa
         __syncwarp();
     }
     if (chunks <= 0) release();
+}
+
+// Cluster split-K: CTA `rank` of the tile's cluster owns rows [r0, r1) of
+// the 128-row tile (shares of R = ceil(128 / k_splits) rows, cut at the
+// tile's last row); c_tile + row * row_stride addresses the tile's C row.
+struct CsplitShare {
+    int32_t n0, r0, r1;
+    int64_t row_stride;
+    float* c_tile;
+};
+template <class Cfg>
+__device__ __forceinline__ CsplitShare csplit_share(const GemmParams& p) {
+    const int32_t S = p.k_splits;
+    const int32_t rank = static_cast<int32_t>(ptx::cluster_ctarank());
+    int32_t mb, nb, cls, j0;
+    tile_coords(p, static_cast<int32_t>(blockIdx.x) / S, mb, nb);
+    a_class_of<Cfg::TILE_M, Cfg::A_CLASSES>(p, mb, cls, j0);
+    const int32_t rows = min(Cfg::BM, a_rows_of<Cfg::A_CLASSES>(p, cls) - j0);
+    const int32_t share = (Cfg::BM + S - 1) / S;
+    CsplitShare c;
+    c.n0 = nb * Cfg::BN;
+    c.r0 = rank * share;
+    c.r1 = min(rows, c.r0 + share);
+    c.row_stride = static_cast<int64_t>(p.a_classes) * p.ldc;
+    c.c_tile = p.C + (cls + static_cast<int64_t>(p.a_classes) * j0) * p.ldc;
+    return c;
+}
+
+// Every warp of the CTA takes two rows of its share at a time, each lane
+// columns lane, lane + 32, lane + 64 and lane + 96 of them; all the loads of
+// the two rows (the k_splits partials through distributed shared memory, and
+// the old C) go out before any is used. An element is the sum of the
+// partials in CTA order, then alpha times it plus beta times the old C (beta
+// == 0: C is not read).
+template <class Cfg>
+__device__ __forceinline__ void csplit_reduce(const GemmParams& p, uint32_t partial) {
+    static_assert(Cfg::BN == 128, "four columns per lane");
+    constexpr int NW = Cfg::THREADS / 32;
+    const int32_t S = p.k_splits;
+    const CsplitShare sh = csplit_share<Cfg>(p);
+    const bool read_c = p.beta != 0.0f;
+    uint32_t src[kMaxClusterSlices];
+#pragma unroll
+    for (int s = 0; s < kMaxClusterSlices; ++s)
+        src[s] = ptx::mapa_shared(partial, static_cast<uint32_t>(s < S ? s : 0));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int32_t row = sh.r0 + warp; row < sh.r1; row += 2 * NW) {
+        float v[kMaxClusterSlices][2][4], c_old[2][4];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int32_t r = row + rr * NW;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int32_t col = sh.n0 + q * 32 + lane;
+                c_old[rr][q] = (read_c && r < sh.r1 && col < p.N)
+                                   ? __ldg(sh.c_tile + static_cast<int64_t>(r) * sh.row_stride + col)
+                                   : 0.0f;
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < kMaxClusterSlices; ++s)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    v[s][rr][q] = (s < S && row + rr * NW < sh.r1)
+                                      ? ptx::ld_cluster_f32(src[s] + partial_off(row + rr * NW, q * 32 + lane))
+                                      : 0.0f;
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int32_t r = row + rr * NW;
+            if (r >= sh.r1) continue;
+            float* c_row = sh.c_tile + static_cast<int64_t>(r) * sh.row_stride;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int32_t col = sh.n0 + q * 32 + lane;
+                if (col >= p.N) continue;
+                float sum = v[0][rr][q];
+#pragma unroll
+                for (int s = 1; s < kMaxClusterSlices; ++s)
+                    if (s < S) sum += v[s][rr][q];
+                const float out = p.alpha * sum;
+                c_row[col] = read_c ? fmaf(p.beta, c_old[rr][q], out) : out;
+            }
+        }
+    }
 }
 
 template <class Cfg>
@@ -1192,6 +1303,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 load_c_chunk(c_tile, row_stride, n0 + g0.out_col + col_half * (g0.width / COL_SPLIT) + lane, p.N,
                              rows, c_cur);
             }
+            if constexpr (Cfg::CSPLIT) {
+                // the old C of this CTA's rows of the tile into L2 while the
+                // slices run (one bulk prefetch per row)
+                if (p.beta != 0.0f) {
+                    const CsplitShare sh = csplit_share<Cfg>(p);
+                    const int32_t r = sh.r0 + (warp - 2) * 32 + lane;
+                    const int32_t cend = min(sh.n0 + BN, p.N);
+                    if (r < sh.r1 && cend > sh.n0) {
+                        const float* c_row = sh.c_tile + static_cast<int64_t>(r) * sh.row_stride;
+                        const uint64_t a = reinterpret_cast<uint64_t>(c_row + sh.n0) & ~uint64_t{15};
+                        const uint64_t e = (reinterpret_cast<uint64_t>(c_row + cend) + 15) & ~uint64_t{15};
+                        ptx::bulk_prefetch_l2(a, static_cast<uint32_t>(e - a));
+                    }
+                }
+            }
             const bool ready = waiter.wait(acc_full_bar(accb), acc_phase);
             if (!__all_sync(0xffffffffu, ready)) {
                 if (lane == 0) waiter.fail(kRoleEpilogue, i);
@@ -1217,6 +1343,31 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
             }
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+            if constexpr (Cfg::CSPLIT) {
+                // this warp's 32 rows and half of the columns of the slice's
+                // accumulator, unscaled, to the partial over the ring (the
+                // tensor core has read the ring for the last time: the
+                // accumulator is full)
+                ptx::fence_proxy_async_smem();
+                const int32_t row = quarter * 32 + lane;
+#pragma unroll 1
+                for (int32_t c = col_half * (BN / COL_SPLIT); c < (col_half + 1) * (BN / COL_SPLIT); c += 32) {
+                    uint32_t r[32];
+                    ptx::tmem_load_32x32b_x32(t_row + static_cast<uint32_t>(accb * BN + c), r);
+                    ptx::tmem_load_wait();
+                    ptx::tmem_regs_ready(r);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        ptx::st_shared_v4(base + Cfg::OFF_A + partial_off(row, c + 4 * q), __uint_as_float(r[4 * q]),
+                                          __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
+                                          __uint_as_float(r[4 * q + 3]));
+                }
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(acc_empty_bar(accb, 0));
+                ++local;
+                continue;
+            }
             // the accumulator's parts in order (one part: the whole item);
             // each part goes back to the MMA warp as soon as it has been read,
             // and parts past the item's width are handed back at once
@@ -1265,6 +1416,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
     ptx::tc_fence_before_sync();
     __syncthreads();
+    if constexpr (Cfg::CSPLIT) {
+        // every slice's partial written; then this CTA's rows of the tile
+        // summed over the cluster's partials, and the peers' reads of this
+        // CTA's partial finished before it exits
+        ptx::cluster_sync();
+        csplit_reduce<Cfg>(p, base + Cfg::OFF_A);
+        ptx::cluster_sync();
+    }
     if constexpr (PAIR) {
         // After an abort the peer's loads into this pair may still be landing:
         // give them a moment before the cluster (and its shared memory) goes away.

@@ -77,6 +77,12 @@ using Cfg320K = TileConfig<320, 3, false, true>;
 using CfgPairK = TileConfig<256, 6, true, true, 2>;
 using CfgWideK = TileConfig<512, 4, true, true>;
 using CfgPair384K = TileConfig<384, 4, true, true, 2>;
+// one-CTA 128 x 128 tiles whose K slices run as one cluster per tile and are
+// summed through distributed shared memory (split-K in clusters)
+using Cfg128C = TileConfig<128, 6, false, false, 1, 1, true>;
+using Cfg128KC = TileConfig<128, 6, false, true, 1, 1, true>;
+// largest cluster (slices per tile) the cluster split-K launches
+constexpr int kMaxClusterSplits = kMaxClusterSlices;
 // stream-K flags per range: one per CTA of the pair and epilogue warp
 constexpr int kSkFlagsPerRange = 2 * CfgPair::EPI_WARPS;
 static_assert(CfgPair::STREAM_K && CfgPair288::STREAM_K && CfgPair320::STREAM_K && CfgPair384::STREAM_K &&
@@ -115,6 +121,8 @@ struct Options {
     int32_t acc16 = 0;              // 1: FP16 accumulators (study variant)
     int32_t reproducible = 0;       // 1: only paths whose summation order is fixed
     int32_t stream_k = 0;           // 0 automatic, 1 never, 2 whenever the tile shape allows
+    int32_t split_reduce = 0;       // 0 automatic (clusters for reproducible calls), 1 atomics /
+                                    // reduce-adds, 2 clusters where possible
     uint64_t wait_limit_ns = kDefaultWaitLimitNs;
 };
 
@@ -409,7 +417,7 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     int64_t splits = 1;
     // (FP16 accumulators never split K: the study variant keeps the whole K
     // range in one FP16 accumulator, as an __half accumulator type would)
-    if (!pair && opt.split_k != 1 && !opt.acc16 && !opt.reproducible) {
+    if (!pair && opt.split_k != 1 && !opt.acc16) {
         if (opt.split_k >= 2)
             splits = opt.split_k;
         else if (beta == 1.0f ? (p.tiles * 2 <= units && k_blocks >= 16) : (p.tiles * 4 <= units && k_blocks >= 32))
@@ -426,6 +434,26 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
         splits = std::max<int64_t>(1, std::min<int64_t>(splits, k_blocks));
         if (splits > 1) splits = ceil_div(k_blocks, ceil_div(k_blocks, splits));  // no empty slice
     }
+    // Split-K in clusters (MPGEMM_OPT_SPLIT_REDUCE): 128 x 128 tiles of at
+    // most 8 slices, every slice of every tile resident at once (one CTA per
+    // item): the slices of a tile run as one cluster and are summed through
+    // distributed shared memory, in a fixed order, into one write of C.
+    // Otherwise they add into C (after a pass applying beta), in the order
+    // they finish, which a reproducible call does not allow. The clusters
+    // cost 1.3-4 us more per call on GB300 (200 x 136 x 617: 11.1 -> 12.4;
+    // 1000 x 800 x 1200, beta 1: 12.4 -> 16.5; 4096 x 16 x 4096: 16.1 ->
+    // 18.7): their two cluster barriers and the partials' round trip
+    // through shared memory are not hidden, where the slices' reduce-adds
+    // run behind the next work. So they are the default only where the
+    // order matters (reproducible calls), which then split K at all.
+    const bool clusters = opt.split_reduce == 2 || (opt.split_reduce == 0 && opt.reproducible);
+    if (splits > kMaxClusterSplits && clusters && p.tile_n == 128)
+        splits = ceil_div(k_blocks, ceil_div(k_blocks, kMaxClusterSplits));
+    p.split_reduce =
+        (splits > 1 && clusters && p.tile_n == 128 && splits <= kMaxClusterSplits && p.tiles * splits <= units)
+            ? 1
+            : 0;
+    if (splits > 1 && !p.split_reduce && opt.reproducible) splits = 1;
     p.k_splits = static_cast<int32_t>(splits);
     if (splits > 1) {
         p.split_tiles = 0;
@@ -714,9 +742,9 @@ cudaError_t launch_tc(int grid, const TensorMaps& ta, const CUtensorMap& tb, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (Cfg::PAIR) {
+    if (Cfg::PAIR || Cfg::CSPLIT) {
         attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.x = Cfg::PAIR ? 2u : static_cast<unsigned>(gp.k_splits);
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
@@ -776,6 +804,8 @@ cudaError_t prepare_kernels() {
     if (e == cudaSuccess) e = set_smem_attr<CfgPair384K>();
     if (e == cudaSuccess) e = set_smem_attr<CfgPair320>();
     if (e == cudaSuccess) e = set_smem_attr<CfgPair288>();
+    if (e == cudaSuccess) e = set_smem_attr<Cfg128C>();
+    if (e == cudaSuccess) e = set_smem_attr<Cfg128KC>();
     return e;
 }
 
@@ -855,6 +885,7 @@ void encode_c(const mpgemm_plan_t& plan, float* C, int64_t M, int64_t N, int64_t
               int32_t c_store, TensorMaps* maps, GemmParams* gp, MapCache* cache = nullptr) {
     gp->c_tma = 0;
     if (c_store == 1 || (beta != 0.0f && plan.k_splits <= 1) || gp->a_classes != 1 || N % 4 != 0) return;
+    if (plan.split_reduce) return;   // the cluster's sums are written per lane
     if (!aligned16(C, ldc, 4)) return;
     if (encode_f32_store(&maps->c, C, M, N, ldc, cache)) gp->c_tma = 1;
 }
@@ -896,7 +927,7 @@ GemmParams make_params(const mpgemm_plan_t& plan, int64_t M, int64_t N, int64_t 
     gp.test_stall = test_stall;
     gp.keep_a = keep_a;
     // split-K slices after the pass that applies beta (launch_plan)
-    gp.overlap_prepass = (plan.k_splits > 1 && beta != 1.0f) ? 1 : 0;
+    gp.overlap_prepass = (plan.k_splits > 1 && !plan.split_reduce && beta != 1.0f) ? 1 : 0;
     if (plan.sk_ranges > 0) {   // (the caller sets sk_flags and sk_epoch)
         gp.sk_units = static_cast<int32_t>(plan.tiles * plan.k_blocks);
         gp.sk_ranges = plan.sk_ranges;
@@ -909,7 +940,7 @@ GemmParams make_params(const mpgemm_plan_t& plan, int64_t M, int64_t N, int64_t 
 cudaError_t launch_plan(const mpgemm_plan_t& plan, bool b_col_major, int max_clusters,
                         const TensorMaps& ta, const CUtensorMap& tb, const GemmParams& gp,
                         cudaStream_t stream) {
-    if (plan.k_splits > 1 && gp.beta != 1.0f) {
+    if (plan.k_splits > 1 && !plan.split_reduce && gp.beta != 1.0f) {
         // the slices add into C: apply beta (or clear C) once, first
         scale_c<<<grid_for(static_cast<int64_t>(gp.M) * gp.N, plan.grid), 256, 0, stream>>>(
             gp.C, gp.ldc, gp.M, gp.N, gp.beta);
@@ -932,6 +963,14 @@ cudaError_t launch_plan(const mpgemm_plan_t& plan, bool b_col_major, int max_clu
         if (plan.tile_n == 288) return launch_tc<CfgPair288>(grid, ta, tb, gp, stream);
         return b_col_major ? launch_tc<CfgPairK>(grid, ta, tb, gp, stream)
                            : launch_tc<CfgPair>(grid, ta, tb, gp, stream);
+    }
+    if (plan.split_reduce) {
+        // one cluster of k_splits CTAs per tile, every CTA one slice
+        if (plan.tile_n != 128 || plan.k_splits < 2 || plan.k_splits > kMaxClusterSplits ||
+            static_cast<int64_t>(plan.grid) != plan.items)
+            return cudaErrorInvalidValue;
+        return b_col_major ? launch_tc<Cfg128KC>(plan.grid, ta, tb, gp, stream)
+                           : launch_tc<Cfg128C>(plan.grid, ta, tb, gp, stream);
     }
     if (plan.tile_n == 320)
         return b_col_major ? launch_tc<Cfg320K>(plan.grid, ta, tb, gp, stream)
@@ -1194,8 +1233,24 @@ mpgemm_status_t mpgemm_set_option(mpgemm_handle_t h, mpgemm_option_t opt, int64_
             if (value < 0 || value > 2) return MPGEMM_ERR_INVALID_VALUE;
             h->opt.stream_k = static_cast<int32_t>(value);
             return MPGEMM_OK;
+        case MPGEMM_OPT_SPLIT_REDUCE:
+            if (value < 0 || value > 2) return MPGEMM_ERR_INVALID_VALUE;
+            h->opt.split_reduce = static_cast<int32_t>(value);
+            return MPGEMM_OK;
     }
     return MPGEMM_ERR_INVALID_VALUE;
+}
+
+mpgemm_status_t mpgemm_plan_call(mpgemm_handle_t h, mpgemm_b_layout_t b_layout, int64_t M, int64_t N,
+                                 int64_t K, float alpha, const void* A, int64_t lda, const void* B,
+                                 int64_t ldb, float beta, const float* C, int64_t ldc, mpgemm_plan_t* out) {
+    if (!h || !out) return MPGEMM_ERR_INVALID_VALUE;
+    if (b_layout != MPGEMM_B_ROW_MAJOR && b_layout != MPGEMM_B_COL_MAJOR) return MPGEMM_ERR_INVALID_VALUE;
+    if (mpgemm_status_t st0 = enter_device(h); st0 != MPGEMM_OK) return st0;
+    Options opt = h->opt;
+    opt.pair_units = h->max_clusters;
+    opt.b_col_major = b_layout == MPGEMM_B_COL_MAJOR ? 1 : 0;
+    return make_plan(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, h->num_sms, opt, out);
 }
 
 mpgemm_status_t mpgemm_run_ex(mpgemm_handle_t h, mpgemm_b_layout_t b_layout, int64_t M, int64_t N,

@@ -278,13 +278,21 @@ __device__ __forceinline__ void st_cluster_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
+// Generic-proxy load from shared memory of a CTA of the cluster (a cluster
+// address from mapa_shared).
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Order this thread's generic-proxy accesses to the shared memory of the
 // cluster's CTAs before its later async-proxy (tensor core, TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_cluster() {
     asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
-// All threads of both CTAs of the cluster.
+// All threads of every CTA of the cluster (two for a CTA pair).
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
                      "memory");

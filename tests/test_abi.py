@@ -250,8 +250,11 @@ def test_tile_selection_and_grid():
     assert p["split_tiles"] == 0 and p["sk_ranges"] == 76
     p = _plan()
     assert p["a_classes"] == 8 and p["tiles"] == 8 * 2                      # 8 classes of 25 rows
-    # 16 tiles of 10 k-blocks (at most an eighth of the SMs): five K slices
-    assert p["k_splits"] == 5 and p["items"] == 16 * 5 and p["grid"] == 80
+    # 16 tiles of 10 k-blocks (at most an eighth of the SMs): five K slices,
+    # added into C (clusters only on request or for reproducible calls)
+    assert p["k_splits"] == 5 and p["items"] == 16 * 5 and p["grid"] == 80 and p["split_reduce"] == 0
+    p = _plan(M=128, N=128, K=8192, lda=8192, ldb=128, ldc=128)   # one tile of 128 k-blocks
+    assert p["k_splits"] == 16 and p["split_reduce"] == 0
     p = _plan(M=611, N=613, K=617, lda=617, ldb=613, ldc=613)
     assert p["tiles"] == 40 and p["k_splits"] == 1
     p = _plan(M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192, tile_n=128, max_ctas=10)

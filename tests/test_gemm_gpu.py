@@ -323,24 +323,92 @@ SPLITK_CASES = [  # (M, N, K, alpha, beta, splits)
 ]
 
 
+@pytest.mark.parametrize("reduce", [1, 2])
 @pytest.mark.parametrize("M,N,K,alpha,beta,splits", SPLITK_CASES)
-def test_split_k(mp, M, N, K, alpha, beta, splits):
+def test_split_k(mp, M, N, K, alpha, beta, splits, reduce):
+    # both ways of summing the slices: into C (reduce 1, the default) and in
+    # clusters through distributed shared memory (reduce 2)
     plan = mp.plan(M, N, K, alpha, 256, K, 256, N, beta, 256, N)
     if splits == 0:
-        assert plan["k_splits"] > 1
+        assert plan["k_splits"] > 1 and plan["split_reduce"] == 0
     with mp.Handle() as h:
         h.set_option(mp.Option.SPLIT_K, splits)
+        h.set_option(mp.Option.SPLIT_REDUCE, reduce)
+        hp = h.plan(M, N, K, alpha, 256, K, 256, N, beta, 256, N)
+        assert hp["k_splits"] > 1 and hp["split_reduce"] == (reduce == 2)
         check_full(h, workloads.make_operands(M, N, K, alpha=alpha, beta=beta, c_dist="normal",
                                               seed=M + N + K))
 
 
-def test_split_k_integer_bitwise_and_column_major(mp):
+@pytest.mark.parametrize("reduce", [1, 2])
+def test_split_k_integer_bitwise_and_column_major(mp, reduce):
     with mp.Handle() as h:
         h.set_option(mp.Option.SPLIT_K, 4)
+        h.set_option(mp.Option.SPLIT_REDUCE, reduce)
         check_full(h, workloads.make_operands(200, 300, 2048, dist="int3", dist_b="int2", seed=86),
                    exact=True)
         check_full(h, workloads.make_operands(200, 300, 2048, dist="int3", dist_b="int2", seed=87,
                                               b_col_major=True), exact=True)
+
+
+CLUSTER_SPLIT_CASES = [  # (M, N, K, lda, beta, splits): slices summed in clusters
+    (200, 136, 617, 617, 0.0, 0),       # the small workload: 16 tiles x 5 slices, A in 8 row classes
+    (1000, 800, 1200, 1200, 1.0, 0),    # beta = 1: two slices
+    (129, 65, 617, 617, 0.5, 8),        # the largest cluster, ragged rows, columns and K
+    (300, 200, 1000, 1003, -0.75, 3),   # 3 slices share 128 rows (43, 43, 42), A in row classes
+    (64, 1000, 4096, 4096, 0.0, 6),     # 8 tiles x 6 slices of 11 k-blocks (the last 9)
+]
+
+
+@pytest.mark.parametrize("M,N,K,lda,beta,splits", CLUSTER_SPLIT_CASES)
+def test_cluster_split_k_identical_bits(mp, M, N, K, lda, beta, splits):
+    # Against the oracle (C NaN-poisoned when beta == 0), then three calls
+    # give identical bits, and exact integers match bit for bit.
+    from parity import device_operands
+    s = torch.cuda.current_stream()
+    with mp.Handle() as h:
+        h.set_option(mp.Option.SPLIT_K, splits)
+        h.set_option(mp.Option.SPLIT_REDUCE, 2)
+        hp = h.plan(M, N, K, 1.25, 256, lda, 256, N, beta, 256, N)
+        assert hp["k_splits"] > 1 and hp["split_reduce"] == 1
+        ops = workloads.make_operands(M, N, K, lda=lda, alpha=1.25, beta=beta,
+                                      c_dist="normal" if beta else "zeros", seed=M + N + K + lda)
+        check_full(h, ops)
+        outs = []
+        for _ in range(3):
+            d = device_operands(ops)
+            h.run(ops.M, ops.N, ops.K, ops.alpha, d["a_ptr"], ops.lda, d["b_ptr"], ops.ldb, ops.beta,
+                  d["c_ptr"], ops.ldc, s.cuda_stream)
+            s.synchronize()
+            outs.append(d["c_buf"].cpu().numpy().view(np.uint32))
+        assert all(np.array_equal(outs[0], o) for o in outs[1:])
+        ints = workloads.make_operands(M, N, K, lda=lda, beta=beta, dist="int3", dist_b="int2",
+                                       c_dist="int3" if beta else "zeros", seed=M + N + K + lda + 1)
+        check_full(h, ints, exact=True)
+
+
+def test_cluster_split_k_plan(mp):
+    # Clusters are the default for reproducible calls, which split K only
+    # that way (cutting more than 8 slices to 8); otherwise the slices add
+    # into C. One tile of 128 k-blocks: 16 slices by the automatic rule.
+    args = (128, 128, 8192, 1.0, 256, 8192, 256, 128, 0.5, 256, 128)
+    assert mp.plan(*args)["k_splits"] == 16 and mp.plan(*args)["split_reduce"] == 0
+    ops = workloads.make_operands(128, 128, 8192, beta=0.5, c_dist="normal", seed=77)
+    with mp.Handle() as h:
+        h.set_option(mp.Option.REPRODUCIBLE, 1)
+        hp = h.plan(*args)
+        assert (hp["k_splits"], hp["split_reduce"], hp["grid"]) == (8, 1, 8)
+        check_full(h, ops)
+        h.set_option(mp.Option.SPLIT_REDUCE, 1)   # reproducible without clusters: no split
+        assert h.plan(*args)["k_splits"] == 1
+    with mp.Handle() as h:
+        h.set_option(mp.Option.SPLIT_K, 16)
+        h.set_option(mp.Option.SPLIT_REDUCE, 2)   # clusters: 16 slices cut to 8
+        assert (h.plan(*args)["k_splits"], h.plan(*args)["split_reduce"]) == (8, 1)
+        check_full(h, ops)
+        h.set_option(mp.Option.SPLIT_REDUCE, 1)   # 16 slices added into C, within the tolerance
+        assert (h.plan(*args)["k_splits"], h.plan(*args)["split_reduce"]) == (16, 0)
+        check_full(h, ops)
 
 
 CLASS_CASES = [  # (M, N, K, lda, a_offset, tile_n, split_k): A read in row classes
@@ -783,7 +851,8 @@ def test_cta_pair_256_repeats_bits_and_reproducible_option(mp):
     # k-blocks and hand each one over before the other thread issues the
     # next, so the accumulator receives the k-blocks in one fixed order:
     # identical calls give identical bits. REPRODUCIBLE = 1 additionally
-    # rules out split-K (whose slices add into C in arrival order).
+    # rules out split-K whose slices add into C in arrival order (slices
+    # summed in clusters stay).
     from parity import device_operands
     s = torch.cuda.current_stream()
 
@@ -805,10 +874,12 @@ def test_cta_pair_256_repeats_bits_and_reproducible_option(mp):
         assert repeat(h, ops)
     ops = workloads.make_operands(4096, 16, 4096, dist="normal", seed=99)
     assert mp.plan(ops.M, ops.N, ops.K, 1.0, 256, ops.lda, 256, ops.ldb, 0.0, 256, ops.ldc)["k_splits"] > 1
-    with mp.Handle() as h:
-        h.set_option(mp.Option.REPRODUCIBLE, 1)
-        check_full(h, ops)
-        assert repeat(h, ops)
+    for reduce in (0, 1):
+        with mp.Handle() as h:
+            h.set_option(mp.Option.REPRODUCIBLE, 1)
+            h.set_option(mp.Option.SPLIT_REDUCE, reduce)
+            check_full(h, ops)
+            assert repeat(h, ops)
 
 
 def test_cta_pair_256_long_k_integer_stress(mp):
