@@ -1365,9 +1365,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 ptx::tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(acc_empty_bar(accb, 0));
-                ++local;
-                continue;
-            }
+            } else {
             // the accumulator's parts in order (one part: the whole item);
             // each part goes back to the MMA warp as soon as it has been read,
             // and parts past the item's width are handed back at once
@@ -1406,6 +1404,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         p.sk_flags + (w.range * Cfg::CTAS + static_cast<int32_t>(rank)) * Cfg::EPI_WARPS + (warp - 2),
                         p.sk_epoch);
             }
+            }   // (not CSPLIT)
             ++local;
         }
         // the TMA stores must have read this CTA's shared memory before the
