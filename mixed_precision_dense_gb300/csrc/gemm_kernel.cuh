@@ -288,12 +288,18 @@ struct TileConfig {
     // before storing any (not in 256 x 384 pairs, whose registers it spills:
     // 100 bytes, 65536 x 384 x 4096 200.0 -> 203.9 us)
     static constexpr bool EPI_BATCH_LOADS = BN != 384;
-    static constexpr int EPI_CHUNK_BYTES = 32 * 32 * 4;  // one warp's 32 x 32 FP32 chunk buffer
+    // chunks of 32 accumulator columns, or (EPI_COLS 16: the 288-wide pair
+    // with three stages of two k-blocks, which leave 22 KB for the buffers) of
+    // 16, each through its warp's buffer of 32 rows (4 or 2 KB, 128- or
+    // 64-byte swizzle, which TMA stores of 32 x 32 or 32 x 16 boxes read)
+    static constexpr int EPI_COLS = (PAIR && BN == 288 && KPS == 2) ? 16 : 32;
+    static constexpr int EPI_CHUNK_BYTES = 32 * EPI_COLS * 4;  // one warp's chunk buffer
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_CHUNK_BYTES;
     // row classes of A the kernel's parameters hold room for (see
-    // kMaxAClasses): 64 for the row-major pairs of 288 and 320 columns,
-    // which run the tall-skinny, memory-bound problems, 8 for the rest
-    static constexpr int A_CLASSES = (PAIR && !B_KMAJOR && (BN == 288 || BN == 320)) ? kMaxAClasses : 8;
+    // kMaxAClasses): 64 for the row-major pairs of 288 and 320 columns of
+    // one k-block per stage, which run the tall-skinny, memory-bound
+    // problems with A in row classes, 8 for the rest
+    static constexpr int A_CLASSES = (PAIR && !B_KMAJOR && (BN == 288 || BN == 320) && KPS == 1) ? kMaxAClasses : 8;
     // (allocations are powers of two: a 320-column accumulator takes 512)
     static constexpr int TMEM_COLS = (STAGGER || ACC_BUFS * BN > 256) ? 512 : 256;
     // full and empty per stage; accumulator full per buffer; accumulator
@@ -620,6 +626,13 @@ __device__ __forceinline__ uint32_t chunk_off(int row, int col) {
     return static_cast<uint32_t>(row * 128 + ((((col >> 2) ^ row) & 7) << 4) + (col & 3) * 4);
 }
 
+// The same for a 32 x 16 chunk (64-byte rows; 16-byte group g of row r at
+// g ^ ((r >> 1) & 3)): a lane writing its row's 16 columns as four 16-byte
+// stores, and 32 lanes reading 16 columns of two rows, touch every bank once.
+__device__ __forceinline__ uint32_t narrow_off(int row, int col) {
+    return static_cast<uint32_t>(row * 64 + ((((col >> 2) ^ (row >> 1)) & 3) << 4) + (col & 3) * 4);
+}
+
 // Byte offset of accumulator element (row, col) of a 128 x 128 FP32 partial
 // (cluster split-K): 512-byte rows, each 128-byte segment swizzled like a
 // chunk buffer, so that a lane writing 32 columns of its row as eight
@@ -773,6 +786,137 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMa
         }
 #pragma unroll
         for (int rr = 0; rr < 32; ++rr) c_cur[rr] = c_next[rr];
+        __syncwarp();
+    }
+    if (chunks <= 0) release();
+}
+
+// 16-column chunks (TileConfig::EPI_COLS 16). A lane's part of a 32 x 16
+// chunk whose first column is col0: column col0 + (lane & 15) of rows
+// 2 i + (lane >> 4), i < 16 (two 64-byte row pieces per warp store
+// instruction). load_c_chunk16 reads the old C values of those elements
+// into v[0..15] (rows at or past `rows`, columns at or past N: 0).
+__device__ __forceinline__ void load_c_chunk16(const float* c_rows, int64_t ldc, int32_t col0, int lane, int32_t N,
+                                               int32_t rows, float (&v)[32]) {
+    const int32_t rh = lane >> 4, col = col0 + (lane & 15);
+    const bool col_ok = col < N;
+    const float* q = c_rows + static_cast<int64_t>(rh) * ldc + col;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        v[i] = (col_ok && 2 * i + rh < rows) ? __ldg(q + static_cast<int64_t>(2 * i) * ldc) : 0.0f;
+}
+
+// One 32 x 16 chunk (accumulator words r, TMEM lane = row = lane) to C
+// without a beta * C term: alpha applied, through the warp's buffer (whose
+// layout is the tensor memory accelerator's 64-byte swizzle), then either a
+// tiled TMA store (reduce-add for split-K) of the 32 x 16 box at C row row0,
+// column col0 (p.c_tma), or read back into r and stored (atomic adds for
+// split-K or a stream-K first piece) lane by lane.
+template <bool SK>
+__device__ __forceinline__ void emit_chunk16(const GemmParams& p, const CUtensorMap* tmap_c, uint32_t (&r)[16],
+                                             float* c_tile, int64_t row_stride, int32_t rows, int32_t row0,
+                                             int32_t col0, uint32_t buf_s, int lane, int32_t sk) {
+    const float alpha = p.alpha;
+    if (chunk_tma<SK>(p, sk)) {
+        // the previous chunk's TMA store must have read the buffer
+        if (lane == 0) ptx::bulk_wait_read_all();
+        __syncwarp();
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        ptx::st_shared_v4(buf_s + narrow_off(lane, 4 * q), alpha * acc_value(r[4 * q], p.acc16),
+                          alpha * acc_value(r[4 * q + 1], p.acc16), alpha * acc_value(r[4 * q + 2], p.acc16),
+                          alpha * acc_value(r[4 * q + 3], p.acc16));
+    if (chunk_tma<SK>(p, sk)) {
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            if (chunk_accumulate<SK>(p, sk))
+                ptx::tma_reduce_add_2d(tmap_c, buf_s, col0, row0);
+            else
+                ptx::tma_store_2d(tmap_c, buf_s, col0, row0);
+            ptx::bulk_commit_group();
+        }
+        return;
+    }
+    __syncwarp();
+    const int32_t rh = lane >> 4, cl = lane & 15;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(ptx::ld_shared_f32(buf_s + narrow_off(2 * i + rh, cl)));
+    const int32_t col = col0 + cl;
+    if (col < p.N) {
+        float* cp = c_tile + col + static_cast<int64_t>(rh) * row_stride;
+        const bool add = chunk_accumulate<SK>(p, sk);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (2 * i + rh < rows) {
+                float* e = cp + static_cast<int64_t>(2 * i) * row_stride;
+                if (add)
+                    atomicAdd(e, __uint_as_float(r[i]));
+                else
+                    *e = __uint_as_float(r[i]);
+            }
+        }
+    }
+    __syncwarp();
+}
+
+// store_tile for 16-column chunks (the same contract): without beta * C the
+// chunks' tensor-memory loads go out two at a time; with beta != 0, c_cur
+// holds the first chunk's old C values (load_c_chunk16's order), and each
+// later chunk's go out before the previous chunk is stored.
+template <bool SK, class Release>
+__device__ __forceinline__ void store_tile16(const GemmParams& p, const CUtensorMap* tmap_c, uint32_t t_row,
+                                            float* c_tile, int64_t row_stride, int32_t rows, int32_t row0,
+                                            int32_t n0, int32_t width, uint32_t buf_s, int lane,
+                                            float (&c_cur)[32], int32_t sk, Release&& release) {
+    const float alpha = p.alpha, beta = p.beta;
+    const bool read_c = beta != 0.0f && p.k_splits <= 1 && (!SK || sk != kSkFirst);
+    const int32_t chunks = (min(width, p.N - n0) + 15) / 16;
+    if (!read_c) {
+        for (int32_t c = 0; c < chunks; c += 2) {
+            uint32_t r0[16], r1[16];
+            const bool two = c + 1 < chunks;
+            ptx::tmem_load_32x32b_x16(t_row + static_cast<uint32_t>(c * 16), r0);
+            if (two) ptx::tmem_load_32x32b_x16(t_row + static_cast<uint32_t>((c + 1) * 16), r1);
+            ptx::tmem_load_wait();
+            ptx::tmem_regs_ready(r0);
+            if (two) ptx::tmem_regs_ready(r1);
+            if (c + 2 >= chunks) release();
+            emit_chunk16<SK>(p, tmap_c, r0, c_tile, row_stride, rows, row0, n0 + c * 16, buf_s, lane, sk);
+            if (two)
+                emit_chunk16<SK>(p, tmap_c, r1, c_tile, row_stride, rows, row0, n0 + (c + 1) * 16, buf_s, lane, sk);
+        }
+        if (chunks <= 0) release();
+        return;
+    }
+    const int32_t rh = lane >> 4, cl = lane & 15;
+    float c_next[32];
+    for (int32_t c = 0; c < chunks; ++c) {
+        uint32_t r[16];
+        ptx::tmem_load_32x32b_x16(t_row + static_cast<uint32_t>(c * 16), r);
+        if (c + 1 < chunks) load_c_chunk16(c_tile, row_stride, n0 + (c + 1) * 16, lane, p.N, rows, c_next);
+        ptx::tmem_load_wait();
+        ptx::tmem_regs_ready(r);
+        if (c + 1 >= chunks) release();   // the part's last tensor-memory load has completed
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            ptx::st_shared_v4(buf_s + narrow_off(lane, 4 * q), alpha * acc_value(r[4 * q], p.acc16),
+                              alpha * acc_value(r[4 * q + 1], p.acc16), alpha * acc_value(r[4 * q + 2], p.acc16),
+                              alpha * acc_value(r[4 * q + 3], p.acc16));
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(ptx::ld_shared_f32(buf_s + narrow_off(2 * i + rh, cl)));
+        const int32_t col = n0 + c * 16 + cl;
+        if (col < p.N) {
+            float* cp = c_tile + col + static_cast<int64_t>(rh) * row_stride;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (2 * i + rh < rows)
+                    cp[static_cast<int64_t>(2 * i) * row_stride] = fmaf(beta, c_cur[i], __uint_as_float(r[i]));
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) c_cur[i] = c_next[i];
         __syncwarp();
     }
     if (chunks <= 0) release();
@@ -1300,8 +1444,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (item_read_c) {
                 // (this warp's first columns of the first part handed back)
                 const AccPart g0 = acc_part<Cfg>(0, accb, w.width);
-                load_c_chunk(c_tile, row_stride, n0 + g0.out_col + col_half * (g0.width / COL_SPLIT) + lane, p.N,
-                             rows, c_cur);
+                const int32_t col0 = n0 + g0.out_col + col_half * (g0.width / COL_SPLIT);
+                if constexpr (Cfg::EPI_COLS == 16)
+                    load_c_chunk16(c_tile, row_stride, col0, lane, p.N, rows, c_cur);
+                else
+                    load_c_chunk(c_tile, row_stride, col0 + lane, p.N, rows, c_cur);
             }
             if constexpr (Cfg::CSPLIT) {
                 // the old C of this CTA's rows of the tile into L2 while the
@@ -1388,9 +1535,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (g.out_col < w.width) {
                     // this warp's columns of the part, within the item
                     const int32_t my_w = min(my_n, w.width - g.out_col - my_off);
-                    if (h > 0 && item_read_c && my_w > 0) load_c_chunk(c_tile, row_stride, pn0 + lane, p.N, rows, c_cur);
-                    store_tile<Cfg::STREAM_K, Cfg::EPI_BATCH_LOADS>(p, &maps.c, t_row + static_cast<uint32_t>(g.tmem_col + my_off), c_tile, row_stride,
-                               rows, jb, pn0, my_w, buf_s, lane, c_cur, sk, release);
+                    if constexpr (Cfg::EPI_COLS == 16) {
+                        if (h > 0 && item_read_c && my_w > 0)
+                            load_c_chunk16(c_tile, row_stride, pn0, lane, p.N, rows, c_cur);
+                        store_tile16<Cfg::STREAM_K>(p, &maps.c, t_row + static_cast<uint32_t>(g.tmem_col + my_off),
+                                                    c_tile, row_stride, rows, jb, pn0, my_w, buf_s, lane, c_cur, sk,
+                                                    release);
+                    } else {
+                        if (h > 0 && item_read_c && my_w > 0)
+                            load_c_chunk(c_tile, row_stride, pn0 + lane, p.N, rows, c_cur);
+                        store_tile<Cfg::STREAM_K, Cfg::EPI_BATCH_LOADS>(p, &maps.c, t_row + static_cast<uint32_t>(g.tmem_col + my_off), c_tile, row_stride,
+                                   rows, jb, pn0, my_w, buf_s, lane, c_cur, sk, release);
+                    }
                 } else {
                     release();
                 }

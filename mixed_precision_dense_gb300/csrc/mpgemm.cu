@@ -58,18 +58,19 @@ using CfgPair384 = TileConfig<384, 4, true, false, 2>;
 // stages fit (N from 289 to 320, row-major B)
 using CfgPair320 = TileConfig<320, 5, true, false, 2>;
 // a CTA pair per 256 x 288 tile: parts of 256 and 32 columns, the 32-column
-// part read in 16-column boxes per CTA (2 KB, 32-byte swizzle), so five 34 KB
-// stages fit (N from 257 to 288, row-major B). Measured on GB300 at 65536 x
-// 257 x 4093 with lda 4093 (L2 flushed, us, beta 0.5 / 0): 256 x 320 pairs
-// 169.2 / 159.8; 256 x 288 pairs 164.2 / 151.6 (A in 128-byte row classes).
-// Three stages of two k-blocks would be faster still (160.5 / 147.3 with
-// the epilogue's chunk buffers shared, wrongly, by two warps each), but
-// leave 22 KB for the 32 KB of chunk buffers: with 16-row buffers the
-// epilogue took 9 us more; with 32 x 16 ones it spilled 276 bytes of
-// registers; with four epilogue warps beta = 0.5 took 169.4 us (the last
-// item's epilogue, exposed, runs at half the rate); two stages of two
-// k-blocks 181.6 us.
+// part read in 16-column boxes per CTA (2 KB, 32-byte swizzle) (N from 257
+// to 288, row-major B). With A in row classes, five 34 KB stages; with A
+// read as it is (aligned or staged), three 68 KB stages of two k-blocks and
+// 16-column epilogue chunks (2 KB buffers). Measured on GB300, L2 flushed,
+// us, five stages of one k-block / three of two: 65536 x 257 x 4093 (lda
+// 4093, 64 row classes) 163.8 / 164.2 at beta 0.5, 151.1 / 153.1 at beta 0;
+// A aligned: 65536 x 280 x 4096, beta 0.5, 156.7 / 149.5; 65536 x 288 x
+// 4096 133.5 / 129.2; 58368 x 264 x 4096 114.6 / 111.6. Before, 256 x 320
+// pairs took 169.2 / 159.8 us on the first shape (A in 16-byte classes); a
+// variant of three stages of two k-blocks whose eight epilogue warps shared
+// four 32-column buffers (wrong results, an upper bound) took 160.5 / 147.3.
 using CfgPair288 = TileConfig<288, 5, true, false, 2>;
+using CfgPair288A = TileConfig<288, 3, true, false, 2, 2>;
 // the same five shapes for a column-major B (a K-major B operand)
 using Cfg256K = TileConfig<256, 4, false, true>;
 using Cfg128K = TileConfig<128, 6, false, true>;
@@ -85,12 +86,14 @@ using Cfg128KC = TileConfig<128, 6, false, true, 1, 1, true>;
 constexpr int kMaxClusterSplits = kMaxClusterSlices;
 // stream-K flags per range: one per CTA of the pair and epilogue warp
 constexpr int kSkFlagsPerRange = 2 * CfgPair::EPI_WARPS;
-static_assert(CfgPair::STREAM_K && CfgPair288::STREAM_K && CfgPair320::STREAM_K && CfgPair384::STREAM_K &&
-                  !CfgWide::STREAM_K && CfgPair288::EPI_WARPS == CfgPair::EPI_WARPS &&
+static_assert(CfgPair::STREAM_K && CfgPair288::STREAM_K && CfgPair288A::STREAM_K && CfgPair320::STREAM_K &&
+                  CfgPair384::STREAM_K && !CfgWide::STREAM_K && CfgPair288::EPI_WARPS == CfgPair::EPI_WARPS &&
+                  CfgPair288A::EPI_WARPS == CfgPair::EPI_WARPS &&
                   CfgPair320::EPI_WARPS == CfgPair::EPI_WARPS && CfgPair384::EPI_WARPS == CfgPair::EPI_WARPS,
               "stream-K shapes");
 // the kernels whose parameters hold 64 row classes of A (the rest hold 8)
 static_assert(CfgPair288::A_CLASSES == kMaxAClasses && CfgPair320::A_CLASSES == kMaxAClasses &&
+                  CfgPair288A::A_CLASSES == kTableAClasses &&
                   CfgPair384::A_CLASSES == kTableAClasses && CfgPair::A_CLASSES == kTableAClasses &&
                   CfgWide::A_CLASSES == kTableAClasses && Cfg320::A_CLASSES == kTableAClasses,
               "row-class capacities");
@@ -99,8 +102,9 @@ static_assert(CfgPair288::A_CLASSES == kMaxAClasses && CfgPair320::A_CLASSES == 
 // thread and register limits at that occupancy
 static_assert(CfgWide::SMEM_BYTES > 232448 / 2 && CfgPair::SMEM_BYTES > 232448 / 2 &&
                   CfgPair384::SMEM_BYTES > 232448 / 2 && CfgPair320::SMEM_BYTES > 232448 / 2 &&
-                  CfgPair288::SMEM_BYTES > 232448 / 2 && CfgWide::THREADS <= 384 && CfgPair::THREADS <= 384 &&
-                  CfgPair384::THREADS <= 384 && CfgPair320::THREADS <= 384 && CfgPair288::THREADS <= 384,
+                  CfgPair288::SMEM_BYTES > 232448 / 2 && CfgPair288A::SMEM_BYTES > 232448 / 2 &&
+                  CfgWide::THREADS <= 384 && CfgPair::THREADS <= 384 && CfgPair384::THREADS <= 384 &&
+                  CfgPair320::THREADS <= 384 && CfgPair288::THREADS <= 384 && CfgPair288A::THREADS <= 384,
               "the wide pair kernel fits wherever the 256 x 256 pair kernel fits");
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -311,13 +315,14 @@ std::vector<int32_t> sk_range_starts(int64_t units, int64_t k_blocks, int64_t R)
     return moved;
 }
 
-// 64-wide k-blocks per pipeline stage of the kernel a plan launches.
-int32_t plan_kps(int32_t tile_m, int32_t tile_n, bool b_col_major) {
+// 64-wide k-blocks per pipeline stage of the kernel a plan launches (the
+// 256 x 288 pair: two for an A read as it is, one for A in row classes).
+int32_t plan_kps(int32_t tile_m, int32_t tile_n, bool b_col_major, bool a_classes = false) {
     if (tile_m == 256) {
         if (tile_n == 512) return b_col_major ? CfgWideK::KPS : CfgWide::KPS;
         if (tile_n == 384) return b_col_major ? CfgPair384K::KPS : CfgPair384::KPS;
         if (tile_n == 320) return CfgPair320::KPS;
-        if (tile_n == 288) return CfgPair288::KPS;
+        if (tile_n == 288) return a_classes ? CfgPair288::KPS : CfgPair288A::KPS;
         return b_col_major ? CfgPairK::KPS : CfgPair::KPS;
     }
     if (tile_n == 320) return b_col_major ? Cfg320K::KPS : Cfg320::KPS;
@@ -391,7 +396,11 @@ mpgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, float alpha, const vo
     p.a_classes = a_classes ? choose_a_classes(lda, M, p.tile_m, class_room) : 0;
     const AClassLayout L = a_class_layout(A, lda, M, p.a_classes, p.tile_m);
     const int64_t m_tiles = L.first_tile[L.P], n_tiles = ceil_div(N, p.tile_n);
-    p.tile_k = 64 * plan_kps(p.tile_m, p.tile_n, opt.b_col_major != 0);
+    p.tile_k = 64 * plan_kps(p.tile_m, p.tile_n, opt.b_col_major != 0, p.a_classes > 0);
+    if (p.tile_m == 256 && p.tile_n == 288 && p.tile_k == 128) {   // A read as it is
+        p.stages = CfgPair288A::STAGES;
+        p.smem_bytes = CfgPair288A::SMEM_BYTES;
+    }
     const int64_t k_blocks = ceil_div(K + L.max_shift, p.tile_k);
     if (m_tiles * n_tiles > kDimLimit / 2) return MPGEMM_ERR_INVALID_VALUE;
     p.m_tiles = static_cast<int32_t>(m_tiles);
@@ -804,6 +813,7 @@ cudaError_t prepare_kernels() {
     if (e == cudaSuccess) e = set_smem_attr<CfgPair384K>();
     if (e == cudaSuccess) e = set_smem_attr<CfgPair320>();
     if (e == cudaSuccess) e = set_smem_attr<CfgPair288>();
+    if (e == cudaSuccess) e = set_smem_attr<CfgPair288A>();
     if (e == cudaSuccess) e = set_smem_attr<Cfg128C>();
     if (e == cudaSuccess) e = set_smem_attr<Cfg128KC>();
     return e;
@@ -856,18 +866,21 @@ bool encode_a(const mpgemm_plan_t& plan, const void* a_use, int64_t lda_use, int
 // Row-major FP32 matrix rows x cols with pitch ld (elements), 32 x 32 boxes,
 // 128-byte swizzle: the tiled TMA store of the epilogue's chunks.
 bool encode_f32_store(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
-                      MapCache* cache = nullptr) {
+                      MapCache* cache = nullptr, uint32_t box_cols = 32) {
+    // (32 x 16 boxes, for 16-column chunks: the 64-byte swizzle)
+    const CUtensorMapSwizzle swizzle = box_cols == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     const uint64_t key[6] = {32, reinterpret_cast<uintptr_t>(base), static_cast<uint64_t>(rows),
-                             static_cast<uint64_t>(cols), static_cast<uint64_t>(ld), (32ull << 32) | 32u};
+                             static_cast<uint64_t>(cols), static_cast<uint64_t>(ld),
+                             (static_cast<uint64_t>(box_cols) << 32) | 32u};
     if (cache && cache->find(key, map)) return true;
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
-    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t box[2] = {box_cols, 32};
     const cuuint32_t estr[2] = {1, 1};
     const bool ok = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     if (ok && cache) cache->put(key, *map);
     return ok;
@@ -887,7 +900,9 @@ void encode_c(const mpgemm_plan_t& plan, float* C, int64_t M, int64_t N, int64_t
     if (c_store == 1 || (beta != 0.0f && plan.k_splits <= 1) || gp->a_classes != 1 || N % 4 != 0) return;
     if (plan.split_reduce) return;   // the cluster's sums are written per lane
     if (!aligned16(C, ldc, 4)) return;
-    if (encode_f32_store(&maps->c, C, M, N, ldc, cache)) gp->c_tma = 1;
+    // (the 256 x 288 pair's 16-column chunks, with A read as it is: boxes of 16 columns)
+    const uint32_t box_cols = (plan.tile_m == 256 && plan.tile_n == 288 && plan.tile_k == 128) ? 16 : 32;
+    if (encode_f32_store(&maps->c, C, M, N, ldc, cache, box_cols)) gp->c_tma = 1;
 }
 
 // The narrow B boxes of 256 x 320 and 256 x 288 pair tiles (32 or 16 columns
@@ -960,7 +975,9 @@ cudaError_t launch_plan(const mpgemm_plan_t& plan, bool b_col_major, int max_clu
             return b_col_major ? launch_tc<CfgPair384K>(grid, ta, tb, gp, stream)
                                : launch_tc<CfgPair384>(grid, ta, tb, gp, stream);
         if (plan.tile_n == 320) return launch_tc<CfgPair320>(grid, ta, tb, gp, stream);
-        if (plan.tile_n == 288) return launch_tc<CfgPair288>(grid, ta, tb, gp, stream);
+        if (plan.tile_n == 288)
+            return plan.tile_k == 128 ? launch_tc<CfgPair288A>(grid, ta, tb, gp, stream)
+                                      : launch_tc<CfgPair288>(grid, ta, tb, gp, stream);
         return b_col_major ? launch_tc<CfgPairK>(grid, ta, tb, gp, stream)
                            : launch_tc<CfgPair>(grid, ta, tb, gp, stream);
     }

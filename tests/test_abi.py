@@ -174,14 +174,16 @@ def test_tile_selection_and_grid():
     with pytest.raises(mp.MpgemmError):
         _plan(tile_m=128, tile_n=512)
     # N = 257 would waste half of the last column band: one tile column of
-    # 256 x 288 CTA pairs (A read once per row block, five 34 KB stages, A in
-    # 64 row classes of 4 pair tiles each)
+    # 256 x 288 CTA pairs (A read once per row block; A in 64 row classes of
+    # 4 pair tiles each, five 34 KB stages)
     p = _plan(M=65536, N=257, K=4093, lda=4093, ldb=257, ldc=257, beta=0.5)
     assert (p["tile_m"], p["tile_n"]) == (256, 288) and p["tiles"] == 256 and p["stages"] == 5
     assert p["tile_k"] == 64 and p["a_classes"] == 64 and p["split_tiles"] == 0
     assert 200 * 1024 < p["smem_bytes"] <= 232448
+    # A aligned: three 68 KB stages of two k-blocks
     p = _plan(M=58368, N=257, K=4096, lda=4096, ldb=264, ldc=257, beta=0.5)
     assert (p["tile_m"], p["tile_n"]) == (256, 288) and p["tiles"] == 228
+    assert (p["stages"], p["tile_k"], p["a_classes"]) == (3, 128, 0) and p["smem_bytes"] <= 232448
     # N from 289 to 320: 256 x 320 pairs (five 36 KB stages)
     p = _plan(M=58368, N=300, K=4096, lda=4096, ldb=304, ldc=300, beta=0.5)
     assert (p["tile_m"], p["tile_n"], p["stages"], p["tile_k"]) == (256, 320, 5, 64) and p["tiles"] == 228
@@ -213,7 +215,8 @@ def test_tile_selection_and_grid():
     with pytest.raises(mp.MpgemmError):
         _plan(tile_m=128, tile_n=288)
     p = _plan(M=5000, N=1000, K=700, lda=700, ldb=1000, ldc=1000, tile_n=288)
-    assert (p["tile_m"], p["tile_n"], p["stages"]) == (256, 288, 5) and p["tiles"] == 20 * 4
+    # (lda 700: 1400-byte rows, read in row classes: five stages of one k-block)
+    assert (p["tile_m"], p["tile_n"], p["stages"], p["tile_k"]) == (256, 288, 5, 64) and p["tiles"] == 20 * 4
     assert p["split_tiles"] == 0
     # forced pairs with a CTA cap: the grid stays even
     p = _plan(M=1000, N=800, K=64, lda=64, ldb=800, ldc=800, tile_m=256, max_ctas=5)

@@ -542,7 +542,9 @@ def test_cta_pair_320_integer_bitwise(mp):
 
 
 PAIR288_SHAPES = [  # (M, N, K, lda, ldb, ldc, beta, max_ctas): 256 x 288 pair tiles, 32-column last part
-    (256, 288, 64, 64, 288, 288, 0.0, 0),       # one full tile (TMA stores)
+    (256, 288, 64, 64, 288, 288, 0.0, 0),       # one full tile (TMA stores of 32 x 16 boxes)
+    (700, 288, 1000, 1000, 288, 288, 0.0, 0),   # A aligned: stages of two k-blocks, TMA stores
+    (1500, 280, 4096, 4096, 280, 280, 0.5, 6),  # A aligned, beta * C, three pairs walk the tiles
     (256, 257, 617, 617, 257, 257, 0.5, 0),     # one column past 256: the 32-column part, 8 row classes
     (1000, 280, 700, 700, 280, 281, 1.0, 4),    # two pairs walk 4 tiles through the staggered layouts
     (511, 700, 129, 129, 700, 700, -0.5, 0),    # three tile columns, the last 124 wide (one 128 unit)
