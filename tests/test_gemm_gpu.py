@@ -943,6 +943,10 @@ STREAM_K_CASES = [  # (tile_m, tile_n, max_ctas, M, N, K, lda, ldb, ldc, beta, b
     (256, 288, 6, 1900, 257, 617, 617, 257, 257, 0.5, False),
     # 256 x 288 pairs, A in 64 line-aligned classes (the walk crosses classes)
     (256, 288, 20, 16384, 260, 300, 301, 260, 260, 0.5, False),
+    # 256 x 288 pairs, A aligned (stages of two k-blocks, 16-column chunks):
+    # whole tiles through TMA stores of 32 x 16 boxes, cut ones per lane
+    (256, 288, 20, 16384, 260, 512, 512, 260, 260, 0.0, False),
+    (256, 288, 12, 4096, 288, 1024, 1024, 288, 288, 0.75, False),
     # 256 x 384 pairs, beta == 1, unaligned A and C, 6 tiles on 5 pairs
     (256, 384, 10, 1300, 380, 333, 335, 380, 383, 1.0, False),
     # 256 x 384 pairs with a column-major B, 4 tiles on 2 pairs (one range = two tiles)
