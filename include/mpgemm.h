@@ -120,7 +120,9 @@ mpgemm_status_t mpgemm_run_ex(mpgemm_handle_t h, mpgemm_b_layout_t b_layout,
  * "Independent gate": C = A * B with A (m x k) row-major, B (k x n)
  * column-major and C (m x n) row-major, all densely packed (lda = k,
  * ldb = k, ldc = n), asynchronous on `stream`. The first call on a device
- * creates a handle for that device that lives until the process exits; all
+ * creates a handle for that device that lives until the process exits (if
+ * that creation fails, its status is returned and the next call on the
+ * device tries again); all
  * calls on a device share its workspace, so calls on different streams of
  * one device must not overlap on the GPU (use mpgemm_run_ex with a handle
  * per stream for that). Host threads may call it concurrently: the calls

@@ -1007,14 +1007,13 @@ using namespace mpgemm;
 struct mpgemm_handle_st;
 
 namespace {
-// mpgemm_solve's handle per device, created on the first call on that device
-// and kept until the process exits.
+// mpgemm_solve's handle per device, created by the first call on that device
+// that succeeds in creating it (a failed creation is returned and the next
+// call tries again) and kept until the process exits.
 constexpr int kSolveMaxDevices = 64;
 struct SolveDevice {
-    std::once_flag once;
-    mpgemm_status_t status = MPGEMM_ERR_CUDA;
     mpgemm_handle_st* handle = nullptr;
-    std::mutex mu;   // the handle's host state (tensor-map cache, workspace) is not thread-safe
+    std::mutex mu;   // guards `handle`; its host state (tensor-map cache, workspace) is not thread-safe
 };
 SolveDevice g_solve_devices[kSolveMaxDevices];
 }  // namespace
@@ -1435,10 +1434,14 @@ mpgemm_status_t mpgemm_solve(const void* a, const void* b, float* c, size_t m, s
     }
     if (dev < 0 || dev >= kSolveMaxDevices) return MPGEMM_ERR_CUDA;
     SolveDevice& d = g_solve_devices[dev];
-    std::call_once(d.once, [&d] { d.status = mpgemm_create(&d.handle); });
-    if (d.status != MPGEMM_OK) return d.status;
     const int64_t M = static_cast<int64_t>(m), N = static_cast<int64_t>(n), K = static_cast<int64_t>(k);
     std::lock_guard<std::mutex> lock(d.mu);
+    if (!d.handle) {
+        mpgemm_handle_st* h = nullptr;
+        const mpgemm_status_t st = mpgemm_create(&h);
+        if (st != MPGEMM_OK) return st;
+        d.handle = h;
+    }
     return mpgemm_run_ex(d.handle, MPGEMM_B_COL_MAJOR, M, N, K, 1.0f, a, K > 1 ? K : 1, b,
                          K > 1 ? K : 1, 0.0f, c, N > 1 ? N : 1, stream);
 }
